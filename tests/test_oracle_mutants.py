@@ -1,0 +1,66 @@
+"""The pins catch plausible mistakes in the oracle (CPU only).
+
+Each case plants one mistake in a copy of ``oracle/kdn_oracle.c`` (a dropped
+term, a sign, a swapped operand or index, an off-by-one step), builds the copy
+with gcc and requires that at least one pin of ``oracle_pins`` fails on it.
+The real oracle is never modified.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kdn_oracle.c")
+
+MUTANTS = {
+    "gate_sign": ("exp(-A[h] * d[bh * T + t])", "exp(A[h] * d[bh * T + t])"),
+    "gate_without_A": ("exp(-A[h] * d[bh * T + t])", "exp(-d[bh * T + t])"),
+    "gate_previous_token": ("exp(-A[h] * d[bh * T + t])", "exp(-A[h] * d[bh * T + (t > 0 ? t - 1 : 0)])"),
+    "gate_head_zero": ("exp(-A[h] * d[bh * T + t])", "exp(-A[0] * d[bh * T + t])"),
+    "drop_prior_leak": ("+ (1.0 - alpha) * I_prior", ""),
+    "prior_leak_sign": ("+ (1.0 - alpha) * I_prior", "- (1.0 - alpha) * I_prior"),
+    "evidence_k_not_squared": ("bt[i] * (kt[j] * kt[j])", "bt[i] * kt[j]"),
+    "evidence_beta_index": ("bt[i] * (kt[j] * kt[j])", "bt[j] * (kt[j] * kt[j])"),
+    "ratio_inverted": ("(I_prev / I_new)", "(I_new / I_prev)"),
+    "drop_ratio": ("alpha * (I_prev / I_new) * mu[e]", "alpha * mu[e]"),
+    "drop_alpha_in_mean": ("alpha * (I_prev / I_new) * mu[e]", "(I_prev / I_new) * mu[e]"),
+    "write_uses_q": ("((bt[i] * vt[i]) * kt[j])", "((bt[i] * vt[i]) * qt[j])"),
+    "write_value_index": ("((bt[i] * vt[i]) * kt[j])", "((bt[i] * vt[j]) * kt[j])"),
+    "write_missing_beta": ("((bt[i] * vt[i]) * kt[j])", "((vt[i]) * kt[j])"),
+    "readout_uses_k": ("s += mu[i * dk + j] * qt[j]", "s += mu[i * dk + j] * kt[j]"),
+    "readout_uses_importance": ("s += mu[i * dk + j] * qt[j]", "s += I[i * dk + j] * qt[j]"),
+    "ignore_initial_importance": ("I[e] = I0 ? I0[bh * dv * dk + e] : I_prior;", "I[e] = I_prior;"),
+    "ignore_initial_mean": ("mu[e] = mu0 ? mu0[bh * dv * dk + e] : 0.0;", "mu[e] = 0.0;"),
+    "mobius_swap_b_c": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
+                        "lam = (a[e] * lam + c[e]) / (b[e] * lam + d[e]);"),
+    "mobius_swap_c_d": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
+                        "lam = (a[e] * lam + b[e]) / (d[e] * lam + c[e]);"),
+    "mobius_output_before_step": (
+        "lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);\n            out[e] = lam;",
+        "out[e] = lam;\n            lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);"),
+    "mobius_ignores_lambda0": ("double lam = lambda0[n];", "double lam = 1.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    oracle.build(force=True, src=str(mut), out=so)
+    lib = oracle.load(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except (FloatingPointError, ZeroDivisionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
