@@ -1,0 +1,782 @@
+// diag_impl.cuh -- the diagonal metaplastic scan with readout, for sm_103a.
+//
+// What is computed ("Learning to Remember, Learn, and Forget in Attention-
+// Based Models", Metodologia 1-2; readout as in "Kalman Linear Attention
+// (KLA)", Metodologia 1), per head, per token t, per state element (i, j):
+//     alpha_t = exp(-A d_t)
+//     I_t  = alpha_t I_{t-1} + (1 - alpha_t) I_prior + beta_i k_j^2
+//     mu_t = alpha_t (I_{t-1}/I_t) mu_{t-1} + beta_i v_i k_j / I_t
+//     o_t[i] = sum_j mu_t[i][j] q_j
+//
+// How it is computed.  Write J = I - I_prior and eta = I mu.  The two
+// updates above are then exactly
+//     J_t   = alpha_t J_{t-1}   + beta_i k_j^2
+//     eta_t = alpha_t eta_{t-1} + beta_i v_i k_j,      mu_t = eta_t / (I_prior + J_t)
+// (the information form).  The kernel stores the state multiplied by a
+// per-head working scale W_t (Jw = W J, Ew = W eta) with
+//     W_t = W_{t-1} / alpha_t * 2^{-r_t},
+// r_t an integer chosen so that W stays in [1, 2^48).  Per element and token
+// the update then needs no multiply by alpha:
+//     Jw <- f_t Jw + (W beta_i) k_j^2,  Ew <- f_t Ew + (W beta_i v_i) k_j,
+// with f_t = 2^{-r_t} = 1 on all but the rare rescaling tokens (where the
+// multiply is exact).  The readout divides per element:
+//     mu q = sigma * q_j Ew / (sigma Jw + sigma W I_prior),  sigma = 2^-24,
+// where sigma centres the scaled denominators on 1 so that products of two
+// of them stay in range.  Pairs of quotients may share one reciprocal,
+// n1/d1 + n2/d2 = (n1 d2 + n2 d1) / (d1 d2), which trades one MUFU op for one
+// FP32 op; PAIRS of the 4 column-pair groups of a lane row are combined that
+// way to balance the FMA pipe (128 lanes/clk/SM) against the MUFU pipe
+// (16 rcp/clk/SM).  Element arithmetic uses packed FFMA2/FMUL2.
+//
+// Work decomposition.  Every state element is an independent scalar
+// recurrence; only the readout reduces over j.  A CTA owns 128 consecutive
+// state rows (whole heads: 128/d_v of them) for a token range and keeps them
+// in registers for the whole range.  It has d_k/16 warps; a lane holds 4 rows
+// x 16 columns (64 elements, 128 fp32 registers) and the d_k/16 lanes of a
+// row set reduce the readout with shuffles.  There is no producer warp (a
+// ninth warp would cap registers at 168 per thread); instead:
+//   * q, k, v, beta, d of each chunk of TC tokens are brought into shared
+//     memory by 1-D bulk TMA copies that complete on an mbarrier; the warp
+//     that finishes a chunk last refills its stage with the chunk three
+//     ahead (no warp ever blocks on stage reuse);
+//   * one chunk ahead of its compute, every warp converts its share of the
+//     next chunk's tokens k -> (k, k^2) and q to fp32 in a bank-conflict-free
+//     interleaved layout, and arrives on the chunk's "params ready" barrier;
+//   * every lane runs the per-head scale recursion (W_t, f_t) itself inside
+//     the token loop (one exp2f per token).
+// All waits are bounded by GPU time and record KDN_ERR_TIMEOUT instead of
+// blocking forever.
+// Long sequences with few heads are split into P token ranges (parts): an
+// aggregate pass (AGG = true: updates only, zero initial state, no readout)
+// gives each part's end state, a carry pass chains them, and the full pass
+// runs every part from its carried start state.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kdn_device.cuh"
+#include "kdn_internal.h"
+
+namespace kdn {
+namespace diag {
+// everything here is instantiated per translation unit (one per input dtype)
+namespace {
+
+constexpr int RT = 4;            // rows per lane
+constexpr int CW = 16;           // columns per lane
+constexpr int NSTAGE = 3;        // chunks in flight
+constexpr int ROWS_PER_CTA = 128;
+constexpr int PAIRS = 3;         // column-pair groups (of 4) per lane row sharing a reciprocal
+constexpr float SIGMA = 5.9604644775390625e-08f;   // 2^-24
+constexpr float W_LIMIT = 281474976710656.0f;      // 2^48
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct AggScale {
+    float W;   // working scale at the end of the part (zero start, W = 1 at its start)
+    int R;     // total power-of-two exponent removed by rescaling within the part
+};
+
+struct Params {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* beta;
+    const void* d;
+    const float* A;
+    float I_prior;
+    const float* I0;
+    const float* mu0;
+    float* out;              // [BH,T,dv] (full pass) or unused (aggregate pass)
+    float* final_state;      // [2,BH,dv,dk] or null
+    float* agg;              // [P-1][BH][2][dv][dk] part end states / carried start states
+    AggScale* agg_scale;     // [P-1][BH]
+    long long BH;
+    int H, T, dv;
+    int part_len;            // tokens per part (multiple of TC)
+    int TC;                  // tokens per chunk
+    int d_tma;               // 1: d staged by TMA (aligned), 0: plain loads
+    long long wait_ns;
+};
+
+template <int DK>
+struct Geo {
+    static constexpr int M = DK / CW;              // lanes sharing a row set
+    static constexpr int RS = 32 / M;              // row sets per warp
+    static constexpr int WR = RS * RT;             // rows per warp
+    static constexpr int NW = ROWS_PER_CTA / WR;   // warps per CTA (= M)
+    static constexpr int NTHREADS = NW * 32;
+    static constexpr int PAR_FLOATS = 3 * DK;      // per token: k, k^2, q (fp32)
+};
+
+// shared-memory layout of one chunk stage for `hpc` heads
+struct Layout {
+    int raw_qk, raw_vb, raw_d, par;   // bytes per head of each region
+    int head, stage;                  // bytes per head, per stage
+    __host__ __device__ Layout(int dk, int dv, int es, int TC, int hpc) {
+        raw_qk = TC * dk * es;
+        raw_vb = TC * dv * es;
+        raw_d = (TC * es + 15) & ~15;
+        par = TC * 3 * dk * 4;
+        head = 2 * raw_qk + 2 * raw_vb + raw_d + par;
+        stage = hpc * head;
+    }
+};
+
+__host__ __device__ inline int smem_bytes(int dk, int dv, int es, int TC) {
+    const int hpc = ROWS_PER_CTA / dv;
+    Layout L(dk, dv, es, TC, hpc);
+    return NSTAGE * L.stage + 2 * NSTAGE * 8 + NSTAGE * 4;
+}
+
+// one error word per translation unit that instantiates these kernels
+__device__ int g_diag_error = 0;
+
+template <typename TIn>
+__device__ __forceinline__ float to_f32(TIn x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// four consecutive inputs -> fp32 (8-byte or 16-byte aligned shared memory)
+__device__ __forceinline__ void load4(const float* p, float* o) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* o) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    o[0] = __uint_as_float(x.x << 16);
+    o[1] = __uint_as_float(x.x & 0xffff0000u);
+    o[2] = __uint_as_float(x.y << 16);
+    o[3] = __uint_as_float(x.y & 0xffff0000u);
+}
+
+// two consecutive inputs -> fp32
+__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load2(const __nv_bfloat16* p) {
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// hardware reciprocal (MUFU), max relative error 2^-23 per the PTX ISA;
+// denormal results flush to zero (the scaled denominators stay normal)
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// Reduce-scatter of 4 row partials over the M lanes of a row set.  On return
+// `val[0..NV)` hold complete sums for rows `row[0..NV)` (indices 0..3) and
+// `store` says whether this lane writes them.
+template <int M>
+struct RowReduce;
+
+template <>
+struct RowReduce<8> {
+    static constexpr int NV = 1;
+    __device__ __forceinline__ static void run(const float p[4], int cg, float val[1], int row[1],
+                                               bool& store) {
+        const bool up = cg & 4;
+        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
+        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
+        k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
+        k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+        const bool up2 = cg & 2;
+        float kk = up2 ? k1 : k0;
+        const float s = up2 ? k0 : k1;
+        kk += __shfl_xor_sync(0xffffffffu, s, 2);
+        kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+        val[0] = kk;
+        row[0] = (up ? 2 : 0) + (up2 ? 1 : 0);
+        store = (cg & 1) == 0;
+    }
+};
+
+template <>
+struct RowReduce<4> {
+    static constexpr int NV = 1;
+    __device__ __forceinline__ static void run(const float p[4], int cg, float val[1], int row[1],
+                                               bool& store) {
+        const bool up = cg & 2;
+        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
+        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
+        k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        const bool up2 = cg & 1;
+        float kk = up2 ? k1 : k0;
+        const float s = up2 ? k0 : k1;
+        kk += __shfl_xor_sync(0xffffffffu, s, 1);
+        val[0] = kk;
+        row[0] = (up ? 2 : 0) + (up2 ? 1 : 0);
+        store = true;
+    }
+};
+
+template <>
+struct RowReduce<2> {
+    static constexpr int NV = 2;
+    __device__ __forceinline__ static void run(const float p[4], int cg, float val[2], int row[2],
+                                               bool& store) {
+        const bool up = cg & 1;
+        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
+        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
+        k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        val[0] = k0;
+        val[1] = k1;
+        row[0] = up ? 2 : 0;
+        row[1] = row[0] + 1;
+        store = true;
+    }
+};
+
+template <>
+struct RowReduce<1> {
+    static constexpr int NV = 4;
+    __device__ __forceinline__ static void run(const float p[4], int, float val[4], int row[4],
+                                               bool& store) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            val[r] = p[r];
+            row[r] = r;
+        }
+        store = true;
+    }
+};
+
+// The per-head scale recursion for one token (see the header comment):
+// returns f_t = 2^-r_t and updates (W, R).  x = A d / ln 2.
+__device__ __forceinline__ float scale_step(float x, float& W, int& R) {
+    float p;
+    int r;
+    if (fabsf(x) <= 64.f) {
+        p = W * exp2f(x);                      // in [2^-64, 2^112)
+        if (p >= 1.f && p < W_LIMIT) {
+            r = 0;
+        } else {
+            r = exponent_of(p);
+            p = __int_as_float(__float_as_int(p) - (r << 23));
+        }
+    } else if (x > 64.f) {                     // very fast forgetting (or +inf)
+        const float n = fminf(floorf(x), 1.0e6f);
+        p = W * exp2f(x - n);                  // x - n in [0, 1)
+        const int e = exponent_of(p);
+        p = __int_as_float(__float_as_int(p) - (e << 23));
+        r = e + static_cast<int>(n);
+        if (!(x < __int_as_float(0x7f800000))) p = 1.f;   // x = +inf: W restarts at 1
+    } else if (x < -64.f) {                    // growth (alpha > 1)
+        const float n = fmaxf(floorf(x), -1.0e6f);
+        p = W * exp2f(x - n);
+        const int e = exponent_of(p);
+        p = __int_as_float(__float_as_int(p) - (e << 23));
+        r = e + static_cast<int>(n);
+    } else {                                   // NaN propagates
+        p = x;
+        r = 0;
+    }
+    // beyond +-4096 the factor is 0 or inf anyway; keep R in int range
+    r = max(-4096, min(4096, r));
+    W = p;
+    R = max(-(1 << 30), min(1 << 30, R + r));
+    return r == 0 ? 1.f : pow2i(-r);
+}
+
+template <int DK, typename TIn, bool AGG>
+__global__ void __launch_bounds__(Geo<DK>::NTHREADS, (DK >= 128 ? 1 : 2))
+diag_scan_kernel(const Params p) {
+    using G = Geo<DK>;
+    constexpr int M = G::M, NW = G::NW, PF = G::PAR_FLOATS;
+    constexpr int ES = sizeof(TIn);
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int dv = p.dv, HPC = ROWS_PER_CTA / dv, TC = p.TC;
+    const Layout L(DK, dv, ES, TC, HPC);
+    uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + NSTAGE * L.stage);
+    uint64_t* full_par = full_raw + NSTAGE;
+    int* done_cnt = reinterpret_cast<int*>(full_par + NSTAGE);
+    auto region = [&](int s, int h, int off) { return smem + s * L.stage + h * L.head + off; };
+    auto raw_q = [&](int s, int h) { return reinterpret_cast<TIn*>(region(s, h, 0)); };
+    auto raw_k = [&](int s, int h) { return reinterpret_cast<TIn*>(region(s, h, L.raw_qk)); };
+    auto raw_v = [&](int s, int h) { return reinterpret_cast<TIn*>(region(s, h, 2 * L.raw_qk)); };
+    auto raw_b = [&](int s, int h) {
+        return reinterpret_cast<TIn*>(region(s, h, 2 * L.raw_qk + L.raw_vb));
+    };
+    auto raw_d = [&](int s, int h) {
+        return reinterpret_cast<TIn*>(region(s, h, 2 * L.raw_qk + 2 * L.raw_vb));
+    };
+    auto par = [&](int s, int h) {
+        return reinterpret_cast<float*>(region(s, h, 2 * L.raw_qk + 2 * L.raw_vb + L.raw_d));
+    };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long head0 = static_cast<long long>(blockIdx.x) * HPC;
+    const int nheads = static_cast<int>(min(static_cast<long long>(HPC), p.BH - head0));
+    const int part = blockIdx.y;
+    const int T = p.T;
+    const int tb = min(T, part * p.part_len);
+    const int te = min(T, tb + p.part_len);
+    const int nchunks = (te - tb + TC - 1) / TC;
+    const TIn* gq = static_cast<const TIn*>(p.q);
+    const TIn* gk = static_cast<const TIn*>(p.k);
+    const TIn* gv = static_cast<const TIn*>(p.v);
+    const TIn* gb = static_cast<const TIn*>(p.beta);
+    const TIn* gd = static_cast<const TIn*>(p.d);
+
+    // Issue the bulk copies of chunk c into its stage (one warp, all lanes).
+    auto issue = [&](int c) {
+        const int s = c % NSTAGE;
+        const int t0 = tb + c * TC, tcn = min(TC, te - t0);
+        const int dbytes = p.d_tma ? tcn * ES : 0;
+        if (lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&full_raw[s],
+                                  static_cast<uint32_t>(nheads * (tcn * ((AGG ? 1 : 2) * DK + 2 * dv) * ES +
+                                                                  dbytes)));
+        }
+        __syncwarp();
+        for (int x = lane; x < nheads * 5; x += 32) {
+            const int h = x / 5, which = x - h * 5;
+            const long long tok = (head0 + h) * T + t0;
+            if (which == 0) {
+                if (!AGG) bulk_g2s(raw_q(s, h), gq + tok * DK, tcn * DK * ES, &full_raw[s]);
+            } else if (which == 1) {
+                bulk_g2s(raw_k(s, h), gk + tok * DK, tcn * DK * ES, &full_raw[s]);
+            } else if (which == 2) {
+                bulk_g2s(raw_v(s, h), gv + tok * dv, tcn * dv * ES, &full_raw[s]);
+            } else if (which == 3) {
+                bulk_g2s(raw_b(s, h), gb + tok * dv, tcn * dv * ES, &full_raw[s]);
+            } else if (dbytes) {
+                bulk_g2s(raw_d(s, h), gd + tok, dbytes, &full_raw[s]);
+            }
+        }
+    };
+
+    bool ok = true;
+    // Convert this warp's tokens (tt = warp, warp + NW, ...) of chunk c:
+    // k -> (k, k^2) and q to fp32, in the interleaved layout in which the
+    // 16-column group cg of a lane is float4 number (s4 * M + cg), s4 = 0..3.
+    auto convert = [&](int c) {
+        const int s = c % NSTAGE;
+        const int t0 = tb + c * TC, tcn = min(TC, te - t0);
+        if (!mbar_wait(&full_raw[s], (c / NSTAGE) & 1, p.wait_ns)) ok = false;
+        constexpr int HP = DK / 2;   // column pairs per token
+        for (int tt = warp; tt < tcn; tt += NW) {
+            for (int x = lane; x < nheads * HP; x += 32) {
+                const int h = x / HP;
+                const int j = 2 * (x - h * HP);
+                const int cg = j / CW, jj = j % CW;
+                const int pos = ((jj >> 2) * M + cg) * 4 + (jj & 3);
+                float* base = par(s, h) + tt * PF;
+                const float2 kv = load2(raw_k(s, h) + tt * DK + j);
+                *reinterpret_cast<float2*>(base + pos) = kv;
+                *reinterpret_cast<float2*>(base + DK + pos) = make_float2(kv.x * kv.x, kv.y * kv.y);
+                if (!AGG) *reinterpret_cast<float2*>(base + 2 * DK + pos) = load2(raw_q(s, h) + tt * DK + j);
+            }
+            if (!p.d_tma && lane < nheads) raw_d(s, lane)[tt] = gd[(head0 + lane) * T + t0 + tt];
+        }
+        mbar_arrive(&full_par[s]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full_raw[s], 1);
+            mbar_init(&full_par[s], NW * 32);
+            done_cnt[s] = 0;
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == 0)
+        for (int c = 0; c < min(NSTAGE, nchunks); ++c) issue(c);
+    if (nchunks > 0) convert(0);
+
+    // ------------------------------ lane state ------------------------------
+    const int rs = lane / M, cg = lane % M;
+    const int crow = warp * G::WR + rs * RT;      // first of my rows within the CTA
+    const int hl = crow / dv, i0 = crow - hl * dv;
+    const bool active = hl < nheads;
+    const long long bh = head0 + hl;
+    const long long S = static_cast<long long>(dv) * DK;
+    const float Ah = (active && nchunks > 0) ? p.A[bh % p.H] : 0.f;
+    const float Ip = p.I_prior;
+
+    float2 J[RT][CW / 2], E[RT][CW / 2];
+    {
+        // initial state of this part, in scaled form (W = 1 at the part start)
+        const float* src_J = nullptr;
+        const float* src_E = nullptr;
+        if (!AGG && part > 0) {
+            src_J = p.agg + (static_cast<long long>(part - 1) * p.BH + bh) * 2 * S;
+            src_E = src_J + S;
+        }
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 2; ++c2) {
+                float2 j2 = make_float2(0.f, 0.f), e2 = make_float2(0.f, 0.f);
+                const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
+                if (active && !AGG) {
+                    if (src_J) {
+                        j2 = *reinterpret_cast<const float2*>(src_J + off);
+                        e2 = *reinterpret_cast<const float2*>(src_E + off);
+                    } else if (part == 0 && (p.I0 || p.mu0)) {
+                        float2 i02 = make_float2(Ip, Ip);
+                        if (p.I0) i02 = *reinterpret_cast<const float2*>(p.I0 + bh * S + off);
+                        j2 = make_float2(i02.x - Ip, i02.y - Ip);
+                        if (p.mu0) {
+                            const float2 m2 = *reinterpret_cast<const float2*>(p.mu0 + bh * S + off);
+                            e2 = make_float2(i02.x * m2.x, i02.y * m2.y);
+                        }
+                    }
+                }
+                J[r][c2] = j2;
+                E[r][c2] = e2;
+            }
+        }
+    }
+
+    float W = 1.f;
+    int R = 0;
+    float* gout = p.out;
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c % NSTAGE;
+        if (c + 1 < nchunks) convert(c + 1);
+        if (!mbar_wait(&full_par[s], (c / NSTAGE) & 1, p.wait_ns)) ok = false;
+        const int t0 = tb + c * TC, tcn = min(TC, te - t0);
+        const TIn* rv = raw_v(s, hl) + i0;
+        const TIn* rb = raw_b(s, hl) + i0;
+        const TIn* rd = raw_d(s, hl);
+        const float* pbase = par(s, hl);
+        for (int tt = 0; tt < tcn; ++tt) {
+            const float* pt = pbase + tt * PF;
+            const float f = scale_step(Ah * to_f32<TIn>(rd[tt]) * LOG2E, W, R);
+            if (f != 1.f) {                          // exact power-of-two rescale
+                const float2 f22 = f2(f);
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int c2 = 0; c2 < CW / 2; ++c2) {
+                        J[r][c2] = __fmul2_rn(J[r][c2], f22);
+                        E[r][c2] = __fmul2_rn(E[r][c2], f22);
+                    }
+            }
+            float bet[RT], val[RT];
+            load4(rb + tt * dv, bet);
+            load4(rv + tt * dv, val);
+            float2 SB[RT], SBV[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+                const float sb = W * bet[r];
+                SB[r] = f2(sb);
+                SBV[r] = f2(sb * val[r]);
+            }
+            const float2 SP = f2(W * Ip * SIGMA), SG = f2(SIGMA);
+            float acc[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) acc[r] = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                // this lane's 8 columns of the half: float4 numbers (2*half+h4)*M + cg
+                float2 kf[4], kk[4], qv[4];
+#pragma unroll
+                for (int h4 = 0; h4 < 2; ++h4) {
+                    const int f4 = ((2 * half + h4) * M + cg) * 4;
+                    const float4 a = *reinterpret_cast<const float4*>(pt + f4);
+                    const float4 b = *reinterpret_cast<const float4*>(pt + DK + f4);
+                    kf[2 * h4] = make_float2(a.x, a.y);
+                    kf[2 * h4 + 1] = make_float2(a.z, a.w);
+                    kk[2 * h4] = make_float2(b.x, b.y);
+                    kk[2 * h4 + 1] = make_float2(b.z, b.w);
+                    if (!AGG) {
+                        const float4 q = *reinterpret_cast<const float4*>(pt + 2 * DK + f4);
+                        qv[2 * h4] = make_float2(q.x, q.y);
+                        qv[2 * h4 + 1] = make_float2(q.z, q.w);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < RT; ++r) {
+                    float2 den[4], num[4];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int c2 = half * 4 + c4;
+                        J[r][c2] = __ffma2_rn(SB[r], kk[c4], J[r][c2]);
+                        E[r][c2] = __ffma2_rn(SBV[r], kf[c4], E[r][c2]);
+                        if (!AGG) {
+                            den[c4] = __ffma2_rn(J[r][c2], SG, SP);
+                            num[c4] = __fmul2_rn(qv[c4], E[r][c2]);
+                        }
+                    }
+                    if (!AGG) {
+                        float2 a2 = make_float2(0.f, 0.f);
+                        // column-pair groups (0,1) and (2,3) of this half; the
+                        // first PAIRS of the row's 4 groups share reciprocals
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const int x = 2 * g, y = 2 * g + 1;
+                            if (half * 2 + g < PAIRS) {
+                                const float2 N = __ffma2_rn(num[x], den[y], __fmul2_rn(num[y], den[x]));
+                                const float2 Dn = __fmul2_rn(den[x], den[y]);
+                                a2 = __ffma2_rn(N, make_float2(rcp_approx(Dn.x), rcp_approx(Dn.y)), a2);
+                            } else {
+                                a2 = __ffma2_rn(num[x], make_float2(rcp_approx(den[x].x), rcp_approx(den[x].y)), a2);
+                                a2 = __ffma2_rn(num[y], make_float2(rcp_approx(den[y].x), rcp_approx(den[y].y)), a2);
+                            }
+                        }
+                        acc[r] += a2.x + a2.y;
+                    }
+                }
+            }
+            if (!AGG) {
+                float val_out[RowReduce<M>::NV];
+                int row_out[RowReduce<M>::NV];
+                bool st;
+                RowReduce<M>::run(acc, cg, val_out, row_out, st);
+                if (st && active) {
+                    float* o = gout + (bh * T + t0 + tt) * dv + i0;
+#pragma unroll
+                    for (int u = 0; u < RowReduce<M>::NV; ++u) __stcs(o + row_out[u], val_out[u] * SIGMA);
+                }
+            }
+        }
+        // the warp that finishes this chunk last refills the stage
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&done_cnt[s], 1) == NW - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            if (lane == 0) done_cnt[s] = 0;
+            if (c + NSTAGE < nchunks) issue(c + NSTAGE);
+        }
+    }
+    if (!ok) record_error(&g_diag_error, KDN_ERR_TIMEOUT);
+    if (!active) return;
+
+    if (AGG) {
+        float* dJ = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S;
+        float* dE = dJ + S;
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 2; ++c2) {
+                const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
+                *reinterpret_cast<float2*>(dJ + off) = J[r][c2];
+                *reinterpret_cast<float2*>(dE + off) = E[r][c2];
+            }
+        if (i0 == 0 && cg == 0) p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, R};
+    } else if (p.final_state && part == static_cast<int>(gridDim.y) - 1) {
+        // mu_T = eta / (I_prior + J) = Ew / (Jw + W I_prior);  I_T = Jw / W + I_prior
+        float* fm = p.final_state + bh * S;
+        float* fi = p.final_state + (p.BH + bh) * S;
+        const float wI = W * Ip;
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 2; ++c2) {
+                const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
+                const float2 j2 = J[r][c2], e2 = E[r][c2];
+                *reinterpret_cast<float2*>(fm + off) =
+                    make_float2(e2.x / (j2.x + wI), e2.y / (j2.y + wI));
+                *reinterpret_cast<float2*>(fi + off) = make_float2(j2.x / W + Ip, j2.y / W + Ip);
+            }
+    }
+}
+
+// Carry pass: chains the part end states.  For part p (p = 0..P-2) the end
+// state from the true start state X is X * prod(alpha) + Delta with
+// prod(alpha) = 2^-R / W_end and Delta = (Jw, Ew) / W_end of the aggregate
+// pass.  Overwrites agg[p] with the start state of part p+1.
+__global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* I0,
+                                  const float* mu0, float I_prior, long long BH, long long S,
+                                  int P) {
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= BH * S) return;
+    const long long bh = idx / S, e = idx - bh * S;
+    float Jv = 0.f, Ev = 0.f;
+    if (I0 || mu0) {
+        const float i0 = I0 ? I0[idx] : I_prior;
+        Jv = i0 - I_prior;
+        Ev = mu0 ? i0 * mu0[idx] : 0.f;
+    }
+    for (int pp = 0; pp + 1 < P; ++pp) {
+        const AggScale a = scl[static_cast<long long>(pp) * BH + bh];
+        float* dJ = agg + (static_cast<long long>(pp) * BH + bh) * 2 * S + e;
+        float* dE = dJ + S;
+        Jv = (ldexpf(Jv, -a.R) + *dJ) / a.W;
+        Ev = (ldexpf(Ev, -a.R) + *dE) / a.W;
+        *dJ = Jv;
+        *dE = Ev;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+struct Cache {
+    bool init[64] = {};
+    int occ[64] = {};
+};
+
+template <int DK, typename TIn, bool AGG>
+cudaError_t prepare(int dev, int smem, int* occ) {
+    static Cache cache;
+    static int smem_set[64] = {};
+    auto kern = diag_scan_kernel<DK, TIn, AGG>;
+    cudaError_t e = cudaSuccess;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (smem > smem_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set[dev] = smem;
+        cache.init[dev] = false;
+    }
+    if (!cache.init[dev]) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Geo<DK>::NTHREADS, smem);
+        if (e != cudaSuccess) return e;
+        cache.occ[dev] = n > 0 ? n : 1;
+        cache.init[dev] = true;
+    }
+    *occ = cache.occ[dev];
+    return e;
+}
+
+// Launch plan of one call: chunk length, token parts, scratch bytes.
+struct Plan {
+    int TC = 16;
+    int smem = 0;
+    int P = 1;
+    int part_len = 1;
+    long long ctas = 0;
+    size_t scratch = 0;
+    int kernels = 0;
+};
+
+template <int DK, typename TIn>
+kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
+    constexpr int ES = sizeof(TIn);
+    const int dv = a.dv;
+    const int hpc = ROWS_PER_CTA / dv;
+    const long long BH = static_cast<long long>(a.B) * a.H;
+    pl->ctas = (BH + hpc - 1) / hpc;
+    if (pl->ctas > 0x7fffffffLL) return KDN_ERR_INVALID_ARG;
+    // chunk length: as long as the three stages fit the budget
+    const int budget = (DK >= 128) ? 200 * 1024 : 100 * 1024;
+    int TC = 16;
+    while (TC > 1 && smem_bytes(DK, dv, ES, TC) > budget) TC >>= 1;
+    pl->TC = TC;
+    pl->smem = smem_bytes(DK, dv, ES, TC);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    int occ = 1, occ_agg = 1;
+    e = prepare<DK, TIn, false>(dev, pl->smem, &occ);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = prepare<DK, TIn, true>(dev, pl->smem, &occ_agg);
+    if (e != cudaSuccess) return from_cuda(e);
+    // token split: enough parts to give every CTA slot work
+    const long long slots = static_cast<long long>(sm_count()) * occ;
+    int P = 1;
+    if (pl->ctas * 2 <= slots && a.T >= 8 * TC) {
+        const long long want = slots / pl->ctas;
+        const long long maxp = a.T / (4 * TC);
+        P = static_cast<int>(want < maxp ? want : maxp);
+        if (P < 1) P = 1;
+    }
+    int part_len = a.T > 0 ? a.T : 1;
+    if (P > 1) {
+        part_len = ((a.T + P - 1) / P + TC - 1) / TC * TC;
+        P = (a.T + part_len - 1) / part_len;
+        if (P <= 1) {
+            P = 1;
+            part_len = a.T;
+        }
+    }
+    pl->P = P;
+    pl->part_len = part_len;
+    const long long S = static_cast<long long>(dv) * DK;
+    pl->scratch = P > 1 ? static_cast<size_t>(P - 1) * BH * (2 * S * sizeof(float) + sizeof(AggScale)) : 0;
+    pl->kernels = P > 1 ? 3 : 1;
+    return KDN_OK;
+}
+
+template <int DK, typename TIn>
+kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
+    constexpr int ES = sizeof(TIn);
+    Plan pl;
+    kdn_status ps = plan_dk<DK, TIn>(a, &pl);
+    if (ps != KDN_OK) return ps;
+    const int dv = a.dv, TC = pl.TC, smem = pl.smem, P = pl.P;
+    const long long BH = static_cast<long long>(a.B) * a.H;
+    const long long ctas = pl.ctas;
+
+    Params prm{};
+    prm.q = a.q; prm.k = a.k; prm.v = a.v; prm.beta = a.beta; prm.d = a.d;
+    prm.A = a.A; prm.I_prior = a.I_prior; prm.I0 = a.I0; prm.mu0 = a.mu0;
+    prm.out = a.out; prm.final_state = a.final_state;
+    prm.BH = BH; prm.H = a.H; prm.T = a.T; prm.dv = dv;
+    prm.part_len = pl.part_len; prm.TC = TC; prm.wait_ns = wait_ns;
+    // d chunks can be bulk-copied when every chunk starts and ends on 16 bytes
+    prm.d_tma = (static_cast<long long>(a.T) * ES % 16 == 0) && (TC * ES % 16 == 0) &&
+                ((reinterpret_cast<uintptr_t>(a.d) & 15u) == 0);
+
+    void* scratch = nullptr;
+    cudaError_t e = cudaSuccess;
+    const long long S = static_cast<long long>(dv) * DK;
+    if (P > 1) {
+        const size_t state_bytes = static_cast<size_t>(P - 1) * BH * 2 * S * sizeof(float);
+        e = cudaMallocAsync(&scratch, pl.scratch, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        prm.agg = static_cast<float*>(scratch);
+        prm.agg_scale = reinterpret_cast<AggScale*>(static_cast<char*>(scratch) + state_bytes);
+        diag_scan_kernel<DK, TIn, true>
+            <<<dim3(static_cast<unsigned>(ctas), P - 1), Geo<DK>::NTHREADS, smem, st>>>(prm);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) {
+            const long long n = BH * S;
+            diag_carry_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+                prm.agg, prm.agg_scale, a.I0, a.mu0, a.I_prior, BH, S, P);
+            e = cudaGetLastError();
+        }
+    }
+    if (e == cudaSuccess) {
+        diag_scan_kernel<DK, TIn, false>
+            <<<dim3(static_cast<unsigned>(ctas), P), Geo<DK>::NTHREADS, smem, st>>>(prm);
+        e = cudaGetLastError();
+    }
+    if (scratch) {
+        const cudaError_t ef = cudaFreeAsync(scratch, st);
+        if (e == cudaSuccess) e = ef;
+    }
+    return from_cuda(e);
+}
+
+template <typename TIn>
+kdn_status plan_any(const DiagArgs& a, Plan* pl) {
+    switch (a.dk) {
+        case 16: return plan_dk<16, TIn>(a, pl);
+        case 32: return plan_dk<32, TIn>(a, pl);
+        case 64: return plan_dk<64, TIn>(a, pl);
+        case 128: return plan_dk<128, TIn>(a, pl);
+        default: return KDN_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename TIn>
+kdn_status launch_any(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
+    switch (a.dk) {
+        case 16: return launch_dk<16, TIn>(a, st, wait_ns);
+        case 32: return launch_dk<32, TIn>(a, st, wait_ns);
+        case 64: return launch_dk<64, TIn>(a, st, wait_ns);
+        case 128: return launch_dk<128, TIn>(a, st, wait_ns);
+        default: return KDN_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+}  // namespace diag
+}  // namespace kdn

@@ -1,0 +1,53 @@
+// kdn_internal.h -- declarations shared by the library's translation units
+// (not part of the public ABI).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "kdn.h"
+
+namespace kdn {
+
+// Arguments of one diagonal-scan call after host-side validation.
+struct DiagArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* beta;
+    const void* d;
+    const float* A;
+    float I_prior;
+    const float* I0;
+    const float* mu0;
+    float* out;
+    float* final_state;
+    int B, H, T, dk, dv;
+    kdn_dtype dtype;
+};
+
+// Per-dtype launchers (diag_bf16.cu / diag_f32.cu).
+kdn_status diag_launch_bf16(const DiagArgs& a, cudaStream_t stream, long long wait_ns);
+kdn_status diag_launch_f32(const DiagArgs& a, cudaStream_t stream, long long wait_ns);
+
+// Launch plans (no launch): token parts, kernels launched, scratch bytes.
+kdn_status diag_plan_bf16(const DiagArgs& a, int* parts, int* kernels, size_t* scratch);
+kdn_status diag_plan_f32(const DiagArgs& a, int* parts, int* kernels, size_t* scratch);
+void mobius_plan(long long N, long long T, int* kernels, size_t* scratch);
+
+// Moebius scan launcher (mobius_scan.cu).
+kdn_status mobius_launch(const float* a, const float* b, const float* c, const float* d,
+                         const float* lambda0, float* out, long long N, long long T,
+                         cudaStream_t stream, long long wait_ns, long long stall_tile);
+
+// Each translation unit that launches kernels with bounded waits owns one
+// device error word; these read-and-clear it on the current device.
+cudaError_t diag_take_device_error(int* status);
+cudaError_t mobius_take_device_error(int* status);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Maps a CUDA error to a status (KDN_OK on cudaSuccess, KDN_ERR_ALLOC on
+// memory allocation errors, KDN_ERR_CUDA otherwise).
+kdn_status from_cuda(cudaError_t e);
+
+}  // namespace kdn

@@ -1,0 +1,315 @@
+// mobius_scan.cu -- parallel prefix scan of the Moebius precision recursion
+//     lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t)
+// ("Kalman Linear Attention (KLA)", Metodologia 2, "Parallelizzazione tramite
+// Trasformazioni di Moebius": the maps compose associatively, so the
+// recursion admits an O(T)-work, O(log T)-depth prefix scan).
+//
+// Each step is the 2x2 matrix M_t = [[a_t, b_t], [c_t, d_t]]; applying M_1
+// then M_2 is the product M_2 M_1, and lambda_t = P_t(lambda_0) with
+// P_t = M_t ... M_1.  Because lambda only depends on the ratio of the
+// homogeneous coordinates, every composed matrix is rescaled by an exact
+// power of two (its largest entry into [1, 2)), which removes overflow and
+// underflow without rounding.
+//
+// Kernel layout (one CTA = one tile of 2048 consecutive steps of a sequence):
+//   1. each thread loads 8 consecutive steps (two float4 per coefficient
+//      array) and composes them sequentially;
+//   2. a warp-shuffle inclusive scan composes the 32 per-thread matrices;
+//   3. warp totals meet in shared memory for the block-level carry;
+//   4. tiles of the same sequence are chained with a decoupled look-back:
+//      a tile publishes its aggregate matrix as soon as it is known, then
+//      walks back over predecessors (composing aggregates) until it finds a
+//      published inclusive value lambda, and publishes its own inclusive
+//      lambda.  Tiles are numbered by an atomic ticket so that every tile's
+//      predecessors were scheduled before it; every wait on a flag is bounded
+//      by GPU time and records KDN_ERR_TIMEOUT instead of hanging;
+//   5. each thread evaluates its 8 outputs sequentially from the lambda at
+//      its first step (the exclusive prefix applied to the tile's carry).
+// Memory traffic is the algorithmic minimum (16 B in, 4 B out per step); the
+// kernel is bound by HBM bandwidth.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kdn_device.cuh"
+#include "kdn_internal.h"
+
+namespace kdn {
+namespace {
+
+constexpr int MB_THREADS = 256;
+constexpr int MB_VPT = 8;                       // steps per thread
+constexpr int MB_TILE = MB_THREADS * MB_VPT;    // steps per CTA
+constexpr int MB_WARPS = MB_THREADS / 32;
+
+constexpr unsigned int FLAG_AGG = 1u;           // aggregate matrix published
+constexpr unsigned int FLAG_PRE = 2u;           // inclusive lambda published
+
+__device__ int g_mobius_error = 0;
+
+struct Mat {
+    float a, b, c, d;  // [[a, b], [c, d]]
+};
+
+__device__ __forceinline__ Mat identity() { return {1.f, 0.f, 0.f, 1.f}; }
+
+// L * R (apply R first, then L)
+__device__ __forceinline__ Mat mul(const Mat& L, const Mat& R) {
+    Mat o;
+    o.a = fmaf(L.a, R.a, L.b * R.c);
+    o.b = fmaf(L.a, R.b, L.b * R.d);
+    o.c = fmaf(L.c, R.a, L.d * R.c);
+    o.d = fmaf(L.c, R.b, L.d * R.d);
+    return o;
+}
+
+// Scale by an exact power of two so that the largest |entry| lies in [1, 2).
+// Zero, denormal-only or non-finite matrices are left alone.
+__device__ __forceinline__ Mat normalize(const Mat& m) {
+    const float mx = fmaxf(fmaxf(fabsf(m.a), fabsf(m.b)), fmaxf(fabsf(m.c), fabsf(m.d)));
+    const int e = exponent_of(mx);
+    if (e <= -127 || e >= 128 || e == 0) return m;
+    const float s = pow2i(e > 126 ? -126 : -e);
+    return {m.a * s, m.b * s, m.c * s, m.d * s};
+}
+
+__device__ __forceinline__ float apply(const Mat& m, float lam) {
+    return fmaf(m.a, lam, m.b) / fmaf(m.c, lam, m.d);
+}
+
+__device__ __forceinline__ Mat shfl_up(const Mat& m, int off) {
+    return {__shfl_up_sync(0xffffffffu, m.a, off), __shfl_up_sync(0xffffffffu, m.b, off),
+            __shfl_up_sync(0xffffffffu, m.c, off), __shfl_up_sync(0xffffffffu, m.d, off)};
+}
+
+struct LookbackScratch {
+    unsigned long long* ticket;   // tile ticket counter (zeroed per launch)
+    unsigned int* flags;          // [num_tiles], zeroed per launch
+    float4* agg;                  // [num_tiles] aggregate matrix (a, b, c, d)
+    float* pre;                   // [num_tiles] inclusive lambda at the tile end
+};
+
+// Bounded wait for a tile flag; returns 0 on timeout.
+__device__ __forceinline__ unsigned int wait_flag(const unsigned int* f, long long limit_ns) {
+    unsigned int v = ld_acquire_u32(f);
+    if (v) return v;
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned int sleep = 32;
+    while (true) {
+        __nanosleep(sleep);
+        if (sleep < 1024) sleep <<= 1;
+        v = ld_acquire_u32(f);
+        if (v) return v;
+        if (static_cast<long long>(globaltimer_ns() - t0) > limit_ns) return 0;
+    }
+}
+
+template <bool VEC, bool LOOKBACK>
+__global__ void __launch_bounds__(MB_THREADS)
+mobius_scan_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                   const float* __restrict__ C, const float* __restrict__ D,
+                   const float* __restrict__ lambda0, float* __restrict__ out,
+                   long long T, long long tiles_per_seq, LookbackScratch sc,
+                   long long wait_ns, long long stall_tile) {
+    __shared__ long long s_tile;
+    __shared__ Mat s_warp[MB_WARPS];
+    __shared__ float s_lam;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    long long tile;
+    if (LOOKBACK) {
+        if (tid == 0) s_tile = static_cast<long long>(atomicAdd(sc.ticket, 1ull));
+        __syncthreads();
+        tile = s_tile;
+    } else {
+        tile = blockIdx.x;
+    }
+    const long long seq = tile / tiles_per_seq;
+    const long long part = tile - seq * tiles_per_seq;
+    const long long t_first = part * MB_TILE + static_cast<long long>(tid) * MB_VPT;
+    const long long base = seq * T;
+
+    // ---- 1. load 8 steps and compose them in order ----------------------
+    float ca[MB_VPT], cb[MB_VPT], cc[MB_VPT], cd[MB_VPT];
+    if (VEC && t_first + MB_VPT <= T) {
+        const float4* pa = reinterpret_cast<const float4*>(A + base + t_first);
+        const float4* pb = reinterpret_cast<const float4*>(B + base + t_first);
+        const float4* pc = reinterpret_cast<const float4*>(C + base + t_first);
+        const float4* pd = reinterpret_cast<const float4*>(D + base + t_first);
+#pragma unroll
+        for (int h = 0; h < MB_VPT / 4; ++h) {
+            const float4 x = __ldcs(pa + h), y = __ldcs(pb + h), z = __ldcs(pc + h),
+                         w = __ldcs(pd + h);
+            ca[4 * h + 0] = x.x; ca[4 * h + 1] = x.y; ca[4 * h + 2] = x.z; ca[4 * h + 3] = x.w;
+            cb[4 * h + 0] = y.x; cb[4 * h + 1] = y.y; cb[4 * h + 2] = y.z; cb[4 * h + 3] = y.w;
+            cc[4 * h + 0] = z.x; cc[4 * h + 1] = z.y; cc[4 * h + 2] = z.z; cc[4 * h + 3] = z.w;
+            cd[4 * h + 0] = w.x; cd[4 * h + 1] = w.y; cd[4 * h + 2] = w.z; cd[4 * h + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < MB_VPT; ++s) {
+            const long long t = t_first + s;
+            const bool in = t < T;
+            ca[s] = in ? __ldcs(A + base + t) : 1.f;
+            cb[s] = in ? __ldcs(B + base + t) : 0.f;
+            cc[s] = in ? __ldcs(C + base + t) : 0.f;
+            cd[s] = in ? __ldcs(D + base + t) : 1.f;
+        }
+    }
+    Mat P = {ca[0], cb[0], cc[0], cd[0]};
+#pragma unroll
+    for (int s = 1; s < MB_VPT; ++s) P = normalize(mul(Mat{ca[s], cb[s], cc[s], cd[s]}, P));
+    P = normalize(P);
+
+    // ---- 2. warp inclusive scan (later steps on the left) ---------------
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const Mat Q = shfl_up(P, off);
+        if (lane >= off) P = normalize(mul(P, Q));
+    }
+    Mat lane_excl = shfl_up(P, 1);
+    if (lane == 0) lane_excl = identity();
+    if (lane == 31) s_warp[warp] = P;
+    __syncthreads();
+
+    // ---- 3. block carry: exclusive prefix of the earlier warps -----------
+    Mat warp_excl = identity();
+    for (int w = 0; w < warp; ++w) warp_excl = normalize(mul(s_warp[w], warp_excl));
+    const Mat thread_excl = normalize(mul(lane_excl, warp_excl));
+
+    // ---- 4. look-back across the tiles of this sequence ------------------
+    if (tid == 0) {
+        Mat agg = identity();
+        for (int w = 0; w < MB_WARPS; ++w) agg = normalize(mul(s_warp[w], agg));
+        const bool stalled = LOOKBACK && tile == stall_tile;   // fault injection
+        float lam;
+        if (!LOOKBACK || part == 0) {
+            lam = lambda0[seq];
+        } else {
+            if (!stalled) {
+                sc.agg[tile] = make_float4(agg.a, agg.b, agg.c, agg.d);
+                __threadfence();
+                st_release_u32(sc.flags + tile, FLAG_AGG);
+            }
+            Mat acc = identity();
+            long long j = tile - 1;
+            while (true) {
+                const unsigned int f = wait_flag(sc.flags + j, wait_ns);
+                if (f == 0) {                      // predecessor never published
+                    record_error(&g_mobius_error, KDN_ERR_TIMEOUT);
+                    lam = apply(acc, lambda0[seq]);
+                    break;
+                }
+                if (f == FLAG_PRE) {
+                    lam = apply(acc, __ldcg(sc.pre + j));
+                    break;
+                }
+                const float4 g = __ldcg(sc.agg + j);
+                acc = normalize(mul(acc, Mat{g.x, g.y, g.z, g.w}));
+                --j;
+            }
+        }
+        if (LOOKBACK && !stalled) {
+            sc.pre[tile] = apply(agg, lam);
+            __threadfence();
+            st_release_u32(sc.flags + tile, FLAG_PRE);
+        }
+        s_lam = lam;
+    }
+    __syncthreads();
+
+    // ---- 5. outputs: sequential recursion from this thread's start ------
+    float lam = apply(thread_excl, s_lam);
+    float res[MB_VPT];
+#pragma unroll
+    for (int s = 0; s < MB_VPT; ++s) {
+        lam = fmaf(ca[s], lam, cb[s]) / fmaf(cc[s], lam, cd[s]);
+        res[s] = lam;
+    }
+    if (VEC && t_first + MB_VPT <= T) {
+        float4* po = reinterpret_cast<float4*>(out + base + t_first);
+#pragma unroll
+        for (int h = 0; h < MB_VPT / 4; ++h)
+            __stcs(po + h, make_float4(res[4 * h], res[4 * h + 1], res[4 * h + 2], res[4 * h + 3]));
+    } else {
+#pragma unroll
+        for (int s = 0; s < MB_VPT; ++s)
+            if (t_first + s < T) __stcs(out + base + t_first + s, res[s]);
+    }
+}
+
+template <bool VEC, bool LB>
+cudaError_t launch(const float* a, const float* b, const float* c, const float* d,
+                   const float* lam0, float* out, long long T, long long tps, long long tiles,
+                   LookbackScratch sc, cudaStream_t st, long long wait_ns, long long stall) {
+    mobius_scan_kernel<VEC, LB><<<static_cast<unsigned>(tiles), MB_THREADS, 0, st>>>(
+        a, b, c, d, lam0, out, T, tps, sc, wait_ns, stall);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+void mobius_plan(long long N, long long T, int* kernels, size_t* scratch) {
+    const long long tps = (T + MB_TILE - 1) / MB_TILE;
+    const long long tiles = N * tps;
+    *kernels = (N > 0 && T > 0) ? 1 : 0;
+    *scratch = 0;
+    if (tps > 1) {
+        const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
+        *scratch = zero_bytes + 16 * static_cast<size_t>(tiles) + 4 * tiles;
+    }
+}
+
+kdn_status mobius_launch(const float* a, const float* b, const float* c, const float* d,
+                         const float* lambda0, float* out, long long N, long long T,
+                         cudaStream_t stream, long long wait_ns, long long stall_tile) {
+    if (N == 0 || T == 0) return KDN_OK;
+    const long long tps = (T + MB_TILE - 1) / MB_TILE;
+    const long long tiles = N * tps;
+    if (tiles > 0x7fffffffLL) return KDN_ERR_INVALID_ARG;
+    auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool vec = (T % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(c) &&
+                     aligned16(d) && aligned16(out);
+    LookbackScratch sc{nullptr, nullptr, nullptr, nullptr};
+    void* scratch = nullptr;
+    cudaError_t e;
+    if (tps > 1) {
+        // [ticket u64][flags u32 x tiles] (zeroed) | [agg float4 x tiles][pre f32 x tiles]
+        const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
+        const size_t bytes = zero_bytes + 16 * static_cast<size_t>(tiles) + 4 * tiles;
+        e = cudaMallocAsync(&scratch, bytes, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        char* p = static_cast<char*>(scratch);
+        sc.ticket = reinterpret_cast<unsigned long long*>(p);
+        sc.flags = reinterpret_cast<unsigned int*>(p + 8);
+        sc.agg = reinterpret_cast<float4*>(p + zero_bytes);
+        sc.pre = reinterpret_cast<float*>(p + zero_bytes + 16 * tiles);
+        e = cudaMemsetAsync(scratch, 0, zero_bytes, stream);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(scratch, stream);
+            return from_cuda(e);
+        }
+        e = vec ? launch<true, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns,
+                                     stall_tile)
+                : launch<false, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
+                                      wait_ns, stall_tile);
+        const cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    } else {
+        e = vec ? launch<true, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
+                                      wait_ns, -1)
+                : launch<false, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
+                                       wait_ns, -1);
+    }
+    return from_cuda(e);
+}
+
+cudaError_t mobius_take_device_error(int* status) {
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_mobius_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (v != 0) e = cudaMemcpyToSymbol(g_mobius_error, &zero, sizeof(int));
+    *status = v;
+    return e;
+}
+
+}  // namespace kdn

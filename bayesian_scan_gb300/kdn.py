@@ -1,0 +1,222 @@
+"""Thin ctypes binding of the C ABI in ``include/kdn.h``.
+
+Argument marshalling only: every step of both scans runs in the CUDA
+kernels of ``_build/libkdn.so``.  PyTorch provides device memory and the
+current stream.  There is no CPU fallback: if the library is missing the
+import of this module raises.
+
+Functions mirror the C names:
+
+* :func:`diag_scan_fwd`  -> ``kdn_diag_scan_fwd``
+* :func:`mobius_scan`    -> ``kdn_mobius_scan``
+* :func:`diag_scan_plan`, :func:`mobius_scan_plan` -> the ``*_plan`` queries
+* :func:`get_device_error`, :func:`set_wait_limit_ns`,
+  :func:`debug_stall_mobius_tile`, :func:`status_string`, :func:`version`
+
+When the tensors passed to :func:`diag_scan_fwd` / :func:`mobius_scan` live in
+host memory, the call stages them to the current device on the current stream
+(pinned memory makes the copies asynchronous), runs the kernels there and
+copies the results back; it returns host tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+KDN_OK, KDN_ERR_INVALID_ARG, KDN_ERR_UNSUPPORTED = 0, -1, -2
+KDN_ERR_CUDA, KDN_ERR_TIMEOUT, KDN_ERR_ALLOC = -3, -4, -5
+KDN_F32, KDN_BF16 = 0, 1
+
+LIB_PATH = _build.LIB
+
+
+class KdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkdn is not built ({LIB_PATH}); run bayesian_scan_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, fp, i, ll = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    lib.kdn_diag_scan_fwd.restype = i
+    lib.kdn_diag_scan_fwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
+                                      i, i, i, i, i, i, vp]
+    lib.kdn_mobius_scan.restype = i
+    lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_status_string.restype = ctypes.c_char_p
+    lib.kdn_status_string.argtypes = [i]
+    lib.kdn_get_device_error.restype = i
+    lib.kdn_get_device_error.argtypes = [vp]
+    lib.kdn_set_wait_limit_ns.restype = None
+    lib.kdn_set_wait_limit_ns.argtypes = [ll]
+    lib.kdn_debug_stall_mobius_tile.restype = None
+    lib.kdn_debug_stall_mobius_tile.argtypes = [ll]
+    ip, llp = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)
+    lib.kdn_diag_scan_plan.restype = i
+    lib.kdn_diag_scan_plan.argtypes = [i, i, i, i, i, i, ip, ip, llp]
+    lib.kdn_mobius_scan_plan.restype = i
+    lib.kdn_mobius_scan_plan.argtypes = [ll, ll, ip, llp]
+    lib.kdn_version.restype = ctypes.c_char_p
+    lib.kdn_version.argtypes = []
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.kdn_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib.kdn_version().decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, dtype=None, shape=None):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
+                  final_state=True, stream=None):
+    """Diagonal metaplastic scan with readout (see ``kdn_diag_scan_fwd``).
+
+    q, k [B,H,T,dk]; v, beta [B,H,T,dv]; d [B,H,T] (bf16 or fp32, all the same);
+    A [H] fp32; I0, mu0 [B,H,dv,dk] fp32 or None.  ``final_state`` may be
+    True (allocate), False/None (skip) or a [2,B,H,dv,dk] fp32 tensor.
+    Returns (out [B,H,T,dv] fp32, final_state or None).
+    """
+    if not q.is_cuda:
+        return _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, final_state)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    _check(q, "q", dt)
+    _check(k, "k", dt, (B, H, T, dk))
+    _check(v, "v", dt, (B, H, T, dv))
+    _check(beta, "beta", dt, (B, H, T, dv))
+    _check(d, "d", dt, (B, H, T))
+    _check(A, "A", torch.float32, (H,))
+    for name, t in (("I0", I0), ("mu0", mu0)):
+        if t is not None:
+            _check(t, name, torch.float32, (B, H, dv, dk))
+    if out is None:
+        out = torch.empty(B, H, T, dv, device=q.device, dtype=torch.float32)
+    _check(out, "out", torch.float32, (B, H, T, dv))
+    if final_state is True:
+        final_state = torch.empty(2, B, H, dv, dk, device=q.device, dtype=torch.float32)
+    elif final_state is False:
+        final_state = None
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, (2, B, H, dv, dk))
+    st = lib.kdn_diag_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                               float(I_prior), _ptr(I0), _ptr(mu0), _ptr(out), _ptr(final_state),
+                               B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
+                               _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_scan_fwd")
+    return out, final_state
+
+
+def mobius_scan(a, b, c, d, lambda0, out=None, stream=None):
+    """Moebius precision recursion (see ``kdn_mobius_scan``): a,b,c,d [N,T]
+    fp32, lambda0 [N] fp32 -> lambda_1..lambda_T [N,T] fp32."""
+    if not a.is_cuda:
+        return _mobius_host(a, b, c, d, lambda0)
+    N, T = a.shape
+    for name, t in (("a", a), ("b", b), ("c", c), ("d", d)):
+        _check(t, name, torch.float32, (N, T))
+    _check(lambda0, "lambda0", torch.float32, (N,))
+    if out is None:
+        out = torch.empty(N, T, device=a.device, dtype=torch.float32)
+    _check(out, "out", torch.float32, (N, T))
+    st = lib.kdn_mobius_scan(_ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(lambda0), _ptr(out),
+                             N, T, _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_mobius_scan")
+    return out
+
+
+def diag_scan_plan(B, H, T, dk, dv, dtype=torch.bfloat16) -> dict:
+    """Launch plan of a diagonal-scan call: token parts, kernels, scratch bytes."""
+    p, k, sb = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+    st = lib.kdn_diag_scan_plan(B, H, T, dk, dv, KDN_BF16 if dtype == torch.bfloat16 else KDN_F32,
+                                ctypes.byref(p), ctypes.byref(k), ctypes.byref(sb))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_scan_plan")
+    return dict(parts=p.value, kernels=k.value, scratch_bytes=sb.value)
+
+
+def mobius_scan_plan(N, T) -> dict:
+    """Launch plan of a Moebius-scan call: kernels and scratch bytes."""
+    k, sb = ctypes.c_int(), ctypes.c_longlong()
+    st = lib.kdn_mobius_scan_plan(N, T, ctypes.byref(k), ctypes.byref(sb))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_mobius_scan_plan")
+    return dict(kernels=k.value, scratch_bytes=sb.value)
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    return int(lib.kdn_get_device_error(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib.kdn_set_wait_limit_ns(int(ns))
+
+
+def debug_stall_mobius_tile(tile: int) -> None:
+    lib.kdn_debug_stall_mobius_tile(int(tile))
+
+
+# ---------------------------------------------------------------------------
+# host-buffer calls: stage to the device, run the kernels, copy back
+
+def _to_dev(t, dev):
+    return None if t is None else t.to(dev, non_blocking=True)
+
+
+def _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, final_state):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    xs = [_to_dev(t, dev) for t in (q, k, v, beta, d, A, I0, mu0)]
+    o, fs = diag_scan_fwd(*xs[:6], I_prior=I_prior, I0=xs[6], mu0=xs[7],
+                          final_state=bool(final_state is not None and final_state is not False))
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    o_h.copy_(o, non_blocking=True)
+    fs_h = None
+    if fs is not None:
+        fs_h = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
+        fs_h.copy_(fs, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return o_h, fs_h
+
+
+def _mobius_host(a, b, c, d, lambda0):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = mobius_scan(*[_to_dev(t, dev) for t in (a, b, c, d, lambda0)])
+    o_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    o_h.copy_(out, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return o_h

@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Throughput of the uncertainty-tracked linear-attention scan hot path.
+
+One step = one pass of the whole path over one batch of synthetic input: the
+diagonal metaplastic scan with readout (kdn_diag_scan_fwd) followed by the
+Moebius precision scan (kdn_mobius_scan) of the same workload, both through
+the C-ABI binding, inputs resident in HBM.  The default workload is the
+750M-shaped layer (B=8, H=16, T=4096, d_k=d_v=128, bf16 inputs, fp32 state,
+one lambda sequence per head).
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch
+of the same shape on its own GPU (heads are independent: no data-path
+collective; weak scaling); the timing is the max over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
+Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
+10 FLOP per state element per token (see the design doc for the count), peak =
+SMs x 128 FP32 lanes x 2 FLOP x max SM clock.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scan tokens/s (B·H·T per s) and % of binding HBM/FP32 roofline, fwd"
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (GB300)
+SM_MAX_MHZ_FALLBACK = 2070.0     # maximum SM clock of GB300
+HBM_GBS_FALLBACK = 6800.0
+DIAG_FLOP_PER_ELEMENT_TOKEN = 10
+MOBIUS_BYTES_PER_STEP = 20
+# dram__bytes_read.sum + dram__bytes_write.sum of one full-pass diagonal-scan
+# launch on the default workload, from the ncu capture summarised in
+# profiles/; None until a capture of the current kernel exists.
+DIAG_TRAFFIC_BYTES = None
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer750m")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.cmd = ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", "100"]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[device_index]
+        return str(device_index)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (barrier and max-over-ranks only; no data collective)
+
+class Dist:
+    def __init__(self, use_gpu: bool):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if use_gpu else "gloo"
+            if use_gpu:
+                import torch
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle arm (baseline leg and --impl reference)
+
+def oracle_sample(w, inputs, n_heads: int, t_tokens: int):
+    """Runs the fp64 oracle on the first n_heads heads (all rows) over the
+    first t_tokens tokens, plus the Moebius scan of those heads' sequences
+    (or of the same number of steps of the standalone sequences).
+    Returns (seconds, token-heads processed, threads used)."""
+    import oracle
+    B, H = w.B, w.H
+    heads = [(bh // H, bh % H) for bh in range(n_heads)]
+    sl = lambda x: x.reshape(B * H, *x.shape[2:])[:n_heads, :t_tokens].unsqueeze(0)
+    q, k, v, beta, d = (sl(inputs[n]) for n in ("q", "k", "v", "beta", "d"))
+    A = inputs["A"][[h for _, h in heads]]
+    # heads of the sample become the H axis of a B=1 batch, each with its own A
+    steps = n_heads * t_tokens
+    mN = min(w.mobius_N, max(1, steps // w.mobius_T)) if not w.mobius_fused else n_heads
+    mT = w.mobius_T if not w.mobius_fused else t_tokens
+    ma, mb, mc, md = (inputs[n][:mN, :mT] for n in ("ma", "mb", "mc", "md"))
+    lam0 = inputs["lam0"][:mN]
+    oracle.load()
+    t0 = time.perf_counter()
+    oracle.diag_scan(q, k, v, beta, d, A, inputs["I_prior"])
+    oracle.mobius_scan(ma, mb, mc, md, lam0)
+    dt = time.perf_counter() - t0
+    return dt, n_heads * t_tokens, min(oracle.max_threads(), n_heads)
+
+
+def calibrate_oracle(w, inputs, budget_s: float):
+    """Pick (n_heads, t_tokens) so one oracle sample takes about budget_s on
+    this host: whole sequences of as many heads as fit (a multiple of the
+    thread count), or a prefix of the tokens when even one round is too long."""
+    import oracle
+    threads = oracle.max_threads()
+    t_cal = min(w.T, 256)
+    dt, _, _ = oracle_sample(w, inputs, 1, t_cal)
+    per_token = dt / t_cal                       # one head, one thread
+    affordable = budget_s * threads / max(per_token, 1e-12)   # token-heads
+    total_heads = w.B * w.H
+    if affordable >= threads * w.T:
+        n_heads = int(affordable // w.T) // threads * threads
+        return max(1, min(total_heads, n_heads)), w.T
+    n_heads = min(total_heads, threads)
+    return n_heads, max(16, min(w.T, int(affordable // n_heads)))
+
+
+def run_reference(args, w, dist):
+    """The reference arm: the fp64 CPU oracle as it stands, on host cores."""
+    from bayesian_scan_gb300 import workloads
+    if dist.rank != 0:
+        return 0
+    inputs = workloads.make(w)
+    per_step_budget = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    n_heads, t_tokens = calibrate_oracle(w, inputs, per_step_budget)
+    for _ in range(args.warmup):
+        oracle_sample(w, inputs, n_heads, t_tokens)
+    tot_t, tot_units, cores = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, units, cores = oracle_sample(w, inputs, n_heads, t_tokens)
+        tot_t += dt
+        tot_units += units
+    value = tot_units / tot_t
+    sample = (f"per step: {n_heads} heads x {t_tokens} tokens of the {w.name} workload "
+              f"(all {w.dv}x{w.dk} state rows) + their Moebius steps, fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.dk, "d_v": w.dv,
+            "inputs": "bf16" if "bfloat16" in str(w.dtype) else "fp32", "state": "fp32",
+            "mobius": f"{w.mobius_N}x{w.mobius_T} fp32" + (" (one per head)" if w.mobius_fused else ""),
+            "l2": "inputs larger than the 129 MB L2, no flush"}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+
+def run_ours(args, w, dist):
+    import torch
+
+    from bayesian_scan_gb300 import kdn, workloads
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    # every rank draws its own batch of the same shape (weak scaling)
+    w_rank = w if dist.rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * dist.rank})
+    host = workloads.make(w_rank)
+    names = ("q", "k", "v", "beta", "d", "A")
+    mnames = ("ma", "mb", "mc", "md", "lam0")
+    x = {n: host[n].to(dev) for n in names + mnames}
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    o_buf = torch.empty(B, H, T, dv, device=dev)
+    fs_buf = torch.empty(2, B, H, dv, dk, device=dev)
+    lam_buf = torch.empty(w.mobius_N, w.mobius_T, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def diag():
+        kdn.diag_scan_fwd(*(x[n] for n in names), I_prior=w.I_prior, out=o_buf,
+                          final_state=fs_buf, stream=stream)
+
+    def mobius():
+        kdn.mobius_scan(*(x[n] for n in mnames), out=lam_buf, stream=stream)
+
+    plan = kdn.diag_scan_plan(B, H, T, dk, dv, w.dtype)
+    mplan = kdn.mobius_scan_plan(w.mobius_N, w.mobius_T)
+    for _ in range(args.warmup):
+        diag()
+        mobius()
+    torch.cuda.synchronize(dev)
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error after warm-up: {kdn.status_string(st)}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(dist.local_rank))
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            diag()
+            ev[i][1].record(stream)
+            mobius()
+            ev[i][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {kdn.status_string(st)}")
+    total_ms = start.elapsed_time(stop)
+    diag_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
+    mob_ms = sum(b.elapsed_time(c) for _, b, c in ev) / K
+    max_ms = dist.max(total_ms)
+    tokens = B * H * T
+    value = dist.world * tokens * K / (max_ms / 1e3)
+
+    peaks = measured_peaks()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK))
+    alu_peak = nsm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12    # TFLOP/s
+    flop = DIAG_FLOP_PER_ELEMENT_TOKEN * dv * dk * tokens
+    achieved = flop / (diag_ms / 1e3) / 1e12
+    hbm_peak = float(peaks.get("hbm_gbs", HBM_GBS_FALLBACK))
+    mbytes = MOBIUS_BYTES_PER_STEP * w.mobius_N * w.mobius_T
+    mob_gbs = mbytes / (mob_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": {"kernel": "diag_scan_kernel (whole kdn_diag_scan_fwd call)", "bound": "alu",
+                     "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": DIAG_TRAFFIC_BYTES,
+                     "peak_source": f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz"
+                                    " (recipe unit counts and max SM clock)",
+                     "ms_per_call": diag_ms, "token_parts": plan["parts"]},
+        "mobius_roofline": {"bound": "hbm", "achieved": mob_gbs, "peak": hbm_peak, "unit": "GB/s",
+                            "frac": mob_gbs / hbm_peak, "ms_per_call": mob_ms,
+                            "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+        "gpu_launches": K * (plan["kernels"] + mplan["kernels"]),
+        "clocks": sampler.summary(),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = measure_e2e(args, w, host, dev, dist)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        n_heads, t_tokens = calibrate_oracle(w, host, 12.0)
+        dt, units, cores = oracle_sample(w, host, n_heads, t_tokens)
+        line["cpu_baseline"] = {
+            "value": units / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_heads} heads x {t_tokens} tokens of the same inputs (all "
+                      f"{dv}x{dk} state rows) + their Moebius steps, fp64 oracle, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_e2e(args, w, host, dev, dist):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory, runs both scans and reads the results
+    back (o, final state, lambda)."""
+    import torch
+
+    from bayesian_scan_gb300 import kdn
+    names = ("q", "k", "v", "beta", "d", "A")
+    mnames = ("ma", "mb", "mc", "md", "lam0")
+    pinned = {n: host[n].pin_memory() for n in names + mnames}
+    K = max(3, min(args.steps, 20))
+    h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in names + mnames)
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    d2h = 4 * (B * H * T * dv + 2 * B * H * dv * dk + w.mobius_N * w.mobius_T)
+
+    def step():
+        kdn.diag_scan_fwd(*(pinned[n] for n in names), I_prior=w.I_prior)
+        kdn.mobius_scan(*(pinned[n] for n in mnames))
+
+    step()   # warm-up (allocator, pinned staging)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    torch.cuda.synchronize(dev)
+    dt = dist.max(time.perf_counter() - t0)
+    dist.barrier()
+    return {"value": dist.world * B * H * T * K / dt, "unit": "tokens/s", "steps": K,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "bayesian_scan_gb300.kdn with pinned host tensors (H2D, kernels, D2H, sync)"}
+
+
+def main():
+    args = parse_args()
+    from bayesian_scan_gb300 import workloads
+    w = workloads.get(args.workload)
+    dist = Dist(use_gpu=args.impl == "ours")
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, dist)
+        return run_ours(args, w, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

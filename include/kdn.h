@@ -1,0 +1,170 @@
+/*
+ * kdn.h -- C ABI of the GB300 (sm_103a) uncertainty-tracked linear-attention
+ * scans.  Plain pointers and sizes only; no C++ or framework types.
+ *
+ * Two operations:
+ *
+ *  kdn_diag_scan_fwd -- the diagonal metaplastic update of
+ *    "Learning to Remember, Learn, and Forget in Attention-Based Models"
+ *    (Metodologia 1: forget gate alpha_t = exp(-A d_t); Metodologia 2: the
+ *    closed-form update of the importance I_t and the mean mu_t), per head a
+ *    d_v x d_k state, with readout o_t = mu_t q_t (the posterior mean read by
+ *    the query, "Kalman Linear Attention (KLA)", Metodologia 1, "Readout"):
+ *        I_t  = alpha_t I_{t-1} + (1-alpha_t) I_prior + beta_t (x) k_t^2
+ *        mu_t = alpha_t (I_{t-1}/I_t) . mu_{t-1} + (1/I_t) . [(beta_t . v_t) (x) k_t]
+ *        o_t[i] = sum_j mu_t[i][j] q_t[j]
+ *    with beta_t on the value axis: (beta (x) k^2)[i][j] = beta_i k_j^2 and
+ *    ((beta . v) (x) k)[i][j] = beta_i v_i k_j.
+ *
+ *  kdn_mobius_scan -- the precision recursion of "Kalman Linear Attention
+ *    (KLA)", Metodologia 2 ("Parallelizzazione tramite Trasformazioni di
+ *    Moebius"):
+ *        lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t),
+ *    computed as a parallel prefix scan of 2x2 matrix products.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are dense, row-major (C order) and contiguous.  Device
+ *    pointers must point to memory of the current CUDA device; they are
+ *    read/written asynchronously on `stream` (a cudaStream_t, or NULL for the
+ *    legacy default stream).  The call returns as soon as the work is queued.
+ *  - The caller owns every buffer.  Entry points may take short-lived
+ *    stream-ordered scratch from the device's default memory pool
+ *    (cudaMallocAsync / cudaFreeAsync on `stream`); the library holds no other
+ *    device memory besides one error word per device.
+ *  - Errors detectable on the host (null pointers, bad sizes, unsupported
+ *    head dimensions, misaligned pointers) are returned before anything is
+ *    launched.  Launch failures return KDN_ERR_CUDA.  Errors found by a
+ *    kernel (a bounded wait that ran out) are recorded in a per-device error
+ *    word and reported by kdn_get_device_error().
+ *  - Values are not checked: non-finite inputs or non-positive Moebius
+ *    denominators propagate as IEEE inf/nan.
+ */
+#ifndef KDN_H_
+#define KDN_H_
+
+#if defined(__GNUC__) || defined(__clang__)
+#define KDN_API __attribute__((visibility("default")))
+#else
+#define KDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDN_OK = 0,
+    KDN_ERR_INVALID_ARG = -1,  /* null pointer, size out of range, misalignment */
+    KDN_ERR_UNSUPPORTED = -2,  /* head dimension or dtype not supported */
+    KDN_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+    KDN_ERR_TIMEOUT = -4,      /* a bounded device-side wait ran out */
+    KDN_ERR_ALLOC = -5         /* scratch allocation failed */
+} kdn_status;
+
+typedef enum {
+    KDN_F32 = 0,   /* IEEE binary32 */
+    KDN_BF16 = 1   /* bfloat16 */
+} kdn_dtype;
+
+/*
+ * kdn_diag_scan_fwd -- forward diagonal metaplastic scan with readout.
+ *
+ *   q, k       [B,H,T,dk]  in_dtype   query and key of each token-head
+ *   v, beta    [B,H,T,dv]  in_dtype   value and input-dependent importance
+ *   d          [B,H,T]     in_dtype   gate input; alpha_t = exp(-A[h] d_t)
+ *   A          [H]         fp32       per-head gate rate
+ *   I_prior                fp32       prior importance (> 0)
+ *   I0, mu0    [B,H,dv,dk] fp32 or NULL   initial importance and mean; both
+ *                          NULL => I_0 = I_prior, mu_0 = 0.  If exactly one is
+ *                          NULL, that one takes its default.
+ *   out        [B,H,T,dv]  fp32       o_t = mu_t q_t (after the token's update)
+ *   final_state [2,B,H,dv,dk] fp32 or NULL   mu_T then I_T; feeding them back
+ *                          as mu0/I0 of a call on the following tokens gives
+ *                          the same result as one call over all tokens.
+ *   B >= 1, H >= 1, T >= 0.  T = 0 writes only final_state (= the initial
+ *   state); q, k, v, beta, d, A and out are then not read and may be NULL.
+ *   dk, dv in {16, 32, 64, 128}, B*H*T*max(dk,dv) < 2^62.
+ *   Pointers must be 16-byte aligned.  in_dtype is KDN_F32 or KDN_BF16.
+ *
+ * Arithmetic: fp32 state and accumulation.  The library computes the same
+ * recurrence in the equivalent information form eta = I . mu with exact
+ * power-of-two rescaling (the kernel source documents the rescaling); results match the
+ * fp64 definition to a few fp32 ulps times the sequence's conditioning.
+ */
+KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v,
+                             const void* beta, const void* d, const float* A,
+                             float I_prior, const float* I0, const float* mu0,
+                             float* out, float* final_state,
+                             int B, int H, int T, int dk, int dv,
+                             kdn_dtype in_dtype, void* stream);
+
+/*
+ * kdn_mobius_scan -- lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t)
+ * for N independent sequences.
+ *
+ *   a, b, c, d [N,T] fp32   coefficients of step t (index t = 0..T-1)
+ *   lambda0    [N]   fp32   initial value of each sequence
+ *   out        [N,T] fp32   lambda_1..lambda_T (lambda0 is not repeated)
+ *   N >= 0, T >= 0, N*T < 2^62; pointers 4-byte aligned (16-byte alignment
+ *   with T % 4 == 0 enables the vector path).
+ *
+ * Uses stream-ordered scratch (cudaMallocAsync) for the cross-block
+ * look-back; returns KDN_ERR_ALLOC if it cannot be had.
+ */
+KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* c,
+                           const float* d, const float* lambda0, float* out,
+                           long long N, long long T, void* stream);
+
+/*
+ * kdn_diag_scan_plan -- how kdn_diag_scan_fwd would run these sizes on the
+ * current device, without launching anything: `parts` = token ranges the
+ * sequence is split into (1 = no split), `kernels` = kernels one call
+ * launches, `scratch_bytes` = stream-ordered scratch one call takes.  Any
+ * output pointer may be NULL.  Needs a CUDA device (occupancy query).
+ */
+KDN_API kdn_status kdn_diag_scan_plan(int B, int H, int T, int dk, int dv, kdn_dtype in_dtype,
+                                      int* parts, int* kernels, long long* scratch_bytes);
+
+/*
+ * kdn_mobius_scan_plan -- kernels one kdn_mobius_scan call launches and the
+ * scratch bytes it takes (plus one cudaMemsetAsync of part of the scratch
+ * when scratch_bytes > 0).  Host arithmetic only.
+ */
+KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
+                                        long long* scratch_bytes);
+
+/* Human-readable name of a status code (static string). */
+KDN_API const char* kdn_status_string(kdn_status s);
+
+/*
+ * kdn_get_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns KDN_OK if no kernel recorded an
+ * error since the last call, else the recorded status (e.g.
+ * KDN_ERR_TIMEOUT), or KDN_ERR_CUDA if synchronisation failed.
+ */
+KDN_API kdn_status kdn_get_device_error(void* stream);
+
+/*
+ * kdn_set_wait_limit_ns -- upper bound, in nanoseconds of GPU time, on any
+ * single device-side wait of later launches (default 2e9).  A wait that runs
+ * out records KDN_ERR_TIMEOUT and the kernel carries on without blocking.
+ * Values <= 0 restore the default.
+ */
+KDN_API void kdn_set_wait_limit_ns(long long ns);
+
+/*
+ * kdn_debug_stall_mobius_tile -- fault injection for tests.  For the next
+ * kdn_mobius_scan launches, the block that takes look-back tile `tile`
+ * (0-based, in scheduling order) never publishes its result, so its
+ * successor's wait must run out (KDN_ERR_TIMEOUT) instead of hanging.
+ * A negative value (the default) disables the injection.
+ */
+KDN_API void kdn_debug_stall_mobius_tile(long long tile);
+
+/* Library version string, e.g. "kdn 0.1.0 sm_103a". */
+KDN_API const char* kdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDN_H_ */

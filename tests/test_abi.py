@@ -1,0 +1,102 @@
+"""The C-ABI library loads, exports every symbol include/kdn.h declares, and
+rejects invalid arguments on the host before any launch (CPU only: none of
+these calls reaches a CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_symbols():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        names += re.findall(r"KDN_API\s+[\w\s\*]+?\b(kdn_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bayesian_scan_gb300 import build
+    build.build()
+    from bayesian_scan_gb300 import kdn
+    return kdn.lib
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("kdn_diag_scan_fwd", "kdn_mobius_scan", "kdn_status_string",
+                     "kdn_get_device_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    from bayesian_scan_gb300 import kdn
+    for s in (0, -1, -2, -3, -4, -5):
+        assert kdn.status_string(s).startswith("KDN_")
+    assert "unknown" in kdn.status_string(7)
+    assert kdn.version().startswith("kdn ")
+
+
+FAKE = 0x10000  # 16-byte aligned fake address: only reached by host checks
+
+
+def _diag(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, I_prior=1.0, I0=None,
+          mu0=None, out=FAKE, fs=None, B=1, H=1, T=8, dk=16, dv=16, dtype=1):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_diag_scan_fwd(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), I_prior, vp(I0),
+                                 vp(mu0), vp(out), vp(fs), B, H, T, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d", "A", "out"])
+def test_diag_null_pointer(lib, field):
+    assert _diag(lib, **{field: None}) == -1
+    # with T = 0 the token tensors are not read, but sizes are still checked
+    assert _diag(lib, T=0, dk=24, **{field: None}) == -2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), -1), (dict(H=0), -1), (dict(T=-1), -1), (dict(B=-3), -1),
+    (dict(dk=8), -2), (dict(dv=256), -2), (dict(dk=48), -2), (dict(dtype=2), -2),
+    (dict(q=FAKE + 8), -1), (dict(v=FAKE + 4), -1), (dict(out=FAKE + 2), -1),
+    (dict(I0=FAKE + 8), -1), (dict(mu0=FAKE + 1), -1), (dict(fs=FAKE + 12), -1),
+    (dict(A=FAKE + 2), -1), (dict(d=FAKE + 1), -1),
+    (dict(B=1 << 30, H=1 << 30, T=1 << 30), -1),
+])
+def test_diag_rejects(lib, kw, status):
+    assert _diag(lib, **kw) == status
+
+
+def _mob(lib, a=FAKE, b=FAKE, c=FAKE, d=FAKE, l0=FAKE, out=FAKE, N=4, T=16):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_mobius_scan(vp(a), vp(b), vp(c), vp(d), vp(l0), vp(out), N, T, None)
+
+
+@pytest.mark.parametrize("field", ["a", "b", "c", "d", "l0", "out"])
+def test_mobius_null_pointer(lib, field):
+    assert _mob(lib, **{field: None}) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=-1), -1), (dict(T=-2), -1), (dict(N=1 << 40, T=1 << 40), -1),
+    (dict(a=FAKE + 1), -1), (dict(out=FAKE + 2), -1),
+])
+def test_mobius_rejects(lib, kw, status):
+    assert _mob(lib, **kw) == status
+
+
+def test_mobius_empty_is_a_no_op(lib):
+    # nothing to compute: returns OK without touching the (null) buffers
+    assert _mob(lib, a=None, b=None, c=None, d=None, l0=None, out=None, N=0, T=16) == 0
+    assert _mob(lib, a=None, b=None, c=None, d=None, l0=None, out=None, N=5, T=0) == 0

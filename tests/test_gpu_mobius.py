@@ -1,0 +1,77 @@
+"""Moebius scan: CUDA path vs the fp64 oracle, over single and multi-tile
+sequences (decoupled look-back), ragged tails, the scalar path, closed
+forms, and a host-injected stall that must end in KDN_ERR_TIMEOUT."""
+import numpy as np
+import pytest
+import torch
+
+from bayesian_scan_gb300 import workloads
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,T", [(1, 1), (1, 7), (3, 2048), (3, 2049), (2, 4100), (5, 5003),
+                                 (1, 70000), (64, 16384), (257, 333)])
+def test_random(N, T):
+    a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=N * 1000 + T)
+    parity.check_mobius(a, b, c, d, lam0)
+
+
+def test_small_workload():
+    inp = workloads.make("small")
+    parity.check_mobius(inp["ma"], inp["mb"], inp["mc"], inp["md"], inp["lam0"])
+
+
+def test_lambda0_varies():
+    a, b, c, d, _ = workloads.draw_mobius(9, 4096, seed=3)
+    lam0 = torch.linspace(0.1, 10.0, 9)
+    parity.check_mobius(a, b, c, d, lam0)
+
+
+def test_product_closed_form():
+    N, T = 4, 6000
+    a, _, _, d, lam0 = workloads.draw_mobius(N, T, seed=11)
+    z = torch.zeros(N, T)
+    out = parity.gpu_mobius(a, z, z, d, lam0)
+    # lambda_t = lambda_0 prod (a/d) in log space (fp64)
+    ref = np.exp(np.cumsum(np.log(a.double().numpy() / d.double().numpy()), axis=1))
+    rel = np.abs(out.double().numpy() / ref - 1.0)
+    assert rel.max() < 1e-4     # pointwise relative error over a product of 6000 factors
+
+
+def test_unaligned_scalar_path():
+    N, T = 3, 4097
+    a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=5)
+    base = torch.empty(4 * N * T + 1)
+    # views at an odd float offset: 4-byte but not 16-byte aligned
+    views = []
+    for i, x in enumerate((a, b, c, d)):
+        v = base[1 + i * N * T: 1 + (i + 1) * N * T].view(N, T)
+        v.copy_(x)
+        views.append(v)
+    from bayesian_scan_gb300 import kdn
+    dev_base = base.cuda()
+    dv = [dev_base[1 + i * N * T: 1 + (i + 1) * N * T].view(N, T) for i in range(4)]
+    out = kdn.mobius_scan(*dv, lam0.cuda())
+    ref = parity.oracle.mobius_scan(a, b, c, d, lam0)
+    assert parity.rel_err(out.cpu(), ref) <= parity.TOL_MOBIUS
+
+
+def test_stalled_tile_times_out_and_recovers():
+    from bayesian_scan_gb300 import kdn
+    N, T = 2, 3 * 2048
+    a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=1)
+    dev = [x.cuda() for x in (a, b, c, d, lam0)]
+    assert kdn.get_device_error() == 0
+    kdn.set_wait_limit_ns(50_000_000)          # 50 ms
+    kdn.debug_stall_mobius_tile(1)              # tile 1 never publishes
+    try:
+        kdn.mobius_scan(*dev)
+        assert kdn.get_device_error() == kdn.KDN_ERR_TIMEOUT
+    finally:
+        kdn.debug_stall_mobius_tile(-1)
+        kdn.set_wait_limit_ns(0)
+    # the context is still usable and the next call is exact again
+    assert kdn.get_device_error() == 0
+    parity.check_mobius(a, b, c, d, lam0)
