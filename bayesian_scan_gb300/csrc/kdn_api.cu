@@ -115,6 +115,20 @@ kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels, long lon
     return KDN_OK;
 }
 
+kdn_status kdn_mobius_scan_noalloc(const float* a, const float* b, const float* c,
+                                   const float* d, const float* lambda0, float* out, long long N,
+                                   long long T, void* stream) {
+    if (N < 0 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (N > 0 && T > 0 && N > (1LL << 62) / T) return KDN_ERR_INVALID_ARG;
+    if (N == 0 || T == 0) return KDN_OK;
+    if (!a || !b || !c || !d || !lambda0 || !out) return KDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {a, b, c, d, lambda0, out};
+    for (const void* p : ptrs)
+        if (!aligned(p, 4)) return KDN_ERR_INVALID_ARG;
+    return mobius_launch_noalloc(a, b, c, d, lambda0, out, N, T, static_cast<cudaStream_t>(stream),
+                                 g_wait_ns.load());
+}
+
 const char* kdn_status_string(kdn_status s) {
     switch (s) {
         case KDN_OK: return "KDN_OK";

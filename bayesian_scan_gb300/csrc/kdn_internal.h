@@ -38,6 +38,12 @@ kdn_status mobius_launch(const float* a, const float* b, const float* c, const f
                          const float* lambda0, float* out, long long N, long long T,
                          cudaStream_t stream, long long wait_ns, long long stall_tile);
 
+// Allocation-free Moebius scan: look-back scratch in a fixed device array.
+kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c, const float* d,
+                                 const float* lambda0, float* out, long long N, long long T,
+                                 cudaStream_t stream, long long wait_ns);
+long long mobius_noalloc_max_tiles();
+
 // Each translation unit that launches kernels with bounded waits owns one
 // device error word; these read-and-clear it on the current device.
 cudaError_t diag_take_device_error(int* status);

@@ -30,6 +30,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kdn_device.cuh"
 #include "kdn_internal.h"
 
@@ -310,6 +312,88 @@ cudaError_t mobius_take_device_error(int* status) {
     if (v != 0) e = cudaMemcpyToSymbol(g_mobius_error, &zero, sizeof(int));
     *status = v;
     return e;
+}
+
+}  // namespace kdn
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (kdn_mobius_scan_noalloc).
+//
+// Some callers must not allocate device memory during a call: for example a
+// process whose framework reserved the GPU's memory up front, so that the
+// default memory pool has nothing left to give, or a latency-critical loop in
+// which allocator calls are not allowed.  For them the look-back scratch of a
+// multi-tile scan lives in the fixed array below, part of the library's
+// device image: every GPU that loads the library holds these 1 MiB until the
+// process exits.  Host code cannot use the array's name as a device address,
+// so set-up fetches the address once per device with cudaGetSymbolAddress.
+namespace kdn {
+
+static __device__ __align__(256) unsigned char g_kdn_noalloc_scratch[1u << 20];
+
+namespace {
+constexpr size_t kNoAllocBytes = sizeof(g_kdn_noalloc_scratch);
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of the array on the current device (set-up on first use).
+cudaError_t noalloc_base(void** base) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_kdn_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *base = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+long long mobius_noalloc_max_tiles() {
+    // largest t with round16(8 + 4 t) + 20 t <= kNoAllocBytes
+    long long t = static_cast<long long>(kNoAllocBytes) / 24;
+    while (t > 0 && (((8 + 4 * static_cast<size_t>(t) + 15) & ~size_t(15)) + 20 * static_cast<size_t>(t)) > kNoAllocBytes) --t;
+    return t;
+}
+
+kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c, const float* d,
+                                 const float* lambda0, float* out, long long N, long long T,
+                                 cudaStream_t stream, long long wait_ns) {
+    if (N == 0 || T == 0) return KDN_OK;
+    const long long tps = (T + MB_TILE - 1) / MB_TILE;
+    const long long tiles = N * tps;
+    if (tiles > 0x7fffffffLL) return KDN_ERR_INVALID_ARG;
+    auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool vec = (T % 4 == 0) && aligned16(a) && aligned16(b) && aligned16(c) &&
+                     aligned16(d) && aligned16(out);
+    LookbackScratch sc{nullptr, nullptr, nullptr, nullptr};
+    cudaError_t e;
+    if (tps > 1) {
+        if (tiles > mobius_noalloc_max_tiles()) return KDN_ERR_INVALID_ARG;
+        void* base = nullptr;
+        e = noalloc_base(&base);
+        if (e != cudaSuccess) return from_cuda(e);
+        const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
+        char* p = static_cast<char*>(base);
+        sc.ticket = reinterpret_cast<unsigned long long*>(p);
+        sc.flags = reinterpret_cast<unsigned int*>(p + 8);
+        sc.agg = reinterpret_cast<float4*>(p + zero_bytes);
+        sc.pre = reinterpret_cast<float*>(p + zero_bytes + 16 * tiles);
+        // the array keeps the previous call's contents: clear ticket and flags
+        e = cudaMemsetAsync(base, 0, zero_bytes, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = vec ? launch<true, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1)
+                : launch<false, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1);
+    } else {
+        e = vec ? launch<true, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1)
+                : launch<false, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1);
+    }
+    return from_cuda(e);
 }
 
 }  // namespace kdn

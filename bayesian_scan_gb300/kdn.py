@@ -9,6 +9,7 @@ Functions mirror the C names:
 
 * :func:`diag_scan_fwd`  -> ``kdn_diag_scan_fwd``
 * :func:`mobius_scan`    -> ``kdn_mobius_scan``
+* :func:`mobius_scan_noalloc` -> ``kdn_mobius_scan_noalloc``
 * :func:`diag_scan_plan`, :func:`mobius_scan_plan` -> the ``*_plan`` queries
 * :func:`get_device_error`, :func:`set_wait_limit_ns`,
   :func:`debug_stall_mobius_tile`, :func:`status_string`, :func:`version`
@@ -50,6 +51,8 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_mobius_scan_noalloc.restype = i
+    lib.kdn_mobius_scan_noalloc.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
     lib.kdn_status_string.restype = ctypes.c_char_p
     lib.kdn_status_string.argtypes = [i]
     lib.kdn_get_device_error.restype = i
@@ -176,6 +179,26 @@ def mobius_scan_plan(N, T) -> dict:
     if st != KDN_OK:
         raise KdnError(st, "kdn_mobius_scan_plan")
     return dict(kernels=k.value, scratch_bytes=sb.value)
+
+
+MOBIUS_NOALLOC_MAX_TILES = 43690   # N * ceil(T / 2048) limit of mobius_scan_noalloc
+
+
+def mobius_scan_noalloc(a, b, c, d, lambda0, out, stream=None):
+    """``kdn_mobius_scan_noalloc``: the Moebius scan for callers that must not
+    allocate device memory during the call (e.g. a framework that reserved
+    the GPU's memory up front).  The caller passes every buffer, ``out``
+    included; the look-back scratch is a fixed 1 MiB array in the library.
+    Calls that overlap on the GPU share that array and race."""
+    N, T = a.shape
+    for name, t in (("a", a), ("b", b), ("c", c), ("d", d), ("out", out)):
+        _check(t, name, torch.float32, (N, T))
+    _check(lambda0, "lambda0", torch.float32, (N,))
+    st = lib.kdn_mobius_scan_noalloc(_ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(lambda0), _ptr(out),
+                                     N, T, _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_mobius_scan_noalloc")
+    return out
 
 
 def get_device_error(stream=None) -> int:

@@ -133,6 +133,28 @@ KDN_API kdn_status kdn_diag_scan_plan(int B, int H, int T, int dk, int dv, kdn_d
 KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
                                         long long* scratch_bytes);
 
+/*
+ * kdn_mobius_scan_noalloc -- kdn_mobius_scan for callers that must not
+ * allocate device memory during a call (for instance a process whose
+ * framework reserved the GPU's memory up front, or a latency-critical loop
+ * where allocator calls are not allowed).  The pages have no counterpart:
+ * this is an interface variant, not part of the method.
+ *
+ * Same arguments, layouts and results as kdn_mobius_scan.  The look-back
+ * scratch lives in a fixed 1 MiB array inside the library's device image,
+ * which every GPU that loads the library holds until the process exits; no
+ * cudaMalloc/cudaMallocAsync/cudaFree is called.  Limit: a sequence longer
+ * than 2048 steps needs look-back scratch, and then N * ceil(T / 2048) may be
+ * at most 43690 (e.g. 4096 sequences of 16384 steps use 32768); larger calls
+ * return KDN_ERR_INVALID_ARG without launching.  The first call on a device fetches the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array: calls whose executions overlap on the GPU
+ * (for example on two streams) race and give wrong results; serialise them.
+ */
+KDN_API kdn_status kdn_mobius_scan_noalloc(const float* a, const float* b, const float* c,
+                                           const float* d, const float* lambda0, float* out,
+                                           long long N, long long T, void* stream);
+
 /* Human-readable name of a status code (static string). */
 KDN_API const char* kdn_status_string(kdn_status s);
 

@@ -1,0 +1,61 @@
+"""kdn_mobius_scan_noalloc, the allocation-free Moebius scan, against
+kdn_mobius_scan.
+
+Some callers cannot allocate device memory during a call (a framework that
+reserved the GPU's memory up front, a loop where allocator calls are not
+allowed); this entry point serves them with look-back scratch in a fixed
+array inside the library.  The test calls it through the C ABI (ctypes) and
+compares it with the allocating entry point on two calls in a row (the second
+call must clear what the first left in the shared array), then checks that a
+call needing more look-back tiles than the array holds is refused.
+
+The file name sorts last so that a run stopping at the first failure has run
+every other test before this one; it also passes alone in a fresh process
+(the first call on the device does the array's set-up)."""
+import ctypes
+
+import pytest
+import torch
+
+from bayesian_scan_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5   # the Moebius parity tolerance used by the other tests
+
+
+def _call(lib, a, b, c, d, lam0, out):
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.kdn_mobius_scan_noalloc(p(a), p(b), p(c), p(d), p(lam0), p(out),
+                                       a.shape[0], a.shape[1], stream)
+
+
+def _rel(x, ref):
+    return float((x.double() - ref.double()).abs().max() / ref.double().abs().max())
+
+
+def test_noalloc_matches_allocating_entry_point_twice():
+    from bayesian_scan_gb300 import kdn
+    lib = kdn.lib
+    for call, (N, T, seed) in enumerate([(48, 9000, 21), (37, 16384, 22)]):
+        a, b, c, d, lam0 = (x.cuda() for x in workloads.draw_mobius(N, T, seed=seed))
+        ref = kdn.mobius_scan(a, b, c, d, lam0)
+        out = torch.full_like(ref, float("nan"))
+        st = _call(lib, a, b, c, d, lam0, out)
+        assert st == 0, kdn.status_string(st)
+        torch.cuda.synchronize()
+        assert kdn.get_device_error() == 0
+        assert torch.isfinite(out).all(), f"call {call}"
+        assert _rel(out, ref) <= TOL, f"call {call}"
+
+
+def test_noalloc_refuses_more_tiles_than_the_array_holds():
+    from bayesian_scan_gb300 import kdn
+    N, T = kdn.MOBIUS_NOALLOC_MAX_TILES // 2 + 1, 4096      # 2 tiles per sequence
+    x = torch.zeros(N, T, device="cuda")
+    lam0 = torch.ones(N, device="cuda")
+    out = torch.full((N, T), -7.0, device="cuda")
+    assert _call(kdn.lib, x, x, x, x, lam0, out) == kdn.KDN_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((out == -7.0).all())        # nothing was launched
