@@ -68,7 +68,7 @@ constexpr int RT = 4;            // rows per lane
 constexpr int CW = 16;           // columns per lane
 constexpr int NSTAGE = 3;        // chunks in flight
 constexpr int ROWS_PER_CTA = 128;
-constexpr int PAIRS = 3;         // column-pair groups (of 4) per lane row sharing a reciprocal
+constexpr int PAIRS = 2;         // of the 4 column-pair groups of a lane row, how many share reciprocals
 constexpr float SIGMA = 5.9604644775390625e-08f;   // 2^-24
 constexpr float W_LIMIT = 281474976710656.0f;      // 2^48
 constexpr float LOG2E = 1.4426950408889634f;
@@ -107,7 +107,7 @@ struct Geo {
     static constexpr int WR = RS * RT;             // rows per warp
     static constexpr int NW = ROWS_PER_CTA / WR;   // warps per CTA (= M)
     static constexpr int NTHREADS = NW * 32;
-    static constexpr int PAR_FLOATS = 3 * DK;      // per token: k, k^2, q (fp32)
+    static constexpr int PAR_FLOATS = 3 * DK + 4;  // per token: k, k^2, q, then (f, W, sigma W I_prior, 0)
 };
 
 // shared-memory layout of one chunk stage for `hpc` heads
@@ -118,7 +118,7 @@ struct Layout {
         raw_qk = TC * dk * es;
         raw_vb = TC * dv * es;
         raw_d = (TC * es + 15) & ~15;
-        par = TC * 3 * dk * 4;
+        par = TC * (3 * dk + 4) * 4;
         head = 2 * raw_qk + 2 * raw_vb + raw_d + par;
         stage = hpc * head;
     }
@@ -127,7 +127,7 @@ struct Layout {
 __host__ __device__ inline int smem_bytes(int dk, int dv, int es, int TC) {
     const int hpc = ROWS_PER_CTA / dv;
     Layout L(dk, dv, es, TC, hpc);
-    return NSTAGE * L.stage + 2 * NSTAGE * 8 + NSTAGE * 4;
+    return NSTAGE * L.stage + 2 * NSTAGE * 8 + NSTAGE * 4 + 2 * hpc * 4;
 }
 
 // one error word per translation unit that instantiates these kernels
@@ -299,6 +299,8 @@ diag_scan_kernel(const Params p) {
     uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + NSTAGE * L.stage);
     uint64_t* full_par = full_raw + NSTAGE;
     int* done_cnt = reinterpret_cast<int*>(full_par + NSTAGE);
+    float* w_state = reinterpret_cast<float*>(done_cnt + NSTAGE);   // [HPC] scale W per head
+    int* r_state = reinterpret_cast<int*>(w_state + HPC);             // [HPC] exponent sum R
     auto region = [&](int s, int h, int off) { return smem + s * L.stage + h * L.head + off; };
     auto raw_q = [&](int s, int h) { return reinterpret_cast<TIn*>(region(s, h, 0)); };
     auto raw_k = [&](int s, int h) { return reinterpret_cast<TIn*>(region(s, h, L.raw_qk)); };
@@ -326,6 +328,7 @@ diag_scan_kernel(const Params p) {
     const TIn* gv = static_cast<const TIn*>(p.v);
     const TIn* gb = static_cast<const TIn*>(p.beta);
     const TIn* gd = static_cast<const TIn*>(p.d);
+    const float Ip = p.I_prior;
 
     // Issue the bulk copies of chunk c into its stage (one warp, all lanes).
     auto issue = [&](int c) {
@@ -357,10 +360,16 @@ diag_scan_kernel(const Params p) {
     };
 
     bool ok = true;
-    // Convert this warp's tokens (tt = warp, warp + NW, ...) of chunk c:
-    // k -> (k, k^2) and q to fp32, in the interleaved layout in which the
-    // 16-column group cg of a lane is float4 number (s4 * M + cg), s4 = 0..3.
-    auto convert = [&](int c) {
+    // Prepare chunk c once its copies have landed:
+    //  * every warp converts its tokens (tt = warp, warp + NW, ...): k ->
+    //    (k, k^2) and q to fp32, interleaved so that the 16-column group cg of
+    //    a lane is float4 number (s4 * M + cg), s4 = 0..3;
+    //  * warp c % NW runs the per-head scale recursion over the chunk's tokens
+    //    (sequential in t; W and R carried across chunks in shared memory) and
+    //    stores (f_t, W_t, sigma W_t I_prior) behind each token's columns.
+    // Callers guarantee that chunk c-1's recursion has finished (they passed
+    // the full_par wait of chunk c-1, which its recursion arrives on).
+    auto prepare = [&](int c) {
         const int s = c % NSTAGE;
         const int t0 = tb + c * TC, tcn = min(TC, te - t0);
         if (!mbar_wait(&full_raw[s], (c / NSTAGE) & 1, p.wait_ns)) ok = false;
@@ -369,15 +378,36 @@ diag_scan_kernel(const Params p) {
             for (int x = lane; x < nheads * HP; x += 32) {
                 const int h = x / HP;
                 const int j = 2 * (x - h * HP);
-                const int cg = j / CW, jj = j % CW;
-                const int pos = ((jj >> 2) * M + cg) * 4 + (jj & 3);
+                const int cgj = j / CW, jj = j % CW;
+                const int pos = ((jj >> 2) * M + cgj) * 4 + (jj & 3);
                 float* base = par(s, h) + tt * PF;
                 const float2 kv = load2(raw_k(s, h) + tt * DK + j);
                 *reinterpret_cast<float2*>(base + pos) = kv;
                 *reinterpret_cast<float2*>(base + DK + pos) = make_float2(kv.x * kv.x, kv.y * kv.y);
                 if (!AGG) *reinterpret_cast<float2*>(base + 2 * DK + pos) = load2(raw_q(s, h) + tt * DK + j);
             }
-            if (!p.d_tma && lane < nheads) raw_d(s, lane)[tt] = gd[(head0 + lane) * T + t0 + tt];
+        }
+        if (warp == c % NW) {
+            if (!p.d_tma) {
+                for (int x = lane; x < nheads * tcn; x += 32) {
+                    const int h = x / tcn, tt = x - h * tcn;
+                    raw_d(s, h)[tt] = gd[(head0 + h) * T + t0 + tt];
+                }
+                __syncwarp();
+            }
+            if (lane < nheads) {
+                const float Ah = p.A[(head0 + lane) % p.H];
+                float W = w_state[lane];
+                int R = r_state[lane];
+                const TIn* rd = raw_d(s, lane);
+                float* ps = par(s, lane) + 3 * DK;
+                for (int tt = 0; tt < tcn; ++tt) {
+                    const float f = scale_step(Ah * to_f32<TIn>(rd[tt]) * LOG2E, W, R);
+                    *reinterpret_cast<float4*>(ps + tt * PF) = make_float4(f, W, W * Ip * SIGMA, 0.f);
+                }
+                w_state[lane] = W;
+                r_state[lane] = R;
+            }
         }
         mbar_arrive(&full_par[s]);
     };
@@ -388,12 +418,16 @@ diag_scan_kernel(const Params p) {
             mbar_init(&full_par[s], NW * 32);
             done_cnt[s] = 0;
         }
+        for (int h = 0; h < HPC; ++h) {
+            w_state[h] = 1.f;
+            r_state[h] = 0;
+        }
         mbar_init_fence();
     }
     __syncthreads();
     if (warp == 0)
         for (int c = 0; c < min(NSTAGE, nchunks); ++c) issue(c);
-    if (nchunks > 0) convert(0);
+    if (nchunks > 0) prepare(0);
 
     // ------------------------------ lane state ------------------------------
     const int rs = lane / M, cg = lane % M;
@@ -402,8 +436,6 @@ diag_scan_kernel(const Params p) {
     const bool active = hl < nheads;
     const long long bh = head0 + hl;
     const long long S = static_cast<long long>(dv) * DK;
-    const float Ah = (active && nchunks > 0) ? p.A[bh % p.H] : 0.f;
-    const float Ip = p.I_prior;
 
     float2 J[RT][CW / 2], E[RT][CW / 2];
     {
@@ -441,22 +473,36 @@ diag_scan_kernel(const Params p) {
     }
 
     float W = 1.f;
-    int R = 0;
     float* gout = p.out;
     for (int c = 0; c < nchunks; ++c) {
         const int s = c % NSTAGE;
-        if (c + 1 < nchunks) convert(c + 1);
         if (!mbar_wait(&full_par[s], (c / NSTAGE) & 1, p.wait_ns)) ok = false;
+        if (c + 1 < nchunks) prepare(c + 1);
         const int t0 = tb + c * TC, tcn = min(TC, te - t0);
         const TIn* rv = raw_v(s, hl) + i0;
         const TIn* rb = raw_b(s, hl) + i0;
-        const TIn* rd = raw_d(s, hl);
         const float* pbase = par(s, hl);
+        // per-token scalars and row values, loaded one token ahead
+        float4 nsc = *reinterpret_cast<const float4*>(pbase + 3 * DK);
+        float nbet[RT], nval[RT];
+        load4(rb, nbet);
+        load4(rv, nval);
         for (int tt = 0; tt < tcn; ++tt) {
             const float* pt = pbase + tt * PF;
-            const float f = scale_step(Ah * to_f32<TIn>(rd[tt]) * LOG2E, W, R);
-            if (f != 1.f) {                          // exact power-of-two rescale
-                const float2 f22 = f2(f);
+            const float4 sc = nsc;
+            float bet[RT], val[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+                bet[r] = nbet[r];
+                val[r] = nval[r];
+            }
+            if (tt + 1 < tcn) {
+                nsc = *reinterpret_cast<const float4*>(pt + PF + 3 * DK);
+                load4(rb + (tt + 1) * dv, nbet);
+                load4(rv + (tt + 1) * dv, nval);
+            }
+            if (sc.x != 1.f) {                       // exact power-of-two rescale
+                const float2 f22 = f2(sc.x);
 #pragma unroll
                 for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -465,9 +511,7 @@ diag_scan_kernel(const Params p) {
                         E[r][c2] = __fmul2_rn(E[r][c2], f22);
                     }
             }
-            float bet[RT], val[RT];
-            load4(rb + tt * dv, bet);
-            load4(rv + tt * dv, val);
+            W = sc.y;
             float2 SB[RT], SBV[RT];
 #pragma unroll
             for (int r = 0; r < RT; ++r) {
@@ -475,10 +519,10 @@ diag_scan_kernel(const Params p) {
                 SB[r] = f2(sb);
                 SBV[r] = f2(sb * val[r]);
             }
-            const float2 SP = f2(W * Ip * SIGMA), SG = f2(SIGMA);
-            float acc[RT];
+            const float2 SP = f2(sc.z), SG = f2(SIGMA);
+            float2 acc[RT];
 #pragma unroll
-            for (int r = 0; r < RT; ++r) acc[r] = 0.f;
+            for (int r = 0; r < RT; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 // this lane's 8 columns of the half: float4 numbers (2*half+h4)*M + cg
@@ -512,30 +556,31 @@ diag_scan_kernel(const Params p) {
                         }
                     }
                     if (!AGG) {
-                        float2 a2 = make_float2(0.f, 0.f);
-                        // column-pair groups (0,1) and (2,3) of this half; the
-                        // first PAIRS of the row's 4 groups share reciprocals
+                        // column-pair groups (0,1) and (2,3) of this half; group
+                        // g of every half shares reciprocals when g < PAIRS / 2
 #pragma unroll
                         for (int g = 0; g < 2; ++g) {
                             const int x = 2 * g, y = 2 * g + 1;
-                            if (half * 2 + g < PAIRS) {
+                            if (2 * g + half < PAIRS) {
                                 const float2 N = __ffma2_rn(num[x], den[y], __fmul2_rn(num[y], den[x]));
                                 const float2 Dn = __fmul2_rn(den[x], den[y]);
-                                a2 = __ffma2_rn(N, make_float2(rcp_approx(Dn.x), rcp_approx(Dn.y)), a2);
+                                acc[r] = __ffma2_rn(N, make_float2(rcp_approx(Dn.x), rcp_approx(Dn.y)), acc[r]);
                             } else {
-                                a2 = __ffma2_rn(num[x], make_float2(rcp_approx(den[x].x), rcp_approx(den[x].y)), a2);
-                                a2 = __ffma2_rn(num[y], make_float2(rcp_approx(den[y].x), rcp_approx(den[y].y)), a2);
+                                acc[r] = __ffma2_rn(num[x], make_float2(rcp_approx(den[x].x), rcp_approx(den[x].y)), acc[r]);
+                                acc[r] = __ffma2_rn(num[y], make_float2(rcp_approx(den[y].x), rcp_approx(den[y].y)), acc[r]);
                             }
                         }
-                        acc[r] += a2.x + a2.y;
                     }
                 }
             }
             if (!AGG) {
+                float rowsum[RT];
+#pragma unroll
+                for (int r = 0; r < RT; ++r) rowsum[r] = acc[r].x + acc[r].y;
                 float val_out[RowReduce<M>::NV];
                 int row_out[RowReduce<M>::NV];
                 bool st;
-                RowReduce<M>::run(acc, cg, val_out, row_out, st);
+                RowReduce<M>::run(rowsum, cg, val_out, row_out, st);
                 if (st && active) {
                     float* o = gout + (bh * T + t0 + tt) * dv + i0;
 #pragma unroll
@@ -567,7 +612,8 @@ diag_scan_kernel(const Params p) {
                 *reinterpret_cast<float2*>(dJ + off) = J[r][c2];
                 *reinterpret_cast<float2*>(dE + off) = E[r][c2];
             }
-        if (i0 == 0 && cg == 0) p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, R};
+        // the head's scale state after the part: W of its last token, total R
+        if (i0 == 0 && cg == 0) p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, r_state[hl]};
     } else if (p.final_state && part == static_cast<int>(gridDim.y) - 1) {
         // mu_T = eta / (I_prior + J) = Ew / (Jw + W I_prior);  I_T = Jw / W + I_prior
         float* fm = p.final_state + bh * S;

@@ -1,0 +1,74 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times (same shapes through the same entry points), on sampled outputs.
+
+State rows are independent (only the readout sums over the key axis), so the
+oracle computes row i of head (b, h) from v[..., i] and beta[..., i] alone:
+the sample is a few rows of a few heads over the whole sequence, compared
+element by element with the GPU's o[b, h, :, i] and final mu/I rows.
+Moebius sequences are independent too: sampled sequences are compared whole.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from bayesian_scan_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = ["heads32_t2048_d64", "layer750m", "layer1p3b", "longctx"]
+
+
+def _sample(w, rng):
+    n_heads = 2 if w.T > 20000 else 3
+    heads = sorted(set(int(x) for x in rng.choice(w.B * w.H, size=n_heads, replace=False)) |
+                   {w.B * w.H - 1})
+    rows = sorted(set(int(x) for x in rng.choice(w.dv, size=3, replace=False)) | {0, w.dv - 1})
+    return heads, rows
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_full_size_sampled(name):
+    from bayesian_scan_gb300 import kdn
+    w = workloads.get(name)
+    inp = workloads.make(w)
+    dev = "cuda"
+    x = [inp[n].to(dev) for n in ("q", "k", "v", "beta", "d", "A")]
+    o, fs = kdn.diag_scan_fwd(*x, I_prior=inp["I_prior"])
+    lam = kdn.mobius_scan(*[inp[n].to(dev) for n in ("ma", "mb", "mc", "md", "lam0")])
+    torch.cuda.synchronize()
+    assert kdn.get_device_error() == 0
+    rng = np.random.default_rng(sum(map(ord, name)))
+    heads, rows = _sample(w, rng)
+    H = w.H
+    for bh in heads:
+        b, h = divmod(bh, H)
+        sl = lambda t: t[b:b + 1, h:h + 1]
+        q, k, d = sl(inp["q"]), sl(inp["k"]), sl(inp["d"])
+        v, beta = sl(inp["v"])[..., rows], sl(inp["beta"])[..., rows]
+        ro, rmu, rI = oracle.diag_scan(q, k, v, beta, d, inp["A"][h:h + 1], inp["I_prior"])
+        go = o[b, h][:, rows].cpu()
+        gmu = fs[0, b, h][rows].cpu()
+        gI = fs[1, b, h][rows].cpu()
+        assert parity.rel_err(go, ro[0, 0]) <= parity.TOL_DIAG, (name, bh)
+        assert parity.rel_err(gmu, rmu[0, 0]) <= parity.TOL_DIAG, (name, bh)
+        assert parity.rel_err(gI, rI[0, 0]) <= parity.TOL_DIAG, (name, bh)
+    seqs = sorted(set(int(s) for s in rng.choice(w.mobius_N, size=min(4, w.mobius_N),
+                                                 replace=False)))
+    ref = oracle.mobius_scan(inp["ma"][seqs], inp["mb"][seqs], inp["mc"][seqs], inp["md"][seqs],
+                             inp["lam0"][seqs])
+    assert parity.rel_err(lam[seqs].cpu(), ref) <= parity.TOL_MOBIUS, name
+
+
+def test_full_size_properties_everywhere():
+    """Properties that hold at any size, checked on every output of the 750M
+    layer: all finite, and I_T >= I_prior (I_0 = I_prior, evidence >= 0)."""
+    from bayesian_scan_gb300 import kdn
+    w = workloads.get("layer750m")
+    inp = workloads.make(w, with_mobius=False)
+    x = [inp[n].to("cuda") for n in ("q", "k", "v", "beta", "d", "A")]
+    o, fs = kdn.diag_scan_fwd(*x, I_prior=inp["I_prior"])
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(fs).all())
+    assert float(fs[1].min()) >= inp["I_prior"] * (1 - 1e-6)
