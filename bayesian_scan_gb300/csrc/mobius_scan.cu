@@ -239,6 +239,155 @@ mobius_scan_kernel(const float* __restrict__ A, const float* __restrict__ B,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Sequence-per-CTA variant for many sequences with 16-byte aligned rows
+// (T % 4 == 0, N at least the number of resident CTAs): a persistent grid
+// (about two CTAs per SM) gives CTA b the sequences b, b + G, b + 2G, ...
+// (G = grid size) and walks their tiles in order, carrying lambda from tile
+// to tile in shared memory, so no cross-CTA look-back (and no scratch) is
+// needed.  The coefficients of the next MP_STAGES - 1 tiles of its stream are
+// kept in flight with 1-D bulk TMA copies (one per coefficient array,
+// completing on an mbarrier) while the current tile is scanned, which keeps
+// HBM busy.  Few long sequences use the one-tile-per-CTA look-back kernel.
+constexpr int MP_STAGES = 3;
+constexpr int MP_STAGE_FLOATS = 4 * MB_TILE;
+
+__host__ __device__ constexpr int mp_smem_bytes() { return MP_STAGES * MP_STAGE_FLOATS * 4 + MP_STAGES * 8; }
+
+__global__ void __launch_bounds__(MB_THREADS)
+mobius_seq_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                  const float* __restrict__ C, const float* __restrict__ D,
+                  const float* __restrict__ lambda0, float* __restrict__ out, long long N,
+                  long long T, long long tiles_per_seq, long long wait_ns) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* buf = reinterpret_cast<float*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + MP_STAGES * MP_STAGE_FLOATS * 4);
+    __shared__ Mat s_warp[MB_WARPS];
+    __shared__ float s_lam;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long G = gridDim.x;
+    // number of tiles in this CTA's stream
+    const long long nseq = blockIdx.x < N ? (N - 1 - blockIdx.x) / G + 1 : 0;
+    const long long ntiles = nseq * tiles_per_seq;
+    auto tile_seq = [&](long long i) { return blockIdx.x + (i / tiles_per_seq) * G; };
+
+    // bulk copies of stream tile i into stage st (thread 0)
+    auto issue = [&](int st, long long i) {
+        const long long seq = tile_seq(i), part = i % tiles_per_seq;
+        const long long t0 = part * MB_TILE;
+        const long long n = min(static_cast<long long>(MB_TILE), T - t0);
+        const uint32_t bytes = static_cast<uint32_t>(n * 4);
+        const long long off = seq * T + t0;
+        float* dst = buf + st * MP_STAGE_FLOATS;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&full[st], 4 * bytes);
+        bulk_g2s(dst, A + off, bytes, &full[st]);
+        bulk_g2s(dst + MB_TILE, B + off, bytes, &full[st]);
+        bulk_g2s(dst + 2 * MB_TILE, C + off, bytes, &full[st]);
+        bulk_g2s(dst + 3 * MB_TILE, D + off, bytes, &full[st]);
+    };
+
+    if (tid == 0) {
+        for (int st = 0; st < MP_STAGES; ++st) mbar_init(&full[st], 1);
+        mbar_init_fence();
+        for (int st = 0; st < MP_STAGES && st < ntiles; ++st) issue(st, st);
+        s_abort = 0;
+    }
+    __syncthreads();
+
+    long long i = 0;
+    for (; i < ntiles; ++i) {
+        if (s_abort) break;
+        const int st = static_cast<int>(i % MP_STAGES);
+        if (!mbar_wait(&full[st], static_cast<uint32_t>((i / MP_STAGES) & 1), wait_ns)) {
+            record_error(&g_mobius_error, KDN_ERR_TIMEOUT);
+            s_abort = 1;
+        }
+        const long long seq = tile_seq(i), part = i % tiles_per_seq;
+        const long long t_first = part * MB_TILE + static_cast<long long>(tid) * MB_VPT;
+        const long long base = seq * T;
+        const int nvalid = static_cast<int>(max(0LL, min(static_cast<long long>(MB_VPT), T - t_first)));
+
+        // ---- 1. this thread's 8 steps from shared memory ---------------
+        float ca[MB_VPT], cb[MB_VPT], cc[MB_VPT], cd[MB_VPT];
+        {
+            const float* sb = buf + st * MP_STAGE_FLOATS + tid * MB_VPT;
+#pragma unroll
+            for (int h = 0; h < MB_VPT / 4; ++h) {
+                const float4 x = *reinterpret_cast<const float4*>(sb + 4 * h);
+                const float4 y = *reinterpret_cast<const float4*>(sb + MB_TILE + 4 * h);
+                const float4 z = *reinterpret_cast<const float4*>(sb + 2 * MB_TILE + 4 * h);
+                const float4 w = *reinterpret_cast<const float4*>(sb + 3 * MB_TILE + 4 * h);
+                ca[4 * h + 0] = x.x; ca[4 * h + 1] = x.y; ca[4 * h + 2] = x.z; ca[4 * h + 3] = x.w;
+                cb[4 * h + 0] = y.x; cb[4 * h + 1] = y.y; cb[4 * h + 2] = y.z; cb[4 * h + 3] = y.w;
+                cc[4 * h + 0] = z.x; cc[4 * h + 1] = z.y; cc[4 * h + 2] = z.z; cc[4 * h + 3] = z.w;
+                cd[4 * h + 0] = w.x; cd[4 * h + 1] = w.y; cd[4 * h + 2] = w.z; cd[4 * h + 3] = w.w;
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < MB_VPT; ++s2)
+                if (s2 >= nvalid) {          // past the end of the sequence: identity steps
+                    ca[s2] = 1.f; cb[s2] = 0.f; cc[s2] = 0.f; cd[s2] = 1.f;
+                }
+        }
+        __syncthreads();   // stage consumed: refill it with stream tile i + MP_STAGES
+        if (tid == 0 && i + MP_STAGES < ntiles && !s_abort) issue(st, i + MP_STAGES);
+
+        // ---- 2. compose and scan ---------------------------------------
+        Mat P = {ca[0], cb[0], cc[0], cd[0]};
+#pragma unroll
+        for (int s2 = 1; s2 < MB_VPT; ++s2) P = normalize(mul(Mat{ca[s2], cb[s2], cc[s2], cd[s2]}, P));
+        P = normalize(P);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const Mat Q = shfl_up(P, off);
+            if (lane >= off) P = normalize(mul(P, Q));
+        }
+        Mat lane_excl = shfl_up(P, 1);
+        if (lane == 0) lane_excl = identity();
+        if (lane == 31) s_warp[warp] = P;
+        __syncthreads();
+        Mat warp_excl = identity();
+        for (int w = 0; w < warp; ++w) warp_excl = normalize(mul(s_warp[w], warp_excl));
+        const Mat thread_excl = normalize(mul(lane_excl, warp_excl));
+        // lambda at the start of the tile: lambda_0 for the first tile of a
+        // sequence, else the carry left by the previous tile
+        const float lam_start = part == 0 ? __ldg(lambda0 + seq) : s_lam;
+        __syncthreads();   // every thread has read s_lam and s_warp
+        if (tid == 0) {
+            Mat agg = identity();
+            for (int w = 0; w < MB_WARPS; ++w) agg = normalize(mul(s_warp[w], agg));
+            s_lam = apply(agg, lam_start);                // carry for the next tile
+        }
+
+        // ---- 3. outputs ----------------------------------------------------
+        float lam = apply(thread_excl, lam_start);
+        float res[MB_VPT];
+#pragma unroll
+        for (int s2 = 0; s2 < MB_VPT; ++s2) {
+            lam = __fdividef(fmaf(ca[s2], lam, cb[s2]), fmaf(cc[s2], lam, cd[s2]));
+            res[s2] = lam;
+        }
+        if (nvalid == MB_VPT) {
+            float4* po = reinterpret_cast<float4*>(out + base + t_first);
+#pragma unroll
+            for (int h = 0; h < MB_VPT / 4; ++h)
+                __stcs(po + h, make_float4(res[4 * h], res[4 * h + 1], res[4 * h + 2], res[4 * h + 3]));
+        } else {
+#pragma unroll
+            for (int s2 = 0; s2 < MB_VPT; ++s2)
+                if (s2 < nvalid) __stcs(out + base + t_first + s2, res[s2]);
+        }
+        __syncthreads();   // s_lam and s_warp are reused by the next tile
+    }
+    // after an abort, wait (bounded) for copies still in flight into this CTA
+    if (s_abort && tid == 0) {
+        for (long long k = i; k < i + MP_STAGES && k < ntiles; ++k)
+            mbar_wait(&full[k % MP_STAGES], static_cast<uint32_t>((k / MP_STAGES) & 1), wait_ns);
+    }
+}
+
 template <bool VEC, bool LB>
 cudaError_t launch(const float* a, const float* b, const float* c, const float* d,
                    const float* lam0, float* out, long long T, long long tps, long long tiles,
@@ -250,12 +399,33 @@ cudaError_t launch(const float* a, const float* b, const float* c, const float* 
 
 }  // namespace
 
+// Resident CTA slots of the sequence-per-CTA kernel on the current device
+// (SMs x CTAs per SM); -1 on a CUDA error.
+int mobius_seq_slots() {
+    static int occ_cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    if (occ_cache[dev] == 0) {
+        const int smem = mp_smem_bytes();
+        if (cudaFuncSetAttribute(mobius_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mobius_seq_kernel, MB_THREADS, smem) !=
+            cudaSuccess)
+            return -1;
+        occ_cache[dev] = n > 0 ? n : 1;
+    }
+    return sm_count() * occ_cache[dev];
+}
+
 void mobius_plan(long long N, long long T, int* kernels, size_t* scratch) {
     const long long tps = (T + MB_TILE - 1) / MB_TILE;
     const long long tiles = N * tps;
     *kernels = (N > 0 && T > 0) ? 1 : 0;
     *scratch = 0;
-    if (tps > 1) {
+    const int slots = (T % 4 == 0) ? mobius_seq_slots() : -1;
+    if (tps > 1 && !(slots > 0 && N >= slots)) {
         const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
         *scratch = zero_bytes + 16 * static_cast<size_t>(tiles) + 4 * tiles;
     }
@@ -274,7 +444,11 @@ kdn_status mobius_launch(const float* a, const float* b, const float* c, const f
     LookbackScratch sc{nullptr, nullptr, nullptr, nullptr};
     void* scratch = nullptr;
     cudaError_t e;
-    if (tps > 1) {
+    const bool lookback = tps > 1;
+    const int slots = vec ? mobius_seq_slots() : 0;
+    if (slots < 0) return KDN_ERR_CUDA;
+    const bool use_seq = vec && N >= slots;
+    if (lookback && !use_seq) {
         // [ticket u64][flags u32 x tiles] (zeroed) | [agg float4 x tiles][pre f32 x tiles]
         const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
         const size_t bytes = zero_bytes + 16 * static_cast<size_t>(tiles) + 4 * tiles;
@@ -290,17 +464,22 @@ kdn_status mobius_launch(const float* a, const float* b, const float* c, const f
             cudaFreeAsync(scratch, stream);
             return from_cuda(e);
         }
-        e = vec ? launch<true, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns,
-                                     stall_tile)
-                : launch<false, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
-                                      wait_ns, stall_tile);
+    }
+    if (use_seq) {
+        // many sequences: one persistent CTA per resident slot, each owning whole sequences
+        mobius_seq_kernel<<<static_cast<unsigned>(slots), MB_THREADS, mp_smem_bytes(), stream>>>(
+            a, b, c, d, lambda0, out, N, T, tps, wait_ns);
+        e = cudaGetLastError();
+    } else if (lookback) {
+        e = vec ? launch<true, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, stall_tile)
+                : launch<false, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, stall_tile);
+    } else {
+        e = vec ? launch<true, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1)
+                : launch<false, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, -1);
+    }
+    if (scratch) {
         const cudaError_t ef = cudaFreeAsync(scratch, stream);
         if (e == cudaSuccess) e = ef;
-    } else {
-        e = vec ? launch<true, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
-                                      wait_ns, -1)
-                : launch<false, false>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream,
-                                       wait_ns, -1);
     }
     return from_cuda(e);
 }

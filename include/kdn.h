@@ -108,8 +108,11 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
  *   N >= 0, T >= 0, N*T < 2^62; pointers 4-byte aligned (16-byte alignment
  *   with T % 4 == 0 enables the vector path).
  *
- * Uses stream-ordered scratch (cudaMallocAsync) for the cross-block
- * look-back; returns KDN_ERR_ALLOC if it cannot be had.
+ * With fewer sequences than the GPU holds resident CTAs, tiles of 2048 steps
+ * are chained by a cross-block look-back that uses stream-ordered scratch
+ * (cudaMallocAsync; KDN_ERR_ALLOC if it cannot be had).  With more (and T %
+ * 4 == 0, 16-byte aligned buffers), each persistent CTA owns whole sequences
+ * and no scratch is taken.
  */
 KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* c,
                            const float* d, const float* lambda0, float* out,
@@ -128,7 +131,9 @@ KDN_API kdn_status kdn_diag_scan_plan(int B, int H, int T, int dk, int dv, kdn_d
 /*
  * kdn_mobius_scan_plan -- kernels one kdn_mobius_scan call launches and the
  * scratch bytes it takes (plus one cudaMemsetAsync of part of the scratch
- * when scratch_bytes > 0).  Host arithmetic only.
+ * when scratch_bytes > 0), for 16-byte aligned buffers on the current device
+ * (the choice between the look-back and the sequence-per-CTA kernel depends
+ * on the device's resident CTA count).
  */
 KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
                                         long long* scratch_bytes);

@@ -18,6 +18,17 @@ def test_random(N, T):
     parity.check_mobius(a, b, c, d, lam0)
 
 
+@pytest.mark.parametrize("N,T", [(400, 4096), (700, 5000), (350, 100), (333, 2048)])
+def test_many_sequences(N, T):
+    # more sequences than resident CTAs: each persistent CTA owns whole
+    # sequences (tiles streamed by TMA, lambda carried from tile to tile)
+    from bayesian_scan_gb300 import kdn
+    assert kdn.mobius_scan_plan(N, T)["scratch_bytes"] == 0
+    a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=N + T)
+    lam0 = lam0 * torch.linspace(0.5, 2.0, N)
+    parity.check_mobius(a, b, c, d, lam0)
+
+
 def test_small_workload():
     inp = workloads.make("small")
     parity.check_mobius(inp["ma"], inp["mb"], inp["mc"], inp["md"], inp["lam0"])
