@@ -22,7 +22,8 @@
 // multiply is exact).  The readout divides per element:
 //     mu q = sigma * q_j Ew / (sigma Jw + sigma W I_prior),  sigma = 2^-24,
 // where sigma centres the scaled denominators on 1 so that products of two
-// of them stay in range.  Pairs of quotients may share one reciprocal,
+// of them stay in range (the row sum is scaled back by sigma).  Pairs of
+// quotients may share one reciprocal,
 // n1/d1 + n2/d2 = (n1 d2 + n2 d1) / (d1 d2), which trades one MUFU op for one
 // FP32 op; PAIRS of the 4 column-pair groups of a lane row are combined that
 // way to balance the FMA pipe (128 lanes/clk/SM) against the MUFU pipe
@@ -41,9 +42,10 @@
 //     ahead (no warp ever blocks on stage reuse);
 //   * one chunk ahead of its compute, every warp converts its share of the
 //     next chunk's tokens k -> (k, k^2) and q to fp32 in a bank-conflict-free
-//     interleaved layout, and arrives on the chunk's "params ready" barrier;
-//   * every lane runs the per-head scale recursion (W_t, f_t) itself inside
-//     the token loop (one exp2f per token).
+//     interleaved layout, and one warp (rotating with the chunk) runs the
+//     per-head scale recursion (W_t, f_t) over the chunk's tokens; lanes then
+//     read (f_t, W_t, sigma W_t I_prior) with one shared load per token; all
+//     arrive on the chunk's "params ready" barrier.
 // All waits are bounded by GPU time and record KDN_ERR_TIMEOUT instead of
 // blocking forever.
 // Long sequences with few heads are split into P token ranges (parts): an
@@ -482,25 +484,12 @@ diag_scan_kernel(const Params p) {
         const TIn* rv = raw_v(s, hl) + i0;
         const TIn* rb = raw_b(s, hl) + i0;
         const float* pbase = par(s, hl);
-        // per-token scalars and row values, loaded one token ahead
-        float4 nsc = *reinterpret_cast<const float4*>(pbase + 3 * DK);
-        float nbet[RT], nval[RT];
-        load4(rb, nbet);
-        load4(rv, nval);
         for (int tt = 0; tt < tcn; ++tt) {
             const float* pt = pbase + tt * PF;
-            const float4 sc = nsc;
+            const float4 sc = *reinterpret_cast<const float4*>(pt + 3 * DK);
             float bet[RT], val[RT];
-#pragma unroll
-            for (int r = 0; r < RT; ++r) {
-                bet[r] = nbet[r];
-                val[r] = nval[r];
-            }
-            if (tt + 1 < tcn) {
-                nsc = *reinterpret_cast<const float4*>(pt + PF + 3 * DK);
-                load4(rb + (tt + 1) * dv, nbet);
-                load4(rv + (tt + 1) * dv, nval);
-            }
+            load4(rb + tt * dv, bet);
+            load4(rv + tt * dv, val);
             if (sc.x != 1.f) {                       // exact power-of-two rescale
                 const float2 f22 = f2(sc.x);
 #pragma unroll
