@@ -403,10 +403,13 @@ diag_scan_kernel(const Params p) {
                 int R = r_state[lane];
                 const TIn* rd = raw_d(s, lane);
                 float* ps = par(s, lane) + 3 * DK;
+                uint32_t mask = 0;   // tokens of the chunk that rescale the state
                 for (int tt = 0; tt < tcn; ++tt) {
                     const float f = scale_step(Ah * to_f32<TIn>(rd[tt]) * LOG2E, W, R);
                     *reinterpret_cast<float4*>(ps + tt * PF) = make_float4(f, W, W * Ip * SIGMA, 0.f);
+                    if (f != 1.f) mask |= 1u << tt;
                 }
+                ps[3] = __uint_as_float(mask);   // 4th scalar of the chunk's first token
                 w_state[lane] = W;
                 r_state[lane] = R;
             }
@@ -484,14 +487,15 @@ diag_scan_kernel(const Params p) {
         const TIn* rv = raw_v(s, hl) + i0;
         const TIn* rb = raw_b(s, hl) + i0;
         const float* pbase = par(s, hl);
-        for (int tt = 0; tt < tcn; ++tt) {
-            const float* pt = pbase + tt * PF;
-            const float4 sc = *reinterpret_cast<const float4*>(pt + 3 * DK);
-            float bet[RT], val[RT];
-            load4(rb + tt * dv, bet);
-            load4(rv + tt * dv, val);
-            if (sc.x != 1.f) {                       // exact power-of-two rescale
-                const float2 f22 = f2(sc.x);
+        // Tokens run in segments between rescaling tokens, so that the token
+        // loop itself has no branch; the segment breaks are the union over
+        // the warp's heads (a lane whose head does not rescale multiplies by 1).
+        const uint32_t mask = __reduce_or_sync(
+            0xffffffffu, active ? __float_as_uint(pbase[3 * DK + 3]) : 0u);
+        int tt = 0;
+        while (tt < tcn) {
+            if ((mask >> tt) & 1u) {                 // exact power-of-two rescale
+                const float2 f22 = f2(pbase[tt * PF + 3 * DK]);
 #pragma unroll
                 for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -500,6 +504,14 @@ diag_scan_kernel(const Params p) {
                         E[r][c2] = __fmul2_rn(E[r][c2], f22);
                     }
             }
+            const uint32_t later = mask >> (tt + 1);   // tt + 1 <= TC <= 16
+            const int stop = later ? min(tcn, tt + __ffs(later)) : tcn;
+        for (; tt < stop; ++tt) {
+            const float* pt = pbase + tt * PF;
+            const float4 sc = *reinterpret_cast<const float4*>(pt + 3 * DK);
+            float bet[RT], val[RT];
+            load4(rb + tt * dv, bet);
+            load4(rv + tt * dv, val);
             W = sc.y;
             float2 SB[RT], SBV[RT];
 #pragma unroll
@@ -576,6 +588,7 @@ diag_scan_kernel(const Params p) {
                     for (int u = 0; u < RowReduce<M>::NV; ++u) __stcs(o + row_out[u], val_out[u] * SIGMA);
                 }
             }
+        }
         }
         // the warp that finishes this chunk last refills the stage
         __syncwarp();
