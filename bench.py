@@ -40,9 +40,10 @@ HBM_GBS_FALLBACK = 6800.0
 DIAG_FLOP_PER_ELEMENT_TOKEN = 10
 MOBIUS_BYTES_PER_STEP = 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one full-pass diagonal-scan
-# launch on the default workload, from the ncu capture summarised in
-# profiles/; None until a capture of the current kernel exists.
-DIAG_TRAFFIC_BYTES = None
+# launch per workload, from the ncu capture of the current kernel summarised
+# in profiles/ (diag_scan_kernel_layer750m.md); workloads without a capture
+# of the current kernel report null.
+DIAG_TRAFFIC_BYTES = {"layer750m": 538_091_776 + 244_662_528}
 
 
 def parse_args():
@@ -337,7 +338,7 @@ def run_ours(args, w, dist):
         "config": workload_config(w),
         "roofline": {"kernel": "diag_scan_kernel (whole kdn_diag_scan_fwd call)", "bound": "alu",
                      "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak, "traffic": DIAG_TRAFFIC_BYTES,
+                     "frac": achieved / alu_peak, "traffic": DIAG_TRAFFIC_BYTES.get(w.name),
                      "peak_source": f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz"
                                     " (recipe unit counts and max SM clock)",
                      "ms_per_call": diag_ms, "token_parts": plan["parts"]},
