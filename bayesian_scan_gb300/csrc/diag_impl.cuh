@@ -70,7 +70,7 @@ constexpr int RT = 4;            // rows per lane
 constexpr int CW = 16;           // columns per lane
 constexpr int NSTAGE = 3;        // chunks in flight
 constexpr int ROWS_PER_CTA = 128;
-constexpr int PAIRS = 2;         // of the 4 column-pair groups of a lane row, how many share reciprocals
+constexpr int PAIRS = 3;         // of the 4 column-pair groups of a lane row, how many share reciprocals
 constexpr float SIGMA = 5.9604644775390625e-08f;   // 2^-24
 constexpr float W_LIMIT = 281474976710656.0f;      // 2^48
 constexpr float LOG2E = 1.4426950408889634f;

@@ -11,22 +11,26 @@
 // power of two (its largest entry into [1, 2)), which removes overflow and
 // underflow without rounding.
 //
-// Kernel layout (one CTA = one tile of 2048 consecutive steps of a sequence):
-//   1. each thread loads 8 consecutive steps (two float4 per coefficient
-//      array) and composes them sequentially;
-//   2. a warp-shuffle inclusive scan composes the 32 per-thread matrices;
-//   3. warp totals meet in shared memory for the block-level carry;
-//   4. tiles of the same sequence are chained with a decoupled look-back:
-//      a tile publishes its aggregate matrix as soon as it is known, then
-//      walks back over predecessors (composing aggregates) until it finds a
-//      published inclusive value lambda, and publishes its own inclusive
-//      lambda.  Tiles are numbered by an atomic ticket so that every tile's
-//      predecessors were scheduled before it; every wait on a flag is bounded
-//      by GPU time and records KDN_ERR_TIMEOUT instead of hanging;
-//   5. each thread evaluates its 8 outputs sequentially from the lambda at
-//      its first step (the exclusive prefix applied to the tile's carry).
+// Two kernels:
+//  * mobius_scan_kernel (few sequences, or rows that are not 16-byte
+//    aligned): one CTA per tile of 2048 consecutive steps of a sequence.
+//    1. each thread loads 8 consecutive steps and composes them in order;
+//    2. a warp-shuffle inclusive scan composes the 32 per-thread matrices;
+//    3. warp totals meet in shared memory for the block-level carry;
+//    4. tiles of the same sequence are chained with a decoupled look-back: a
+//       tile publishes its aggregate matrix as soon as it is known, then walks
+//       back over predecessors (composing aggregates) until it finds a
+//       published inclusive value lambda, and publishes its own inclusive
+//       lambda.  Tiles are numbered by an atomic ticket so that every tile's
+//       predecessors were scheduled before it; every wait on a flag is
+//       bounded by GPU time and records KDN_ERR_TIMEOUT instead of hanging;
+//    5. each thread evaluates its 8 outputs sequentially from the lambda at
+//       its first step (the exclusive prefix applied to the tile's carry).
+//  * mobius_seq_kernel (at least as many sequences as resident CTAs): a
+//    persistent CTA owns whole sequences and streams their tiles (described
+//    at the kernel).
 // Memory traffic is the algorithmic minimum (16 B in, 4 B out per step); the
-// kernel is bound by HBM bandwidth.
+// kernels are bound by HBM bandwidth once the sequences fill the GPU.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -64,13 +68,15 @@ __device__ __forceinline__ Mat mul(const Mat& L, const Mat& R) {
     return o;
 }
 
-// Scale by an exact power of two so that the largest |entry| lies in [1, 2).
-// Zero, denormal-only or non-finite matrices are left alone.
+// Scale by an exact power of two so that the largest |entry| lies in [1, 2):
+// the factor is built from the exponent field of the largest magnitude.  A
+// zero matrix stays zero; a largest entry at or above 2^126 is brought into
+// [1, 4) (the factor stays a normal number); infinities stay infinite and
+// NaN propagates through the products.
 __device__ __forceinline__ Mat normalize(const Mat& m) {
     const float mx = fmaxf(fmaxf(fabsf(m.a), fabsf(m.b)), fmaxf(fabsf(m.c), fabsf(m.d)));
-    const int e = exponent_of(mx);
-    if (e <= -127 || e >= 128 || e == 0) return m;
-    const float s = pow2i(e > 126 ? -126 : -e);
+    const uint32_t e = min(__float_as_uint(mx) & 0x7f800000u, 0x7e800000u);   // biased exponent E <= 253
+    const float s = __uint_as_float(0x7f000000u - e);                           // 2^(127 - E)
     return {m.a * s, m.b * s, m.c * s, m.d * s};
 }
 
@@ -240,105 +246,132 @@ mobius_scan_kernel(const float* __restrict__ A, const float* __restrict__ B,
 }
 
 // ---------------------------------------------------------------------------
-// Sequence-per-CTA variant for many sequences with 16-byte aligned rows
-// (T % 4 == 0, N at least the number of resident CTAs): a persistent grid
-// (about two CTAs per SM) gives CTA b the sequences b, b + G, b + 2G, ...
-// (G = grid size) and walks their tiles in order, carrying lambda from tile
-// to tile in shared memory, so no cross-CTA look-back (and no scratch) is
-// needed.  The coefficients of the next MP_STAGES - 1 tiles of its stream are
-// kept in flight with 1-D bulk TMA copies (one per coefficient array,
-// completing on an mbarrier) while the current tile is scanned, which keeps
-// HBM busy.  Few long sequences use the one-tile-per-CTA look-back kernel.
-constexpr int MP_STAGES = 3;
-constexpr int MP_STAGE_FLOATS = 4 * MB_TILE;
+// Sequence-per-CTA kernel for 16-byte aligned rows (T % 4 == 0), chosen by
+// mobius_choose_seq (many sequences, or short ones).  A persistent grid of at
+// most SQ_CTAS_PER_SM CTAs per SM gives CTA b the sequences b, b + G, b + 2G,
+// ... (G = grid size) and walks their tiles in order, so no cross-CTA
+// look-back (and no scratch) is needed:
+//   * the coefficients of the next SQ_STAGES - 1 tiles of the CTA's stream are
+//     in flight as 1-D bulk TMA copies (one per coefficient array, completing
+//     on an mbarrier) while the current tile is scanned;
+//   * each of the 256 threads owns 8 consecutive steps: it composes them as a
+//     balanced tree, a warp-shuffle scan and the 8 warp totals give its
+//     exclusive prefix, and it evaluates its 8 outputs sequentially from the
+//     lambda at its first step;
+//   * lambda at the start of the next tile is the last output of this one
+//     (the last thread's final step), so consecutive tiles continue exactly
+//     from the value that was written.
+// Two barriers per tile; the per-tile shared words (warp totals, carried
+// lambda) are double-buffered by tile parity.
+constexpr int SQ_THREADS = 256;
+constexpr int SQ_WARPS = SQ_THREADS / 32;
+constexpr int SQ_VPT = 8;                           // steps per thread
+constexpr int SQ_TILE = SQ_THREADS * SQ_VPT;        // 2048 steps
+constexpr int SQ_STAGES = 2;
+constexpr int SQ_CTAS_PER_SM = 3;
+constexpr int SQ_STAGE_FLOATS = 4 * SQ_TILE;
+static_assert(SQ_TILE == MB_TILE, "both kernels count tiles of the same length");
+static_assert((SQ_VPT & (SQ_VPT - 1)) == 0 && SQ_VPT % 4 == 0, "tree composition of float4 groups");
 
-__host__ __device__ constexpr int mp_smem_bytes() { return MP_STAGES * MP_STAGE_FLOATS * 4 + MP_STAGES * 8; }
+__host__ __device__ constexpr int sq_smem_bytes() { return SQ_STAGES * SQ_STAGE_FLOATS * 4 + SQ_STAGES * 8; }
 
-__global__ void __launch_bounds__(MB_THREADS)
+__global__ void __launch_bounds__(SQ_THREADS, SQ_CTAS_PER_SM)
 mobius_seq_kernel(const float* __restrict__ A, const float* __restrict__ B,
                   const float* __restrict__ C, const float* __restrict__ D,
                   const float* __restrict__ lambda0, float* __restrict__ out, long long N,
-                  long long T, long long tiles_per_seq, long long wait_ns) {
+                  long long T, int tiles_per_seq, long long wait_ns) {
     extern __shared__ __align__(128) unsigned char smem[];
     float* buf = reinterpret_cast<float*>(smem);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + MP_STAGES * MP_STAGE_FLOATS * 4);
-    __shared__ Mat s_warp[MB_WARPS];
-    __shared__ float s_lam;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SQ_STAGES * SQ_STAGE_FLOATS * 4);
+    __shared__ Mat s_warp[2][SQ_WARPS];
+    __shared__ float s_lam[2];
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long G = gridDim.x;
-    // number of tiles in this CTA's stream
     const long long nseq = blockIdx.x < N ? (N - 1 - blockIdx.x) / G + 1 : 0;
     const long long ntiles = nseq * tiles_per_seq;
-    auto tile_seq = [&](long long i) { return blockIdx.x + (i / tiles_per_seq) * G; };
 
-    // bulk copies of stream tile i into stage st (thread 0)
-    auto issue = [&](int st, long long i) {
-        const long long seq = tile_seq(i), part = i % tiles_per_seq;
-        const long long t0 = part * MB_TILE;
-        const long long n = min(static_cast<long long>(MB_TILE), T - t0);
+    // producer state (thread 0): next stream tile to issue
+    long long iss_i = 0, iss_seq = blockIdx.x;
+    int iss_part = 0, iss_st = 0;
+    auto issue_next = [&]() {
+        const long long t0 = static_cast<long long>(iss_part) * SQ_TILE;
+        const long long n = min(static_cast<long long>(SQ_TILE), T - t0);
         const uint32_t bytes = static_cast<uint32_t>(n * 4);
-        const long long off = seq * T + t0;
-        float* dst = buf + st * MP_STAGE_FLOATS;
+        const long long off = iss_seq * T + t0;
+        float* dst = buf + iss_st * SQ_STAGE_FLOATS;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&full[st], 4 * bytes);
-        bulk_g2s(dst, A + off, bytes, &full[st]);
-        bulk_g2s(dst + MB_TILE, B + off, bytes, &full[st]);
-        bulk_g2s(dst + 2 * MB_TILE, C + off, bytes, &full[st]);
-        bulk_g2s(dst + 3 * MB_TILE, D + off, bytes, &full[st]);
+        mbar_arrive_expect_tx(&full[iss_st], 4 * bytes);
+        bulk_g2s(dst, A + off, bytes, &full[iss_st]);
+        bulk_g2s(dst + SQ_TILE, B + off, bytes, &full[iss_st]);
+        bulk_g2s(dst + 2 * SQ_TILE, C + off, bytes, &full[iss_st]);
+        bulk_g2s(dst + 3 * SQ_TILE, D + off, bytes, &full[iss_st]);
+        ++iss_i;
+        if (++iss_part == tiles_per_seq) { iss_part = 0; iss_seq += G; }
+        if (++iss_st == SQ_STAGES) iss_st = 0;
     };
 
     if (tid == 0) {
-        for (int st = 0; st < MP_STAGES; ++st) mbar_init(&full[st], 1);
+        for (int st = 0; st < SQ_STAGES; ++st) mbar_init(&full[st], 1);
         mbar_init_fence();
-        for (int st = 0; st < MP_STAGES && st < ntiles; ++st) issue(st, st);
+        while (iss_i < SQ_STAGES && iss_i < ntiles) issue_next();
         s_abort = 0;
     }
     __syncthreads();
 
+    long long seq = blockIdx.x;
+    int part = 0, st = 0;
+    uint32_t phase = 0;
     long long i = 0;
     for (; i < ntiles; ++i) {
-        if (s_abort) break;
-        const int st = static_cast<int>(i % MP_STAGES);
-        if (!mbar_wait(&full[st], static_cast<uint32_t>((i / MP_STAGES) & 1), wait_ns)) {
+        const int par = static_cast<int>(i & 1);
+        if (!mbar_wait(&full[st], phase, wait_ns)) {
             record_error(&g_mobius_error, KDN_ERR_TIMEOUT);
             s_abort = 1;
         }
-        const long long seq = tile_seq(i), part = i % tiles_per_seq;
-        const long long t_first = part * MB_TILE + static_cast<long long>(tid) * MB_VPT;
-        const long long base = seq * T;
-        const int nvalid = static_cast<int>(max(0LL, min(static_cast<long long>(MB_VPT), T - t_first)));
+        const long long t_first = static_cast<long long>(part) * SQ_TILE + tid * SQ_VPT;
+        const int nvalid = static_cast<int>(max(0LL, min(static_cast<long long>(SQ_VPT), T - t_first)));
 
-        // ---- 1. this thread's 8 steps from shared memory ---------------
-        float ca[MB_VPT], cb[MB_VPT], cc[MB_VPT], cd[MB_VPT];
+        // ---- 1. this thread's 16 steps from shared memory ----------------
+        Mat m[SQ_VPT];
         {
-            const float* sb = buf + st * MP_STAGE_FLOATS + tid * MB_VPT;
+            const float* sb = buf + st * SQ_STAGE_FLOATS + tid * SQ_VPT;
 #pragma unroll
-            for (int h = 0; h < MB_VPT / 4; ++h) {
+            for (int h = 0; h < SQ_VPT / 4; ++h) {
                 const float4 x = *reinterpret_cast<const float4*>(sb + 4 * h);
-                const float4 y = *reinterpret_cast<const float4*>(sb + MB_TILE + 4 * h);
-                const float4 z = *reinterpret_cast<const float4*>(sb + 2 * MB_TILE + 4 * h);
-                const float4 w = *reinterpret_cast<const float4*>(sb + 3 * MB_TILE + 4 * h);
-                ca[4 * h + 0] = x.x; ca[4 * h + 1] = x.y; ca[4 * h + 2] = x.z; ca[4 * h + 3] = x.w;
-                cb[4 * h + 0] = y.x; cb[4 * h + 1] = y.y; cb[4 * h + 2] = y.z; cb[4 * h + 3] = y.w;
-                cc[4 * h + 0] = z.x; cc[4 * h + 1] = z.y; cc[4 * h + 2] = z.z; cc[4 * h + 3] = z.w;
-                cd[4 * h + 0] = w.x; cd[4 * h + 1] = w.y; cd[4 * h + 2] = w.z; cd[4 * h + 3] = w.w;
+                const float4 y = *reinterpret_cast<const float4*>(sb + SQ_TILE + 4 * h);
+                const float4 z = *reinterpret_cast<const float4*>(sb + 2 * SQ_TILE + 4 * h);
+                const float4 w = *reinterpret_cast<const float4*>(sb + 3 * SQ_TILE + 4 * h);
+                m[4 * h + 0] = {x.x, y.x, z.x, w.x};
+                m[4 * h + 1] = {x.y, y.y, z.y, w.y};
+                m[4 * h + 2] = {x.z, y.z, z.z, w.z};
+                m[4 * h + 3] = {x.w, y.w, z.w, w.w};
             }
 #pragma unroll
-            for (int s2 = 0; s2 < MB_VPT; ++s2)
-                if (s2 >= nvalid) {          // past the end of the sequence: identity steps
-                    ca[s2] = 1.f; cb[s2] = 0.f; cc[s2] = 0.f; cd[s2] = 1.f;
-                }
+            for (int s2 = 0; s2 < SQ_VPT; ++s2)
+                if (s2 >= nvalid) m[s2] = identity();   // past the end of the sequence
         }
-        __syncthreads();   // stage consumed: refill it with stream tile i + MP_STAGES
-        if (tid == 0 && i + MP_STAGES < ntiles && !s_abort) issue(st, i + MP_STAGES);
+        __syncthreads();   // stage consumed: refill it with the next stream tile
+        // s_abort is only set during the waits above (before this barrier) or
+        // in the next tile's waits (after the barrier below): all threads read
+        // the same value here
+        if (s_abort) break;
+        if (tid == 0 && iss_i < ntiles) issue_next();
+        // lambda at the start of the tile: lambda_0 for the first tile of a
+        // sequence, else the last output of the previous tile (written after
+        // the previous tile's second barrier)
+        const float lam_start = part == 0 ? __ldg(lambda0 + seq) : s_lam[par];
 
-        // ---- 2. compose and scan ---------------------------------------
-        Mat P = {ca[0], cb[0], cc[0], cd[0]};
+        // ---- 2. compose (balanced tree, later steps on the left) and scan --
+        Mat tree[SQ_VPT];
 #pragma unroll
-        for (int s2 = 1; s2 < MB_VPT; ++s2) P = normalize(mul(Mat{ca[s2], cb[s2], cc[s2], cd[s2]}, P));
-        P = normalize(P);
+        for (int k = 0; k < SQ_VPT; ++k) tree[k] = m[k];
+#pragma unroll
+        for (int w = SQ_VPT; w > 1; w /= 2)
+#pragma unroll
+            for (int k = 0; k < w / 2; ++k) tree[k] = normalize(mul(tree[2 * k + 1], tree[2 * k]));
+        Mat P = tree[0];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const Mat Q = shfl_up(P, off);
@@ -346,45 +379,39 @@ mobius_seq_kernel(const float* __restrict__ A, const float* __restrict__ B,
         }
         Mat lane_excl = shfl_up(P, 1);
         if (lane == 0) lane_excl = identity();
-        if (lane == 31) s_warp[warp] = P;
+        if (lane == 31) s_warp[par][warp] = P;
         __syncthreads();
         Mat warp_excl = identity();
-        for (int w = 0; w < warp; ++w) warp_excl = normalize(mul(s_warp[w], warp_excl));
+        for (int w = 0; w < warp; ++w) warp_excl = normalize(mul(s_warp[par][w], warp_excl));
         const Mat thread_excl = normalize(mul(lane_excl, warp_excl));
-        // lambda at the start of the tile: lambda_0 for the first tile of a
-        // sequence, else the carry left by the previous tile
-        const float lam_start = part == 0 ? __ldg(lambda0 + seq) : s_lam;
-        __syncthreads();   // every thread has read s_lam and s_warp
-        if (tid == 0) {
-            Mat agg = identity();
-            for (int w = 0; w < MB_WARPS; ++w) agg = normalize(mul(s_warp[w], agg));
-            s_lam = apply(agg, lam_start);                // carry for the next tile
-        }
 
-        // ---- 3. outputs ----------------------------------------------------
+        // ---- 3. outputs ------------------------------------------------------
         float lam = apply(thread_excl, lam_start);
-        float res[MB_VPT];
+        float res[SQ_VPT];
 #pragma unroll
-        for (int s2 = 0; s2 < MB_VPT; ++s2) {
-            lam = __fdividef(fmaf(ca[s2], lam, cb[s2]), fmaf(cc[s2], lam, cd[s2]));
+        for (int s2 = 0; s2 < SQ_VPT; ++s2) {
+            lam = __fdividef(fmaf(m[s2].a, lam, m[s2].b), fmaf(m[s2].c, lam, m[s2].d));
             res[s2] = lam;
         }
-        if (nvalid == MB_VPT) {
-            float4* po = reinterpret_cast<float4*>(out + base + t_first);
+        if (tid == SQ_THREADS - 1) s_lam[par ^ 1] = lam;   // carry (unused after a sequence's last tile)
+        float* po = out + seq * T + t_first;
+        if (nvalid == SQ_VPT) {
 #pragma unroll
-            for (int h = 0; h < MB_VPT / 4; ++h)
-                __stcs(po + h, make_float4(res[4 * h], res[4 * h + 1], res[4 * h + 2], res[4 * h + 3]));
+            for (int h = 0; h < SQ_VPT / 4; ++h)
+                __stcs(reinterpret_cast<float4*>(po) + h,
+                       make_float4(res[4 * h], res[4 * h + 1], res[4 * h + 2], res[4 * h + 3]));
         } else {
 #pragma unroll
-            for (int s2 = 0; s2 < MB_VPT; ++s2)
-                if (s2 < nvalid) __stcs(out + base + t_first + s2, res[s2]);
+            for (int s2 = 0; s2 < SQ_VPT; ++s2)
+                if (s2 < nvalid) __stcs(po + s2, res[s2]);
         }
-        __syncthreads();   // s_lam and s_warp are reused by the next tile
+        if (++part == tiles_per_seq) { part = 0; seq += G; }
+        if (++st == SQ_STAGES) { st = 0; phase ^= 1u; }
     }
-    // after an abort, wait (bounded) for copies still in flight into this CTA
+    // after an abort, wait (bounded) for the copies still in flight into this CTA
     if (s_abort && tid == 0) {
-        for (long long k = i; k < i + MP_STAGES && k < ntiles; ++k)
-            mbar_wait(&full[k % MP_STAGES], static_cast<uint32_t>((k / MP_STAGES) & 1), wait_ns);
+        for (long long k = i; k < iss_i; ++k)
+            mbar_wait(&full[k % SQ_STAGES], static_cast<uint32_t>((k / SQ_STAGES) & 1), wait_ns);
     }
 }
 
@@ -406,17 +433,35 @@ int mobius_seq_slots() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
     if (occ_cache[dev] == 0) {
-        const int smem = mp_smem_bytes();
+        const int smem = sq_smem_bytes();
         if (cudaFuncSetAttribute(mobius_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mobius_seq_kernel, MB_THREADS, smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mobius_seq_kernel, SQ_THREADS, smem) !=
             cudaSuccess)
             return -1;
         occ_cache[dev] = n > 0 ? n : 1;
     }
     return sm_count() * occ_cache[dev];
+}
+
+// Whether a scan of N sequences x tps tiles runs on the sequence-per-CTA
+// kernel (needs 16-byte aligned rows).  It takes no scratch and no look-back,
+// but each CTA walks its tiles one after another.  It is chosen when every
+// resident CTA has sequences to stream; for fewer sequences the two kernels'
+// costs are compared with a model fitted to GB300 timings (microseconds): the
+// walk costs about 3.5 + 1.6 tps; the look-back kernel about 9 + 0.0224 per
+// tile of the grid + 0.31 per look-back hop, and never less than 19 (scratch
+// allocation, flag clearing and release on the stream).  Single-tile
+// sequences need no look-back and stay on the tile kernel.
+bool mobius_choose_seq(long long N, long long tps, bool vec, int slots) {
+    if (!vec || slots <= 0 || tps < 2) return false;
+    if (N >= slots) return true;
+    const double n = static_cast<double>(N), t = static_cast<double>(tps);
+    const double walk = 3.5 + 1.6 * t;
+    const double lookback = fmax(19.0, 9.0 + 0.0224 * n * t + 0.31 * t);
+    return walk <= lookback;
 }
 
 void mobius_plan(long long N, long long T, int* kernels, size_t* scratch) {
@@ -425,7 +470,7 @@ void mobius_plan(long long N, long long T, int* kernels, size_t* scratch) {
     *kernels = (N > 0 && T > 0) ? 1 : 0;
     *scratch = 0;
     const int slots = (T % 4 == 0) ? mobius_seq_slots() : -1;
-    if (tps > 1 && !(slots > 0 && N >= slots)) {
+    if (tps > 1 && !mobius_choose_seq(N, tps, T % 4 == 0, slots)) {
         const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
         *scratch = zero_bytes + 16 * static_cast<size_t>(tiles) + 4 * tiles;
     }
@@ -447,7 +492,7 @@ kdn_status mobius_launch(const float* a, const float* b, const float* c, const f
     const bool lookback = tps > 1;
     const int slots = vec ? mobius_seq_slots() : 0;
     if (slots < 0) return KDN_ERR_CUDA;
-    const bool use_seq = vec && N >= slots;
+    const bool use_seq = mobius_choose_seq(N, tps, vec, slots);
     if (lookback && !use_seq) {
         // [ticket u64][flags u32 x tiles] (zeroed) | [agg float4 x tiles][pre f32 x tiles]
         const size_t zero_bytes = (8 + 4 * static_cast<size_t>(tiles) + 15) & ~size_t(15);
@@ -467,8 +512,10 @@ kdn_status mobius_launch(const float* a, const float* b, const float* c, const f
     }
     if (use_seq) {
         // many sequences: one persistent CTA per resident slot, each owning whole sequences
-        mobius_seq_kernel<<<static_cast<unsigned>(slots), MB_THREADS, mp_smem_bytes(), stream>>>(
-            a, b, c, d, lambda0, out, N, T, tps, wait_ns);
+        // one persistent CTA per resident slot (at most one per sequence)
+        mobius_seq_kernel<<<static_cast<unsigned>(min(static_cast<long long>(slots), N)), SQ_THREADS,
+                            sq_smem_bytes(), stream>>>(a, b, c, d, lambda0, out, N, T,
+                                                       static_cast<int>(tps), wait_ns);
         e = cudaGetLastError();
     } else if (lookback) {
         e = vec ? launch<true, true>(a, b, c, d, lambda0, out, T, tps, tiles, sc, stream, wait_ns, stall_tile)
@@ -552,6 +599,14 @@ kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c,
                      aligned16(d) && aligned16(out);
     LookbackScratch sc{nullptr, nullptr, nullptr, nullptr};
     cudaError_t e;
+    const int slots = vec ? mobius_seq_slots() : 0;
+    if (slots < 0) return KDN_ERR_CUDA;
+    if (mobius_choose_seq(N, tps, vec, slots)) {   // no scratch at all
+        mobius_seq_kernel<<<static_cast<unsigned>(min(static_cast<long long>(slots), N)), SQ_THREADS,
+                            sq_smem_bytes(), stream>>>(a, b, c, d, lambda0, out, N, T,
+                                                       static_cast<int>(tps), wait_ns);
+        return from_cuda(cudaGetLastError());
+    }
     if (tps > 1) {
         if (tiles > mobius_noalloc_max_tiles()) return KDN_ERR_INVALID_ARG;
         void* base = nullptr;

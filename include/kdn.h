@@ -108,11 +108,14 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
  *   N >= 0, T >= 0, N*T < 2^62; pointers 4-byte aligned (16-byte alignment
  *   with T % 4 == 0 enables the vector path).
  *
- * With fewer sequences than the GPU holds resident CTAs, tiles of 2048 steps
- * are chained by a cross-block look-back that uses stream-ordered scratch
- * (cudaMallocAsync; KDN_ERR_ALLOC if it cannot be had).  With more (and T %
- * 4 == 0, 16-byte aligned buffers), each persistent CTA owns whole sequences
- * and no scratch is taken.
+ * Sequences are cut into tiles of 2048 steps.  With T % 4 == 0 and 16-byte
+ * aligned buffers, multi-tile sequences normally run on persistent CTAs that
+ * each own whole sequences, with no scratch.  A few long sequences (too few
+ * to fill the GPU, each long enough that walking it tile by tile costs more
+ * than a look-back) and unaligned rows instead chain the tiles of a sequence
+ * by a cross-block look-back that uses stream-ordered scratch
+ * (cudaMallocAsync; KDN_ERR_ALLOC if it cannot be had).  kdn_mobius_scan_plan
+ * tells which for given sizes.
  */
 KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* c,
                            const float* d, const float* lambda0, float* out,
@@ -148,10 +151,11 @@ KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
  * Same arguments, layouts and results as kdn_mobius_scan.  The look-back
  * scratch lives in a fixed 1 MiB array inside the library's device image,
  * which every GPU that loads the library holds until the process exits; no
- * cudaMalloc/cudaMallocAsync/cudaFree is called.  Limit: a sequence longer
- * than 2048 steps needs look-back scratch, and then N * ceil(T / 2048) may be
- * at most 43690 (e.g. 4096 sequences of 16384 steps use 32768); larger calls
- * return KDN_ERR_INVALID_ARG without launching.  The first call on a device fetches the array's device address
+ * cudaMalloc/cudaMallocAsync/cudaFree is called.  Limit: when kdn_mobius_scan
+ * would take scratch (its plan reports scratch_bytes > 0), N * ceil(T / 2048)
+ * may be at most 43690; larger calls return KDN_ERR_INVALID_ARG without
+ * launching.  Calls that kdn_mobius_scan runs without scratch have no limit.
+ * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one array: calls whose executions overlap on the GPU
  * (for example on two streams) race and give wrong results; serialise them.

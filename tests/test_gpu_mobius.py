@@ -1,6 +1,7 @@
 """Moebius scan: CUDA path vs the fp64 oracle, over single and multi-tile
-sequences (decoupled look-back), ragged tails, the scalar path, closed
-forms, and a host-injected stall that must end in KDN_ERR_TIMEOUT."""
+sequences (decoupled look-back and sequence-per-CTA kernels), ragged tails,
+the scalar path, closed forms, and a host-injected stall that must end in
+KDN_ERR_TIMEOUT."""
 import numpy as np
 import pytest
 import torch
@@ -18,10 +19,11 @@ def test_random(N, T):
     parity.check_mobius(a, b, c, d, lam0)
 
 
-@pytest.mark.parametrize("N,T", [(400, 4096), (700, 5000), (350, 100), (333, 2048)])
+@pytest.mark.parametrize("N,T", [(400, 4096), (700, 5000), (350, 100), (333, 2048), (500, 12288),
+                                 (100, 8192)])
 def test_many_sequences(N, T):
-    # more sequences than resident CTAs: each persistent CTA owns whole
-    # sequences (tiles streamed by TMA, lambda carried from tile to tile)
+    # many or short sequences: each persistent CTA owns whole sequences
+    # (tiles streamed by TMA, lambda carried from tile to tile), no scratch
     from bayesian_scan_gb300 import kdn
     assert kdn.mobius_scan_plan(N, T)["scratch_bytes"] == 0
     a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=N + T)
@@ -71,7 +73,8 @@ def test_unaligned_scalar_path():
 
 def test_stalled_tile_times_out_and_recovers():
     from bayesian_scan_gb300 import kdn
-    N, T = 2, 3 * 2048
+    N, T = 2, 16 * 2048                        # few long sequences: look-back kernel
+    assert kdn.mobius_scan_plan(N, T)["scratch_bytes"] > 0
     a, b, c, d, lam0 = workloads.draw_mobius(N, T, seed=1)
     dev = [x.cuda() for x in (a, b, c, d, lam0)]
     assert kdn.get_device_error() == 0

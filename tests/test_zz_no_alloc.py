@@ -38,7 +38,9 @@ def _rel(x, ref):
 def test_noalloc_matches_allocating_entry_point_twice():
     from bayesian_scan_gb300 import kdn
     lib = kdn.lib
-    for call, (N, T, seed) in enumerate([(48, 9000, 21), (37, 16384, 22)]):
+    # two look-back calls in a row (unaligned rows; few long sequences), then
+    # one that the sequence-per-CTA kernel runs without any scratch
+    for call, (N, T, seed) in enumerate([(48, 9001, 21), (5, 30000, 22), (600, 6144, 23)]):
         a, b, c, d, lam0 = (x.cuda() for x in workloads.draw_mobius(N, T, seed=seed))
         ref = kdn.mobius_scan(a, b, c, d, lam0)
         out = torch.full_like(ref, float("nan"))
@@ -52,7 +54,8 @@ def test_noalloc_matches_allocating_entry_point_twice():
 
 def test_noalloc_refuses_more_tiles_than_the_array_holds():
     from bayesian_scan_gb300 import kdn
-    N, T = kdn.MOBIUS_NOALLOC_MAX_TILES // 2 + 1, 4096      # 2 tiles per sequence
+    # T % 4 != 0 keeps the call on the look-back kernel: 3 tiles per sequence
+    N, T = kdn.MOBIUS_NOALLOC_MAX_TILES // 3 + 1, 4097
     x = torch.zeros(N, T, device="cuda")
     lam0 = torch.ones(N, device="cuda")
     out = torch.full((N, T), -7.0, device="cuda")
