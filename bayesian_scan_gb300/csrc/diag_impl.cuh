@@ -33,9 +33,12 @@
 // recurrence; only the readout reduces over j.  A CTA owns 128 consecutive
 // state rows (whole heads: 128/d_v of them) for a token range and keeps them
 // in registers for the whole range.  It has d_k/16 warps; a lane holds 4 rows
-// x 16 columns (64 elements, 128 fp32 registers) and the d_k/16 lanes of a
-// row set reduce the readout with shuffles.  There is no producer warp (a
-// ninth warp would cap registers at 168 per thread); instead:
+// x 16 columns (64 elements, 128 fp32 registers).  The readout's row sums
+// over the d_k/16 lanes of a row set go through shared memory: each lane
+// stores its 4 row partials every token, and every RB tokens the warp adds
+// the partials of each row and writes whole 16-byte row quads (no shuffle
+// latency on the token loop).  There is no producer warp (a ninth warp would
+// cap registers at 168 per thread); instead:
 //   * q, k, v, beta, d of each chunk of TC tokens are brought into shared
 //     memory by 1-D bulk TMA copies that complete on an mbarrier; the warp
 //     that finishes a chunk last refills its stage with the chunk three
@@ -74,6 +77,20 @@ constexpr int PAIRS = 3;         // of the 4 column-pair groups of a lane row, h
 constexpr float SIGMA = 5.9604644775390625e-08f;   // 2^-24
 constexpr float W_LIMIT = 281474976710656.0f;      // 2^48
 constexpr float LOG2E = 1.4426950408889634f;
+// Readout reduction through shared memory: every token each lane stores its 4
+// row partials; every RB tokens the warp sums the column groups of each row
+// and stores whole 16-byte row quads.
+constexpr int RB = 8;
+
+// Floats one token's row partials take in a warp's reduction buffer, laid
+// out [row set][column group][4 rows]: a row set takes 4 M + 4 floats and the
+// token 16 (mod 32) more than a multiple of 32, so that the 16-byte stores of
+// a quarter warp and the summing reads of consecutive row sets and tokens
+// fall on different banks.  m = lanes per row set (d_k / 16).
+__host__ __device__ constexpr int red_rs_stride(int m) { return 4 * m + 4; }
+__host__ __device__ constexpr int red_token_stride(int m) {
+    return (32 / m) * red_rs_stride(m) + (16 - ((32 / m) * red_rs_stride(m)) % 32 + 32) % 32;
+}
 
 struct AggScale {
     float W;   // working scale at the end of the part (zero start, W = 1 at its start)
@@ -126,10 +143,14 @@ struct Layout {
     }
 };
 
+// per warp: RB tokens of row partials
+__host__ __device__ constexpr int red_bytes_per_warp(int dk) { return RB * red_token_stride(dk / CW) * 4; }
+
 __host__ __device__ inline int smem_bytes(int dk, int dv, int es, int TC) {
     const int hpc = ROWS_PER_CTA / dv;
     Layout L(dk, dv, es, TC, hpc);
-    return NSTAGE * L.stage + 2 * NSTAGE * 8 + NSTAGE * 4 + 2 * hpc * 4;
+    const int nw = dk / CW;   // warps per CTA
+    return NSTAGE * L.stage + nw * red_bytes_per_warp(dk) + 2 * NSTAGE * 8 + NSTAGE * 4 + 2 * hpc * 4;
 }
 
 // one error word per translation unit that instantiates these kernels
@@ -171,85 +192,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-
-// Reduce-scatter of 4 row partials over the M lanes of a row set.  On return
-// `val[0..NV)` hold complete sums for rows `row[0..NV)` (indices 0..3) and
-// `store` says whether this lane writes them.
-template <int M>
-struct RowReduce;
-
-template <>
-struct RowReduce<8> {
-    static constexpr int NV = 1;
-    __device__ __forceinline__ static void run(const float p[4], int cg, float val[1], int row[1],
-                                               bool& store) {
-        const bool up = cg & 4;
-        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
-        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
-        const bool up2 = cg & 2;
-        float kk = up2 ? k1 : k0;
-        const float s = up2 ? k0 : k1;
-        kk += __shfl_xor_sync(0xffffffffu, s, 2);
-        kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-        val[0] = kk;
-        row[0] = (up ? 2 : 0) + (up2 ? 1 : 0);
-        store = (cg & 1) == 0;
-    }
-};
-
-template <>
-struct RowReduce<4> {
-    static constexpr int NV = 1;
-    __device__ __forceinline__ static void run(const float p[4], int cg, float val[1], int row[1],
-                                               bool& store) {
-        const bool up = cg & 2;
-        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
-        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-        const bool up2 = cg & 1;
-        float kk = up2 ? k1 : k0;
-        const float s = up2 ? k0 : k1;
-        kk += __shfl_xor_sync(0xffffffffu, s, 1);
-        val[0] = kk;
-        row[0] = (up ? 2 : 0) + (up2 ? 1 : 0);
-        store = true;
-    }
-};
-
-template <>
-struct RowReduce<2> {
-    static constexpr int NV = 2;
-    __device__ __forceinline__ static void run(const float p[4], int cg, float val[2], int row[2],
-                                               bool& store) {
-        const bool up = cg & 1;
-        float k0 = up ? p[2] : p[0], k1 = up ? p[3] : p[1];
-        const float s0 = up ? p[0] : p[2], s1 = up ? p[1] : p[3];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-        val[0] = k0;
-        val[1] = k1;
-        row[0] = up ? 2 : 0;
-        row[1] = row[0] + 1;
-        store = true;
-    }
-};
-
-template <>
-struct RowReduce<1> {
-    static constexpr int NV = 4;
-    __device__ __forceinline__ static void run(const float p[4], int, float val[4], int row[4],
-                                               bool& store) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            val[r] = p[r];
-            row[r] = r;
-        }
-        store = true;
-    }
-};
 
 // The per-head scale recursion for one token (see the header comment):
 // returns f_t = 2^-r_t and updates (W, R).  x = A d / ln 2.
@@ -298,7 +240,9 @@ diag_scan_kernel(const Params p) {
 
     const int dv = p.dv, HPC = ROWS_PER_CTA / dv, TC = p.TC;
     const Layout L(DK, dv, ES, TC, HPC);
-    uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + NSTAGE * L.stage);
+    constexpr int RSS = red_rs_stride(M), RTS = red_token_stride(M);
+    float* red_all = reinterpret_cast<float*>(smem + NSTAGE * L.stage);   // [NW][RB][RTS]
+    uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + NSTAGE * L.stage + NW * red_bytes_per_warp(DK));
     uint64_t* full_par = full_raw + NSTAGE;
     int* done_cnt = reinterpret_cast<int*>(full_par + NSTAGE);
     float* w_state = reinterpret_cast<float*>(done_cnt + NSTAGE);   // [HPC] scale W per head
@@ -479,6 +423,35 @@ diag_scan_kernel(const Params p) {
 
     float W = 1.f;
     float* gout = p.out;
+    float* red = red_all + warp * (RB * RTS);
+    // Sum the row partials of tokens t_first .. t_first + ntok - 1 (slots
+    // 0 .. ntok-1) over the M column groups and store them: a work item is one
+    // token and one row set (4 consecutive rows) of this warp.
+    auto flush = [&](int t_first, int ntok) {
+        constexpr int QUADS = G::RS;   // row sets per warp
+        __syncwarp();
+        for (int g = lane; g < ntok * QUADS; g += 32) {
+            const int ts = g / QUADS, qd = g - ts * QUADS;
+            const float* src = red + ts * RTS + qd * RSS;
+            const float4 x0 = *reinterpret_cast<const float4*>(src);
+            float2 lo = make_float2(x0.x, x0.y), hi = make_float2(x0.z, x0.w);
+#pragma unroll
+            for (int c = 1; c < M; ++c) {
+                const float4 x = *reinterpret_cast<const float4*>(src + 4 * c);
+                lo = __fadd2_rn(lo, make_float2(x.x, x.y));
+                hi = __fadd2_rn(hi, make_float2(x.z, x.w));
+            }
+            const int crow_q = warp * G::WR + RT * qd;         // CTA row of the row set
+            const int hq = crow_q / dv, iq = crow_q - hq * dv;
+            if (hq < nheads) {
+                lo = __fmul2_rn(lo, f2(SIGMA));
+                hi = __fmul2_rn(hi, f2(SIGMA));
+                float* o = gout + ((head0 + hq) * T + t_first + ts) * dv + iq;
+                __stcs(reinterpret_cast<float4*>(o), make_float4(lo.x, lo.y, hi.x, hi.y));
+            }
+        }
+        __syncwarp();
+    };
     for (int c = 0; c < nchunks; ++c) {
         const int s = c % NSTAGE;
         if (!mbar_wait(&full_par[s], (c / NSTAGE) & 1, p.wait_ns)) ok = false;
@@ -575,18 +548,11 @@ diag_scan_kernel(const Params p) {
                 }
             }
             if (!AGG) {
-                float rowsum[RT];
-#pragma unroll
-                for (int r = 0; r < RT; ++r) rowsum[r] = acc[r].x + acc[r].y;
-                float val_out[RowReduce<M>::NV];
-                int row_out[RowReduce<M>::NV];
-                bool st;
-                RowReduce<M>::run(rowsum, cg, val_out, row_out, st);
-                if (st && active) {
-                    float* o = gout + (bh * T + t0 + tt) * dv + i0;
-#pragma unroll
-                    for (int u = 0; u < RowReduce<M>::NV; ++u) __stcs(o + row_out[u], val_out[u] * SIGMA);
-                }
+                const int slot = tt & (RB - 1);
+                *reinterpret_cast<float4*>(red + slot * RTS + rs * RSS + 4 * cg) =
+                    make_float4(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y,
+                                acc[3].x + acc[3].y);
+                if (slot == RB - 1 || tt == tcn - 1) flush(t0 + tt - slot, slot + 1);
             }
         }
         }
