@@ -1,0 +1,294 @@
+// diag_agg_tc.cuh -- the aggregate pass of a token-split diagonal scan on the
+// tensor cores (d_k = d_v = 128, bf16 inputs).
+//
+// When a long sequence is split into token parts, each part p < P-1 needs
+// only its end state from a zero start ("Learning to Remember, Learn, and
+// Forget in Attention-Based Models", Metodologia 2, unrolled over the part):
+//     Delta J[i][j]   = sum_t w_t beta_t[i] k_t[j]^2
+//     Delta eta[i][j] = sum_t w_t beta_t[i] v_t[i] k_t[j],
+//     w_t = prod_{s > t in the part} alpha_s = 2^-(sum_{s>t} A d_s log2 e),
+// plus the part's total decay prod alpha = 2^-L.  Both sums are dense
+// contractions over the part's tokens, [d_v x T_p] x [T_p x d_k]: here they
+// run as tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor
+// memory), K = 32 tokens per chunk.
+//
+// Precision.  k is a bf16 input, so k is exact in bf16 and k^2 (at most 16
+// significant bits) is exactly hi + lo of two bf16.  The weighted row
+// factors w beta and w beta v are split the same way (hi = bf16(x), lo =
+// bf16(x - hi), relative error about 2^-16).  Delta J takes three products
+// (hi*hi2 + hi*lo2 + lo*hi2) and Delta eta two (hi*k + lo*k), all
+// accumulated in fp32.  The decay exponents are summed in fp64 (the part's
+// suffix sums) and w_t = 2^-floor(S) * exp2(-frac(S)).
+//
+// Output: the same (J_w, eta_w) = W (Delta J, Delta eta) and (W, R) with
+// 2^-R / W = 2^-L, W in [1, 2), that the CUDA-core aggregate pass leaves for
+// the carry kernel.
+//
+// Per CTA: one (head, part); 256 threads.  Chunks of the part are visited
+// from the last to the first (so the suffix sums accumulate): warp 0 computes
+// the chunk's w_t, all threads build the 7 operand tiles (128 x 32 bf16 each,
+// core-matrix layout) from the raw chunk (k, beta, v, brought in by 1-D bulk
+// copies two chunks ahead), one thread issues the 10 MMAs of the chunk and
+// commits them to an mbarrier; operand tiles are double-buffered on that
+// barrier.  All waits are bounded by GPU time.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kdn_device.cuh"
+
+namespace kdn {
+namespace diag {
+namespace {
+
+constexpr int AG_KC = 32;                          // tokens per chunk
+constexpr int AG_THREADS = 256;
+constexpr int AG_D = 128;                          // d_k = d_v
+constexpr int AG_TILE = AG_D * AG_KC * 2;          // one 128 x 32 bf16 operand tile, bytes
+constexpr int AG_NTILE = 7;                        // A_J hi/lo, A_E hi/lo, B_k, B_k2 hi/lo
+constexpr int AG_OPS = AG_NTILE * AG_TILE;         // one operand buffer
+constexpr int AG_RAW = AG_KC * AG_D * 2;           // one raw array (k, beta or v) of a chunk
+constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta in [128,256)
+// core-matrix strides of an operand tile (K-major, no swizzle)
+constexpr uint32_t AG_LBO = 128;                   // next 8 tokens (K)
+constexpr uint32_t AG_SBO = (AG_KC / 8) * 128;     // next 8 rows (M or N)
+
+__host__ __device__ constexpr int agg_tc_smem_bytes() {
+    return 2 * AG_OPS + 2 * 3 * AG_RAW + 2 * AG_KC * 4 + 4 * 8 + 16;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// hi = bf16(x), lo = bf16(x - hi) as 16-bit patterns
+__device__ __forceinline__ void split_bf16(float x, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi = __bfloat16_as_ushort(h);
+    lo = bf16_bits(x - __bfloat162float(h));
+}
+
+// 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
+// exp2 of the fractional part; 0 for S beyond the float range, NaN stays NaN.
+__device__ __forceinline__ float exp2_neg(double S) {
+    if (!(S < 1.0e9)) return S != S ? __int_as_float(0x7fc00000) : 0.f;
+    const double n = floor(S);
+    const float f = static_cast<float>(S - n);                  // [0, 1)
+    const int e = static_cast<int>(fmax(fmin(n, 300.0), -300.0));
+    return ldexpf(exp2f(-f), -e);
+}
+
+struct AggArgs {
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* beta;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* d;
+    const float* A;
+    float* agg;              // [P-1][BH][2][128][128]
+    AggScale* agg_scale;     // [P-1][BH]
+    long long BH;
+    int H, T;
+    int part_len;
+    long long wait_ns;
+};
+
+__global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArgs p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ops = smem;                                  // [2][7 tiles]
+    unsigned char* raw = smem + 2 * AG_OPS;                     // [2 stages][k, beta, v]
+    float* wbuf = reinterpret_cast<float*>(raw + 2 * 3 * AG_RAW);   // [2][KC]
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(wbuf + 2 * AG_KC);
+    uint64_t* mma_done = raw_full + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 2);
+    float* s_wend = reinterpret_cast<float*>(tmem_holder + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long bh = blockIdx.x;
+    const int part = blockIdx.y;
+    const int T = p.T;
+    const int tb = part * p.part_len;
+    const int te = min(T, tb + p.part_len);
+    const int nch = (te - tb + AG_KC - 1) / AG_KC;
+    const long long S = static_cast<long long>(AG_D) * AG_D;
+    bool ok = true;
+
+    // raw chunk of iteration `it` (chunk nch-1-it) into stage st (thread 0)
+    auto issue = [&](int it) {
+        const int st = it & 1;
+        const int c = nch - 1 - it;
+        const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
+        const uint32_t bytes = static_cast<uint32_t>(n * AG_D * 2);
+        const long long off = (bh * T + t0) * AG_D;
+        unsigned char* dst = raw + st * 3 * AG_RAW;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&raw_full[st], 3 * bytes);
+        bulk_g2s(dst, p.k + off, bytes, &raw_full[st]);
+        bulk_g2s(dst + AG_RAW, p.beta + off, bytes, &raw_full[st]);
+        bulk_g2s(dst + 2 * AG_RAW, p.v + off, bytes, &raw_full[st]);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&mma_done[i], 1);
+        }
+        mbar_init_fence();
+        for (int it = 0; it < 2 && it < nch; ++it) issue(it);
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, AG_TMEM_COLS);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    const float Ah = p.A[bh % p.H];
+    double Z = 0.0;   // warp 0: sum of the decay exponents of the tokens after the chunk
+    const int rho = tid & (AG_D - 1);       // operand row (A: value row i, B: key column j)
+    const int kp = tid >> 7;                // this thread's two groups of 8 tokens: 2kp, 2kp+1
+    constexpr uint32_t IDESC = umma_idesc_bf16_f32(AG_D, AG_D);
+
+    for (int it = 0; it < nch; ++it) {
+        const int st = it & 1, ob = it & 1;
+        const int c = nch - 1 - it;
+        const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
+        if (!mbar_wait(&raw_full[st], (it >> 1) & 1, p.wait_ns)) ok = false;
+        if (warp == 0) {
+            // w_t of the chunk's tokens (lane = token)
+            const bool valid = lane < n;
+            const float x = valid ? Ah * __bfloat162float(p.d[bh * T + t0 + lane]) * LOG2E : 0.f;
+            double P = x;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, P, off);
+                if (lane >= off) P += y;
+            }
+            const double tot = __shfl_sync(0xffffffffu, P, 31);
+            wbuf[st * AG_KC + lane] = valid ? exp2_neg(tot - P + Z) : 0.f;
+            Z += tot;
+        }
+        // the operand buffer was last read by the MMAs of iteration it - 2
+        if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
+        __syncthreads();
+
+        // ---- build the 7 operand tiles of this chunk --------------------
+        {
+            const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(raw + st * 3 * AG_RAW);
+            const __nv_bfloat16* rb = rk + AG_KC * AG_D;
+            const __nv_bfloat16* rv = rb + AG_KC * AG_D;
+            const float* w = wbuf + st * AG_KC;
+            unsigned char* o = ops + ob * AG_OPS;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int kg = 2 * kp + g;
+                uint32_t aj_hi[4], aj_lo[4], ae_hi[4], ae_lo[4], bk[4], bk2_hi[4], bk2_lo[4];
+#pragma unroll
+                for (int u2 = 0; u2 < 4; ++u2) {
+                    uint32_t h[7][2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = kg * 8 + 2 * u2 + e;
+                        const bool valid = tok < n;
+                        const float wt = w[tok];
+                        const float b = valid ? __bfloat162float(rb[tok * AG_D + rho]) : 0.f;
+                        const float vv = valid ? __bfloat162float(rv[tok * AG_D + rho]) : 0.f;
+                        const __nv_bfloat16 kb = valid ? rk[tok * AG_D + rho] : __float2bfloat16_rn(0.f);
+                        const float kf = __bfloat162float(kb);
+                        const float aj = wt * b;
+                        split_bf16(aj, h[0][e], h[1][e]);
+                        split_bf16(aj * vv, h[2][e], h[3][e]);
+                        h[4][e] = __bfloat16_as_ushort(kb);
+                        split_bf16(kf * kf, h[5][e], h[6][e]);
+                    }
+                    aj_hi[u2] = h[0][0] | (h[0][1] << 16);
+                    aj_lo[u2] = h[1][0] | (h[1][1] << 16);
+                    ae_hi[u2] = h[2][0] | (h[2][1] << 16);
+                    ae_lo[u2] = h[3][0] | (h[3][1] << 16);
+                    bk[u2] = h[4][0] | (h[4][1] << 16);
+                    bk2_hi[u2] = h[5][0] | (h[5][1] << 16);
+                    bk2_lo[u2] = h[6][0] | (h[6][1] << 16);
+                }
+                // core matrix (rho / 8, kg), row rho % 8
+                const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;
+                auto put = [&](int tile, const uint32_t x[4]) {
+                    *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) = make_uint4(x[0], x[1], x[2], x[3]);
+                };
+                put(0, aj_hi); put(1, aj_lo); put(2, ae_hi); put(3, ae_lo);
+                put(4, bk); put(5, bk2_hi); put(6, bk2_lo);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();   // operands written, raw stage consumed
+
+        if (tid == 0) {
+            if (it + 2 < nch) issue(it + 2);
+            tc_fence_after_sync();
+            const uint32_t base = smem_addr(ops + ob * AG_OPS);
+#pragma unroll
+            for (int s = 0; s < AG_KC / 16; ++s) {
+                auto desc = [&](int tile) {
+                    return umma_desc_kmajor(base + tile * AG_TILE + s * 2 * 128, AG_LBO, AG_SBO);
+                };
+                const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
+                umma_bf16(tmem, desc(0), desc(5), IDESC, first);           // J += A_J hi  B_k2 hi
+                umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);              //    + A_J hi  B_k2 lo
+                umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);              //    + A_J lo  B_k2 hi
+                umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, first);    // eta += A_E hi B_k
+                umma_bf16(tmem + AG_D, desc(3), desc(4), IDESC, 1u);       //      + A_E lo B_k
+            }
+            umma_commit(&mma_done[ob]);
+        }
+    }
+
+    // ---- end state and scale of the part -------------------------------------
+    if (nch > 0 && !mbar_wait(&mma_done[(nch - 1) & 1], ((nch - 1) >> 1) & 1, p.wait_ns)) ok = false;
+    if (tid == 0) {
+        // Z (thread 0 is in warp 0) = L, the part's total decay exponent
+        int R;
+        float W;
+        if (!(Z < 1073741824.0)) {                 // decays to 0 (or NaN): 2^-R underflows
+            R = 1 << 30;
+            W = 1.f;
+        } else if (!(Z > -1073741824.0)) {         // growth beyond any float
+            R = -(1 << 30);
+            W = 1.f;
+        } else {
+            const double fl = floor(Z);
+            R = static_cast<int>(fl);
+            W = exp2f(static_cast<float>(Z - fl));
+        }
+        *s_wend = W;
+        p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, R};
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    {
+        const float W = *s_wend;
+        const int q = warp & 3, half = warp >> 2;   // lane quarter, J (0) or eta (1)
+        const int row = 32 * q + lane;
+        float* dst = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S +
+                     static_cast<long long>(row) * AG_D;
+        for (int c0 = 0; c0 < AG_D; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * AG_D + c0, v);
+            if (nch == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + c0 + j) =
+                    make_float4(v[j] * W, v[j + 1] * W, v[j + 2] * W, v[j + 3] * W);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, AG_TMEM_COLS);
+    if (!ok) record_error(&g_diag_error, KDN_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace diag
+}  // namespace kdn

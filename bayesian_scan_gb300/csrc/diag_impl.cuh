@@ -60,6 +60,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kdn_device.cuh"
 #include "kdn_internal.h"
@@ -627,6 +628,17 @@ __global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* 
     }
 }
 
+}  // namespace
+}  // namespace diag
+}  // namespace kdn
+
+// the aggregate pass on the tensor cores (uses AggScale, LOG2E, g_diag_error)
+#include "diag_agg_tc.cuh"
+
+namespace kdn {
+namespace diag {
+namespace {
+
 // ---------------------------------------------------------------------------
 // host side
 
@@ -634,6 +646,22 @@ struct Cache {
     bool init[64] = {};
     int occ[64] = {};
 };
+
+// Opt the tensor-core aggregate kernel into its shared memory (once per device).
+cudaError_t agg_tc_prepare() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(diag_agg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 agg_tc_smem_bytes());
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
 
 template <int DK, typename TIn, bool AGG>
 cudaError_t prepare(int dev, int smem, int* occ) {
@@ -747,9 +775,23 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         if (e != cudaSuccess) return from_cuda(e);
         prm.agg = static_cast<float*>(scratch);
         prm.agg_scale = reinterpret_cast<AggScale*>(static_cast<char*>(scratch) + state_bytes);
-        diag_scan_kernel<DK, TIn, true>
-            <<<dim3(static_cast<unsigned>(ctas), P - 1), Geo<DK>::NTHREADS, smem, st>>>(prm);
-        e = cudaGetLastError();
+        bool on_tc = false;   // d_k = d_v = 128 with bf16 inputs: tensor-core aggregate pass
+        if constexpr (DK == 128 && std::is_same<TIn, __nv_bfloat16>::value) on_tc = dv == 128;
+        if (on_tc) {
+            e = agg_tc_prepare();
+            if (e == cudaSuccess) {
+                AggArgs ag{static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.beta),
+                           static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.d),
+                           a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, pl.part_len, wait_ns};
+                diag_agg_tc_kernel<<<dim3(static_cast<unsigned>(BH), P - 1), AG_THREADS,
+                                     agg_tc_smem_bytes(), st>>>(ag);
+                e = cudaGetLastError();
+            }
+        } else {
+            diag_scan_kernel<DK, TIn, true>
+                <<<dim3(static_cast<unsigned>(ctas), P - 1), Geo<DK>::NTHREADS, smem, st>>>(prm);
+            e = cudaGetLastError();
+        }
         if (e == cudaSuccess) {
             const long long n = BH * S;
             diag_carry_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(

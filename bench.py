@@ -43,7 +43,7 @@ MOBIUS_BYTES_PER_STEP = 20
 # launch per workload, from the ncu capture of the current kernel summarised
 # in profiles/ (diag_scan_kernel_layer750m.md); workloads without a capture
 # of the current kernel report null.
-DIAG_TRAFFIC_BYTES = {"layer750m": 538_091_776 + 244_662_528}
+DIAG_TRAFFIC_BYTES = {"layer750m": 538_256_384 + 244_887_296}
 
 
 def parse_args():

@@ -65,6 +65,30 @@ def test_token_split_path(T):
     parity.check_diag(draw(1, 2, T, 64, 64, A_law=("const", 1.0)))
 
 
+@pytest.mark.parametrize("law", [("const", 0.0), ("uniform", 0.1, 1.0), ("const", 30.0)])
+@pytest.mark.parametrize("T", [2048, 3001])
+def test_token_split_tensor_core_aggregates(law, T):
+    # d_k = d_v = 128 with bf16 inputs: the parts' end states come from the
+    # tensor-core aggregate pass (no decay, slow decay, decay that underflows;
+    # a ragged last chunk for T = 3001)
+    from bayesian_scan_gb300 import kdn
+    assert kdn.diag_scan_plan(1, 2, T, 128, 128)["parts"] > 1
+    parity.check_diag(draw(1, 2, T, 128, 128, A_law=law, seed=T))
+
+
+def test_token_split_tensor_core_aggregates_initial_state():
+    inp = draw(1, 1, 2600, 128, 128, A_law=("const", 0.02))
+    g = torch.Generator().manual_seed(10)
+    I0 = 0.5 + torch.rand(1, 1, 128, 128, generator=g)
+    mu0 = torch.randn(1, 1, 128, 128, generator=g)
+    parity.check_diag(inp, I0, mu0)
+
+
+def test_token_split_fp32_inputs_d128():
+    # fp32 inputs keep the CUDA-core aggregate pass
+    parity.check_diag(draw(1, 1, 2500, 128, 128, dtype=torch.float32, A_law=("uniform", 0.1, 1.0)))
+
+
 def test_token_split_with_initial_state():
     inp = draw(1, 1, 2500, 64, 64, A_law=("const", 0.05))
     g = torch.Generator().manual_seed(9)
