@@ -25,12 +25,14 @@
 // the carry kernel.
 //
 // Per CTA: one (head, part); 256 threads.  Chunks of the part are visited
-// from the last to the first (so the suffix sums accumulate): warp 0 computes
-// the chunk's w_t, all threads build the 7 operand tiles (128 x 32 bf16 each,
-// core-matrix layout) from the raw chunk (k, beta, v, brought in by 1-D bulk
-// copies two chunks ahead), one thread issues the 10 MMAs of the chunk and
-// commits them to an mbarrier; operand tiles are double-buffered on that
-// barrier.  All waits are bounded by GPU time.
+// from the last to the first (so the suffix sums accumulate).  The weights
+// w_t of 2048 tokens at a time are prepared by all threads (8 tokens each,
+// fp64 suffix sums across the CTA); per chunk all threads build the 7 operand
+// tiles (128 x 32 bf16 each, core-matrix layout) from the raw chunk (k, beta,
+// v, brought in by 1-D bulk copies two chunks ahead), then one thread issues
+// the 10 MMAs of the chunk and commits them to an mbarrier; operand tiles are
+// double-buffered on that barrier, so a chunk's MMAs run while the next is
+// built.  One CTA barrier per chunk; all waits are bounded by GPU time.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,19 +57,11 @@ constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta 
 constexpr uint32_t AG_LBO = 128;                   // next 8 tokens (K)
 constexpr uint32_t AG_SBO = (AG_KC / 8) * 128;     // next 8 rows (M or N)
 
+constexpr int AG_SUP = 2048;                       // tokens per super-chunk of decay weights
+static_assert(AG_SUP == 8 * AG_THREADS, "a thread prepares 8 weights of a super-chunk");
+
 __host__ __device__ constexpr int agg_tc_smem_bytes() {
-    return 2 * AG_OPS + 2 * 3 * AG_RAW + 2 * AG_KC * 4 + 4 * 8 + 16;
-}
-
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
-}
-
-// hi = bf16(x), lo = bf16(x - hi) as 16-bit patterns
-__device__ __forceinline__ void split_bf16(float x, uint32_t& hi, uint32_t& lo) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi = __bfloat16_as_ushort(h);
-    lo = bf16_bits(x - __bfloat162float(h));
+    return 2 * AG_OPS + 2 * 3 * AG_RAW + AG_SUP * 4 + 8 * 8 + 4 * 8 + 16;
 }
 
 // 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
@@ -78,6 +72,15 @@ __device__ __forceinline__ float exp2_neg(double S) {
     const float f = static_cast<float>(S - n);                  // [0, 1)
     const int e = static_cast<int>(fmax(fmin(n, 300.0), -300.0));
     return ldexpf(exp2f(-f), -e);
+}
+
+// (x0, x1) -> bf16x2 hi = rn(x), lo = rn(x - hi), low half = x0
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    const float b0 = __uint_as_float(hi << 16), b1 = __uint_as_float(hi & 0xffff0000u);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - b0, x1 - b1);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 struct AggArgs {
@@ -98,8 +101,9 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ops = smem;                                  // [2][7 tiles]
     unsigned char* raw = smem + 2 * AG_OPS;                     // [2 stages][k, beta, v]
-    float* wbuf = reinterpret_cast<float*>(raw + 2 * 3 * AG_RAW);   // [2][KC]
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(wbuf + 2 * AG_KC);
+    float* wsup = reinterpret_cast<float*>(raw + 2 * 3 * AG_RAW);   // [AG_SUP] weights of a super-chunk
+    double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [8] warp totals
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);
     uint64_t* mma_done = raw_full + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 2);
     float* s_wend = reinterpret_cast<float*>(tmem_holder + 1);
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     const long long S = static_cast<long long>(AG_D) * AG_D;
     bool ok = true;
 
-    // raw chunk of iteration `it` (chunk nch-1-it) into stage st (thread 0)
+    // raw chunk of iteration `it` (chunk nch-1-it) into stage it & 1 (thread 0)
     auto issue = [&](int it) {
         const int st = it & 1;
         const int c = nch - 1 - it;
@@ -144,78 +148,108 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     const uint32_t tmem = *tmem_holder;
 
     const float Ah = p.A[bh % p.H];
-    double Z = 0.0;   // warp 0: sum of the decay exponents of the tokens after the chunk
-    const int rho = tid & (AG_D - 1);       // operand row (A: value row i, B: key column j)
-    const int kp = tid >> 7;                // this thread's two groups of 8 tokens: 2kp, 2kp+1
+    double Z = 0.0;          // sum of the decay exponents of the tokens after the current super-chunk
+    int sup0 = tb;           // first token of the current super-chunk
+    const int pr = tid & 63;                // this thread's operand rows 2 pr, 2 pr + 1
+    const int kg = tid >> 6;                // and its group of 8 tokens of a chunk
     constexpr uint32_t IDESC = umma_idesc_bf16_f32(AG_D, AG_D);
 
     for (int it = 0; it < nch; ++it) {
         const int st = it & 1, ob = it & 1;
         const int c = nch - 1 - it;
         const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
-        if (!mbar_wait(&raw_full[st], (it >> 1) & 1, p.wait_ns)) ok = false;
-        if (warp == 0) {
-            // w_t of the chunk's tokens (lane = token)
-            const bool valid = lane < n;
-            const float x = valid ? Ah * __bfloat162float(p.d[bh * T + t0 + lane]) * LOG2E : 0.f;
-            double P = x;
+        if (it == 0 || ((c + 1) % (AG_SUP / AG_KC)) == 0) {
+            // ---- decay weights of this chunk's super-chunk: chunks
+            // [SC, SC + AG_SUP / AG_KC) of the part, SC a multiple of it, so
+            // super-chunks hold whole chunks.  Every thread passed the barrier
+            // after the last build that read wsup.
+            sup0 = tb + (c / (AG_SUP / AG_KC)) * AG_SUP;
+            const int s1 = min(te, sup0 + AG_SUP);
+            const int u0 = sup0 + 8 * tid;
+            double x[8], loc = 0.0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = u0 + u;
+                x[u] = t < s1 ? static_cast<double>(Ah * __bfloat162float(p.d[bh * T + t]) * LOG2E) : 0.0;
+                loc += x[u];
+            }
+            // exclusive suffix sum over the threads after this one
+            double suf = loc;      // inclusive suffix within the warp
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, P, off);
-                if (lane >= off) P += y;
+                const double y = __shfl_down_sync(0xffffffffu, suf, off);
+                if (lane + off < 32) suf += y;
             }
-            const double tot = __shfl_sync(0xffffffffu, P, 31);
-            wbuf[st * AG_KC + lane] = valid ? exp2_neg(tot - P + Z) : 0.f;
-            Z += tot;
+            if (lane == 0) wtot[warp] = suf;
+            __syncthreads();
+            double later = suf - loc;
+            double all = 0.0;
+#pragma unroll
+            for (int w = 0; w < AG_THREADS / 32; ++w) {
+                const double tw = wtot[w];
+                all += tw;
+                if (w > warp) later += tw;
+            }
+            later += Z;
+#pragma unroll
+            for (int u = 7; u >= 0; --u) {
+                wsup[8 * tid + u] = u0 + u < s1 ? exp2_neg(later) : 0.f;
+                later += x[u];
+            }
+            Z += all;
+            __syncthreads();   // weights ready; wtot may be reused
         }
+        if (!mbar_wait(&raw_full[st], (it >> 1) & 1, p.wait_ns)) ok = false;
         // the operand buffer was last read by the MMAs of iteration it - 2
         if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
-        __syncthreads();
 
-        // ---- build the 7 operand tiles of this chunk --------------------
+        // ---- build the 7 operand tiles of this chunk (rows 2pr, 2pr+1; tokens 8kg..8kg+7) ----
         {
-            const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(raw + st * 3 * AG_RAW);
-            const __nv_bfloat16* rb = rk + AG_KC * AG_D;
-            const __nv_bfloat16* rv = rb + AG_KC * AG_D;
-            const float* w = wbuf + st * AG_KC;
+            const unsigned char* rk = raw + st * 3 * AG_RAW;
+            const unsigned char* rb = rk + AG_RAW;
+            const unsigned char* rv = rb + AG_RAW;
+            const float* w = wsup + (t0 - sup0);
+            uint32_t t[7][2][4];   // [tile][row of the pair][4 x bf16x2 along the tokens]
+#pragma unroll
+            for (int u2 = 0; u2 < 4; ++u2) {
+                float aj[2][2], ae[2][2], kf[2][2];
+                uint32_t kbits[2][2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = kg * 8 + 2 * u2 + e;
+                    const bool valid = tok < n;
+                    const float wt = valid ? w[tok] : 0.f;
+                    const int o4 = (tok * AG_D + 2 * pr) * 2;
+                    const uint32_t bb = valid ? *reinterpret_cast<const uint32_t*>(rb + o4) : 0u;
+                    const uint32_t vv = valid ? *reinterpret_cast<const uint32_t*>(rv + o4) : 0u;
+                    const uint32_t kk = valid ? *reinterpret_cast<const uint32_t*>(rk + o4) : 0u;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float bf = __uint_as_float(r ? (bb & 0xffff0000u) : (bb << 16));
+                        const float vf = __uint_as_float(r ? (vv & 0xffff0000u) : (vv << 16));
+                        kbits[r][e] = r ? (kk >> 16) : (kk & 0xffffu);
+                        kf[r][e] = __uint_as_float(kbits[r][e] << 16);
+                        aj[r][e] = wt * bf;
+                        ae[r][e] = aj[r][e] * vf;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    split2(aj[r][0], aj[r][1], t[0][r][u2], t[1][r][u2]);
+                    split2(ae[r][0], ae[r][1], t[2][r][u2], t[3][r][u2]);
+                    t[4][r][u2] = kbits[r][0] | (kbits[r][1] << 16);
+                    split2(kf[r][0] * kf[r][0], kf[r][1] * kf[r][1], t[5][r][u2], t[6][r][u2]);
+                }
+            }
             unsigned char* o = ops + ob * AG_OPS;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int kg = 2 * kp + g;
-                uint32_t aj_hi[4], aj_lo[4], ae_hi[4], ae_lo[4], bk[4], bk2_hi[4], bk2_lo[4];
+            for (int r = 0; r < 2; ++r) {
+                const int rho = 2 * pr + r;
+                const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;   // core matrix (rho/8, kg)
 #pragma unroll
-                for (int u2 = 0; u2 < 4; ++u2) {
-                    uint32_t h[7][2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = kg * 8 + 2 * u2 + e;
-                        const bool valid = tok < n;
-                        const float wt = w[tok];
-                        const float b = valid ? __bfloat162float(rb[tok * AG_D + rho]) : 0.f;
-                        const float vv = valid ? __bfloat162float(rv[tok * AG_D + rho]) : 0.f;
-                        const __nv_bfloat16 kb = valid ? rk[tok * AG_D + rho] : __float2bfloat16_rn(0.f);
-                        const float kf = __bfloat162float(kb);
-                        const float aj = wt * b;
-                        split_bf16(aj, h[0][e], h[1][e]);
-                        split_bf16(aj * vv, h[2][e], h[3][e]);
-                        h[4][e] = __bfloat16_as_ushort(kb);
-                        split_bf16(kf * kf, h[5][e], h[6][e]);
-                    }
-                    aj_hi[u2] = h[0][0] | (h[0][1] << 16);
-                    aj_lo[u2] = h[1][0] | (h[1][1] << 16);
-                    ae_hi[u2] = h[2][0] | (h[2][1] << 16);
-                    ae_lo[u2] = h[3][0] | (h[3][1] << 16);
-                    bk[u2] = h[4][0] | (h[4][1] << 16);
-                    bk2_hi[u2] = h[5][0] | (h[5][1] << 16);
-                    bk2_lo[u2] = h[6][0] | (h[6][1] << 16);
-                }
-                // core matrix (rho / 8, kg), row rho % 8
-                const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;
-                auto put = [&](int tile, const uint32_t x[4]) {
-                    *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) = make_uint4(x[0], x[1], x[2], x[3]);
-                };
-                put(0, aj_hi); put(1, aj_lo); put(2, ae_hi); put(3, ae_lo);
-                put(4, bk); put(5, bk2_hi); put(6, bk2_lo);
+                for (int tile = 0; tile < AG_NTILE; ++tile)
+                    *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) =
+                        make_uint4(t[tile][r][0], t[tile][r][1], t[tile][r][2], t[tile][r][3]);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -244,7 +278,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     // ---- end state and scale of the part -------------------------------------
     if (nch > 0 && !mbar_wait(&mma_done[(nch - 1) & 1], ((nch - 1) >> 1) & 1, p.wait_ns)) ok = false;
     if (tid == 0) {
-        // Z (thread 0 is in warp 0) = L, the part's total decay exponent
+        // Z = L, the part's total decay exponent
         int R;
         float W;
         if (!(Z < 1073741824.0)) {                 // decays to 0 (or NaN): 2^-R underflows
