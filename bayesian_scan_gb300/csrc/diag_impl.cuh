@@ -687,6 +687,12 @@ cudaError_t prepare(int dev, int smem, int* occ) {
     return e;
 }
 
+// Whether a split call's aggregate pass runs on the tensor cores.
+template <int DK, typename TIn>
+constexpr bool tc_aggregates(int dv) {
+    return DK == AG_D && std::is_same<TIn, __nv_bfloat16>::value && dv == AG_D;
+}
+
 // Launch plan of one call: chunk length, token parts, scratch bytes.
 struct Plan {
     int TC = 16;
@@ -728,6 +734,33 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
         const long long maxp = a.T / (4 * TC);
         P = static_cast<int>(want < maxp ? want : maxp);
         if (P < 1) P = 1;
+    }
+    // Fill split.  With d_k = d_v = 128 and bf16 inputs the aggregate pass
+    // runs on the tensor cores and costs little, so when the CTAs leave SMs
+    // idle, shorter parts in several waves can finish sooner.  Estimate in
+    // full-pass token steps of one CTA: waves x part length, plus about 0.47
+    // per extra (head, part) (aggregate, carry and start-state traffic) and
+    // 23 for the two extra launches (fitted to GB300 timings of the 750M-shaped
+    // layer); taken when it saves more than 2 %.
+    if (P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas < slots && a.T >= 32 * TC) {
+        auto est = [&](int parts, int plen) {
+            const long long waves = (pl->ctas * parts + slots - 1) / slots;
+            return static_cast<double>(waves) * plen +
+                   (parts > 1 ? 23.0 + 0.47 * static_cast<double>(BH) * (parts - 1) : 0.0);
+        };
+        const double one = est(1, a.T);
+        double best = one;
+        for (int cand = 2; cand <= 32; ++cand) {
+            const int plen = ((a.T + cand - 1) / cand + TC - 1) / TC * TC;
+            if (plen < 8 * TC) break;
+            const int pe = (a.T + plen - 1) / plen;
+            const double e = est(pe, plen);
+            if (e < best) {
+                best = e;
+                P = pe;
+            }
+        }
+        if (!(best < 0.98 * one)) P = 1;
     }
     int part_len = a.T > 0 ? a.T : 1;
     if (P > 1) {
@@ -775,9 +808,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         if (e != cudaSuccess) return from_cuda(e);
         prm.agg = static_cast<float*>(scratch);
         prm.agg_scale = reinterpret_cast<AggScale*>(static_cast<char*>(scratch) + state_bytes);
-        bool on_tc = false;   // d_k = d_v = 128 with bf16 inputs: tensor-core aggregate pass
-        if constexpr (DK == 128 && std::is_same<TIn, __nv_bfloat16>::value) on_tc = dv == 128;
-        if (on_tc) {
+        if (tc_aggregates<DK, TIn>(dv)) {
             e = agg_tc_prepare();
             if (e == cudaSuccess) {
                 AggArgs ag{static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.beta),

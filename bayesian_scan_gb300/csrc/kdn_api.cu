@@ -73,6 +73,38 @@ kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v, const 
     return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
 }
 
+kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v, const void* beta,
+                                  const void* d, const float* A, float I_prior, const float* I0,
+                                  const float* mu0, float* out, float* final_state, int B, int H,
+                                  int T, int dk, int dv, kdn_dtype in_dtype, void* stream) {
+    if (B < 1 || H < 1 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !beta || !d || !A || !out)) return KDN_ERR_INVALID_ARG;
+    if (in_dtype != KDN_F32 && in_dtype != KDN_BF16) return KDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long dmax = dk > dv ? dk : dv;
+    if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / dmax) return KDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, beta, d, A, I0, mu0, out, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned(p, in_dtype == KDN_BF16 ? 2 : 4)) return KDN_ERR_INVALID_ARG;
+    DiagArgs a{q, k, v, beta, d, A, I_prior, I0, mu0, out, final_state, B, H, T, dk, dv, in_dtype};
+    return diag_host(a, static_cast<cudaStream_t>(stream), g_wait_ns.load());
+}
+
+kdn_status kdn_mobius_scan_host(const float* a, const float* b, const float* c, const float* d,
+                                const float* lambda0, float* out, long long N, long long T,
+                                void* stream) {
+    if (N < 0 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (N > 0 && T > 0 && N > (1LL << 62) / T) return KDN_ERR_INVALID_ARG;
+    if (N == 0 || T == 0) return KDN_OK;
+    if (!a || !b || !c || !d || !lambda0 || !out) return KDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {a, b, c, d, lambda0, out};
+    for (const void* p : ptrs)
+        if (!aligned(p, 4)) return KDN_ERR_INVALID_ARG;
+    return mobius_host(a, b, c, d, lambda0, out, N, T, static_cast<cudaStream_t>(stream),
+                       g_wait_ns.load());
+}
+
 kdn_status kdn_mobius_scan(const float* a, const float* b, const float* c, const float* d,
                            const float* lambda0, float* out, long long N, long long T,
                            void* stream) {

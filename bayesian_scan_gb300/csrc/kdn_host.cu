@@ -1,0 +1,295 @@
+// kdn_host.cu -- entry points that take every tensor in host memory
+// (kdn_diag_scan_fwd_host, kdn_mobius_scan_host).
+//
+// The work is cut into chunks that are pipelined over three streams: the
+// caller's stream runs the kernels, one internal stream copies chunk c+1's
+// inputs in while chunk c is scanned, another copies chunk c-1's outputs
+// out.  The diagonal scan is cut along the tokens (every head of a chunk
+// runs in one launch, so the GPU stays full) and carries the state from one
+// chunk to the next on the device through the scan's own final-state /
+// initial-state interface; the Moebius scan is cut along the sequences,
+// which are independent.  Host buffers should be page-locked for the copies
+// to run asynchronously; pageable memory works, with the copies serialised.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kdn.h"
+#include "kdn_internal.h"
+
+namespace kdn {
+namespace {
+
+constexpr int kMaxDev = 64;
+
+struct CopyStreams {
+    cudaStream_t in = nullptr;
+    cudaStream_t out = nullptr;
+};
+CopyStreams g_streams[kMaxDev];
+std::mutex g_streams_mu;
+
+// The two copy streams of the current device (created once per device).
+cudaError_t copy_streams(CopyStreams* cs) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_streams_mu);
+    CopyStreams& s = g_streams[dev];
+    if (!s.in) {
+        e = cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            cudaStreamDestroy(s.in);
+            s.in = nullptr;
+            return e;
+        }
+    }
+    *cs = s;
+    return cudaSuccess;
+}
+
+// Six events (in/compute/out for two chunk buffers), released on scope exit.
+struct ChunkEvents {
+    cudaEvent_t in[2] = {}, comp[2] = {}, out[2] = {}, start = nullptr;
+    cudaError_t create() {
+        cudaEvent_t* all[] = {&in[0], &in[1], &comp[0], &comp[1], &out[0], &out[1], &start};
+        for (cudaEvent_t* ev : all) {
+            const cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    ~ChunkEvents() {
+        cudaEvent_t all[] = {in[0], in[1], comp[0], comp[1], out[0], out[1], start};
+        for (cudaEvent_t ev : all)
+            if (ev) cudaEventDestroy(ev);
+    }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Tokens per chunk of a host-buffer diagonal scan: about eight chunks, at
+// least 512 tokens, a multiple of 16.
+int diag_chunk_tokens(int T) {
+    int tc = (T + 7) / 8;
+    tc = (tc + 15) / 16 * 16;
+    if (tc < 512) tc = 512;
+    return tc < T ? tc : T;
+}
+
+// Propagates the first error; keeps going so that every queued operation
+// stays ordered before the final free and synchronisation.
+struct Status {
+    cudaError_t e = cudaSuccess;
+    kdn_status k = KDN_OK;
+    void cuda(cudaError_t x) {
+        if (e == cudaSuccess && k == KDN_OK && x != cudaSuccess) e = x;
+    }
+    void kdn(kdn_status x) {
+        if (e == cudaSuccess && k == KDN_OK && x != KDN_OK) k = x;
+    }
+    bool ok() const { return e == cudaSuccess && k == KDN_OK; }
+    kdn_status result() const { return k != KDN_OK ? k : from_cuda(e); }
+};
+
+}  // namespace
+
+kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
+    const int B = h.B, H = h.H, T = h.T, dk = h.dk, dv = h.dv;
+    const size_t es = h.dtype == KDN_BF16 ? 2 : 4;
+    const long long BH = static_cast<long long>(B) * H;
+    const size_t S = static_cast<size_t>(dv) * dk;
+    const int Tc = T > 0 ? diag_chunk_tokens(T) : 0;
+    const int nc = T > 0 ? (T + Tc - 1) / Tc : 0;
+
+    CopyStreams cs;
+    cudaError_t e = copy_streams(&cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    ChunkEvents ev;
+    e = ev.create();
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // device layout: two chunk buffer sets, two carried states, A, I0, mu0
+    const size_t qk_b = align256(BH * static_cast<size_t>(Tc) * dk * es);
+    const size_t vb_b = align256(BH * static_cast<size_t>(Tc) * dv * es);
+    const size_t d_b = align256(BH * static_cast<size_t>(Tc) * es);
+    const size_t o_b = align256(BH * static_cast<size_t>(Tc) * dv * 4);
+    const size_t set_b = 2 * qk_b + 2 * vb_b + d_b + o_b;
+    const size_t st_b = align256(2 * BH * S * 4);
+    const size_t a_b = align256(static_cast<size_t>(H) * 4);
+    const size_t init_b = align256(BH * S * 4);
+    const size_t total = 2 * set_b + 2 * st_b + a_b + (h.I0 ? init_b : 0) + (h.mu0 ? init_b : 0);
+    char* base = nullptr;
+    e = cudaMallocAsync(reinterpret_cast<void**>(&base), total, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    auto set = [&](int b) { return base + b * set_b; };
+    char* state[2] = {base + 2 * set_b, base + 2 * set_b + st_b};
+    float* A_d = reinterpret_cast<float*>(base + 2 * set_b + 2 * st_b);
+    char* tail = base + 2 * set_b + 2 * st_b + a_b;
+    float* I0_d = h.I0 ? reinterpret_cast<float*>(tail) : nullptr;
+    float* mu0_d = h.mu0 ? reinterpret_cast<float*>(tail + (h.I0 ? init_b : 0)) : nullptr;
+
+    Status s;
+    if (T > 0) s.cuda(cudaMemcpyAsync(A_d, h.A, static_cast<size_t>(H) * 4, cudaMemcpyHostToDevice, st));
+    if (I0_d) s.cuda(cudaMemcpyAsync(I0_d, h.I0, BH * S * 4, cudaMemcpyHostToDevice, st));
+    if (mu0_d) s.cuda(cudaMemcpyAsync(mu0_d, h.mu0, BH * S * 4, cudaMemcpyHostToDevice, st));
+    // the copy streams start after the allocation
+    s.cuda(cudaEventRecord(ev.start, st));
+    s.cuda(cudaStreamWaitEvent(cs.in, ev.start, 0));
+    s.cuda(cudaStreamWaitEvent(cs.out, ev.start, 0));
+
+    const char* hq = static_cast<const char*>(h.q);
+    const char* hk = static_cast<const char*>(h.k);
+    const char* hv = static_cast<const char*>(h.v);
+    const char* hb = static_cast<const char*>(h.beta);
+    const char* hd = static_cast<const char*>(h.d);
+    for (int c = 0; c < nc && s.ok(); ++c) {
+        const int b = c & 1;
+        const int t0 = c * Tc, n = (T - t0 < Tc) ? T - t0 : Tc;
+        char* in = set(b);
+        char* dq = in;
+        char* dkp = in + qk_b;
+        char* dvp = in + 2 * qk_b;
+        char* dbp = in + 2 * qk_b + vb_b;
+        char* ddp = in + 2 * qk_b + 2 * vb_b;
+        float* dout = reinterpret_cast<float*>(in + 2 * qk_b + 2 * vb_b + d_b);
+        // inputs of chunk c (buffer b was last read by chunk c - 2)
+        if (c >= 2) s.cuda(cudaStreamWaitEvent(cs.in, ev.comp[b], 0));
+        auto rows_in = [&](char* dst, const char* src, size_t row_elems) {
+            const size_t w = static_cast<size_t>(n) * row_elems * es;
+            s.cuda(cudaMemcpy2DAsync(dst, w, src + static_cast<size_t>(t0) * row_elems * es,
+                                     static_cast<size_t>(T) * row_elems * es, w, BH,
+                                     cudaMemcpyHostToDevice, cs.in));
+        };
+        rows_in(dq, hq, dk);
+        rows_in(dkp, hk, dk);
+        rows_in(dvp, hv, dv);
+        rows_in(dbp, hb, dv);
+        rows_in(ddp, hd, 1);
+        s.cuda(cudaEventRecord(ev.in[b], cs.in));
+        // scan of chunk c from the state chunk c - 1 left
+        s.cuda(cudaStreamWaitEvent(st, ev.in[b], 0));
+        if (c >= 2) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
+        DiagArgs a = h;
+        a.q = dq;
+        a.k = dkp;
+        a.v = dvp;
+        a.beta = dbp;
+        a.d = ddp;
+        a.A = A_d;
+        if (c == 0) {
+            a.I0 = I0_d;
+            a.mu0 = mu0_d;
+        } else {
+            const float* prev = reinterpret_cast<const float*>(state[(c - 1) & 1]);
+            a.mu0 = prev;
+            a.I0 = prev + BH * S;
+        }
+        a.out = dout;
+        a.final_state = reinterpret_cast<float*>(state[c & 1]);
+        a.T = n;
+        if (s.ok()) s.kdn(a.dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns)
+                                              : diag_launch_f32(a, st, wait_ns));
+        s.cuda(cudaEventRecord(ev.comp[b], st));
+        // outputs of chunk c
+        s.cuda(cudaStreamWaitEvent(cs.out, ev.comp[b], 0));
+        const size_t w = static_cast<size_t>(n) * dv * 4;
+        s.cuda(cudaMemcpy2DAsync(h.out + static_cast<size_t>(t0) * dv, static_cast<size_t>(T) * dv * 4, dout, w,
+                                 w, BH, cudaMemcpyDeviceToHost, cs.out));
+        s.cuda(cudaEventRecord(ev.out[b], cs.out));
+    }
+    if (h.final_state && s.ok()) {
+        if (nc > 0) {
+            s.cuda(cudaMemcpyAsync(h.final_state, state[(nc - 1) & 1], 2 * BH * S * 4,
+                                   cudaMemcpyDeviceToHost, st));
+        } else {
+            // no tokens: the final state is the initial one
+            DiagArgs a = h;
+            a.A = A_d;
+            a.I0 = I0_d;
+            a.mu0 = mu0_d;
+            a.out = nullptr;
+            a.final_state = reinterpret_cast<float*>(state[0]);
+            a.T = 0;
+            s.kdn(a.dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns));
+            s.cuda(cudaMemcpyAsync(h.final_state, state[0], 2 * BH * S * 4, cudaMemcpyDeviceToHost, st));
+        }
+    }
+    // every copy is ordered before the release and the final synchronisation
+    for (int b = 0; b < 2; ++b) {
+        if (nc > b) {
+            cudaStreamWaitEvent(st, ev.in[b], 0);
+            cudaStreamWaitEvent(st, ev.out[b], 0);
+        }
+    }
+    s.cuda(cudaFreeAsync(base, st));
+    s.cuda(cudaStreamSynchronize(st));
+    return s.result();
+}
+
+kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const float* hd,
+                       const float* hl, float* hout, long long N, long long T, cudaStream_t st,
+                       long long wait_ns) {
+    if (N == 0 || T == 0) return KDN_OK;
+    // groups of whole sequences: about eight, each with at least 16 MB of
+    // coefficients (smaller scans run as one group)
+    long long G = (N + 7) / 8;
+    const long long min_rows = (16LL << 20) / (16 * T) + 1;
+    if (G < min_rows) G = min_rows;
+    if (G > N) G = N;
+    const int ng = static_cast<int>((N + G - 1) / G);
+    CopyStreams cs;
+    cudaError_t e = copy_streams(&cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    ChunkEvents ev;
+    e = ev.create();
+    if (e != cudaSuccess) return from_cuda(e);
+    const size_t coef_b = align256(static_cast<size_t>(G) * T * 4);
+    const size_t lam_b = align256(static_cast<size_t>(G) * 4);
+    const size_t set_b = 5 * coef_b + lam_b;   // a, b, c, d, out, lambda0
+    char* base = nullptr;
+    e = cudaMallocAsync(reinterpret_cast<void**>(&base), 2 * set_b, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    Status s;
+    s.cuda(cudaEventRecord(ev.start, st));
+    s.cuda(cudaStreamWaitEvent(cs.in, ev.start, 0));
+    s.cuda(cudaStreamWaitEvent(cs.out, ev.start, 0));
+    for (int g = 0; g < ng && s.ok(); ++g) {
+        const int b = g & 1;
+        const long long r0 = g * G, rows = (N - r0 < G) ? N - r0 : G;
+        const size_t bytes = static_cast<size_t>(rows) * T * 4;
+        char* set = base + b * set_b;
+        float* dco[4] = {reinterpret_cast<float*>(set), reinterpret_cast<float*>(set + coef_b),
+                         reinterpret_cast<float*>(set + 2 * coef_b), reinterpret_cast<float*>(set + 3 * coef_b)};
+        float* dout = reinterpret_cast<float*>(set + 4 * coef_b);
+        float* dlam = reinterpret_cast<float*>(set + 5 * coef_b);
+        if (g >= 2) s.cuda(cudaStreamWaitEvent(cs.in, ev.comp[b], 0));
+        const float* hco[4] = {ha, hb, hc, hd};
+        for (int i = 0; i < 4; ++i)
+            s.cuda(cudaMemcpyAsync(dco[i], hco[i] + r0 * T, bytes, cudaMemcpyHostToDevice, cs.in));
+        s.cuda(cudaMemcpyAsync(dlam, hl + r0, static_cast<size_t>(rows) * 4, cudaMemcpyHostToDevice, cs.in));
+        s.cuda(cudaEventRecord(ev.in[b], cs.in));
+        s.cuda(cudaStreamWaitEvent(st, ev.in[b], 0));
+        if (g >= 2) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
+        if (s.ok()) s.kdn(mobius_launch(dco[0], dco[1], dco[2], dco[3], dlam, dout, rows, T, st, wait_ns, -1));
+        s.cuda(cudaEventRecord(ev.comp[b], st));
+        s.cuda(cudaStreamWaitEvent(cs.out, ev.comp[b], 0));
+        s.cuda(cudaMemcpyAsync(hout + r0 * T, dout, bytes, cudaMemcpyDeviceToHost, cs.out));
+        s.cuda(cudaEventRecord(ev.out[b], cs.out));
+    }
+    for (int b = 0; b < 2; ++b) {
+        if (ng > b) {
+            cudaStreamWaitEvent(st, ev.in[b], 0);
+            cudaStreamWaitEvent(st, ev.out[b], 0);
+        }
+    }
+    s.cuda(cudaFreeAsync(base, st));
+    s.cuda(cudaStreamSynchronize(st));
+    return s.result();
+}
+
+}  // namespace kdn

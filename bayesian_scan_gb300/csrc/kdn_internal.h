@@ -44,6 +44,13 @@ kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c,
                                  cudaStream_t stream, long long wait_ns);
 long long mobius_noalloc_max_tiles();
 
+// Host-buffer pipelines (kdn_host.cu): arguments validated, every pointer a
+// host pointer; synchronous.
+kdn_status diag_host(const DiagArgs& a, cudaStream_t stream, long long wait_ns);
+kdn_status mobius_host(const float* a, const float* b, const float* c, const float* d,
+                       const float* lambda0, float* out, long long N, long long T,
+                       cudaStream_t stream, long long wait_ns);
+
 // Each translation unit that launches kernels with bounded waits owns one
 // device error word; these read-and-clear it on the current device.
 cudaError_t diag_take_device_error(int* status);

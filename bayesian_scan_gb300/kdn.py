@@ -51,6 +51,11 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_diag_scan_fwd_host.restype = i
+    lib.kdn_diag_scan_fwd_host.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
+                                           i, i, i, i, i, i, vp]
+    lib.kdn_mobius_scan_host.restype = i
+    lib.kdn_mobius_scan_host.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
     lib.kdn_mobius_scan_noalloc.restype = i
     lib.kdn_mobius_scan_noalloc.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
     lib.kdn_status_string.restype = ctypes.c_char_p
@@ -107,10 +112,12 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     q, k [B,H,T,dk]; v, beta [B,H,T,dv]; d [B,H,T] (bf16 or fp32, all the same);
     A [H] fp32; I0, mu0 [B,H,dv,dk] fp32 or None.  ``final_state`` may be
     True (allocate), False/None (skip) or a [2,B,H,dv,dk] fp32 tensor.
-    Returns (out [B,H,T,dv] fp32, final_state or None).
+    Returns (out [B,H,T,dv] fp32, final_state or None).  With host tensors
+    the call goes to ``kdn_diag_scan_fwd_host`` (pipelined copies; outputs
+    are host tensors, page-locked when allocated here).
     """
     if not q.is_cuda:
-        return _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, final_state)
+        return _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, out, final_state, stream)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -145,9 +152,10 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
 
 def mobius_scan(a, b, c, d, lambda0, out=None, stream=None):
     """Moebius precision recursion (see ``kdn_mobius_scan``): a,b,c,d [N,T]
-    fp32, lambda0 [N] fp32 -> lambda_1..lambda_T [N,T] fp32."""
+    fp32, lambda0 [N] fp32 -> lambda_1..lambda_T [N,T] fp32.  Host tensors go
+    to ``kdn_mobius_scan_host``."""
     if not a.is_cuda:
-        return _mobius_host(a, b, c, d, lambda0)
+        return _mobius_host(a, b, c, d, lambda0, out, stream)
     N, T = a.shape
     for name, t in (("a", a), ("b", b), ("c", c), ("d", d)):
         _check(t, name, torch.float32, (N, T))
@@ -215,31 +223,62 @@ def debug_stall_mobius_tile(tile: int) -> None:
 
 
 # ---------------------------------------------------------------------------
-# host-buffer calls: stage to the device, run the kernels, copy back
+# host-buffer calls: kdn_diag_scan_fwd_host / kdn_mobius_scan_host copy in,
+# scan and copy out in pipelined chunks (page-locked tensors let the copies
+# overlap the scans); results land in host tensors.
 
-def _to_dev(t, dev):
-    return None if t is None else t.to(dev, non_blocking=True)
-
-
-def _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, final_state):
-    dev = torch.device("cuda", torch.cuda.current_device())
-    xs = [_to_dev(t, dev) for t in (q, k, v, beta, d, A, I0, mu0)]
-    o, fs = diag_scan_fwd(*xs[:6], I_prior=I_prior, I0=xs[6], mu0=xs[7],
-                          final_state=bool(final_state is not None and final_state is not False))
-    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    o_h.copy_(o, non_blocking=True)
-    fs_h = None
-    if fs is not None:
-        fs_h = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
-        fs_h.copy_(fs, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
-    return o_h, fs_h
+def _host_out(t, name, shape):
+    """A caller-given host output (checked) or a new page-locked one."""
+    if t is None:
+        return torch.empty(shape, dtype=torch.float32, pin_memory=True)
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor when the inputs are")
+    _check(t, name, torch.float32, shape)
+    return t
 
 
-def _mobius_host(a, b, c, d, lambda0):
-    dev = torch.device("cuda", torch.cuda.current_device())
-    out = mobius_scan(*[_to_dev(t, dev) for t in (a, b, c, d, lambda0)])
-    o_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    o_h.copy_(out, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
-    return o_h
+def _diag_host(q, k, v, beta, d, A, I_prior, I0, mu0, out, final_state, stream):
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    for name, t, shape, dtype in (("q", q, (B, H, T, dk), dt), ("k", k, (B, H, T, dk), dt),
+                                  ("v", v, (B, H, T, dv), dt), ("beta", beta, (B, H, T, dv), dt),
+                                  ("d", d, (B, H, T), dt), ("A", A, (H,), torch.float32),
+                                  ("I0", I0, (B, H, dv, dk), torch.float32),
+                                  ("mu0", mu0, (B, H, dv, dk), torch.float32)):
+        if t is not None:
+            if t.is_cuda:
+                raise ValueError(f"{name} must be a host tensor like q")
+            _check(t, name, dtype, shape)
+    out = _host_out(out, "out", (B, H, T, dv))
+    if final_state is True:
+        final_state = None
+        fs = _host_out(None, "final_state", (2, B, H, dv, dk))
+    elif final_state is False or final_state is None:
+        fs = None
+    else:
+        fs = _host_out(final_state, "final_state", (2, B, H, dv, dk))
+    st = lib.kdn_diag_scan_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                                    float(I_prior), _ptr(I0), _ptr(mu0), _ptr(out), _ptr(fs),
+                                    B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
+                                    _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_scan_fwd_host")
+    return out, fs
+
+
+def _mobius_host(a, b, c, d, lambda0, out, stream):
+    N, T = a.shape
+    for name, t in (("a", a), ("b", b), ("c", c), ("d", d)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor like a")
+        _check(t, name, torch.float32, (N, T))
+    _check(lambda0, "lambda0", torch.float32, (N,))
+    out = _host_out(out, "out", (N, T))
+    st = lib.kdn_mobius_scan_host(_ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(lambda0), _ptr(out),
+                                  N, T, _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_mobius_scan_host")
+    return out

@@ -122,6 +122,40 @@ KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* 
                            long long N, long long T, void* stream);
 
 /*
+ * kdn_diag_scan_fwd_host -- kdn_diag_scan_fwd with every tensor (inputs,
+ * A, I0, mu0, out, final_state) in host memory: same arguments, layouts and
+ * results; pointers need only their element alignment.  The call returns when
+ * the results are in host memory.
+ *
+ * The tokens are cut into about eight chunks (at least 512 tokens each) that
+ * are pipelined: chunk c+1's inputs are copied to the device on an internal
+ * stream while chunk c is scanned on `stream` and chunk c-1's outputs are
+ * copied back on another internal stream; the state passes from chunk to
+ * chunk on the device.  Page-locked host buffers (cudaHostAlloc,
+ * cudaHostRegister, pinned framework tensors) let the copies overlap the
+ * scan; pageable buffers give the same results with serialised copies.
+ * Device memory for two chunks, the carried states and A/I0/mu0 comes from
+ * cudaMallocAsync on `stream` (KDN_ERR_ALLOC if it cannot be had) and is
+ * released before returning.
+ */
+KDN_API kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v,
+                                          const void* beta, const void* d, const float* A,
+                                          float I_prior, const float* I0, const float* mu0,
+                                          float* out, float* final_state, int B, int H, int T,
+                                          int dk, int dv, kdn_dtype in_dtype, void* stream);
+
+/*
+ * kdn_mobius_scan_host -- kdn_mobius_scan with a, b, c, d, lambda0 and out in
+ * host memory; returns when out is written.  The sequences are cut into
+ * groups (about eight, at least 16 MB of coefficients each) whose copies in
+ * and out overlap the scans of their neighbours, as for
+ * kdn_diag_scan_fwd_host; scratch from cudaMallocAsync on `stream`.
+ */
+KDN_API kdn_status kdn_mobius_scan_host(const float* a, const float* b, const float* c,
+                                        const float* d, const float* lambda0, float* out,
+                                        long long N, long long T, void* stream);
+
+/*
  * kdn_diag_scan_plan -- how kdn_diag_scan_fwd would run these sizes on the
  * current device, without launching anything: `parts` = token ranges the
  * sequence is split into (1 = no split), `kernels` = kernels one call
