@@ -93,6 +93,7 @@ struct AggArgs {
     AggScale* agg_scale;     // [P-1][BH]
     long long BH;
     int H, T;
+    long long d_ld;          // tokens between consecutive heads' rows of d
     int part_len;
     long long wait_ns;
 };
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int t = u0 + u;
-                x[u] = t < s1 ? static_cast<double>(Ah * __bfloat162float(p.d[bh * T + t]) * LOG2E) : 0.0;
+                x[u] = t < s1 ? static_cast<double>(Ah * __bfloat162float(p.d[bh * p.d_ld + t]) * LOG2E) : 0.0;
                 loc += x[u];
             }
             // exclusive suffix sum over the threads after this one

@@ -108,7 +108,9 @@ struct Params {
     float I_prior;
     const float* I0;
     const float* mu0;
-    float* out;              // [BH,T,dv] (full pass) or unused (aggregate pass)
+    float* out;              // [BH, out_ld, dv] (full pass) or unused (aggregate pass)
+    long long out_ld;        // tokens between consecutive heads' rows of out
+    long long d_ld;          // tokens between consecutive heads' rows of d
     float* final_state;      // [2,BH,dv,dk] or null
     float* agg;              // [P-1][BH][2][dv][dk] part end states / carried start states
     AggScale* agg_scale;     // [P-1][BH]
@@ -301,7 +303,7 @@ diag_scan_kernel(const Params p) {
             } else if (which == 3) {
                 bulk_g2s(raw_b(s, h), gb + tok * dv, tcn * dv * ES, &full_raw[s]);
             } else if (dbytes) {
-                bulk_g2s(raw_d(s, h), gd + tok, dbytes, &full_raw[s]);
+                bulk_g2s(raw_d(s, h), gd + (head0 + h) * p.d_ld + t0, dbytes, &full_raw[s]);
             }
         }
     };
@@ -338,7 +340,7 @@ diag_scan_kernel(const Params p) {
             if (!p.d_tma) {
                 for (int x = lane; x < nheads * tcn; x += 32) {
                     const int h = x / tcn, tt = x - h * tcn;
-                    raw_d(s, h)[tt] = gd[(head0 + h) * T + t0 + tt];
+                    raw_d(s, h)[tt] = gd[(head0 + h) * p.d_ld + t0 + tt];
                 }
                 __syncwarp();
             }
@@ -447,7 +449,7 @@ diag_scan_kernel(const Params p) {
             if (hq < nheads) {
                 lo = __fmul2_rn(lo, f2(SIGMA));
                 hi = __fmul2_rn(hi, f2(SIGMA));
-                float* o = gout + ((head0 + hq) * T + t_first + ts) * dv + iq;
+                float* o = gout + ((head0 + hq) * p.out_ld + t_first + ts) * dv + iq;
                 __stcs(reinterpret_cast<float4*>(o), make_float4(lo.x, lo.y, hi.x, hi.y));
             }
         }
@@ -793,11 +795,13 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
     prm.q = a.q; prm.k = a.k; prm.v = a.v; prm.beta = a.beta; prm.d = a.d;
     prm.A = a.A; prm.I_prior = a.I_prior; prm.I0 = a.I0; prm.mu0 = a.mu0;
     prm.out = a.out; prm.final_state = a.final_state;
+    prm.out_ld = a.out_ld > 0 ? a.out_ld : a.T;
+    prm.d_ld = a.d_ld > 0 ? a.d_ld : a.T;
     prm.BH = BH; prm.H = a.H; prm.T = a.T; prm.dv = dv;
     prm.part_len = pl.part_len; prm.TC = TC; prm.wait_ns = wait_ns;
     // d chunks can be bulk-copied when every chunk starts and ends on 16 bytes
     prm.d_tma = (static_cast<long long>(a.T) * ES % 16 == 0) && (TC * ES % 16 == 0) &&
-                ((reinterpret_cast<uintptr_t>(a.d) & 15u) == 0);
+                (prm.d_ld * ES % 16 == 0) && ((reinterpret_cast<uintptr_t>(a.d) & 15u) == 0);
 
     void* scratch = nullptr;
     cudaError_t e = cudaSuccess;
@@ -813,7 +817,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
             if (e == cudaSuccess) {
                 AggArgs ag{static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.beta),
                            static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.d),
-                           a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, pl.part_len, wait_ns};
+                           a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, prm.d_ld, pl.part_len, wait_ns};
                 diag_agg_tc_kernel<<<dim3(static_cast<unsigned>(BH), P - 1), AG_THREADS,
                                      agg_tc_smem_bytes(), st>>>(ag);
                 e = cudaGetLastError();

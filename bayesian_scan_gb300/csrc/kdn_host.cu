@@ -1,10 +1,10 @@
 // kdn_host.cu -- entry points that take every tensor in host memory
 // (kdn_diag_scan_fwd_host, kdn_mobius_scan_host).
 //
-// The work is cut into chunks that are pipelined over three streams: the
-// caller's stream runs the kernels, one internal stream copies chunk c+1's
+// The work is cut into chunks that are pipelined over four streams: the
+// caller's stream runs the kernels, two internal streams copy chunk c+1's
 // inputs in while chunk c is scanned, another copies chunk c-1's outputs
-// out.  The diagonal scan is cut along the tokens (every head of a chunk
+// out (or the scan writes them straight into page-locked host memory).  The diagonal scan is cut along the tokens (every head of a chunk
 // runs in one launch, so the GPU stays full) and carries the state from one
 // chunk to the next on the device through the scan's own final-state /
 // initial-state interface; the Moebius scan is cut along the sequences,
@@ -23,8 +23,11 @@ namespace {
 
 constexpr int kMaxDev = 64;
 
+// Two streams for the copies in (one stream runs back-to-back pitched
+// host-to-device copies at about 130 GB/s on GB300, two reach the link's
+// ~200 GB/s) and one for the copies out.
 struct CopyStreams {
-    cudaStream_t in = nullptr;
+    cudaStream_t in[2] = {nullptr, nullptr};
     cudaStream_t out = nullptr;
 };
 CopyStreams g_streams[kMaxDev];
@@ -38,35 +41,81 @@ cudaError_t copy_streams(CopyStreams* cs) {
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_streams_mu);
     CopyStreams& s = g_streams[dev];
-    if (!s.in) {
-        e = cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking);
-        if (e != cudaSuccess) return e;
-        e = cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            cudaStreamDestroy(s.in);
-            s.in = nullptr;
-            return e;
+    if (!s.out) {
+        CopyStreams n;
+        cudaStream_t* all[] = {&n.in[0], &n.in[1], &n.out};
+        for (cudaStream_t* p : all) {
+            e = cudaStreamCreateWithFlags(p, cudaStreamNonBlocking);
+            if (e != cudaSuccess) {
+                for (cudaStream_t* q : all)
+                    if (*q) cudaStreamDestroy(*q);
+                return e;
+            }
         }
+        s = n;
     }
     *cs = s;
     return cudaSuccess;
 }
 
-// Six events (in/compute/out for two chunk buffers), released on scope exit.
-struct ChunkEvents {
-    cudaEvent_t in[2] = {}, comp[2] = {}, out[2] = {}, start = nullptr;
-    cudaError_t create() {
-        cudaEvent_t* all[] = {&in[0], &in[1], &comp[0], &comp[1], &out[0], &out[1], &start};
-        for (cudaEvent_t* ev : all) {
-            const cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-            if (e != cudaSuccess) return e;
+// The host-buffer calls' device scratch comes from a memory pool of the
+// library's own (one per device, created on first use) that keeps freed
+// memory instead of returning it to the driver at every synchronisation: a
+// call then reuses the previous call's buffers.  The pool holds at most the
+// largest scratch one call needed.
+cudaMemPool_t g_pools[kMaxDev] = {};
+
+cudaError_t host_pool(cudaMemPool_t* pool) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_streams_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        e = cudaMemPoolCreate(&p, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = ~0ull;
+        e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return e;
         }
-        return cudaSuccess;
+        g_pools[dev] = p;
+    }
+    *pool = g_pools[dev];
+    return cudaSuccess;
+}
+
+// Chunk buffers in flight: with three, the copies of chunk c+2 run while
+// chunk c is scanned and neither the copy streams nor the scan wait on each
+// other in steady state (two leave both idle part of the time).
+constexpr int kBufs = 3;
+
+// Events of the chunk buffers (copies in on either copy stream, scan, copies
+// out) and of the start, released on scope exit.
+struct ChunkEvents {
+    cudaEvent_t in[kBufs][2] = {}, comp[kBufs] = {}, out[kBufs] = {}, start = nullptr;
+    cudaError_t create() {
+        cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+        for (int b = 0; b < kBufs && e == cudaSuccess; ++b) {
+            cudaEvent_t* all[] = {&in[b][0], &in[b][1], &comp[b], &out[b]};
+            for (cudaEvent_t* ev : all)
+                if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        }
+        return e;
     }
     ~ChunkEvents() {
-        cudaEvent_t all[] = {in[0], in[1], comp[0], comp[1], out[0], out[1], start};
-        for (cudaEvent_t ev : all)
-            if (ev) cudaEventDestroy(ev);
+        if (start) cudaEventDestroy(start);
+        for (int b = 0; b < kBufs; ++b) {
+            cudaEvent_t all[] = {in[b][0], in[b][1], comp[b], out[b]};
+            for (cudaEvent_t ev : all)
+                if (ev) cudaEventDestroy(ev);
+        }
     }
 };
 
@@ -116,20 +165,24 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
     // device layout: two chunk buffer sets, two carried states, A, I0, mu0
     const size_t qk_b = align256(BH * static_cast<size_t>(Tc) * dk * es);
     const size_t vb_b = align256(BH * static_cast<size_t>(Tc) * dv * es);
-    const size_t d_b = align256(BH * static_cast<size_t>(Tc) * es);
     const size_t o_b = align256(BH * static_cast<size_t>(Tc) * dv * 4);
-    const size_t set_b = 2 * qk_b + 2 * vb_b + d_b + o_b;
+    const size_t set_b = 2 * qk_b + 2 * vb_b + o_b;
     const size_t st_b = align256(2 * BH * S * 4);
     const size_t a_b = align256(static_cast<size_t>(H) * 4);
     const size_t init_b = align256(BH * S * 4);
-    const size_t total = 2 * set_b + 2 * st_b + a_b + (h.I0 ? init_b : 0) + (h.mu0 ? init_b : 0);
+    const size_t dall_b = align256(BH * static_cast<size_t>(T) * es);   // the whole d
+    const size_t total = kBufs * set_b + 2 * st_b + a_b + dall_b + (h.I0 ? init_b : 0) + (h.mu0 ? init_b : 0);
+    cudaMemPool_t pool = nullptr;
+    e = host_pool(&pool);
+    if (e != cudaSuccess) return from_cuda(e);
     char* base = nullptr;
-    e = cudaMallocAsync(reinterpret_cast<void**>(&base), total, st);
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), total, pool, st);
     if (e != cudaSuccess) return from_cuda(e);
     auto set = [&](int b) { return base + b * set_b; };
-    char* state[2] = {base + 2 * set_b, base + 2 * set_b + st_b};
-    float* A_d = reinterpret_cast<float*>(base + 2 * set_b + 2 * st_b);
-    char* tail = base + 2 * set_b + 2 * st_b + a_b;
+    char* state[2] = {base + kBufs * set_b, base + kBufs * set_b + st_b};
+    float* A_d = reinterpret_cast<float*>(base + kBufs * set_b + 2 * st_b);
+    char* d_all = base + kBufs * set_b + 2 * st_b + a_b;
+    char* tail = d_all + dall_b;
     float* I0_d = h.I0 ? reinterpret_cast<float*>(tail) : nullptr;
     float* mu0_d = h.mu0 ? reinterpret_cast<float*>(tail + (h.I0 ? init_b : 0)) : nullptr;
 
@@ -139,47 +192,61 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
     if (mu0_d) s.cuda(cudaMemcpyAsync(mu0_d, h.mu0, BH * S * 4, cudaMemcpyHostToDevice, st));
     // the copy streams start after the allocation
     s.cuda(cudaEventRecord(ev.start, st));
-    s.cuda(cudaStreamWaitEvent(cs.in, ev.start, 0));
-    s.cuda(cudaStreamWaitEvent(cs.out, ev.start, 0));
+    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
 
+    // A page-locked host `out` is written by the scan itself through its
+    // device mapping (no copy-engine traffic back); other memory is staged
+    // and copied out per chunk.
+    float* out_mapped = nullptr;
+    if (T > 0) {
+        cudaPointerAttributes pa;
+        // (the scan stores 16-byte row quads: the mapping must be 16-byte aligned)
+        if (cudaPointerGetAttributes(&pa, h.out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer && (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15u) == 0)
+            out_mapped = static_cast<float*>(pa.devicePointer);
+        cudaGetLastError();
+    }
     const char* hq = static_cast<const char*>(h.q);
     const char* hk = static_cast<const char*>(h.k);
     const char* hv = static_cast<const char*>(h.v);
     const char* hb = static_cast<const char*>(h.beta);
-    const char* hd = static_cast<const char*>(h.d);
+    // all of d in one contiguous copy (its per-chunk slices are too short for
+    // an efficient pitched copy); the scan reads each chunk's slice in place
+    if (T > 0) s.cuda(cudaMemcpyAsync(d_all, h.d, BH * static_cast<size_t>(T) * es, cudaMemcpyHostToDevice, cs.in[0]));
     for (int c = 0; c < nc && s.ok(); ++c) {
-        const int b = c & 1;
+        const int b = c % kBufs;
         const int t0 = c * Tc, n = (T - t0 < Tc) ? T - t0 : Tc;
         char* in = set(b);
         char* dq = in;
         char* dkp = in + qk_b;
         char* dvp = in + 2 * qk_b;
         char* dbp = in + 2 * qk_b + vb_b;
-        char* ddp = in + 2 * qk_b + 2 * vb_b;
-        float* dout = reinterpret_cast<float*>(in + 2 * qk_b + 2 * vb_b + d_b);
+        float* dout = reinterpret_cast<float*>(in + 2 * qk_b + 2 * vb_b);
         // inputs of chunk c (buffer b was last read by chunk c - 2)
-        if (c >= 2) s.cuda(cudaStreamWaitEvent(cs.in, ev.comp[b], 0));
-        auto rows_in = [&](char* dst, const char* src, size_t row_elems) {
+        // (buffer b was last read by the scan of chunk c - kBufs)
+        if (c >= kBufs)
+            for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
+        auto rows_in = [&](char* dst, const char* src, size_t row_elems, cudaStream_t cpy) {
             const size_t w = static_cast<size_t>(n) * row_elems * es;
             s.cuda(cudaMemcpy2DAsync(dst, w, src + static_cast<size_t>(t0) * row_elems * es,
                                      static_cast<size_t>(T) * row_elems * es, w, BH,
-                                     cudaMemcpyHostToDevice, cs.in));
+                                     cudaMemcpyHostToDevice, cpy));
         };
-        rows_in(dq, hq, dk);
-        rows_in(dkp, hk, dk);
-        rows_in(dvp, hv, dv);
-        rows_in(dbp, hb, dv);
-        rows_in(ddp, hd, 1);
-        s.cuda(cudaEventRecord(ev.in[b], cs.in));
+        rows_in(dq, hq, dk, cs.in[0]);
+        rows_in(dkp, hk, dk, cs.in[1]);
+        rows_in(dvp, hv, dv, cs.in[0]);
+        rows_in(dbp, hb, dv, cs.in[1]);
+        for (int i = 0; i < 2; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
         // scan of chunk c from the state chunk c - 1 left
-        s.cuda(cudaStreamWaitEvent(st, ev.in[b], 0));
-        if (c >= 2) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
+        for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
+        if (c >= kBufs) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
         DiagArgs a = h;
         a.q = dq;
         a.k = dkp;
         a.v = dvp;
         a.beta = dbp;
-        a.d = ddp;
+        a.d = d_all + static_cast<size_t>(t0) * es;
+        a.d_ld = T;
         a.A = A_d;
         if (c == 0) {
             a.I0 = I0_d;
@@ -189,7 +256,12 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
             a.mu0 = prev;
             a.I0 = prev + BH * S;
         }
-        a.out = dout;
+        if (out_mapped) {
+            a.out = out_mapped + static_cast<size_t>(t0) * dv;
+            a.out_ld = T;
+        } else {
+            a.out = dout;
+        }
         a.final_state = reinterpret_cast<float*>(state[c & 1]);
         a.T = n;
         if (s.ok()) s.kdn(a.dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns)
@@ -197,9 +269,11 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
         s.cuda(cudaEventRecord(ev.comp[b], st));
         // outputs of chunk c
         s.cuda(cudaStreamWaitEvent(cs.out, ev.comp[b], 0));
-        const size_t w = static_cast<size_t>(n) * dv * 4;
-        s.cuda(cudaMemcpy2DAsync(h.out + static_cast<size_t>(t0) * dv, static_cast<size_t>(T) * dv * 4, dout, w,
-                                 w, BH, cudaMemcpyDeviceToHost, cs.out));
+        if (!out_mapped) {
+            const size_t w = static_cast<size_t>(n) * dv * 4;
+            s.cuda(cudaMemcpy2DAsync(h.out + static_cast<size_t>(t0) * dv, static_cast<size_t>(T) * dv * 4, dout,
+                                     w, w, BH, cudaMemcpyDeviceToHost, cs.out));
+        }
         s.cuda(cudaEventRecord(ev.out[b], cs.out));
     }
     if (h.final_state && s.ok()) {
@@ -220,9 +294,10 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
         }
     }
     // every copy is ordered before the release and the final synchronisation
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBufs; ++b) {
         if (nc > b) {
-            cudaStreamWaitEvent(st, ev.in[b], 0);
+            cudaStreamWaitEvent(st, ev.in[b][0], 0);
+            cudaStreamWaitEvent(st, ev.in[b][1], 0);
             cudaStreamWaitEvent(st, ev.out[b], 0);
         }
     }
@@ -251,15 +326,17 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
     const size_t coef_b = align256(static_cast<size_t>(G) * T * 4);
     const size_t lam_b = align256(static_cast<size_t>(G) * 4);
     const size_t set_b = 5 * coef_b + lam_b;   // a, b, c, d, out, lambda0
+    cudaMemPool_t pool = nullptr;
+    e = host_pool(&pool);
+    if (e != cudaSuccess) return from_cuda(e);
     char* base = nullptr;
-    e = cudaMallocAsync(reinterpret_cast<void**>(&base), 2 * set_b, st);
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), kBufs * set_b, pool, st);
     if (e != cudaSuccess) return from_cuda(e);
     Status s;
     s.cuda(cudaEventRecord(ev.start, st));
-    s.cuda(cudaStreamWaitEvent(cs.in, ev.start, 0));
-    s.cuda(cudaStreamWaitEvent(cs.out, ev.start, 0));
+    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
     for (int g = 0; g < ng && s.ok(); ++g) {
-        const int b = g & 1;
+        const int b = g % kBufs;
         const long long r0 = g * G, rows = (N - r0 < G) ? N - r0 : G;
         const size_t bytes = static_cast<size_t>(rows) * T * 4;
         char* set = base + b * set_b;
@@ -267,23 +344,25 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
                          reinterpret_cast<float*>(set + 2 * coef_b), reinterpret_cast<float*>(set + 3 * coef_b)};
         float* dout = reinterpret_cast<float*>(set + 4 * coef_b);
         float* dlam = reinterpret_cast<float*>(set + 5 * coef_b);
-        if (g >= 2) s.cuda(cudaStreamWaitEvent(cs.in, ev.comp[b], 0));
+        if (g >= kBufs)
+            for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
         const float* hco[4] = {ha, hb, hc, hd};
         for (int i = 0; i < 4; ++i)
-            s.cuda(cudaMemcpyAsync(dco[i], hco[i] + r0 * T, bytes, cudaMemcpyHostToDevice, cs.in));
-        s.cuda(cudaMemcpyAsync(dlam, hl + r0, static_cast<size_t>(rows) * 4, cudaMemcpyHostToDevice, cs.in));
-        s.cuda(cudaEventRecord(ev.in[b], cs.in));
-        s.cuda(cudaStreamWaitEvent(st, ev.in[b], 0));
-        if (g >= 2) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
+            s.cuda(cudaMemcpyAsync(dco[i], hco[i] + r0 * T, bytes, cudaMemcpyHostToDevice, cs.in[i & 1]));
+        s.cuda(cudaMemcpyAsync(dlam, hl + r0, static_cast<size_t>(rows) * 4, cudaMemcpyHostToDevice, cs.in[0]));
+        for (int i = 0; i < 2; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
+        for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
+        if (g >= kBufs) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
         if (s.ok()) s.kdn(mobius_launch(dco[0], dco[1], dco[2], dco[3], dlam, dout, rows, T, st, wait_ns, -1));
         s.cuda(cudaEventRecord(ev.comp[b], st));
         s.cuda(cudaStreamWaitEvent(cs.out, ev.comp[b], 0));
         s.cuda(cudaMemcpyAsync(hout + r0 * T, dout, bytes, cudaMemcpyDeviceToHost, cs.out));
         s.cuda(cudaEventRecord(ev.out[b], cs.out));
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBufs; ++b) {
         if (ng > b) {
-            cudaStreamWaitEvent(st, ev.in[b], 0);
+            cudaStreamWaitEvent(st, ev.in[b][0], 0);
+            cudaStreamWaitEvent(st, ev.in[b][1], 0);
             cudaStreamWaitEvent(st, ev.out[b], 0);
         }
     }

@@ -22,6 +22,10 @@ struct DiagArgs {
     float* final_state;
     int B, H, T, dk, dv;
     kdn_dtype dtype;
+    // tokens between the rows of consecutive heads in `out` and in `d` (0: T,
+    // i.e. [B,H,T,...]); lets a call use a token range of longer tensors
+    long long out_ld = 0;
+    long long d_ld = 0;
 };
 
 // Per-dtype launchers (diag_bf16.cu / diag_f32.cu).

@@ -30,7 +30,8 @@
  *  - The caller owns every buffer.  Entry points may take short-lived
  *    stream-ordered scratch from the device's default memory pool
  *    (cudaMallocAsync / cudaFreeAsync on `stream`); the library holds no other
- *    device memory besides one error word per device.
+ *    device memory besides one error word per device, the fixed array of
+ *    kdn_mobius_scan_noalloc and the pool of the host-buffer calls.
  *  - Errors detectable on the host (null pointers, bad sizes, unsupported
  *    head dimensions, misaligned pointers) are returned before anything is
  *    launched.  Launch failures return KDN_ERR_CUDA.  Errors found by a
@@ -128,15 +129,20 @@ KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* 
  * the results are in host memory.
  *
  * The tokens are cut into about eight chunks (at least 512 tokens each) that
- * are pipelined: chunk c+1's inputs are copied to the device on an internal
- * stream while chunk c is scanned on `stream` and chunk c-1's outputs are
- * copied back on another internal stream; the state passes from chunk to
- * chunk on the device.  Page-locked host buffers (cudaHostAlloc,
+ * are pipelined over three device buffers: later chunks' inputs are copied
+ * to the device on two internal streams while chunk c is scanned on
+ * `stream`; outputs go straight into page-locked 16-byte aligned host memory
+ * from the scan, or are copied back on a third internal stream; the state
+ * passes from chunk to chunk on the device.  Page-locked host buffers (cudaHostAlloc,
  * cudaHostRegister, pinned framework tensors) let the copies overlap the
  * scan; pageable buffers give the same results with serialised copies.
- * Device memory for two chunks, the carried states and A/I0/mu0 comes from
- * cudaMallocAsync on `stream` (KDN_ERR_ALLOC if it cannot be had) and is
- * released before returning.
+ * Device memory for three chunks, the carried states, d, A, I0 and mu0 comes,
+ * stream-ordered on `stream`, from a memory pool of the library's own (one
+ * per device) that keeps freed memory for the next host-buffer call instead
+ * of returning it to the driver: after a call the pool holds up to the
+ * largest scratch a host-buffer call has needed (about 3 x 5 chunk buffers;
+ * 0.35 GB for 128 heads x 4096 tokens at d = 128).  KDN_ERR_ALLOC if the
+ * memory cannot be had.
  */
 KDN_API kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v,
                                           const void* beta, const void* d, const float* A,
@@ -149,7 +155,7 @@ KDN_API kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const vo
  * host memory; returns when out is written.  The sequences are cut into
  * groups (about eight, at least 16 MB of coefficients each) whose copies in
  * and out overlap the scans of their neighbours, as for
- * kdn_diag_scan_fwd_host; scratch from cudaMallocAsync on `stream`.
+ * kdn_diag_scan_fwd_host; scratch from the same library pool.
  */
 KDN_API kdn_status kdn_mobius_scan_host(const float* a, const float* b, const float* c,
                                         const float* d, const float* lambda0, float* out,

@@ -73,6 +73,27 @@ def test_host_diag_outputs_given_and_state_skipped():
     assert parity.rel_err(o, ro) <= parity.TOL_DIAG
 
 
+@pytest.mark.parametrize("where", ["pinned", "pinned_offset", "pageable"])
+def test_host_diag_output_buffers(where):
+    # page-locked 16-byte aligned outputs are written by the scan through
+    # their mapping; an offset page-locked view and pageable memory are staged
+    from bayesian_scan_gb300 import kdn
+    inp = draw(1, 2, 1300, 64, 64, seed=11)
+    shape = (1, 2, 1300, 64)
+    n = 1 * 2 * 1300 * 64
+    if where == "pinned":
+        out = torch.full(shape, float("nan")).pin_memory()
+    elif where == "pinned_offset":
+        out = torch.full((n + 1,), float("nan")).pin_memory()[1:].view(shape)
+    else:
+        out = torch.full(shape, float("nan"))
+    o, _ = kdn.diag_scan_fwd(*(inp[n_].pin_memory() for n_ in ("q", "k", "v", "beta", "d", "A")),
+                             I_prior=1.0, out=out, final_state=False)
+    assert o.data_ptr() == out.data_ptr()
+    ro, _, _ = parity.oracle_diag(inp)
+    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
+
+
 def test_host_diag_zero_length_returns_initial_state():
     inp = draw(1, 2, 0, 16, 16)
     g = torch.Generator().manual_seed(2)
