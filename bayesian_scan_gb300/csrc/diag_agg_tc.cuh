@@ -45,24 +45,26 @@ namespace kdn {
 namespace diag {
 namespace {
 
-constexpr int AG_KC = 32;                          // tokens per chunk
-constexpr int AG_THREADS = 256;
 constexpr int AG_D = 128;                          // d_k = d_v
-constexpr int AG_TILE = AG_D * AG_KC * 2;          // one 128 x 32 bf16 operand tile, bytes
 constexpr int AG_NTILE = 7;                        // A_J hi/lo, A_E hi/lo, B_k, B_k2 hi/lo
-constexpr int AG_OPS = AG_NTILE * AG_TILE;         // one operand buffer
-constexpr int AG_RAW = AG_KC * AG_D * 2;           // one raw array (k, beta or v) of a chunk
 constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta in [128,256)
-// core-matrix strides of an operand tile (K-major, no swizzle)
-constexpr uint32_t AG_LBO = 128;                   // next 8 tokens (K)
-constexpr uint32_t AG_SBO = (AG_KC / 8) * 128;     // next 8 rows (M or N)
+constexpr uint32_t AG_LBO = 128;                   // core matrices: next 8 tokens (K)
 
-constexpr int AG_SUP = 2048;                       // tokens per super-chunk of decay weights
-static_assert(AG_SUP == 8 * AG_THREADS, "a thread prepares 8 weights of a super-chunk");
-
-__host__ __device__ constexpr int agg_tc_smem_bytes() {
-    return 2 * AG_OPS + 2 * 3 * AG_RAW + AG_SUP * 4 + 8 * 8 + 4 * 8 + 16;
-}
+// Chunk shapes: KC tokens per chunk, 8 KC threads (one per row pair and
+// group of 8 tokens).  KC = 32: 256 threads, one CTA per SM; KC = 16: 128
+// threads, two CTAs per SM (each holding 256 of the SM's 512 TMEM columns),
+// for grids with at least two CTAs per SM.
+template <int KC>
+struct AggShape {
+    static constexpr int THREADS = 8 * KC;
+    static constexpr int CTAS_PER_SM = KC == 16 ? 2 : 1;
+    static constexpr int TILE = AG_D * KC * 2;          // one 128 x KC bf16 operand tile, bytes
+    static constexpr int OPS = AG_NTILE * TILE;         // one operand buffer
+    static constexpr int RAW = KC * AG_D * 2;           // one raw array (k, beta or v) of a chunk
+    static constexpr uint32_t SBO = (KC / 8) * 128;     // core matrices: next 8 rows (M or N)
+    static constexpr int SUP = 8 * THREADS;             // tokens per super-chunk of decay weights
+    static constexpr int SMEM = 2 * OPS + 2 * 3 * RAW + SUP * 4 + 8 * 8 + 4 * 8 + 16;
+};
 
 // 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
 // exp2 of the fractional part; 0 for S beyond the float range, NaN stays NaN.
@@ -98,12 +100,18 @@ struct AggArgs {
     long long wait_ns;
 };
 
-__global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArgs p) {
+template <int KC>
+__global__ void __launch_bounds__(AggShape<KC>::THREADS, AggShape<KC>::CTAS_PER_SM)
+diag_agg_tc_kernel(const AggArgs p) {
+    using Sh = AggShape<KC>;
+    constexpr int AG_KC = KC, AG_THREADS = Sh::THREADS, AG_TILE = Sh::TILE, AG_OPS = Sh::OPS,
+                  AG_RAW = Sh::RAW, AG_SUP = Sh::SUP;
+    constexpr uint32_t AG_SBO = Sh::SBO;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ops = smem;                                  // [2][7 tiles]
     unsigned char* raw = smem + 2 * AG_OPS;                     // [2 stages][k, beta, v]
     float* wsup = reinterpret_cast<float*>(raw + 2 * 3 * AG_RAW);   // [AG_SUP] weights of a super-chunk
-    double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [8] warp totals
+    double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [warps] warp totals
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);
     uint64_t* mma_done = raw_full + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 2);
@@ -152,7 +160,9 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     double Z = 0.0;          // sum of the decay exponents of the tokens after the current super-chunk
     int sup0 = tb;           // first token of the current super-chunk
     const int pr = tid & 63;                // this thread's operand rows 2 pr, 2 pr + 1
-    const int kg = tid >> 6;                // and its group of 8 tokens of a chunk
+    const int kg = tid >> 6;                // and its group of 8 tokens of a chunk (AG_KC / 8 groups)
+    static_assert(AG_THREADS == 64 * (AG_KC / 8), "one thread per (row pair, token group)");
+    static_assert(AG_SUP == 8 * AG_THREADS, "a thread prepares 8 weights of a super-chunk");
     constexpr uint32_t IDESC = umma_idesc_bf16_f32(AG_D, AG_D);
 
     for (int it = 0; it < nch; ++it) {
@@ -301,11 +311,16 @@ __global__ void __launch_bounds__(AG_THREADS, 1) diag_agg_tc_kernel(const AggArg
     tc_fence_after_sync();
     {
         const float W = *s_wend;
-        const int q = warp & 3, half = warp >> 2;   // lane quarter, J (0) or eta (1)
+        // warp w reads TMEM lanes 32 (w % 4) .. + 31; the warps of a lane
+        // quarter share its 256 columns (J, then eta)
+        constexpr int QW = AG_THREADS / 128;                 // warps per lane quarter
+        const int q = warp & 3;
         const int row = 32 * q + lane;
-        float* dst = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S +
-                     static_cast<long long>(row) * AG_D;
-        for (int c0 = 0; c0 < AG_D; c0 += 32) {
+        const int c_begin = (warp >> 2) * (2 * AG_D / QW), c_end = c_begin + 2 * AG_D / QW;
+        for (int cc = c_begin; cc < c_end; cc += 32) {
+            const int half = cc / AG_D, c0 = cc - half * AG_D;   // J (0) or eta (1)
+            float* dst = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S +
+                         static_cast<long long>(row) * AG_D;
             float v[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * AG_D + c0, v);
             if (nch == 0) {

@@ -610,25 +610,36 @@ diag_scan_kernel(const Params p) {
 __global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* I0,
                                   const float* mu0, float I_prior, long long BH, long long S,
                                   int P) {
-    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // four consecutive elements of one head per thread (S is a multiple of 4)
+    const long long idx = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
     if (idx >= BH * S) return;
     const long long bh = idx / S, e = idx - bh * S;
-    float Jv = 0.f, Ev = 0.f;
+    float4 Jv = make_float4(0.f, 0.f, 0.f, 0.f), Ev = Jv;
     if (I0 || mu0) {
-        const float i0 = I0 ? I0[idx] : I_prior;
-        Jv = i0 - I_prior;
-        Ev = mu0 ? i0 * mu0[idx] : 0.f;
+        const float4 i0 = I0 ? *reinterpret_cast<const float4*>(I0 + idx)
+                             : make_float4(I_prior, I_prior, I_prior, I_prior);
+        Jv = make_float4(i0.x - I_prior, i0.y - I_prior, i0.z - I_prior, i0.w - I_prior);
+        if (mu0) {
+            const float4 m = *reinterpret_cast<const float4*>(mu0 + idx);
+            Ev = make_float4(i0.x * m.x, i0.y * m.y, i0.z * m.z, i0.w * m.w);
+        }
     }
+    auto step = [](float x, int R, float d, float W) { return (ldexpf(x, -R) + d) / W; };
+#pragma unroll 4
     for (int pp = 0; pp + 1 < P; ++pp) {
         const AggScale a = scl[static_cast<long long>(pp) * BH + bh];
-        float* dJ = agg + (static_cast<long long>(pp) * BH + bh) * 2 * S + e;
-        float* dE = dJ + S;
-        Jv = (ldexpf(Jv, -a.R) + *dJ) / a.W;
-        Ev = (ldexpf(Ev, -a.R) + *dE) / a.W;
+        float4* dJ = reinterpret_cast<float4*>(agg + (static_cast<long long>(pp) * BH + bh) * 2 * S + e);
+        float4* dE = reinterpret_cast<float4*>(reinterpret_cast<float*>(dJ) + S);
+        const float4 j = *dJ, h = *dE;
+        Jv = make_float4(step(Jv.x, a.R, j.x, a.W), step(Jv.y, a.R, j.y, a.W), step(Jv.z, a.R, j.z, a.W),
+                         step(Jv.w, a.R, j.w, a.W));
+        Ev = make_float4(step(Ev.x, a.R, h.x, a.W), step(Ev.y, a.R, h.y, a.W), step(Ev.z, a.R, h.z, a.W),
+                         step(Ev.w, a.R, h.w, a.W));
         *dJ = Jv;
         *dE = Ev;
     }
 }
+
 
 }  // namespace
 }  // namespace diag
@@ -649,7 +660,8 @@ struct Cache {
     int occ[64] = {};
 };
 
-// Opt the tensor-core aggregate kernel into its shared memory (once per device).
+// Opt the tensor-core aggregate kernels into their shared memory (once per
+// device).
 cudaError_t agg_tc_prepare() {
     static bool done[64] = {};
     int dev = 0;
@@ -657,8 +669,11 @@ cudaError_t agg_tc_prepare() {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) dev = 0;
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(diag_agg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 agg_tc_smem_bytes());
+        e = cudaFuncSetAttribute(diag_agg_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AggShape<16>::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(diag_agg_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AggShape<32>::SMEM);
         if (e != cudaSuccess) return e;
         done[dev] = true;
     }
@@ -818,8 +833,12 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                 AggArgs ag{static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.beta),
                            static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.d),
                            a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, prm.d_ld, pl.part_len, wait_ns};
-                diag_agg_tc_kernel<<<dim3(static_cast<unsigned>(BH), P - 1), AG_THREADS,
-                                     agg_tc_smem_bytes(), st>>>(ag);
+                // two CTAs per SM when the grid fills them, else one wider CTA per SM
+                const dim3 grid(static_cast<unsigned>(BH), P - 1);
+                if (BH * (P - 1) >= 2LL * sm_count())
+                    diag_agg_tc_kernel<16><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
+                else
+                    diag_agg_tc_kernel<32><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
                 e = cudaGetLastError();
             }
         } else {
@@ -828,8 +847,8 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
-            const long long n = BH * S;
-            diag_carry_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+            const long long n4 = BH * S / 4;
+            diag_carry_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
                 prm.agg, prm.agg_scale, a.I0, a.mu0, a.I_prior, BH, S, P);
             e = cudaGetLastError();
         }
