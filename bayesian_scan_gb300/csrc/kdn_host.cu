@@ -1,8 +1,8 @@
 // kdn_host.cu -- entry points that take every tensor in host memory
 // (kdn_diag_scan_fwd_host, kdn_mobius_scan_host).
 //
-// The work is cut into chunks that are pipelined over four streams: the
-// caller's stream runs the kernels, two internal streams copy chunk c+1's
+// The work is cut into chunks that are pipelined over six streams: the
+// caller's stream runs the kernels, four internal streams copy later chunks'
 // inputs in while chunk c is scanned, another copies chunk c-1's outputs
 // out (or the scan writes them straight into page-locked host memory).  The diagonal scan is cut along the tokens (every head of a chunk
 // runs in one launch, so the GPU stays full) and carries the state from one
@@ -23,11 +23,12 @@ namespace {
 
 constexpr int kMaxDev = 64;
 
-// Two streams for the copies in (one stream runs back-to-back pitched
-// host-to-device copies at about 130 GB/s on GB300, two reach the link's
-// ~200 GB/s) and one for the copies out.
+// Streams for the copies in (one stream runs back-to-back pitched
+// host-to-device copies at about 130 GB/s on GB300, several reach the link's
+// ~200 GB/s), one per input array of a chunk, and one for the copies out.
+constexpr int kIn = 4;
 struct CopyStreams {
-    cudaStream_t in[2] = {nullptr, nullptr};
+    cudaStream_t in[kIn] = {};
     cudaStream_t out = nullptr;
 };
 CopyStreams g_streams[kMaxDev];
@@ -43,7 +44,7 @@ cudaError_t copy_streams(CopyStreams* cs) {
     CopyStreams& s = g_streams[dev];
     if (!s.out) {
         CopyStreams n;
-        cudaStream_t* all[] = {&n.in[0], &n.in[1], &n.out};
+        cudaStream_t* all[] = {&n.in[0], &n.in[1], &n.in[2], &n.in[3], &n.out};
         for (cudaStream_t* p : all) {
             e = cudaStreamCreateWithFlags(p, cudaStreamNonBlocking);
             if (e != cudaSuccess) {
@@ -99,11 +100,11 @@ constexpr int kBufs = 3;
 // Events of the chunk buffers (copies in on either copy stream, scan, copies
 // out) and of the start, released on scope exit.
 struct ChunkEvents {
-    cudaEvent_t in[kBufs][2] = {}, comp[kBufs] = {}, out[kBufs] = {}, start = nullptr;
+    cudaEvent_t in[kBufs][kIn] = {}, comp[kBufs] = {}, out[kBufs] = {}, start = nullptr;
     cudaError_t create() {
         cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
         for (int b = 0; b < kBufs && e == cudaSuccess; ++b) {
-            cudaEvent_t* all[] = {&in[b][0], &in[b][1], &comp[b], &out[b]};
+            cudaEvent_t* all[] = {&in[b][0], &in[b][1], &in[b][2], &in[b][3], &comp[b], &out[b]};
             for (cudaEvent_t* ev : all)
                 if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
         }
@@ -112,7 +113,7 @@ struct ChunkEvents {
     ~ChunkEvents() {
         if (start) cudaEventDestroy(start);
         for (int b = 0; b < kBufs; ++b) {
-            cudaEvent_t all[] = {in[b][0], in[b][1], comp[b], out[b]};
+            cudaEvent_t all[] = {in[b][0], in[b][1], in[b][2], in[b][3], comp[b], out[b]};
             for (cudaEvent_t ev : all)
                 if (ev) cudaEventDestroy(ev);
         }
@@ -192,7 +193,7 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
     if (mu0_d) s.cuda(cudaMemcpyAsync(mu0_d, h.mu0, BH * S * 4, cudaMemcpyHostToDevice, st));
     // the copy streams start after the allocation
     s.cuda(cudaEventRecord(ev.start, st));
-    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
+    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.in[2], cs.in[3], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
 
     // A page-locked host `out` is written by the scan itself through its
     // device mapping (no copy-engine traffic back); other memory is staged
@@ -225,7 +226,7 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
         // inputs of chunk c (buffer b was last read by chunk c - 2)
         // (buffer b was last read by the scan of chunk c - kBufs)
         if (c >= kBufs)
-            for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
+            for (int i = 0; i < kIn; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
         auto rows_in = [&](char* dst, const char* src, size_t row_elems, cudaStream_t cpy) {
             const size_t w = static_cast<size_t>(n) * row_elems * es;
             s.cuda(cudaMemcpy2DAsync(dst, w, src + static_cast<size_t>(t0) * row_elems * es,
@@ -234,11 +235,11 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
         };
         rows_in(dq, hq, dk, cs.in[0]);
         rows_in(dkp, hk, dk, cs.in[1]);
-        rows_in(dvp, hv, dv, cs.in[0]);
-        rows_in(dbp, hb, dv, cs.in[1]);
-        for (int i = 0; i < 2; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
+        rows_in(dvp, hv, dv, cs.in[2]);
+        rows_in(dbp, hb, dv, cs.in[3]);
+        for (int i = 0; i < kIn; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
         // scan of chunk c from the state chunk c - 1 left
-        for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
+        for (int i = 0; i < kIn; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
         if (c >= kBufs) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
         DiagArgs a = h;
         a.q = dq;
@@ -296,8 +297,7 @@ kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
     // every copy is ordered before the release and the final synchronisation
     for (int b = 0; b < kBufs; ++b) {
         if (nc > b) {
-            cudaStreamWaitEvent(st, ev.in[b][0], 0);
-            cudaStreamWaitEvent(st, ev.in[b][1], 0);
+            for (int i = 0; i < kIn; ++i) cudaStreamWaitEvent(st, ev.in[b][i], 0);
             cudaStreamWaitEvent(st, ev.out[b], 0);
         }
     }
@@ -334,7 +334,7 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
     if (e != cudaSuccess) return from_cuda(e);
     Status s;
     s.cuda(cudaEventRecord(ev.start, st));
-    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
+    for (cudaStream_t x : {cs.in[0], cs.in[1], cs.in[2], cs.in[3], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
     for (int g = 0; g < ng && s.ok(); ++g) {
         const int b = g % kBufs;
         const long long r0 = g * G, rows = (N - r0 < G) ? N - r0 : G;
@@ -345,13 +345,13 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
         float* dout = reinterpret_cast<float*>(set + 4 * coef_b);
         float* dlam = reinterpret_cast<float*>(set + 5 * coef_b);
         if (g >= kBufs)
-            for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
+            for (int i = 0; i < kIn; ++i) s.cuda(cudaStreamWaitEvent(cs.in[i], ev.comp[b], 0));
         const float* hco[4] = {ha, hb, hc, hd};
         for (int i = 0; i < 4; ++i)
-            s.cuda(cudaMemcpyAsync(dco[i], hco[i] + r0 * T, bytes, cudaMemcpyHostToDevice, cs.in[i & 1]));
+            s.cuda(cudaMemcpyAsync(dco[i], hco[i] + r0 * T, bytes, cudaMemcpyHostToDevice, cs.in[i]));
         s.cuda(cudaMemcpyAsync(dlam, hl + r0, static_cast<size_t>(rows) * 4, cudaMemcpyHostToDevice, cs.in[0]));
-        for (int i = 0; i < 2; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
-        for (int i = 0; i < 2; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
+        for (int i = 0; i < kIn; ++i) s.cuda(cudaEventRecord(ev.in[b][i], cs.in[i]));
+        for (int i = 0; i < kIn; ++i) s.cuda(cudaStreamWaitEvent(st, ev.in[b][i], 0));
         if (g >= kBufs) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
         if (s.ok()) s.kdn(mobius_launch(dco[0], dco[1], dco[2], dco[3], dlam, dout, rows, T, st, wait_ns, -1));
         s.cuda(cudaEventRecord(ev.comp[b], st));
@@ -361,8 +361,7 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
     }
     for (int b = 0; b < kBufs; ++b) {
         if (ng > b) {
-            cudaStreamWaitEvent(st, ev.in[b][0], 0);
-            cudaStreamWaitEvent(st, ev.in[b][1], 0);
+            for (int i = 0; i < kIn; ++i) cudaStreamWaitEvent(st, ev.in[b][i], 0);
             cudaStreamWaitEvent(st, ev.out[b], 0);
         }
     }
