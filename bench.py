@@ -39,11 +39,12 @@ SM_MAX_MHZ_FALLBACK = 2070.0     # maximum SM clock of GB300
 HBM_GBS_FALLBACK = 6800.0
 DIAG_FLOP_PER_ELEMENT_TOKEN = 10
 MOBIUS_BYTES_PER_STEP = 20
-# dram__bytes_read.sum + dram__bytes_write.sum of one full-pass diagonal-scan
-# launch per workload, from the ncu capture of the current kernel summarised
-# in profiles/ (diag_scan_kernel_layer750m.md); workloads without a capture
-# of the current kernel report null.
-DIAG_TRAFFIC_BYTES = {"layer750m": 538_256_384 + 244_887_296}
+# dram__bytes_read.sum + dram__bytes_write.sum of one kdn_diag_scan_fwd call
+# (all its kernels: tensor-core aggregates, carry, full pass) per workload,
+# from the ncu capture of the current kernels summarised in profiles/
+# (launches_layer750m.md); workloads without such a capture report null.
+DIAG_TRAFFIC_BYTES = {"layer750m": (350_351_616 + 68_281_088) + (100_694_784 + 36_312_064)
+                      + (638_839_296 + 241_371_904)}
 
 
 def parse_args():
