@@ -73,6 +73,24 @@ kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v, const 
     return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
 }
 
+kdn_status kdn_diag_step(const void* q, const void* k, const void* v, const void* beta, const void* d,
+                         const float* A, float I_prior, float* state, float* out, int B, int H, int dk,
+                         int dv, kdn_dtype in_dtype, void* stream) {
+    if (B < 1 || H < 1) return KDN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !beta || !d || !A || !state || !out) return KDN_ERR_INVALID_ARG;
+    if (in_dtype != KDN_F32 && in_dtype != KDN_BF16) return KDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > (1LL << 40)) return KDN_ERR_INVALID_ARG;
+    const size_t es = in_dtype == KDN_BF16 ? 2 : 4;
+    const void* ins[] = {q, k, v, beta, d};
+    for (const void* p : ins)
+        if (!aligned(p, es)) return KDN_ERR_INVALID_ARG;
+    if (!aligned(A, 4) || !aligned(out, 4) || !aligned(state, 16)) return KDN_ERR_INVALID_ARG;
+    return diag_step_launch(q, k, v, beta, d, A, I_prior, state, out, B, H, dk, dv, in_dtype,
+                            static_cast<cudaStream_t>(stream));
+}
+
 kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v, const void* beta,
                                   const void* d, const float* A, float I_prior, const float* I0,
                                   const float* mu0, float* out, float* final_state, int B, int H,
@@ -84,9 +102,12 @@ kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v, c
     const long long BH = static_cast<long long>(B) * H;
     const long long dmax = dk > dv ? dk : dv;
     if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / dmax) return KDN_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, beta, d, A, I0, mu0, out, final_state};
-    for (const void* p : ptrs)
+    const void* ins[] = {q, k, v, beta, d};
+    for (const void* p : ins)
         if (p && !aligned(p, in_dtype == KDN_BF16 ? 2 : 4)) return KDN_ERR_INVALID_ARG;
+    const void* f32s[] = {A, I0, mu0, out, final_state};
+    for (const void* p : f32s)
+        if (p && !aligned(p, 4)) return KDN_ERR_INVALID_ARG;
     DiagArgs a{q, k, v, beta, d, A, I_prior, I0, mu0, out, final_state, B, H, T, dk, dv, in_dtype};
     return diag_host(a, static_cast<cudaStream_t>(stream), g_wait_ns.load());
 }

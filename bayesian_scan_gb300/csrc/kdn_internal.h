@@ -48,6 +48,12 @@ kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c,
                                  cudaStream_t stream, long long wait_ns);
 long long mobius_noalloc_max_tiles();
 
+// One-token step of the diagonal update on a device-resident state
+// (diag_step.cu); arguments validated.
+kdn_status diag_step_launch(const void* q, const void* k, const void* v, const void* beta,
+                            const void* d, const float* A, float I_prior, float* state, float* out,
+                            int B, int H, int dk, int dv, kdn_dtype dtype, cudaStream_t stream);
+
 // Host-buffer pipelines (kdn_host.cu): arguments validated, every pointer a
 // host pointer; synchronous.
 kdn_status diag_host(const DiagArgs& a, cudaStream_t stream, long long wait_ns);

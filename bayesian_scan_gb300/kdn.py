@@ -51,6 +51,8 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_diag_step.restype = i
+    lib.kdn_diag_step.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, i, i, i, i, i, vp]
     lib.kdn_diag_scan_fwd_host.restype = i
     lib.kdn_diag_scan_fwd_host.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
                                            i, i, i, i, i, i, vp]
@@ -148,6 +150,34 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     if st != KDN_OK:
         raise KdnError(st, "kdn_diag_scan_fwd")
     return out, final_state
+
+
+def diag_step(q, k, v, beta, d, A, state, I_prior=1.0, out=None, stream=None):
+    """One token of the diagonal update on a device-resident state (see
+    ``kdn_diag_step``): q, k [B,H,dk]; v, beta [B,H,dv]; d [B,H] (bf16 or
+    fp32); A [H] fp32; state [2,B,H,dv,dk] fp32 (mu then I), updated in place.
+    Returns out [B,H,dv] fp32."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    for name, t, shape, dtype in (("q", q, (B, H, dk), dt), ("k", k, (B, H, dk), dt),
+                                  ("v", v, (B, H, dv), dt), ("beta", beta, (B, H, dv), dt),
+                                  ("d", d, (B, H), dt), ("A", A, (H,), torch.float32),
+                                  ("state", state, (2, B, H, dv, dk), torch.float32)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        _check(t, name, dtype, shape)
+    if out is None:
+        out = torch.empty(B, H, dv, device=q.device, dtype=torch.float32)
+    _check(out, "out", torch.float32, (B, H, dv))
+    st = lib.kdn_diag_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A), float(I_prior),
+                           _ptr(state), _ptr(out), B, H, dk, dv,
+                           KDN_BF16 if dt == torch.bfloat16 else KDN_F32, _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_step")
+    return out
 
 
 def mobius_scan(a, b, c, d, lambda0, out=None, stream=None):

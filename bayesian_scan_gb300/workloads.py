@@ -76,7 +76,16 @@ WORKLOADS = {
     "longctx": Workload("longctx", 1, 16, 65536, 128, 128, torch.bfloat16,
                         ("uniform", 0.1, 1.0), 4096, 16384, False, 1004),
 }
-# the same five in the order the configuration list gives them
+# batched decoding (one token per head per step on a device-resident state):
+# 128 x 16 heads of d=128, whose 268 MB state is twice the 129 MB L2; 32
+# tokens of inputs for successive steps
+DECODE = {
+    "decode2k": Workload("decode2k", 128, 16, 32, 128, 128, torch.bfloat16,
+                         ("uniform", 0.5, 4.0), 0, 0, False, 1005),
+}
+WORKLOADS.update(DECODE)
+
+# the five scan configurations in the order the configuration list gives them
 ORDER = ["small", "heads32_t2048_d64", "layer750m", "layer1p3b", "longctx"]
 
 

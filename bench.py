@@ -364,6 +364,120 @@ def run_ours(args, w, dist):
     return 0
 
 
+def run_decode(args, w, dist):
+    """Batched decoding: each step is one kdn_diag_step over all B x H heads
+    (one token each) on a device-resident state larger than L2; `value` is
+    token-heads per second, the roofline HBM (16 bytes of state per element
+    plus the token's inputs and outputs)."""
+    import torch
+
+    from bayesian_scan_gb300 import kdn, workloads
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w_rank = w if dist.rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * dist.rank})
+    host = workloads.make(w_rank, with_mobius=False)
+    names = ("q", "k", "v", "beta", "d")
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    # contiguous per-token inputs [B,H,...] for T successive steps
+    tok = [{n: host[n][:, :, t].contiguous().to(dev) for n in names} for t in range(T)]
+    A = host["A"].to(dev)
+    state = torch.stack([torch.zeros(B, H, dv, dk), torch.full((B, H, dv, dk), w.I_prior)]).to(dev)
+    out = torch.empty(B, H, dv, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x = tok[i % T]
+        kdn.diag_step(*(x[n] for n in names), A, state, I_prior=w.I_prior, out=out, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(dist.local_rank))
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        start.record(stream)
+        for i in range(K):
+            step(i)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {kdn.status_string(st)}")
+    ms = start.elapsed_time(stop)
+    max_ms = dist.max(ms)
+    heads = B * H
+    value = dist.world * heads * K / (max_ms / 1e3)
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    step_bytes = heads * dv * dk * 16 + heads * (2 * dk + 2 * dv + 1) * es + heads * dv * 4
+    gbs = step_bytes / (ms / K / 1e3) / 1e9
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", HBM_GBS_FALLBACK))
+    line = {
+        "metric": "decode token-heads/s (one kdn_diag_step over B x H heads per step)",
+        "value": value, "unit": "token-heads/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "d_k": dk, "d_v": dv,
+                   "inputs": "bf16" if es == 2 else "fp32", "state": "fp32, device resident, "
+                   f"{2 * heads * dv * dk * 4 / 1e6:.0f} MB (larger than the 129 MB L2, no flush)"},
+        "roofline": {"kernel": "diag_step_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None,
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+        "gpu_launches": K,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_e2e:
+        # each step: the token's inputs from page-locked host memory, the step,
+        # the outputs back (the state stays on the device)
+        pin = [{n: host[n][:, :, t].contiguous().pin_memory() for n in names} for t in range(T)]
+        out_h = torch.empty(B, H, dv).pin_memory()
+        xs = {n: torch.empty_like(tok[0][n]) for n in names}
+
+        def e2e_step(i):
+            for n in names:
+                xs[n].copy_(pin[i % T][n], non_blocking=True)
+            kdn.diag_step(*(xs[n] for n in names), A, state, I_prior=w.I_prior, out=out, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+
+        e2e_step(0)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for i in range(K):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        dt = dist.max(time.perf_counter() - t0)
+        line["e2e"] = {"value": dist.world * heads * K / dt, "unit": "token-heads/s", "steps": K,
+                       "h2d_bytes_per_step": heads * (2 * dk + 2 * dv + 1) * es,
+                       "d2h_bytes_per_step": heads * dv * 4,
+                       "path": "page-locked token inputs -> device copies -> kdn.diag_step -> "
+                               "page-locked output (state device resident)"}
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n_heads = min(heads, 64)
+        sl = lambda x: x.reshape(B * H, *x.shape[2:])[:n_heads].reshape(1, n_heads, *x.shape[2:])
+        args_o = [sl(host[n][:, :, :1]) for n in names]
+        A_o = host["A"].repeat(B)[:n_heads].contiguous()
+        I0 = torch.full((1, n_heads, dv, dk), w.I_prior)
+        mu0 = torch.zeros(1, n_heads, dv, dk)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0:
+            oracle.diag_scan(*args_o, A_o, w.I_prior, I0, mu0)
+            reps += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": reps * n_heads / dt, "unit": "token-heads/s",
+                                "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": f"{reps} one-token oracle steps over {n_heads} heads "
+                                          f"({dv}x{dk} state rows), fp64, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def measure_e2e(args, w, host, dev, dist):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory, runs both scans and reads the results
@@ -409,6 +523,14 @@ def main():
     w = workloads.get(args.workload)
     dist = Dist(use_gpu=args.impl == "ours")
     try:
+        if w.name in workloads.DECODE:
+            if args.impl == "reference":
+                if dist.rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                                      "oracle on the scan workloads; decode steps are timed by our arm's "
+                                      "cpu_baseline"}), flush=True)
+                return 0
+            return run_decode(args, w, dist)
         if args.impl == "reference":
             return run_reference(args, w, dist)
         return run_ours(args, w, dist)

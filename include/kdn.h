@@ -123,6 +123,30 @@ KDN_API kdn_status kdn_mobius_scan(const float* a, const float* b, const float* 
                            long long N, long long T, void* stream);
 
 /*
+ * kdn_diag_step -- one token of kdn_diag_scan_fwd's update for B x H heads
+ * whose state is kept on the device between calls (batched decoding), the
+ * state read and overwritten in place.  The same equations for T = 1:
+ *     alpha = exp(-A d); I' = alpha I + (1 - alpha) I_prior + beta_i k_j^2;
+ *     mu' = (alpha I mu + beta_i v_i k_j) / I';  o_i = sum_j mu'_ij q_j.
+ *
+ *   q, k     [B,H,dk]  in_dtype     v, beta [B,H,dv] in_dtype   d [B,H] in_dtype
+ *   A        [H] fp32               I_prior scalar
+ *   state    [2,B,H,dv,dk] fp32, 16-byte aligned: mu then I (the layout of
+ *            kdn_diag_scan_fwd's final_state and of its mu0 / I0); read and
+ *            overwritten with the state after the token
+ *   out      [B,H,dv] fp32
+ *
+ * Equal to kdn_diag_scan_fwd with T = 1, mu0 = state[0], I0 = state[1] and
+ * final_state = state, up to rounding.  The step reads and writes each state
+ * element once (16 bytes) and is bound by HBM bandwidth.  Asynchronous on
+ * `stream`; no scratch.
+ */
+KDN_API kdn_status kdn_diag_step(const void* q, const void* k, const void* v, const void* beta,
+                                 const void* d, const float* A, float I_prior, float* state,
+                                 float* out, int B, int H, int dk, int dv, kdn_dtype in_dtype,
+                                 void* stream);
+
+/*
  * kdn_diag_scan_fwd_host -- kdn_diag_scan_fwd with every tensor (inputs,
  * A, I0, mu0, out, final_state) in host memory: same arguments, layouts and
  * results; pointers need only their element alignment.  The call returns when

@@ -100,3 +100,47 @@ def test_mobius_empty_is_a_no_op(lib):
     # nothing to compute: returns OK without touching the (null) buffers
     assert _mob(lib, a=None, b=None, c=None, d=None, l0=None, out=None, N=0, T=16) == 0
     assert _mob(lib, a=None, b=None, c=None, d=None, l0=None, out=None, N=5, T=0) == 0
+
+
+def _step(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, state=FAKE, out=FAKE, B=1, H=1,
+          dk=16, dv=16, dtype=1):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_diag_step(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), 1.0, vp(state), vp(out),
+                             B, H, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d", "A", "state", "out"])
+def test_step_null_pointer(lib, field):
+    assert _step(lib, **{field: None}) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), -1), (dict(H=-1), -1), (dict(dk=8), -2), (dict(dv=96), -2), (dict(dtype=5), -2),
+    (dict(state=FAKE + 8), -1), (dict(q=FAKE + 1), -1), (dict(out=FAKE + 2), -1),
+    (dict(A=FAKE + 2), -1), (dict(q=FAKE + 2, dtype=0), -1),
+])
+def test_step_rejects(lib, kw, status):
+    assert _step(lib, **kw) == status
+
+
+def _host(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, out=FAKE, B=1, H=1, T=8,
+          dk=16, dv=16, dtype=1):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_diag_scan_fwd_host(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), 1.0, None, None,
+                                      vp(out), None, B, H, T, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(out=None), -1), (dict(B=0), -1), (dict(T=-1), -1),
+    (dict(dk=12), -2), (dict(dtype=3), -2), (dict(q=FAKE + 1), -1), (dict(A=FAKE + 2), -1),
+])
+def test_host_diag_rejects(lib, kw, status):
+    assert _host(lib, **kw) == status
+
+
+def test_host_mobius_rejects(lib):
+    vp = ctypes.c_void_p
+    assert lib.kdn_mobius_scan_host(None, vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 16, None) == -1
+    assert lib.kdn_mobius_scan_host(vp(FAKE + 1), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 16,
+                                    None) == -1
+    assert lib.kdn_mobius_scan_host(None, None, None, None, None, None, 0, 16, None) == 0
