@@ -40,9 +40,12 @@ __device__ __forceinline__ float in_f32<__nv_bfloat16>(const __nv_bfloat16* p, l
 }
 
 // DK columns per row, 4 per lane: LPR = DK / 4 lanes per row (4..32), RPW =
-// 32 / LPR rows per warp.
+// 32 / LPR rows per warp; UNR row groups per warp and iteration, whose state
+// loads are all issued before any arithmetic (more bytes in flight per warp).
+constexpr int STEP_UNR = 2;
+
 template <int DK, typename TIn>
-__global__ void __launch_bounds__(STEP_THREADS)
+__global__ void __launch_bounds__(STEP_THREADS, 4)
 diag_step_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
                  const TIn* __restrict__ beta, const TIn* __restrict__ d, const float* __restrict__ A,
                  float I_prior, float* __restrict__ state, float* __restrict__ out, long long BH,
@@ -56,35 +59,48 @@ diag_step_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn
     const long long rows = BH * dv;
     const long long warps = static_cast<long long>(gridDim.x) * (STEP_THREADS / 32);
     const long long w0 = static_cast<long long>(blockIdx.x) * (STEP_THREADS / 32) + (threadIdx.x >> 5);
-    for (long long rg = w0 * RPW; rg < rows; rg += warps * RPW) {
-        const long long row = rg + sub;               // global state row (head, i)
-        const bool valid = row < rows;
-        const long long bh = valid ? row / dv : 0;
-        const int i = valid ? static_cast<int>(row - bh * dv) : 0;
-        float part = 0.f;
-        if (valid) {
-            const float alpha = exp2f(-A[bh % H] * in_f32(d, bh) * STEP_LOG2E);
-            const float b = in_f32(beta, bh * dv + i), bv = b * in_f32(v, bh * dv + i);
-            const long long e = bh * S + static_cast<long long>(i) * DK + col;
-            const float4 m4 = *reinterpret_cast<const float4*>(mu_s + e);
-            const float4 i4 = *reinterpret_cast<const float4*>(I_s + e);
-            const float mu[4] = {m4.x, m4.y, m4.z, m4.w}, Iv[4] = {i4.x, i4.y, i4.z, i4.w};
-            float mo[4], io[4];
+    for (long long rg = w0 * RPW * STEP_UNR; rg < rows; rg += warps * RPW * STEP_UNR) {
+        long long row[STEP_UNR], e[STEP_UNR];
+        bool valid[STEP_UNR];
+        float4 m4[STEP_UNR], i4[STEP_UNR];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float kj = in_f32(k, bh * DK + col + c), qj = in_f32(q, bh * DK + col + c);
-                const float In = alpha * Iv[c] + (1.f - alpha) * I_prior + b * (kj * kj);
-                mo[c] = (alpha * Iv[c] * mu[c] + bv * kj) / In;
-                io[c] = In;
-                part += mo[c] * qj;
+        for (int u = 0; u < STEP_UNR; ++u) {
+            row[u] = rg + u * RPW + sub;                      // global state row (head, i)
+            valid[u] = row[u] < rows;
+            const long long bh = valid[u] ? row[u] / dv : 0;
+            e[u] = bh * S + (row[u] - bh * dv) * DK + col;
+            if (valid[u]) {
+                m4[u] = __ldcs(reinterpret_cast<const float4*>(mu_s + e[u]));
+                i4[u] = __ldcs(reinterpret_cast<const float4*>(I_s + e[u]));
             }
-            *reinterpret_cast<float4*>(mu_s + e) = make_float4(mo[0], mo[1], mo[2], mo[3]);
-            *reinterpret_cast<float4*>(I_s + e) = make_float4(io[0], io[1], io[2], io[3]);
         }
-        // row sum over the LPR lanes of the row (an aligned group of the warp)
 #pragma unroll
-        for (int off = LPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (valid && lane % LPR == 0) out[bh * dv + i] = part;
+        for (int u = 0; u < STEP_UNR; ++u) {
+            float part = 0.f;
+            const long long bh = valid[u] ? row[u] / dv : 0;
+            const int i = valid[u] ? static_cast<int>(row[u] - bh * dv) : 0;
+            if (valid[u]) {
+                const float alpha = exp2f(-A[bh % H] * in_f32(d, bh) * STEP_LOG2E);
+                const float b = in_f32(beta, bh * dv + i), bv = b * in_f32(v, bh * dv + i);
+                const float mu[4] = {m4[u].x, m4[u].y, m4[u].z, m4[u].w};
+                const float Iv[4] = {i4[u].x, i4[u].y, i4[u].z, i4[u].w};
+                float mo[4], io[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float kj = in_f32(k, bh * DK + col + c), qj = in_f32(q, bh * DK + col + c);
+                    const float In = alpha * Iv[c] + (1.f - alpha) * I_prior + b * (kj * kj);
+                    mo[c] = (alpha * Iv[c] * mu[c] + bv * kj) / In;
+                    io[c] = In;
+                    part += mo[c] * qj;
+                }
+                __stcs(reinterpret_cast<float4*>(mu_s + e[u]), make_float4(mo[0], mo[1], mo[2], mo[3]));
+                __stcs(reinterpret_cast<float4*>(I_s + e[u]), make_float4(io[0], io[1], io[2], io[3]));
+            }
+            // row sum over the LPR lanes of the row (an aligned group of the warp)
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (valid[u] && lane % LPR == 0) out[bh * dv + i] = part;
+        }
     }
 }
 
@@ -94,7 +110,7 @@ cudaError_t launch_step(const void* q, const void* k, const void* v, const void*
                         int dv, cudaStream_t st) {
     constexpr int RPW = 32 / (DK / 4);
     const long long rows = BH * dv;
-    const long long warps_needed = (rows + RPW - 1) / RPW;
+    const long long warps_needed = (rows + RPW * STEP_UNR - 1) / (RPW * STEP_UNR);
     long long blocks = (warps_needed + (STEP_THREADS / 32) - 1) / (STEP_THREADS / 32);
     const long long cap = static_cast<long long>(sm_count()) * 16;   // grid-stride beyond this
     if (blocks > cap) blocks = cap;
