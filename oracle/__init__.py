@@ -67,6 +67,10 @@ def _declare(lib):
                                      dp, dp, dp, L, L, L, L, L]
     lib.oracle_mobius_scan.restype = ctypes.c_int
     lib.oracle_mobius_scan.argtypes = [dp, dp, dp, dp, dp, dp, L, L]
+    lib.oracle_diag_scan_bwd.restype = ctypes.c_int
+    lib.oracle_diag_scan_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double, dp, dp,
+                                         dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                         L, L, L, L, L]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -121,6 +125,39 @@ def diag_scan(q, k, v, beta, d, A, I_prior, I0=None, mu0=None, lib=None):
     if rc != 0:
         raise RuntimeError(f"oracle_diag_scan failed ({rc})")
     return out, mu_T, I_T
+
+
+def diag_scan_bwd(q, k, v, beta, d, A, I_prior, I0=None, mu0=None, dout=None,
+                  dmu_T=None, dI_T=None, lib=None):
+    """Oracle of the backward pass: reverse-mode derivative of ``diag_scan``
+    for L = sum(dout * out) + sum(dmu_T * mu_T) + sum(dI_T * I_T).
+
+    ``dout`` [B,H,T,dv] is required; ``dmu_T``, ``dI_T`` [B,H,dv,dk] may be
+    None (zero).  Returns a dict of fp64 arrays: dq, dk [B,H,T,dk]; dv, dbeta
+    [B,H,T,dv]; dd [B,H,T]; dA [H] (summed over the batch); dI0, dmu0
+    [B,H,dv,dk].  Keeps every state of a head: (T+1)*dv*dk*16 bytes per head
+    being processed.
+    """
+    lib = lib or load()
+    q, k, v, beta, d, A = (_f64(x) for x in (q, k, v, beta, d, A))
+    I0, mu0, dout, dmu_T, dI_T = (_f64(x) for x in (I0, mu0, dout, dmu_T, dI_T))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    assert dout is not None and dout.shape == (B, H, T, dv)
+    for x in (I0, mu0, dmu_T, dI_T):
+        assert x is None or x.shape == (B, H, dv, dk)
+    g = dict(dq=np.empty((B, H, T, dk)), dk=np.empty((B, H, T, dk)), dv=np.empty((B, H, T, dv)),
+             dbeta=np.empty((B, H, T, dv)), dd=np.empty((B, H, T)), dA_bh=np.empty((B, H)),
+             dI0=np.empty((B, H, dv, dk)), dmu0=np.empty((B, H, dv, dk)))
+    rc = lib.oracle_diag_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                                  float(I_prior), _ptr(I0), _ptr(mu0), _ptr(dout), _ptr(dmu_T),
+                                  _ptr(dI_T), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                  _ptr(g["dbeta"]), _ptr(g["dd"]), _ptr(g["dA_bh"]),
+                                  _ptr(g["dI0"]), _ptr(g["dmu0"]), B, H, T, dk, dv)
+    if rc != 0:
+        raise RuntimeError(f"oracle_diag_scan_bwd failed ({rc})")
+    g["dA"] = g.pop("dA_bh").sum(axis=0)
+    return g
 
 
 def mobius_scan(a, b, c, d, lambda0, lib=None):

@@ -37,6 +37,17 @@
  *      they are unrelated to the forget gate and importance above).  Step t
  *      uses the coefficients of index t and the output is lambda_1..lambda_T.
  *
+ *  (3) Backward pass of (1) -- the pages' kernels exist for training on GPUs
+ *      ("Learning to Remember, Learn, and Forget in Attention-Based Models",
+ *      Contributi Chiave).  oracle_diag_scan_bwd is plain reverse-mode
+ *      differentiation of the loop of (1), statement by statement, for the
+ *      scalar  L = sum dout . o + sum dmu_T . mu_T + sum dI_T . I_T:
+ *      every state of every token is kept, and the chain rule is applied to
+ *      the two update statements and the readout in reverse order.  The
+ *      outputs are dL/dq, dL/dk, dL/dv, dL/dbeta, dL/dd, dL/dA (per (b,h),
+ *      summed over b by the caller), dL/dI_0 and dL/dmu_0.  I_prior is a
+ *      fixed hyperparameter here and gets no gradient.
+ *
  * Parity pins (tests/test_oracle_pins.py) tie every term of these loops to
  * closed forms, special cases and brute force; see that file.
  *
@@ -154,4 +165,123 @@ int oracle_mobius_scan(const double* a, const double* b, const double* c,
         }
     }
     return 0;
+}
+
+/* Reverse-mode derivative of oracle_diag_scan (see (3) in the header).
+ * dout: [B,H,T,dv]; dmu_T, dI_T: [B,H,dv,dk] or NULL (zero).
+ * Outputs (all written): dq, dk: [B,H,T,dk]; dv, dbeta: [B,H,T,dv];
+ * dd: [B,H,T]; dA_bh: [B,H] (the head's dA contribution of batch b);
+ * dI0, dmu0: [B,H,dv,dk] (gradients of the initial state actually used).
+ * Memory: (T+1) * dv * dk * 2 doubles per head in flight. */
+int oracle_diag_scan_bwd(const double* q, const double* k, const double* v,
+                         const double* beta, const double* d, const double* A,
+                         double I_prior, const double* I0, const double* mu0,
+                         const double* dout, const double* dmu_T, const double* dI_T,
+                         double* dq, double* dk_out, double* dv_out, double* dbeta,
+                         double* dd, double* dA_bh, double* dI0, double* dmu0,
+                         long B, long H, long T, long dk, long dv) {
+    if (B < 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return -1;
+    long BH = B * H;
+    long S = dv * dk;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long bh = 0; bh < BH; ++bh) {
+        long h = bh % H;
+        /* Is[t], Ms[t]: I and mu after token t (t = 0: the initial state) */
+        double* Is = (double*)malloc(sizeof(double) * (T + 1) * S);
+        double* Ms = (double*)malloc(sizeof(double) * (T + 1) * S);
+        double* gI = (double*)malloc(sizeof(double) * S);
+        double* gM = (double*)malloc(sizeof(double) * S);
+        if (!Is || !Ms || !gI || !gM) {
+            failed = 1;
+            free(Is);
+            free(Ms);
+            free(gI);
+            free(gM);
+            continue;
+        }
+        /* ---- forward: the loop of oracle_diag_scan, keeping every state ---- */
+        for (long e = 0; e < S; ++e) {
+            Is[e] = I0 ? I0[bh * S + e] : I_prior;
+            Ms[e] = mu0 ? mu0[bh * S + e] : 0.0;
+        }
+        for (long t = 0; t < T; ++t) {
+            const double* kt = k + (bh * T + t) * dk;
+            const double* vt = v + (bh * T + t) * dv;
+            const double* bt = beta + (bh * T + t) * dv;
+            double alpha = exp(-A[h] * d[bh * T + t]);
+            const double* Ip = Is + t * S;
+            const double* Mp = Ms + t * S;
+            double* In = Is + (t + 1) * S;
+            double* Mn = Ms + (t + 1) * S;
+            for (long i = 0; i < dv; ++i)
+                for (long j = 0; j < dk; ++j) {
+                    long e = i * dk + j;
+                    In[e] = alpha * Ip[e] + (1.0 - alpha) * I_prior + bt[i] * (kt[j] * kt[j]);
+                    Mn[e] = alpha * (Ip[e] / In[e]) * Mp[e] + (1.0 / In[e]) * ((bt[i] * vt[i]) * kt[j]);
+                }
+        }
+        /* ---- reverse: adjoints gI, gM of I_t, mu_t, from t = T down to 1 ---- */
+        for (long e = 0; e < S; ++e) {
+            gI[e] = dI_T ? dI_T[bh * S + e] : 0.0;
+            gM[e] = dmu_T ? dmu_T[bh * S + e] : 0.0;
+        }
+        double gA = 0.0;
+        for (long t = T - 1; t >= 0; --t) {
+            const double* qt = q + (bh * T + t) * dk;
+            const double* kt = k + (bh * T + t) * dk;
+            const double* vt = v + (bh * T + t) * dv;
+            const double* bt = beta + (bh * T + t) * dv;
+            const double* ot_bar = dout + (bh * T + t) * dv;
+            double* dqt = dq + (bh * T + t) * dk;
+            double* dkt = dk_out + (bh * T + t) * dk;
+            double* dvt = dv_out + (bh * T + t) * dv;
+            double* dbt = dbeta + (bh * T + t) * dv;
+            double alpha = exp(-A[h] * d[bh * T + t]);
+            const double* Ip = Is + t * S;
+            const double* Mp = Ms + t * S;
+            const double* In = Is + (t + 1) * S;
+            const double* Mn = Ms + (t + 1) * S;
+            for (long j = 0; j < dk; ++j) dqt[j] = dkt[j] = 0.0;
+            for (long i = 0; i < dv; ++i) dvt[i] = dbt[i] = 0.0;
+            double g_alpha = 0.0;
+            for (long i = 0; i < dv; ++i)
+                for (long j = 0; j < dk; ++j) {
+                    long e = i * dk + j;
+                    /* readout o_t[i] = sum_j mu_t[i][j] q_t[j] */
+                    double gmu = gM[e] + ot_bar[i] * qt[j];
+                    dqt[j] += ot_bar[i] * Mn[e];
+                    /* mu_t = alpha (I_{t-1}/I_t) mu_{t-1} + (1/I_t) (beta_i v_i) k_j */
+                    double g_In = gI[e] - gmu * Mn[e] / In[e];
+                    g_alpha += gmu * (Ip[e] / In[e]) * Mp[e];
+                    double g_Ip = gmu * alpha * Mp[e] / In[e];
+                    double g_Mp = gmu * alpha * Ip[e] / In[e];
+                    dbt[i] += gmu * vt[i] * kt[j] / In[e];
+                    dvt[i] += gmu * bt[i] * kt[j] / In[e];
+                    dkt[j] += gmu * bt[i] * vt[i] / In[e];
+                    /* I_t = alpha I_{t-1} + (1 - alpha) I_prior + beta_i k_j^2 */
+                    g_alpha += g_In * (Ip[e] - I_prior);
+                    g_Ip += g_In * alpha;
+                    dbt[i] += g_In * kt[j] * kt[j];
+                    dkt[j] += g_In * 2.0 * bt[i] * kt[j];
+                    gI[e] = g_Ip;
+                    gM[e] = g_Mp;
+                }
+            /* alpha_t = exp(-A d_t) */
+            dd[bh * T + t] = g_alpha * (-A[h] * alpha);
+            gA += g_alpha * (-d[bh * T + t] * alpha);
+        }
+        dA_bh[bh] = gA;
+        for (long e = 0; e < S; ++e) {
+            dI0[bh * S + e] = gI[e];
+            dmu0[bh * S + e] = gM[e];
+        }
+        free(Is);
+        free(Ms);
+        free(gI);
+        free(gM);
+    }
+    return failed ? -2 : 0;
 }

@@ -246,6 +246,110 @@ def pin_resume(lib):
 
 
 # ----------------------------------------------------------------------------
+# Backward-pass pins: the reverse-mode oracle against derivatives obtained
+# without it
+
+_GRAD_OF = dict(q="dq", k="dk", v="dv", beta="dbeta", d="dd", A="dA", I0="dI0", mu0="dmu0")
+
+
+def _cotangents(x, seed):
+    rng = np.random.default_rng(seed)
+    B, H, T, dv = x["v"].shape
+    dk = x["q"].shape[-1]
+    return (rng.standard_normal((B, H, T, dv)), rng.standard_normal((B, H, dv, dk)),
+            rng.standard_normal((B, H, dv, dk)))
+
+
+def _loss(lib, x, cot):
+    dout, dmu, dI = cot
+    o, muT, IT = _run(lib, x)
+    return float(np.sum(dout * o) + np.sum(dmu * muT) + np.sum(dI * IT))
+
+
+def _bwd(lib, x, cot):
+    dout, dmu, dI = cot
+    return oracle.diag_scan_bwd(x["q"], x["k"], x["v"], x["beta"], x["d"], x["A"], x["I_prior"],
+                                x["I0"], x["mu0"], dout, dmu, dI, lib=lib)
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient equals the central difference of the forward oracle's
+    L = sum dout.o + sum dmu_T.mu_T + sum dI_T.I_T, element by element (fp64,
+    relative step 1e-6; truncation and rounding stay below 1e-8)."""
+    x = _inputs(B=1, H=2, T=5, dk=3, dv=2, with_state=True)
+    cot = _cotangents(x, seed=7)
+    g = _bwd(lib, x, cot)
+    for name, gname in _GRAD_OF.items():
+        base = x[name]
+        num = np.empty_like(base)
+        for idx in np.ndindex(base.shape):
+            h = 1e-6 * max(1.0, abs(base[idx]))
+            xp, xm = dict(x), dict(x)
+            xp[name] = base.copy()
+            xm[name] = base.copy()
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            num[idx] = (_loss(lib, xp, cot) - _loss(lib, xm, cot)) / (2 * h)
+        assert _rel(g[gname], num) < 1e-6, (name, _rel(g[gname], num))
+
+
+def _torch_forward(x):
+    """The forward update as vectorised fp64 torch operations per token (a
+    second statement of the definition, differentiated by torch.autograd)."""
+    import torch
+    t = {n: torch.tensor(x[n], dtype=torch.float64, requires_grad=True)
+         for n in ("q", "k", "v", "beta", "d", "A", "I0", "mu0")}
+    I, mu = t["I0"], t["mu0"]
+    outs = []
+    for s in range(t["q"].shape[2]):
+        alpha = torch.exp(-t["A"][None, :] * t["d"][:, :, s])[:, :, None, None]
+        bet = t["beta"][:, :, s, :, None]
+        kk = t["k"][:, :, s, None, :]
+        I_new = alpha * I + (1 - alpha) * x["I_prior"] + bet * kk * kk
+        mu = alpha * I / I_new * mu + bet * t["v"][:, :, s, :, None] * kk / I_new
+        I = I_new
+        outs.append((mu * t["q"][:, :, s, None, :]).sum(-1))
+    return t, torch.stack(outs, dim=2), mu, I
+
+
+def pin_bwd_autograd(lib):
+    """The reverse-mode oracle equals torch.autograd applied to the forward
+    written as tensor operations (d_k != d_v, several heads and batches)."""
+    import torch
+    x = _inputs(B=2, H=3, T=13, dk=4, dv=6, A=(0.7, 1.9, 0.2), with_state=True)
+    cot = _cotangents(x, seed=11)
+    g = _bwd(lib, x, cot)
+    t, o, mu, I = _torch_forward(x)
+    L = (o * torch.tensor(cot[0])).sum() + (mu * torch.tensor(cot[1])).sum() + \
+        (I * torch.tensor(cot[2])).sum()
+    L.backward()
+    for name, gname in _GRAD_OF.items():
+        assert _rel(g[gname], t[name].grad.numpy()) < 1e-11, name
+
+
+def pin_bwd_chain(lib):
+    """Backward over [0,T) equals the backward of [h,T) from the carried state,
+    whose initial-state gradients seed the backward of [0,h) as final-state
+    gradients (the chain rule across the split)."""
+    x = _inputs(B=2, H=2, T=12, with_state=True)
+    cot = _cotangents(x, seed=3)
+    full = _bwd(lib, x, cot)
+    h = 5
+    x1, x2 = dict(x), dict(x)
+    for n in ("q", "k", "v", "beta", "d"):
+        x1[n] = x[n][:, :, :h]
+        x2[n] = x[n][:, :, h:]
+    _, mu1, I1 = _run(lib, x1)
+    x2["I0"], x2["mu0"] = I1, mu1
+    g2 = _bwd(lib, x2, (cot[0][:, :, h:], cot[1], cot[2]))
+    g1 = _bwd(lib, x1, (cot[0][:, :, :h], g2["dmu0"], g2["dI0"]))
+    for gname in ("dq", "dk", "dv", "dbeta", "dd"):
+        assert _rel(np.concatenate([g1[gname], g2[gname]], axis=2), full[gname]) < 1e-12, gname
+    assert _rel(g1["dA"] + g2["dA"], full["dA"]) < 1e-12
+    assert _rel(g1["dI0"], full["dI0"]) < 1e-12 and _rel(g1["dmu0"], full["dmu0"]) < 1e-12
+
+
+# ----------------------------------------------------------------------------
 # Moebius pins
 
 def _mob_inputs(N=3, T=7, seed=RNG_SEED):
@@ -340,4 +444,5 @@ DIAG_PINS = [pin_information_form, pin_eta_identity, pin_alpha_one_posterior_mea
              pin_resume]
 MOBIUS_PINS = [pin_mobius_bracketings, pin_mobius_matrix_power, pin_mobius_affine,
                pin_mobius_product, pin_mobius_resume]
-ALL_PINS = DIAG_PINS + MOBIUS_PINS
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_chain]
+ALL_PINS = DIAG_PINS + MOBIUS_PINS + BWD_PINS

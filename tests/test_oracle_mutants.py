@@ -34,6 +34,19 @@ MUTANTS = {
     "readout_uses_importance": ("s += mu[i * dk + j] * qt[j]", "s += I[i * dk + j] * qt[j]"),
     "ignore_initial_importance": ("I[e] = I0 ? I0[bh * dv * dk + e] : I_prior;", "I[e] = I_prior;"),
     "ignore_initial_mean": ("mu[e] = mu0 ? mu0[bh * dv * dk + e] : 0.0;", "mu[e] = 0.0;"),
+    "bwd_drop_mean_over_importance": ("double g_In = gI[e] - gmu * Mn[e] / In[e];", "double g_In = gI[e];"),
+    "bwd_dq_previous_state": ("dqt[j] += ot_bar[i] * Mn[e];", "dqt[j] += ot_bar[i] * Mp[e];"),
+    "bwd_dk_factor_two": ("dkt[j] += g_In * 2.0 * bt[i] * kt[j];", "dkt[j] += g_In * bt[i] * kt[j];"),
+    "bwd_alpha_prior_term": ("g_alpha += g_In * (Ip[e] - I_prior);", "g_alpha += g_In * Ip[e];"),
+    "bwd_dd_sign": ("dd[bh * T + t] = g_alpha * (-A[h] * alpha);", "dd[bh * T + t] = g_alpha * (A[h] * alpha);"),
+    "bwd_dA_uses_A": ("gA += g_alpha * (-d[bh * T + t] * alpha);", "gA += g_alpha * (-A[h] * alpha);"),
+    "bwd_mean_carry_without_alpha": ("double g_Mp = gmu * alpha * Ip[e] / In[e];",
+                                     "double g_Mp = gmu * Ip[e] / In[e];"),
+    "bwd_dv_missing_beta": ("dvt[i] += gmu * bt[i] * kt[j] / In[e];", "dvt[i] += gmu * kt[j] / In[e];"),
+    "bwd_readout_cotangent_uses_k": ("double gmu = gM[e] + ot_bar[i] * qt[j];",
+                                     "double gmu = gM[e] + ot_bar[i] * kt[j];"),
+    "bwd_final_importance_ignored": ("gI[e] = dI_T ? dI_T[bh * S + e] : 0.0;", "gI[e] = 0.0;"),
+    "bwd_importance_carry_without_alpha": ("g_Ip += g_In * alpha;", "g_Ip += g_In;"),
     "mobius_swap_b_c": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
                         "lam = (a[e] * lam + c[e]) / (b[e] * lam + d[e]);"),
     "mobius_swap_c_d": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
