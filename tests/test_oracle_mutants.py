@@ -1,7 +1,8 @@
 """The pins catch plausible mistakes in the oracle (CPU only).
 
 Each case plants one mistake in a copy of ``oracle/kdn_oracle.c`` (a dropped
-term, a sign, a swapped operand or index, an off-by-one step), builds the copy
+term, a sign, a swapped operand or index, an off-by-one step; ``bwd_*`` cases
+in the backward function), builds the copy
 with gcc and requires that at least one pin of ``oracle_pins`` fails on it.
 The real oracle is never modified.
 """
@@ -46,6 +47,7 @@ MUTANTS = {
     "bwd_readout_cotangent_uses_k": ("double gmu = gM[e] + ot_bar[i] * qt[j];",
                                      "double gmu = gM[e] + ot_bar[i] * kt[j];"),
     "bwd_final_importance_ignored": ("gI[e] = dI_T ? dI_T[bh * S + e] : 0.0;", "gI[e] = 0.0;"),
+    "bwd_forward_drop_prior_leak": ("+ (1.0 - alpha) * I_prior", ""),
     "bwd_importance_carry_without_alpha": ("g_Ip += g_In * alpha;", "g_Ip += g_In;"),
     "mobius_swap_b_c": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
                         "lam = (a[e] * lam + c[e]) / (b[e] * lam + d[e]);"),
@@ -62,9 +64,15 @@ MUTANTS = {
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    # the backward restates the forward loop: bwd_* mutants edit the backward
+    # function, the others the forward functions before it
+    cut = src.index("int oracle_diag_scan_bwd(")
+    head, tail = src[:cut], src[cut:]
+    part = tail if name.startswith("bwd_") else head
+    assert part.count(old) == 1, f"mutation site for {name} not unique"
+    part = part.replace(old, new)
     mut = tmp_path / "mutant.c"
-    mut.write_text(src.replace(old, new))
+    mut.write_text(head + part if name.startswith("bwd_") else part + tail)
     so = str(tmp_path / "libmutant.so")
     oracle.build(force=True, src=str(mut), out=so)
     lib = oracle.load(so)
