@@ -73,6 +73,36 @@ kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v, const 
     return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
 }
 
+kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v, const void* beta,
+                             const void* d, const float* A, float I_prior, const float* I0,
+                             const float* mu0, const float* grad_out, const float* grad_final_state,
+                             float* grad_q, float* grad_k, float* grad_v, float* grad_beta,
+                             float* grad_d, float* grad_A, float* grad_init_state, int B, int H,
+                             int T, int dk, int dv, kdn_dtype in_dtype, void* stream) {
+    if (B < 1 || H < 1 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !beta || !d || !A || !grad_out || !grad_q || !grad_k ||
+                  !grad_v || !grad_beta || !grad_d))
+        return KDN_ERR_INVALID_ARG;
+    if (in_dtype != KDN_F32 && in_dtype != KDN_BF16) return KDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long dmax = dk > dv ? dk : dv;
+    if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / (dmax * dmax)) return KDN_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, beta, grad_out, I0, mu0, grad_final_state, grad_q, grad_k,
+                            grad_v, grad_beta, grad_init_state};
+    for (const void* p : ptrs16)
+        if (p && !aligned(p, 16)) return KDN_ERR_INVALID_ARG;
+    const void* ptrs4[] = {A, grad_d, grad_A};
+    for (const void* p : ptrs4)
+        if (p && !aligned(p, 4)) return KDN_ERR_INVALID_ARG;
+    if (d && !aligned(d, in_dtype == KDN_BF16 ? 2 : 4)) return KDN_ERR_INVALID_ARG;
+    if (T == 0 && !grad_init_state && !grad_A) return KDN_OK;
+    DiagBwdArgs a{q, k, v, beta, d, A, I_prior, I0, mu0, grad_out, grad_final_state, grad_q,
+                  grad_k, grad_v, grad_beta, grad_d, grad_A, grad_init_state, B, H, T, dk, dv,
+                  in_dtype};
+    return diag_bwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 kdn_status kdn_diag_step(const void* q, const void* k, const void* v, const void* beta, const void* d,
                          const float* A, float I_prior, float* state, float* out, int B, int H, int dk,
                          int dv, kdn_dtype in_dtype, void* stream) {

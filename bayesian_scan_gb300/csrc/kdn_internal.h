@@ -54,6 +54,31 @@ kdn_status diag_step_launch(const void* q, const void* k, const void* v, const v
                             const void* d, const float* A, float I_prior, float* state, float* out,
                             int B, int H, int dk, int dv, kdn_dtype dtype, cudaStream_t stream);
 
+// Arguments of one backward call after host-side validation (diag_bwd.cu).
+struct DiagBwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* beta;
+    const void* d;
+    const float* A;
+    float I_prior;
+    const float* I0;
+    const float* mu0;
+    const float* grad_out;
+    const float* grad_final_state;
+    float* grad_q;
+    float* grad_k;
+    float* grad_v;
+    float* grad_beta;
+    float* grad_d;
+    float* grad_A;
+    float* grad_init_state;
+    int B, H, T, dk, dv;
+    kdn_dtype dtype;
+};
+kdn_status diag_bwd_launch(const DiagBwdArgs& a, cudaStream_t stream);
+
 // Host-buffer pipelines (kdn_host.cu): arguments validated, every pointer a
 // host pointer; synchronous.
 kdn_status diag_host(const DiagArgs& a, cudaStream_t stream, long long wait_ns);

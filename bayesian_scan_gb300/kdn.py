@@ -51,6 +51,9 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_diag_scan_bwd.restype = i
+    lib.kdn_diag_scan_bwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
+                                      fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
     lib.kdn_diag_step.restype = i
     lib.kdn_diag_step.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, i, i, i, i, i, vp]
     lib.kdn_diag_scan_fwd_host.restype = i
@@ -150,6 +153,57 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     if st != KDN_OK:
         raise KdnError(st, "kdn_diag_scan_fwd")
     return out, final_state
+
+
+def diag_scan_bwd(q, k, v, beta, d, A, grad_out, I_prior=1.0, I0=None, mu0=None,
+                  grad_final_state=None, grad_init_state=True, stream=None):
+    """Backward pass of ``diag_scan_fwd`` (see ``kdn_diag_scan_bwd``).
+
+    Inputs as for ``diag_scan_fwd`` (device tensors); ``grad_out`` [B,H,T,dv]
+    fp32; ``grad_final_state`` [2,B,H,dv,dk] fp32 or None.  ``grad_init_state``
+    True (allocate), False/None (skip) or a [2,B,H,dv,dk] fp32 tensor.
+    Returns a dict: q, k [B,H,T,dk]; v, beta [B,H,T,dv]; d [B,H,T]; A [H];
+    init_state [2,B,H,dv,dk] or None (all fp32).
+    """
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    if not q.is_cuda:
+        raise ValueError("diag_scan_bwd takes device tensors")
+    _check(q, "q", dt)
+    _check(k, "k", dt, (B, H, T, dk))
+    _check(v, "v", dt, (B, H, T, dv))
+    _check(beta, "beta", dt, (B, H, T, dv))
+    _check(d, "d", dt, (B, H, T))
+    _check(A, "A", torch.float32, (H,))
+    _check(grad_out, "grad_out", torch.float32, (B, H, T, dv))
+    for name, t in (("I0", I0), ("mu0", mu0)):
+        if t is not None:
+            _check(t, name, torch.float32, (B, H, dv, dk))
+    if grad_final_state is not None:
+        _check(grad_final_state, "grad_final_state", torch.float32, (2, B, H, dv, dk))
+    f32 = dict(device=q.device, dtype=torch.float32)
+    g = dict(q=torch.empty(B, H, T, dk, **f32), k=torch.empty(B, H, T, dk, **f32),
+             v=torch.empty(B, H, T, dv, **f32), beta=torch.empty(B, H, T, dv, **f32),
+             d=torch.empty(B, H, T, **f32), A=torch.empty(H, **f32))
+    if grad_init_state is True:
+        grad_init_state = torch.empty(2, B, H, dv, dk, **f32)
+    elif grad_init_state is False:
+        grad_init_state = None
+    if grad_init_state is not None:
+        _check(grad_init_state, "grad_init_state", torch.float32, (2, B, H, dv, dk))
+    g["init_state"] = grad_init_state
+    st = lib.kdn_diag_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                               float(I_prior), _ptr(I0), _ptr(mu0), _ptr(grad_out),
+                               _ptr(grad_final_state), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]),
+                               _ptr(g["beta"]), _ptr(g["d"]), _ptr(g["A"]), _ptr(grad_init_state),
+                               B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
+                               _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_scan_bwd")
+    return g
 
 
 def diag_step(q, k, v, beta, d, A, state, I_prior=1.0, out=None, stream=None):

@@ -115,6 +115,15 @@ def draw_diag(B, H, T, dk, dv, dtype=torch.bfloat16, A_law=("const", 1.0), seed=
     return cast(q), cast(k), cast(v), cast(beta), cast(d), A.contiguous()
 
 
+def draw_cotangents(B, H, T, dk, dv, seed=0, gen: torch.Generator | None = None):
+    """Draw the gradients that flow into a backward call: grad_out
+    [B,H,T,dv] and grad_final_state [2,B,H,dv,dk], fp32 N(0,1)."""
+    g = gen if gen is not None else torch.Generator().manual_seed(seed)
+    gout = torch.randn(B, H, T, dv, generator=g, dtype=torch.float32)
+    gfs = torch.randn(2, B, H, dv, dk, generator=g, dtype=torch.float32)
+    return gout, gfs
+
+
 def draw_mobius(N, T, seed=0, gen: torch.Generator | None = None):
     """Draw Moebius coefficients a, b, c, d [N,T] and lambda0 [N] (fp32)."""
     g = gen if gen is not None else torch.Generator().manual_seed(seed)

@@ -100,6 +100,49 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
                              kdn_dtype in_dtype, void* stream);
 
 /*
+ * kdn_diag_scan_bwd -- backward pass of kdn_diag_scan_fwd (the pages' kernels
+ * serve training on GPUs: "Learning to Remember, Learn, and Forget in
+ * Attention-Based Models", Contributi Chiave).  For the scalar
+ *     L = sum grad_out . out + sum dmu_T . mu_T + sum dI_T . I_T
+ * of the forward call with the same inputs, writes dL/d(input) for every
+ * input.  The forward is recomputed inside the call (nothing from a forward
+ * call is needed).
+ *
+ *   q, k, v, beta, d, A, I_prior, I0, mu0   as for kdn_diag_scan_fwd
+ *   grad_out          [B,H,T,dv] fp32   dL/d out
+ *   grad_final_state  [2,B,H,dv,dk] fp32 or NULL   dL/d mu_T then dL/d I_T
+ *                                    (NULL: the final state is not used)
+ *   grad_q, grad_k    [B,H,T,dk] fp32   written
+ *   grad_v, grad_beta [B,H,T,dv] fp32   written
+ *   grad_d            [B,H,T]    fp32   written
+ *   grad_A            [H] fp32 or NULL  written: summed over the batch
+ *   grad_init_state   [2,B,H,dv,dk] fp32 or NULL   written: dL/d mu_0 then
+ *                     dL/d I_0 (of the initial state used, given or default)
+ *   I_prior gets no gradient (a fixed hyperparameter).
+ *
+ *   B >= 1, H >= 1, T >= 0; dk, dv in {16, 32, 64, 128};
+ *   B*H*T*max(dk,dv)^2 < 2^62.  Array pointers 16-byte aligned (d and A:
+ *   element-aligned; grad_d, grad_A: 4-byte aligned).  With T = 0 only
+ *   grad_init_state (= grad_final_state) and grad_A (= 0) are written.
+ *
+ * Scratch: one stream-ordered allocation (cudaMallocAsync, freed on the
+ * stream before return; KDN_ERR_ALLOC if it cannot be had) of about
+ * B*H*T*dv*dk + 8*B*H*T*dv bytes (every 8th token's state, and per-column-
+ * block row sums).  Each CTA owns all of its SM's tensor memory while it
+ * runs.  Arithmetic: fp32 (the information form eta = I mu, J = I - I_prior);
+ * results are deterministic (fixed summation order).
+ */
+KDN_API kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v,
+                             const void* beta, const void* d, const float* A,
+                             float I_prior, const float* I0, const float* mu0,
+                             const float* grad_out, const float* grad_final_state,
+                             float* grad_q, float* grad_k, float* grad_v,
+                             float* grad_beta, float* grad_d, float* grad_A,
+                             float* grad_init_state,
+                             int B, int H, int T, int dk, int dv,
+                             kdn_dtype in_dtype, void* stream);
+
+/*
  * kdn_mobius_scan -- lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t)
  * for N independent sequences.
  *

@@ -12,6 +12,12 @@ import oracle
 
 TOL_DIAG = 2e-3
 TOL_MOBIUS = 1e-5
+# backward pass (every gradient, fp32 arithmetic): an fp32 model of the same
+# algorithm (information-form adjoints, checkpointed recompute) stays within
+# 5e-7 of the fp64 oracle on T <= 300; the bar leaves room for the GPU's
+# summation order, its approximate reciprocal (2^-21 relative) and longer
+# adjoint recurrences.
+TOL_BWD = 2e-4
 
 
 def rel_err(x, ref):
@@ -66,3 +72,36 @@ def check_mobius(a, b, c, d, lam0, tol=TOL_MOBIUS):
     e = rel_err(out, ref)
     assert e <= tol, e
     return e
+
+
+def gpu_bwd(inp, gout, gfs=None, I0=None, mu0=None):
+    from bayesian_scan_gb300 import kdn
+    dev = "cuda"
+    args = [inp[n].to(dev) for n in ("q", "k", "v", "beta", "d", "A")]
+    g = kdn.diag_scan_bwd(*args, gout.to(dev), I_prior=inp["I_prior"],
+                          I0=None if I0 is None else I0.to(dev),
+                          mu0=None if mu0 is None else mu0.to(dev),
+                          grad_final_state=None if gfs is None else gfs.to(dev))
+    torch.cuda.synchronize()
+    assert kdn.get_device_error() == 0
+    return {n: (t.cpu() if t is not None else None) for n, t in g.items()}
+
+
+def oracle_bwd(inp, gout, gfs=None, I0=None, mu0=None):
+    return oracle.diag_scan_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d"], inp["A"],
+                                inp["I_prior"], I0, mu0, gout,
+                                None if gfs is None else gfs[0], None if gfs is None else gfs[1])
+
+
+BWD_NAMES = dict(q="dq", k="dk", v="dv", beta="dbeta", d="dd", A="dA")
+
+
+def check_bwd(inp, gout, gfs=None, I0=None, mu0=None, tol=TOL_BWD):
+    g = gpu_bwd(inp, gout, gfs, I0, mu0)
+    r = oracle_bwd(inp, gout, gfs, I0, mu0)
+    errs = {n: rel_err(g[n], r[o]) for n, o in BWD_NAMES.items()}
+    errs["mu0"] = rel_err(g["init_state"][0], r["dmu0"])
+    errs["I0"] = rel_err(g["init_state"][1], r["dI0"])
+    for k_, e in errs.items():
+        assert e <= tol, (k_, errs)
+    return errs

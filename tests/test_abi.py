@@ -144,3 +144,34 @@ def test_host_mobius_rejects(lib):
     assert lib.kdn_mobius_scan_host(vp(FAKE + 1), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 4, 16,
                                     None) == -1
     assert lib.kdn_mobius_scan_host(None, None, None, None, None, None, 0, 16, None) == 0
+
+
+def _bwd(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, I0=None, mu0=None, go=FAKE,
+         gfs=None, gq=FAKE, gk=FAKE, gv=FAKE, gb=FAKE, gd=FAKE, gA=FAKE, gis=None, B=1, H=1, T=8,
+         dk=16, dv=16, dtype=1):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_diag_scan_bwd(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), 1.0, vp(I0), vp(mu0),
+                                 vp(go), vp(gfs), vp(gq), vp(gk), vp(gv), vp(gb), vp(gd), vp(gA),
+                                 vp(gis), B, H, T, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d", "A", "go", "gq", "gk", "gv", "gb", "gd"])
+def test_bwd_null_pointer(lib, field):
+    assert _bwd(lib, **{field: None}) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), -1), (dict(H=-2), -1), (dict(T=-1), -1), (dict(dk=8), -2), (dict(dv=80), -2),
+    (dict(dtype=4), -2), (dict(q=FAKE + 2), -1), (dict(go=FAKE + 4), -1), (dict(gq=FAKE + 8), -1),
+    (dict(gis=FAKE + 4), -1), (dict(gfs=FAKE + 8), -1), (dict(I0=FAKE + 4), -1),
+    (dict(gd=FAKE + 2), -1), (dict(gA=FAKE + 1), -1), (dict(d=FAKE + 1), -1),
+    (dict(B=1 << 20, H=1 << 20, T=1 << 20), -1),
+])
+def test_bwd_rejects(lib, kw, status):
+    assert _bwd(lib, **kw) == status
+
+
+def test_bwd_empty_without_state_outputs_is_a_no_op(lib):
+    # T = 0 and nothing to write: OK without touching any buffer
+    assert _bwd(lib, q=None, k=None, v=None, beta=None, d=None, A=None, go=None, gq=None, gk=None,
+                gv=None, gb=None, gd=None, gA=None, T=0) == 0
