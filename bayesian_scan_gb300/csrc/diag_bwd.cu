@@ -59,7 +59,6 @@ namespace bwd {
 namespace {
 
 constexpr int C = 8;             // tokens per chunk (TMEM history depth)
-constexpr int MAX_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MIN_SMEM = 120 * 1024;   // keeps one CTA per SM (the CTA owns all of TMEM)
 constexpr unsigned FULL = 0xffffffffu;
@@ -83,46 +82,44 @@ struct Args {
     float* prow;           // [NCB][BH*T][2*dv]
     float* pD;             // [NCB][BH*T]  partial dL/dalpha_t
     long long BH;
-    int H, T, dk, dv, cwb, ncb, nt, nC;
+    int H, T, dk, ncb, nC;
 };
 
-// Shared-memory carve-up of one CTA (byte offsets, all 16-byte aligned).
-struct Layout {
-    int s_k, s_kk, s_q, s_b, s_bv, s_al;           // converted chunk inputs (fp32)
-    int raw[2];                                     // raw chunk buffers (cp.async targets)
-    int r_k, r_q, r_b, r_v, r_do, r_ck;             // offsets inside a raw buffer
-    int s_row, s_dq, s_dk, s_D, holder;
-    int total;
+__host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
+
+// Tile of one CTA: all DV rows x CWB key columns; a thread owns 4 rows x 4
+// columns (NR row quads x NCQ column quads; lanes run over the row quads).
+template <typename TIn, int DV, int CWB>
+struct Tile {
+    static constexpr int ES = sizeof(TIn);
+    static constexpr int NR = DV / 4, NCQ = CWB / 4, NTA = NR * NCQ;
+    static constexpr int NT = NTA < 32 ? 32 : NTA, NW = NT / 32;
+    static_assert(NT <= 256, "at most 8 warps (two per TMEM lane quarter)");
+    // shared memory (byte offsets)
+    static constexpr int s_k = 0;
+    static constexpr int s_kk = s_k + align16(C * CWB * 4);
+    static constexpr int s_q = s_kk + align16(C * CWB * 4);
+    static constexpr int s_b = s_q + align16(C * CWB * 4);
+    static constexpr int s_bv = s_b + align16(C * DV * 4);
+    static constexpr int s_al = s_bv + align16(C * DV * 4);
+    static constexpr int r_k = 0;                                 // inside a raw buffer
+    static constexpr int r_q = r_k + align16(C * CWB * ES);
+    static constexpr int r_b = r_q + align16(C * CWB * ES);
+    static constexpr int r_v = r_b + align16(C * DV * ES);
+    static constexpr int r_do = r_v + align16(C * DV * ES);
+    static constexpr int r_ck = r_do + align16(C * DV * 4);
+    static constexpr int RAW = r_ck + align16(32 * NT * 4);
+    static constexpr int raw0 = s_al + align16(C * 4);
+    static constexpr int raw1 = raw0 + RAW;
+    static constexpr int s_row = raw1 + RAW;
+    static constexpr int s_dq = s_row + align16(C * 2 * NCQ * DV * 4);
+    static constexpr int s_dk = s_dq + align16(C * CWB * 4);
+    static constexpr int s_D = s_dk + align16(C * CWB * 4);
+    static constexpr int holder = s_D + align16(C * NW * 4);
+    static constexpr int used = holder + 16;
+    static constexpr int SMEM = used < MIN_SMEM ? MIN_SMEM : used;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
-
-__host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
-
-__host__ __device__ inline Layout make_layout(int dv, int cwb, int nt, int es) {
-    Layout L{};
-    int o = 0;
-    L.s_k = o;  o += align16(C * cwb * 4);
-    L.s_kk = o; o += align16(C * cwb * 4);
-    L.s_q = o;  o += align16(C * cwb * 4);
-    L.s_b = o;  o += align16(C * dv * 4);
-    L.s_bv = o; o += align16(C * dv * 4);
-    L.s_al = o; o += align16(C * 4);
-    int r = 0;
-    L.r_k = r;  r += align16(C * cwb * es);
-    L.r_q = r;  r += align16(C * cwb * es);
-    L.r_b = r;  r += align16(C * dv * es);
-    L.r_v = r;  r += align16(C * dv * es);
-    L.r_do = r; r += align16(C * dv * 4);
-    L.r_ck = r; r += align16(32 * nt * 4);
-    L.raw[0] = o; o += r;
-    L.raw[1] = o; o += r;
-    L.s_row = o; o += align16(C * 2 * (cwb / 4) * dv * 4);
-    L.s_dq = o;  o += align16(C * cwb * 4);
-    L.s_dk = o;  o += align16(C * cwb * 4);
-    L.s_D = o;   o += align16(C * (MAX_THREADS / 32) * 4);
-    L.holder = o; o += 16;
-    L.total = o < MIN_SMEM ? MIN_SMEM : o;
-    return L;
-}
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
@@ -137,9 +134,6 @@ template <>
 __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-template <typename TIn>
-__device__ __forceinline__ float load_in(const TIn* p) { return to_f<TIn>(*p); }
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
@@ -164,119 +158,210 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float v[32]) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Load without waiting; the registers are valid after tmem_wait_ld / tmem_dep.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float v[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+          "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
+          "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
+          "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+// Waits for this thread's outstanding TMEM loads; `v` is passed through so
+// that no use of the loaded registers moves above the wait.
+__device__ __forceinline__ void tmem_wait_ld(float v[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                   "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                   "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                   "+f"(v[30]), "+f"(v[31])
+                 :
+                 : "memory");
+}
+// Compiler-only dependency: registers of a load covered by an earlier wait.
+__device__ __forceinline__ void tmem_dep(float v[32]) {
+    asm volatile(""
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                   "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                   "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                   "+f"(v[30]), "+f"(v[31]));
+}
+
 // Issue the cp.async copies of chunk c (tokens [c*C, c*C + n)) into raw
 // buffer `rb`: the CTA's k (and q) column block, beta, v (and dout) rows and,
 // in the backward sweep, the chunk's checkpoint.
-template <typename TIn>
-__device__ void issue_chunk(const Args& p, unsigned char* rb, const Layout& L, long long bh, int cb,
-                            int c, int n, bool bwd, int tid) {
-    const int es = sizeof(TIn);
+template <typename TIn, int DV, int CWB>
+__device__ __forceinline__ void issue_chunk(const Args& p, unsigned char* rb, long long bh, int cb,
+                                            int c, int n, bool bwd, int tid) {
+    using Tl = Tile<TIn, DV, CWB>;
+    constexpr int ES = Tl::ES, NT = Tl::NT;
+    constexpr int KP = CWB * ES / 16;                      // 16-byte pieces per token row
     const long long tok0 = bh * p.T + static_cast<long long>(c) * C;
-    // column-block slices: n rows of cwb*es bytes
-    const int kp = p.cwb * es / 16;                      // 16-byte pieces per token row
-    const char* kg = static_cast<const char*>(p.k) + (tok0 * p.dk + cb * p.cwb) * es;
-    const char* qg = static_cast<const char*>(p.q) + (tok0 * p.dk + cb * p.cwb) * es;
-    for (int i = tid; i < n * kp; i += p.nt) {
-        const int s = i / kp, w = i % kp;
-        cp_async16(rb + L.r_k + s * p.cwb * es + w * 16, kg + static_cast<long long>(s) * p.dk * es + w * 16);
-        if (bwd)
-            cp_async16(rb + L.r_q + s * p.cwb * es + w * 16, qg + static_cast<long long>(s) * p.dk * es + w * 16);
+    const char* kg = static_cast<const char*>(p.k) + (tok0 * p.dk + cb * CWB) * ES;
+    const char* qg = static_cast<const char*>(p.q) + (tok0 * p.dk + cb * CWB) * ES;
+    for (int i = tid; i < n * KP; i += NT) {
+        const int s = i / KP, w = i % KP;
+        cp_async16(rb + Tl::r_k + i * 16, kg + static_cast<long long>(s) * p.dk * ES + w * 16);
+        if (bwd) cp_async16(rb + Tl::r_q + i * 16, qg + static_cast<long long>(s) * p.dk * ES + w * 16);
     }
-    // rows: n * dv contiguous elements
-    const int rp = n * p.dv * es / 16;
-    const char* bg = static_cast<const char*>(p.beta) + tok0 * p.dv * es;
-    const char* vg = static_cast<const char*>(p.v) + tok0 * p.dv * es;
-    for (int i = tid; i < rp; i += p.nt) {
-        cp_async16(rb + L.r_b + i * 16, bg + i * 16);
-        cp_async16(rb + L.r_v + i * 16, vg + i * 16);
+    const int rp = n * (DV * ES / 16);
+    const char* bg = static_cast<const char*>(p.beta) + tok0 * DV * ES;
+    const char* vg = static_cast<const char*>(p.v) + tok0 * DV * ES;
+    for (int i = tid; i < rp; i += NT) {
+        cp_async16(rb + Tl::r_b + i * 16, bg + i * 16);
+        cp_async16(rb + Tl::r_v + i * 16, vg + i * 16);
     }
     if (bwd) {
-        const int op = n * p.dv * 4 / 16;
-        const char* og = reinterpret_cast<const char*>(p.dout + tok0 * p.dv);
-        for (int i = tid; i < op; i += p.nt) cp_async16(rb + L.r_do + i * 16, og + i * 16);
+        const int op = n * (DV / 4);
+        const char* og = reinterpret_cast<const char*>(p.dout + tok0 * DV);
+        for (int i = tid; i < op; i += NT) cp_async16(rb + Tl::r_do + i * 16, og + i * 16);
         const char* cg = reinterpret_cast<const char*>(
-            p.ckpt + ((bh * p.ncb + cb) * p.nC + c) * 32LL * p.nt);
-        for (int i = tid; i < 32 * p.nt / 4; i += p.nt) cp_async16(rb + L.r_ck + i * 16, cg + i * 16);
+            p.ckpt + ((bh * p.ncb + cb) * p.nC + c) * 32LL * NT);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) cp_async16(rb + Tl::r_ck + (m * NT + tid) * 16, cg + (m * NT + tid) * 16);
     }
     cp_async_commit();
 }
 
 // Converts the raw chunk inputs to fp32 (k, k^2, q, beta, beta v, alpha).
-template <typename TIn>
-__device__ void convert_chunk(const Args& p, unsigned char* sm, const unsigned char* rb,
-                              const Layout& L, int n, bool bwd, float alpha, int tid) {
-    const TIn* rk = reinterpret_cast<const TIn*>(rb + L.r_k);
-    const TIn* rq = reinterpret_cast<const TIn*>(rb + L.r_q);
-    const TIn* rbt = reinterpret_cast<const TIn*>(rb + L.r_b);
-    const TIn* rv = reinterpret_cast<const TIn*>(rb + L.r_v);
-    float* sk = reinterpret_cast<float*>(sm + L.s_k);
-    float* skk = reinterpret_cast<float*>(sm + L.s_kk);
-    float* sq = reinterpret_cast<float*>(sm + L.s_q);
-    float* sb = reinterpret_cast<float*>(sm + L.s_b);
-    float* sbv = reinterpret_cast<float*>(sm + L.s_bv);
-    for (int i = tid; i < n * p.cwb; i += p.nt) {
+template <typename TIn, int DV, int CWB>
+__device__ __forceinline__ void convert_chunk(unsigned char* sm, const unsigned char* rb, int n,
+                                              bool bwd, TIn d_raw, float A_h, int tid) {
+    using Tl = Tile<TIn, DV, CWB>;
+    constexpr int NT = Tl::NT;
+    const TIn* rk = reinterpret_cast<const TIn*>(rb + Tl::r_k);
+    const TIn* rq = reinterpret_cast<const TIn*>(rb + Tl::r_q);
+    const TIn* rbt = reinterpret_cast<const TIn*>(rb + Tl::r_b);
+    const TIn* rv = reinterpret_cast<const TIn*>(rb + Tl::r_v);
+    float* sk = reinterpret_cast<float*>(sm + Tl::s_k);
+    float* skk = reinterpret_cast<float*>(sm + Tl::s_kk);
+    float* sq = reinterpret_cast<float*>(sm + Tl::s_q);
+    float* sb = reinterpret_cast<float*>(sm + Tl::s_b);
+    float* sbv = reinterpret_cast<float*>(sm + Tl::s_bv);
+    for (int i = tid; i < n * CWB; i += NT) {
         const float kv = to_f<TIn>(rk[i]);
         sk[i] = kv;
         skk[i] = kv * kv;
         if (bwd) sq[i] = to_f<TIn>(rq[i]);
     }
-    for (int i = tid; i < n * p.dv; i += p.nt) {
+    for (int i = tid; i < n * DV; i += NT) {
         const float b = to_f<TIn>(rbt[i]);
         sb[i] = b;
         sbv[i] = b * to_f<TIn>(rv[i]);
     }
-    if (tid < n) reinterpret_cast<float*>(sm + L.s_al)[tid] = alpha;
+    if (tid < n) reinterpret_cast<float*>(sm + Tl::s_al)[tid] = expf(-A_h * to_f<TIn>(d_raw));
 }
 
-// alpha of token t of head bh (t < T), from d and A.
+// d of token t of head bh (t < T), raw: converted when the chunk is (the
+// load stays in flight across a chunk's compute)
 template <typename TIn>
-__device__ __forceinline__ float alpha_of(const Args& p, long long bh, long long t) {
-    const float dd = load_in<TIn>(static_cast<const TIn*>(p.d) + bh * p.T + t);
-    return expf(-p.A[bh % p.H] * dd);
+__device__ __forceinline__ TIn d_of(const Args& p, long long bh, long long t) {
+    return static_cast<const TIn*>(p.d)[bh * p.T + t];
 }
 
 // Sum over the NR lanes sharing a column quad of 12 values (3 per column:
 // dq, dk-from-J, dk-from-eta partials).  Two halving levels leave each lane
 // 3 values that are then summed over the remaining levels; afterwards a lane
 // holds the totals of column g = 2 [rq & NR/2] + [rq & NR/4].
-__device__ __forceinline__ void column_reduce(float v[12], int NR, int rq) {
-    int o = NR >> 1;
-    bool up = (rq & o) != 0;
+template <int NR>
+__device__ __forceinline__ void column_reduce(float v[12], int rq) {
+    constexpr int o1 = NR / 2, o2 = NR / 4;
+    const bool up1 = (rq & o1) != 0, up2 = (rq & o2) != 0;
 #pragma unroll
     for (int m = 0; m < 6; ++m) {
-        const float send = up ? v[m] : v[m + 6];
-        const float keep = up ? v[m + 6] : v[m];
-        v[m] = keep + __shfl_xor_sync(FULL, send, o);
+        const float send = up1 ? v[m] : v[m + 6];
+        const float keep = up1 ? v[m + 6] : v[m];
+        v[m] = keep + __shfl_xor_sync(FULL, send, o1);
     }
-    o >>= 1;
-    up = (rq & o) != 0;
 #pragma unroll
     for (int m = 0; m < 3; ++m) {
-        const float send = up ? v[m] : v[m + 3];
-        const float keep = up ? v[m + 3] : v[m];
-        v[m] = keep + __shfl_xor_sync(FULL, send, o);
+        const float send = up2 ? v[m] : v[m + 3];
+        const float keep = up2 ? v[m + 3] : v[m];
+        v[m] = keep + __shfl_xor_sync(FULL, send, o2);
     }
-    for (o >>= 1; o > 0; o >>= 1) {
+#pragma unroll
+    for (int o = o2 / 2; o > 0; o /= 2)
 #pragma unroll
         for (int m = 0; m < 3; ++m) v[m] += __shfl_xor_sync(FULL, v[m], o);
-    }
 }
 
-template <typename TIn>
-__global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) {
+// Per-token inputs of one thread: its 4 rows and 4 columns.
+struct TokIn {
+    float bet[4], bvv[4], dov[4];
+    float2 kf[2], kq[2], qf[2];
+};
+
+// One adjoint step (token t, state st = (J_t, eta_t) as stored in TMEM): the
+// alpha sum of token t+1 with the adjoints as they come in, then the
+// adjoints of token t, then token t's partial sums.
+__device__ __forceinline__ void adjoint_step(const float st[32], const TokIn& in, float alpha_next,
+                                             float Ip, float2 (&GJ)[4][2], float2 (&GE)[4][2],
+                                             float cv[12], float rsum[8], float& dsum) {
+    const float2 ap = f2(alpha_next), ipp = f2(Ip);
+    float2 cdq[2], cck[2], cce[2], dacc[2];
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) cdq[c2] = cck[c2] = cce[c2] = dacc[c2] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float2 rsb = make_float2(0.f, 0.f), rse = rsb;
+        const float2 dov = f2(in.dov[r]), bet = f2(in.bet[r]), bvv = f2(in.bvv[r]);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const float2 Jt = make_float2(st[4 * r + 2 * c2], st[4 * r + 2 * c2 + 1]);
+            const float2 Et = make_float2(st[16 + 4 * r + 2 * c2], st[16 + 4 * r + 2 * c2 + 1]);
+            const float2 den = __fadd2_rn(Jt, ipp);
+            const float2 rr = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+            const float2 mu = __fmul2_rn(Et, rr);
+            const float2 a = __fmul2_rn(__fmul2_rn(dov, in.qf[c2]), rr);
+            dacc[c2] = __ffma2_rn(GJ[r][c2], Jt, dacc[c2]);
+            dacc[c2] = __ffma2_rn(GE[r][c2], Et, dacc[c2]);
+            GE[r][c2] = __ffma2_rn(ap, GE[r][c2], a);
+            const float2 am = __fmul2_rn(a, mu);
+            GJ[r][c2] = __ffma2_rn(ap, GJ[r][c2], make_float2(-am.x, -am.y));
+            cdq[c2] = __ffma2_rn(dov, mu, cdq[c2]);
+            rsb = __ffma2_rn(GJ[r][c2], in.kq[c2], rsb);
+            rse = __ffma2_rn(GE[r][c2], in.kf[c2], rse);
+            cck[c2] = __ffma2_rn(bet, GJ[r][c2], cck[c2]);
+            cce[c2] = __ffma2_rn(bvv, GE[r][c2], cce[c2]);
+        }
+        rsum[r] = rsb.x + rsb.y;
+        rsum[4 + r] = rse.x + rse.y;
+    }
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+        cv[3 * (2 * c2)] = cdq[c2].x;
+        cv[3 * (2 * c2) + 1] = cck[c2].x;
+        cv[3 * (2 * c2) + 2] = cce[c2].x;
+        cv[3 * (2 * c2 + 1)] = cdq[c2].y;
+        cv[3 * (2 * c2 + 1) + 1] = cck[c2].y;
+        cv[3 * (2 * c2 + 1) + 2] = cce[c2].y;
+    }
+    const float2 ds = __fadd2_rn(dacc[0], dacc[1]);
+    dsum = ds.x + ds.y;
+}
+
+template <typename TIn, int DV, int CWB>
+__global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(const Args p) {
+    using Tl = Tile<TIn, DV, CWB>;
+    constexpr int NR = Tl::NR, NCQ = Tl::NCQ, NT = Tl::NT, NW = Tl::NW;
     extern __shared__ __align__(128) unsigned char sm[];
-    const int es = sizeof(TIn);
-    const Layout L = make_layout(p.dv, p.cwb, p.nt, es);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long bh = blockIdx.x / p.ncb;
     const int cb = blockIdx.x % p.ncb;
-    const int NR = p.dv / 4, NCQ = p.cwb / 4;
-    const bool valid = tid < NR * NCQ;
+    const bool valid = tid < Tl::NTA;
     const int rq = valid ? tid % NR : 0, cq = valid ? tid / NR : 0;
     const int row0 = 4 * rq, col0 = 4 * cq;                    // inside the tile
-    const long long S = static_cast<long long>(p.dv) * p.dk;
+    const long long S = static_cast<long long>(DV) * p.dk;
     const float Ip = p.Ip;
-    uint32_t* holder = reinterpret_cast<uint32_t*>(sm + L.holder);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(sm + Tl::holder);
 
     if (warp == 0) tmem_alloc(holder, TMEM_COLS);
     tc_fence_before_sync();
@@ -290,7 +375,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
     float2 J[4][2], E[4][2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * p.cwb + col0;
+        const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
         float4 i4 = make_float4(Ip, Ip, Ip, Ip), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid && p.I0) i4 = *reinterpret_cast<const float4*>(p.I0 + off);
         if (valid && p.mu0) m4 = *reinterpret_cast<const float4*>(p.mu0 + off);
@@ -300,61 +385,62 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
         E[r][1] = make_float2(i4.z * m4.z, i4.w * m4.w);
     }
 
-    auto raw = [&](int i) { return sm + (i ? L.raw[1] : L.raw[0]); };
-    const float* sk = reinterpret_cast<const float*>(sm + L.s_k);
-    const float* skk = reinterpret_cast<const float*>(sm + L.s_kk);
-    const float* sq = reinterpret_cast<const float*>(sm + L.s_q);
-    const float* sb = reinterpret_cast<const float*>(sm + L.s_b);
-    const float* sbv = reinterpret_cast<const float*>(sm + L.s_bv);
-    const float* sal = reinterpret_cast<const float*>(sm + L.s_al);
-    float* ckpt_cta = p.ckpt + (bh * p.ncb + cb) * static_cast<long long>(p.nC) * 32 * p.nt;
+    auto raw = [&](int i) { return sm + (i ? Tl::raw1 : Tl::raw0); };
+    const float* sk = reinterpret_cast<const float*>(sm + Tl::s_k);
+    const float* skk = reinterpret_cast<const float*>(sm + Tl::s_kk);
+    const float* sq = reinterpret_cast<const float*>(sm + Tl::s_q);
+    const float* sb = reinterpret_cast<const float*>(sm + Tl::s_b);
+    const float* sbv = reinterpret_cast<const float*>(sm + Tl::s_bv);
+    const float* sal = reinterpret_cast<const float*>(sm + Tl::s_al);
+    float* ckpt_cta = p.ckpt + (bh * p.ncb + cb) * static_cast<long long>(p.nC) * 32 * NT;
     const int nC = p.nC;
     auto ntok = [&](int c) { return min(C, p.T - c * C); };
+    // one forward step of the tile on token s of the converted chunk
+    auto forward_step = [&](int s) {
+        const float2 al = f2(sal[s]);
+        const float4 b4 = *reinterpret_cast<const float4*>(sb + s * DV + row0);
+        const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * DV + row0);
+        const float4 k4 = *reinterpret_cast<const float4*>(sk + s * CWB + col0);
+        const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * CWB + col0);
+        const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
+        const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
+        const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
+                E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
+            }
+    };
 
     // ---- forward sweep: checkpoints every C tokens -------------------------
-    float dreg = 1.f;   // alpha of token (chunk start + tid), prefetched
+    const float A_h = p.A[bh % p.H];
+    TIn dreg{};   // d of token (chunk start + tid), prefetched
     if (nC > 0) {
-        issue_chunk<TIn>(p, raw(0), L, bh, cb, 0, ntok(0), false, tid);
-        if (tid < ntok(0)) dreg = alpha_of<TIn>(p, bh, tid);
+        issue_chunk<TIn, DV, CWB>(p, raw(0), bh, cb, 0, ntok(0), false, tid);
+        if (tid < ntok(0)) dreg = d_of<TIn>(p, bh, tid);
     }
     for (int c = 0; c < nC; ++c) {
         const int n = ntok(c);
-        // checkpoint: the tile's state before chunk c
-        {
-            float* dst = ckpt_cta + static_cast<long long>(c) * 32 * p.nt;
+        {   // checkpoint: the tile's state before chunk c
+            float4* dst = reinterpret_cast<float4*>(ckpt_cta + static_cast<long long>(c) * 32 * NT);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                reinterpret_cast<float4*>(dst)[(2 * r) * p.nt + tid] =
-                    make_float4(J[r][0].x, J[r][0].y, J[r][1].x, J[r][1].y);
-                reinterpret_cast<float4*>(dst)[(2 * r + 1) * p.nt + tid] =
-                    make_float4(E[r][0].x, E[r][0].y, E[r][1].x, E[r][1].y);
+                dst[(2 * r) * NT + tid] = make_float4(J[r][0].x, J[r][0].y, J[r][1].x, J[r][1].y);
+                dst[(2 * r + 1) * NT + tid] = make_float4(E[r][0].x, E[r][0].y, E[r][1].x, E[r][1].y);
             }
         }
         cp_async_wait_all();
         __syncthreads();   // chunk c landed; chunk c-1's compute finished
-        convert_chunk<TIn>(p, sm, raw(c & 1), L, n, false, dreg, tid);
+        convert_chunk<TIn, DV, CWB>(sm, raw(c & 1), n, false, dreg, A_h, tid);
         if (c + 1 < nC) {
-            issue_chunk<TIn>(p, raw((c + 1) & 1), L, bh, cb, c + 1, ntok(c + 1), false, tid);
-            if (tid < ntok(c + 1)) dreg = alpha_of<TIn>(p, bh, static_cast<long long>(c + 1) * C + tid);
+            issue_chunk<TIn, DV, CWB>(p, raw((c + 1) & 1), bh, cb, c + 1, ntok(c + 1), false, tid);
+            if (tid < ntok(c + 1)) dreg = d_of<TIn>(p, bh, static_cast<long long>(c + 1) * C + tid);
         }
         __syncthreads();
-        for (int s = 0; s < n; ++s) {
-            const float2 al = f2(sal[s]);
-            const float4 b4 = *reinterpret_cast<const float4*>(sb + s * p.dv + row0);
-            const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * p.dv + row0);
-            const float4 k4 = *reinterpret_cast<const float4*>(sk + s * p.cwb + col0);
-            const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * p.cwb + col0);
-            const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
-            const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
-            const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
-                    E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
-                }
-        }
+#pragma unroll 1
+        for (int s = 0; s < n; ++s) forward_step(s);
     }
     // checkpoints written by other threads are read back through cp.async
     __threadfence();
@@ -364,7 +450,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
     float2 GJ[4][2], GE[4][2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * p.cwb + col0;
+        const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
         float4 dm = make_float4(0.f, 0.f, 0.f, 0.f), di = dm;
         if (valid && p.dfinal) {
             dm = *reinterpret_cast<const float4*>(p.dfinal + off);
@@ -384,19 +470,18 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
     }
 
     // ---- backward sweep over the chunks, last first ------------------------
-    float* s_row = reinterpret_cast<float*>(sm + L.s_row);
-    float* s_dq = reinterpret_cast<float*>(sm + L.s_dq);
-    float* s_dk = reinterpret_cast<float*>(sm + L.s_dk);
-    float* s_D = reinterpret_cast<float*>(sm + L.s_D);
-    const int nwarps = p.nt / 32;
-    const int o1 = NR >> 1, o2 = NR >> 2;
+    float* s_row = reinterpret_cast<float*>(sm + Tl::s_row);
+    float* s_dq = reinterpret_cast<float*>(sm + Tl::s_dq);
+    float* s_dk = reinterpret_cast<float*>(sm + Tl::s_dk);
+    float* s_D = reinterpret_cast<float*>(sm + Tl::s_D);
+    constexpr int o1 = NR / 2, o2 = NR / 4;
     const int g = 2 * ((rq & o1) ? 1 : 0) + ((rq & o2) ? 1 : 0);
     const bool col_writer = valid && (rq & (o2 - 1)) == 0;
     float alpha_next = 1.f;   // alpha of the token after the one being processed
     if (nC > 0) {
         const int c = nC - 1;
-        issue_chunk<TIn>(p, raw(c & 1), L, bh, cb, c, ntok(c), true, tid);
-        if (tid < ntok(c)) dreg = alpha_of<TIn>(p, bh, static_cast<long long>(c) * C + tid);
+        issue_chunk<TIn, DV, CWB>(p, raw(c & 1), bh, cb, c, ntok(c), true, tid);
+        if (tid < ntok(c)) dreg = d_of<TIn>(p, bh, static_cast<long long>(c) * C + tid);
     }
     for (int c = nC - 1; c >= 0; --c) {
         const int n = ntok(c);
@@ -404,17 +489,16 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
         cp_async_wait_all();
         __syncthreads();   // chunk c landed; the previous chunk's epilogue finished
         unsigned char* rb = raw(c & 1);
-        convert_chunk<TIn>(p, sm, rb, L, n, true, dreg, tid);
+        convert_chunk<TIn, DV, CWB>(sm, rb, n, true, dreg, A_h, tid);
         if (c > 0) {
-            issue_chunk<TIn>(p, raw((c - 1) & 1), L, bh, cb, c - 1, C, true, tid);
-            if (tid < C) dreg = alpha_of<TIn>(p, bh, t0 - C + tid);
+            issue_chunk<TIn, DV, CWB>(p, raw((c - 1) & 1), bh, cb, c - 1, C, true, tid);
+            if (tid < C) dreg = d_of<TIn>(p, bh, t0 - C + tid);
         }
-        // the chunk's checkpoint
-        {
-            const float4* src = reinterpret_cast<const float4*>(rb + L.r_ck);
+        {   // the chunk's checkpoint
+            const float4* src = reinterpret_cast<const float4*>(rb + Tl::r_ck);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const float4 a = src[(2 * r) * p.nt + tid], b = src[(2 * r + 1) * p.nt + tid];
+                const float4 a = src[(2 * r) * NT + tid], b = src[(2 * r + 1) * NT + tid];
                 J[r][0] = make_float2(a.x, a.y);
                 J[r][1] = make_float2(a.z, a.w);
                 E[r][0] = make_float2(b.x, b.y);
@@ -423,128 +507,110 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
         }
         __syncthreads();   // converted inputs visible
         // forward again through the chunk; token s's state goes to TMEM slot s
-        for (int s = 0; s < n; ++s) {
-            const float2 al = f2(sal[s]);
-            const float4 b4 = *reinterpret_cast<const float4*>(sb + s * p.dv + row0);
-            const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * p.dv + row0);
-            const float4 k4 = *reinterpret_cast<const float4*>(sk + s * p.cwb + col0);
-            const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * p.cwb + col0);
-            const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
-            const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
-            const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+        auto fwd_store = [&](int s) {
+            forward_step(s);
             float st[32];
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                    J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
-                    E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
                     st[4 * r + 2 * c2] = J[r][c2].x;
                     st[4 * r + 2 * c2 + 1] = J[r][c2].y;
                     st[16 + 4 * r + 2 * c2] = E[r][c2].x;
                     st[16 + 4 * r + 2 * c2 + 1] = E[r][c2].y;
                 }
             tmem_st32(tlane + static_cast<uint32_t>(s * 32), st);
-        }
+        };
+#pragma unroll 1
+        for (int s = 0; s < n; ++s) fwd_store(s);
         tmem_wait_st();
-        const float* sdo = reinterpret_cast<const float*>(rb + L.r_do);
-        for (int s = n - 1; s >= 0; --s) {
-            float st[32];
-            tmem_ld32(tlane + static_cast<uint32_t>(s * 32), st);
-            const float2 ap = f2(alpha_next);
-            const float4 b4 = *reinterpret_cast<const float4*>(sb + s * p.dv + row0);
-            const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * p.dv + row0);
-            const float4 o4 = *reinterpret_cast<const float4*>(sdo + s * p.dv + row0);
-            const float4 k4 = *reinterpret_cast<const float4*>(sk + s * p.cwb + col0);
-            const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * p.cwb + col0);
-            const float4 q4 = *reinterpret_cast<const float4*>(sq + s * p.cwb + col0);
-            const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
-            const float dov[4] = {o4.x, o4.y, o4.z, o4.w};
-            const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
-            const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
-            const float2 qf[2] = {make_float2(q4.x, q4.y), make_float2(q4.z, q4.w)};
-            float2 cdq[2], cck[2], cce[2], rsb[4], rse[4], dacc = make_float2(0.f, 0.f);
-            // dL/dalpha of token t+1: its adjoints (not yet moved) against this
-            // token's state, the previous state of token t+1
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) cdq[c2] = cck[c2] = cce[c2] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                rsb[r] = rse[r] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const float2 Jt = make_float2(st[4 * r + 2 * c2], st[4 * r + 2 * c2 + 1]);
-                    const float2 Et = make_float2(st[16 + 4 * r + 2 * c2], st[16 + 4 * r + 2 * c2 + 1]);
-                    const float2 den = __fadd2_rn(Jt, f2(Ip));
-                    const float2 rr = make_float2(rcp_approx(den.x), rcp_approx(den.y));
-                    const float2 mu = __fmul2_rn(Et, rr);
-                    const float2 a = __fmul2_rn(__fmul2_rn(f2(dov[r]), qf[c2]), rr);
-                    dacc = __ffma2_rn(GJ[r][c2], Jt, dacc);
-                    dacc = __ffma2_rn(GE[r][c2], Et, dacc);
-                    GE[r][c2] = __ffma2_rn(ap, GE[r][c2], a);
-                    const float2 am = __fmul2_rn(a, mu);
-                    GJ[r][c2] = __ffma2_rn(ap, GJ[r][c2], make_float2(-am.x, -am.y));
-                    cdq[c2] = __ffma2_rn(f2(dov[r]), mu, cdq[c2]);
-                    rsb[r] = __ffma2_rn(GJ[r][c2], kq[c2], rsb[r]);
-                    rse[r] = __ffma2_rn(GE[r][c2], kf[c2], rse[r]);
-                    cck[c2] = __ffma2_rn(f2(bet[r]), GJ[r][c2], cck[c2]);
-                    cce[c2] = __ffma2_rn(f2(bvv[r]), GE[r][c2], cce[c2]);
-                }
-            }
-            alpha_next = sal[s];
-            // column sums over the d_v rows: lanes sharing the column quad
-            float cv[12];
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                cv[3 * (2 * c2)] = cdq[c2].x;
-                cv[3 * (2 * c2) + 1] = cck[c2].x;
-                cv[3 * (2 * c2) + 2] = cce[c2].x;
-                cv[3 * (2 * c2 + 1)] = cdq[c2].y;
-                cv[3 * (2 * c2 + 1) + 1] = cck[c2].y;
-                cv[3 * (2 * c2 + 1) + 2] = cce[c2].y;
-            }
-            column_reduce(cv, NR, rq);
+        const float* sdo = reinterpret_cast<const float*>(rb + Tl::r_do);
+        auto load_in = [&](int s, TokIn& in) {
+            const float4 b4 = *reinterpret_cast<const float4*>(sb + s * DV + row0);
+            const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * DV + row0);
+            const float4 o4 = *reinterpret_cast<const float4*>(sdo + s * DV + row0);
+            const float4 k4 = *reinterpret_cast<const float4*>(sk + s * CWB + col0);
+            const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * CWB + col0);
+            const float4 q4 = *reinterpret_cast<const float4*>(sq + s * CWB + col0);
+            in.bet[0] = b4.x; in.bet[1] = b4.y; in.bet[2] = b4.z; in.bet[3] = b4.w;
+            in.bvv[0] = v4.x; in.bvv[1] = v4.y; in.bvv[2] = v4.z; in.bvv[3] = v4.w;
+            in.dov[0] = o4.x; in.dov[1] = o4.y; in.dov[2] = o4.z; in.dov[3] = o4.w;
+            in.kf[0] = make_float2(k4.x, k4.y); in.kf[1] = make_float2(k4.z, k4.w);
+            in.kq[0] = make_float2(kk4.x, kk4.y); in.kq[1] = make_float2(kk4.z, kk4.w);
+            in.qf[0] = make_float2(q4.x, q4.y); in.qf[1] = make_float2(q4.z, q4.w);
+        };
+        // a token's partial sums into shared memory (column sums reduced here)
+        auto emit = [&](int s, float cv[12], const float rsum[8], float dsum) {
+            column_reduce<NR>(cv, rq);
             if (col_writer) {
                 const int j = col0 + g;
-                s_dq[s * p.cwb + j] = cv[0];
-                s_dk[s * p.cwb + j] = 2.f * sk[s * p.cwb + j] * cv[1] + cv[2];
+                s_dq[s * CWB + j] = cv[0];
+                s_dk[s * CWB + j] = 2.f * sk[s * CWB + j] * cv[1] + cv[2];
             }
-            // row partials over this thread's 4 columns
             if (valid) {
-                float* rowp = s_row + static_cast<long long>(s) * 2 * NCQ * p.dv;
-                *reinterpret_cast<float4*>(rowp + cq * p.dv + row0) =
-                    make_float4(rsb[0].x + rsb[0].y, rsb[1].x + rsb[1].y, rsb[2].x + rsb[2].y,
-                                rsb[3].x + rsb[3].y);
-                *reinterpret_cast<float4*>(rowp + (NCQ + cq) * p.dv + row0) =
-                    make_float4(rse[0].x + rse[0].y, rse[1].x + rse[1].y, rse[2].x + rse[2].y,
-                                rse[3].x + rse[3].y);
+                float* rowp = s_row + s * 2 * NCQ * DV;
+                *reinterpret_cast<float4*>(rowp + cq * DV + row0) =
+                    make_float4(rsum[0], rsum[1], rsum[2], rsum[3]);
+                *reinterpret_cast<float4*>(rowp + (NCQ + cq) * DV + row0) =
+                    make_float4(rsum[4], rsum[5], rsum[6], rsum[7]);
             }
-            float dsum = valid ? dacc.x + dacc.y : 0.f;
+            if (!valid) dsum = 0.f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(FULL, dsum, o);
-            if (lane == 0) s_D[s * (MAX_THREADS / 32) + warp] = dsum;
+            if (lane == 0) s_D[s * NW + warp] = dsum;
+        };
+        // adjoint steps from the chunk's last token down.  Token s+1's sums are
+        // reduced in the same step as token s's element arithmetic (the two are
+        // independent), so the shuffle latency overlaps arithmetic.
+        float cur[32], cv[12], rsum[8], dsum;
+        tmem_ld32_async(tlane + static_cast<uint32_t>((n - 1) * 32), cur);
+        tmem_wait_ld(cur);
+        {
+            TokIn in;
+            load_in(n - 1, in);
+            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cv, rsum, dsum);
+            alpha_next = sal[n - 1];
         }
+#pragma unroll 1
+        for (int s = n - 2; s >= 0; --s) {
+            tmem_ld32_async(tlane + static_cast<uint32_t>(s * 32), cur);
+            tmem_wait_ld(cur);
+            TokIn in;
+            load_in(s, in);
+            float cv2[12], rsum2[8], dsum2;
+            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cv2, rsum2, dsum2);
+            emit(s + 1, cv, rsum, dsum);
+            alpha_next = sal[s];
+#pragma unroll
+            for (int m = 0; m < 12; ++m) cv[m] = cv2[m];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) rsum[m] = rsum2[m];
+            dsum = dsum2;
+        }
+        emit(0, cv, rsum, dsum);
         __syncthreads();   // the chunk's partials are complete
-        // ---- epilogue of the chunk: row partials, D partials, dq, dk -------
+        // ---- epilogue of the chunk: row partials, alpha sums, dq, dk -------
         {
             const long long tokbase = bh * p.T + t0;
-            float* prow = p.prow + (static_cast<long long>(cb) * p.BH * p.T + tokbase) * 2 * p.dv;
-            for (int i = tid; i < n * 2 * p.dv; i += p.nt) {
-                const int s = i / (2 * p.dv), rem = i % (2 * p.dv), qi = rem / p.dv, row = rem % p.dv;
-                const float* src = s_row + static_cast<long long>(s) * 2 * NCQ * p.dv + qi * NCQ * p.dv + row;
+            float* prow = p.prow + (static_cast<long long>(cb) * p.BH * p.T + tokbase) * 2 * DV;
+            for (int i = tid; i < n * 2 * DV; i += NT) {
+                const int ss = i / (2 * DV), rem = i % (2 * DV), qi = rem / DV, row = rem % DV;
+                const float* src = s_row + ss * 2 * NCQ * DV + qi * NCQ * DV + row;
                 float acc = 0.f;
-                for (int x = 0; x < NCQ; ++x) acc += src[x * p.dv];
+#pragma unroll
+                for (int x = 0; x < NCQ; ++x) acc += src[x * DV];
                 prow[i] = acc;
             }
             // slot s holds token t0 + s + 1 (none after the last token)
             if (tid < n && t0 + tid + 1 < p.T) {
                 float acc = 0.f;
-                for (int w = 0; w < nwarps; ++w) acc += s_D[tid * (MAX_THREADS / 32) + w];
+#pragma unroll
+                for (int w = 0; w < NW; ++w) acc += s_D[tid * NW + w];
                 p.pD[static_cast<long long>(cb) * p.BH * p.T + tokbase + tid + 1] = acc;
             }
-            for (int i = tid; i < n * p.cwb; i += p.nt) {
-                const int s = i / p.cwb, j = i % p.cwb;
-                const long long o = (tokbase + s) * p.dk + cb * p.cwb + j;
+            for (int i = tid; i < n * CWB; i += NT) {
+                const int ss = i / CWB, j = i % CWB;
+                const long long o = (tokbase + ss) * p.dk + cb * CWB + j;
                 p.gq[o] = s_dq[i];
                 p.gk[o] = s_dk[i];
             }
@@ -558,7 +624,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
         float dsum = 0.f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * p.cwb + col0;
+            const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
             float4 i4 = make_float4(Ip, Ip, Ip, Ip), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (valid && p.I0) i4 = *reinterpret_cast<const float4*>(p.I0 + off);
             if (valid && p.mu0) m4 = *reinterpret_cast<const float4*>(p.mu0 + off);
@@ -584,7 +650,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1) diag_bwd_kernel(const Args p) 
         __syncthreads();
         if (tid == 0 && p.T > 0) {
             float acc = 0.f;
-            for (int w = 0; w < nwarps; ++w) acc += s_D[w];
+#pragma unroll
+            for (int w = 0; w < NW; ++w) acc += s_D[w];
             p.pD[static_cast<long long>(cb) * p.BH * p.T + bh * p.T] = acc;
         }
     }
@@ -647,25 +714,67 @@ __global__ void __launch_bounds__(256) diag_bwd_dA_kernel(const float* __restric
     if (threadIdx.x == 0) dA[h] = red[0];
 }
 
+template <typename TIn, int DV, int CWB>
+cudaError_t launch_main(const Args& p, long long grid, cudaStream_t st) {
+    using Tl = Tile<TIn, DV, CWB>;
+    cudaError_t e = cudaFuncSetAttribute(diag_bwd_kernel<TIn, DV, CWB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::SMEM);
+    if (e != cudaSuccess) return e;
+    diag_bwd_kernel<TIn, DV, CWB><<<static_cast<unsigned>(grid), Tl::NT, Tl::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TIn, int CWB>
+cudaError_t launch_dv(int dv, const Args& p, long long grid, cudaStream_t st) {
+    switch (dv) {
+        case 16: return launch_main<TIn, 16, CWB>(p, grid, st);
+        case 32: return launch_main<TIn, 32, CWB>(p, grid, st);
+        case 64: return launch_main<TIn, 64, CWB>(p, grid, st);
+        default: return launch_main<TIn, 128, CWB>(p, grid, st);
+    }
+}
+
+template <typename TIn>
+int threads_of(int dv, int cwb) {
+    const int nta = (dv / 4) * (cwb / 4);
+    return nta < 32 ? 32 : nta;
+}
+
+// Scratch of one call: checkpoints, row partials, alpha partials, dA terms.
+struct Scratch {
+    size_t ck, row, pd, ea, total;
+};
+
+inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
+    const long long BH = static_cast<long long>(B) * H;
+    const int cwb = dk < 32 ? dk : 32;
+    const int ncb = dk / cwb;
+    const int nta = (dv / 4) * (cwb / 4);
+    const int nt = nta < 32 ? 32 : nta;
+    const long long nC = (static_cast<long long>(T) + C - 1) / C;
+    Scratch s{};
+    s.ck = up256(static_cast<size_t>(BH) * ncb * nC * 32 * nt * 4);
+    s.row = up256(static_cast<size_t>(ncb) * BH * T * 2 * dv * 4);
+    s.pd = up256(static_cast<size_t>(ncb) * BH * T * 4);
+    s.ea = up256(static_cast<size_t>(BH) * T * 4);
+    s.total = s.ck + s.row + s.pd + s.ea;
+    return s;
+}
+
 template <typename TIn>
 kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     const long long BH = static_cast<long long>(a.B) * a.H;
     const int cwb = a.dk < 32 ? a.dk : 32;
     const int ncb = a.dk / cwb;
-    const int nta = (a.dv / 4) * (cwb / 4);
-    const int nt = nta < 32 ? 32 : nta;
     const int nC = (a.T + C - 1) / C;
-    const Layout L = make_layout(a.dv, cwb, nt, static_cast<int>(sizeof(TIn)));
-    const size_t ck_bytes = static_cast<size_t>(BH) * ncb * nC * 32 * nt * 4;
-    const size_t row_bytes = static_cast<size_t>(ncb) * BH * a.T * 2 * a.dv * 4;
-    const size_t pd_bytes = static_cast<size_t>(ncb) * BH * a.T * 4;
-    const size_t ea_bytes = static_cast<size_t>(BH) * a.T * 4;
-    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t total = up(ck_bytes) + up(row_bytes) + up(pd_bytes) + up(ea_bytes);
-    void* scratch = nullptr;
+    const Scratch sc = scratch_of(a.B, a.H, a.T, a.dk, a.dv);
+    void* scratch = a.workspace;
     cudaError_t e = cudaSuccess;
-    if (total > 0) {
-        e = cudaMallocAsync(&scratch, total, st);
+    const bool own = scratch == nullptr && sc.total > 0;
+    if (own) {
+        e = cudaMallocAsync(&scratch, sc.total, st);
         if (e != cudaSuccess) return from_cuda(e);
     }
     unsigned char* base = static_cast<unsigned char*>(scratch);
@@ -674,16 +783,12 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     p.I0 = a.I0; p.mu0 = a.mu0; p.dout = a.grad_out; p.dfinal = a.grad_final_state;
     p.gq = a.grad_q; p.gk = a.grad_k; p.dinit = a.grad_init_state;
     p.ckpt = reinterpret_cast<float*>(base);
-    p.prow = reinterpret_cast<float*>(base + up(ck_bytes));
-    p.pD = reinterpret_cast<float*>(base + up(ck_bytes) + up(row_bytes));
-    float* eA = reinterpret_cast<float*>(base + up(ck_bytes) + up(row_bytes) + up(pd_bytes));
-    p.BH = BH; p.H = a.H; p.T = a.T; p.dk = a.dk; p.dv = a.dv; p.cwb = cwb; p.ncb = ncb; p.nt = nt;
-    p.nC = nC;
-    e = cudaFuncSetAttribute(diag_bwd_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-    if (e == cudaSuccess) {
-        diag_bwd_kernel<TIn><<<static_cast<unsigned>(BH * ncb), nt, L.total, st>>>(p);
-        e = cudaGetLastError();
-    }
+    p.prow = reinterpret_cast<float*>(base + sc.ck);
+    p.pD = reinterpret_cast<float*>(base + sc.ck + sc.row);
+    float* eA = reinterpret_cast<float*>(base + sc.ck + sc.row + sc.pd);
+    p.BH = BH; p.H = a.H; p.T = a.T; p.dk = a.dk; p.ncb = ncb; p.nC = nC;
+    const long long grid = BH * ncb;
+    e = cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
     if (e == cudaSuccess && a.T > 0) {
         const long long BHT = BH * a.T;
         diag_bwd_finalize_kernel<TIn><<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
@@ -699,7 +804,7 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
             e = cudaMemsetAsync(a.grad_A, 0, sizeof(float) * a.H, st);
         }
     }
-    if (scratch) {
+    if (own) {
         const cudaError_t ef = cudaFreeAsync(scratch, st);
         if (e == cudaSuccess) e = ef;
     }
@@ -708,6 +813,10 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 }  // namespace bwd
+
+long long diag_bwd_workspace_bytes(int B, int H, int T, int dk, int dv) {
+    return static_cast<long long>(bwd::scratch_of(B, H, T, dk, dv).total);
+}
 
 kdn_status diag_bwd_launch(const DiagBwdArgs& a, cudaStream_t st) {
     return a.dtype == KDN_BF16 ? bwd::launch<__nv_bfloat16>(a, st) : bwd::launch<float>(a, st);

@@ -78,7 +78,8 @@ kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v, const 
                              const float* mu0, const float* grad_out, const float* grad_final_state,
                              float* grad_q, float* grad_k, float* grad_v, float* grad_beta,
                              float* grad_d, float* grad_A, float* grad_init_state, int B, int H,
-                             int T, int dk, int dv, kdn_dtype in_dtype, void* stream) {
+                             int T, int dk, int dv, kdn_dtype in_dtype, void* workspace,
+                             long long workspace_bytes, void* stream) {
     if (B < 1 || H < 1 || T < 0) return KDN_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !beta || !d || !A || !grad_out || !grad_q || !grad_k ||
                   !grad_v || !grad_beta || !grad_d))
@@ -96,11 +97,25 @@ kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v, const 
     for (const void* p : ptrs4)
         if (p && !aligned(p, 4)) return KDN_ERR_INVALID_ARG;
     if (d && !aligned(d, in_dtype == KDN_BF16 ? 2 : 4)) return KDN_ERR_INVALID_ARG;
+    if (workspace && (!aligned(workspace, 256) ||
+                      workspace_bytes < diag_bwd_workspace_bytes(B, H, T, dk, dv)))
+        return KDN_ERR_INVALID_ARG;
     if (T == 0 && !grad_init_state && !grad_A) return KDN_OK;
     DiagBwdArgs a{q, k, v, beta, d, A, I_prior, I0, mu0, grad_out, grad_final_state, grad_q,
                   grad_k, grad_v, grad_beta, grad_d, grad_A, grad_init_state, B, H, T, dk, dv,
-                  in_dtype};
+                  in_dtype, workspace};
     return diag_bwd_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+kdn_status kdn_diag_scan_bwd_workspace(int B, int H, int T, int dk, int dv,
+                                       long long* workspace_bytes) {
+    if (B < 1 || H < 1 || T < 0 || !workspace_bytes) return KDN_ERR_INVALID_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long dmax = dk > dv ? dk : dv;
+    if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / (dmax * dmax)) return KDN_ERR_INVALID_ARG;
+    *workspace_bytes = diag_bwd_workspace_bytes(B, H, T, dk, dv);
+    return KDN_OK;
 }
 
 kdn_status kdn_diag_step(const void* q, const void* k, const void* v, const void* beta, const void* d,

@@ -76,8 +76,10 @@ struct DiagBwdArgs {
     float* grad_init_state;
     int B, H, T, dk, dv;
     kdn_dtype dtype;
+    void* workspace;   // caller's scratch of diag_bwd_workspace_bytes, or null
 };
 kdn_status diag_bwd_launch(const DiagBwdArgs& a, cudaStream_t stream);
+long long diag_bwd_workspace_bytes(int B, int H, int T, int dk, int dv);
 
 // Host-buffer pipelines (kdn_host.cu): arguments validated, every pointer a
 // host pointer; synchronous.

@@ -53,7 +53,9 @@ def _load():
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
     lib.kdn_diag_scan_bwd.restype = i
     lib.kdn_diag_scan_bwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
-                                      fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
+                                      fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp, ll, vp]
+    lib.kdn_diag_scan_bwd_workspace.restype = i
+    lib.kdn_diag_scan_bwd_workspace.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_longlong)]
     lib.kdn_diag_step.restype = i
     lib.kdn_diag_step.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, i, i, i, i, i, vp]
     lib.kdn_diag_scan_fwd_host.restype = i
@@ -155,15 +157,26 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     return out, final_state
 
 
+def diag_scan_bwd_workspace(B, H, T, dk, dv) -> int:
+    """Bytes of device workspace ``diag_scan_bwd`` needs."""
+    n = ctypes.c_longlong(0)
+    st = lib.kdn_diag_scan_bwd_workspace(B, H, T, dk, dv, ctypes.byref(n))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_scan_bwd_workspace")
+    return int(n.value)
+
+
 def diag_scan_bwd(q, k, v, beta, d, A, grad_out, I_prior=1.0, I0=None, mu0=None,
-                  grad_final_state=None, grad_init_state=True, stream=None):
+                  grad_final_state=None, grad_init_state=True, workspace=None, stream=None):
     """Backward pass of ``diag_scan_fwd`` (see ``kdn_diag_scan_bwd``).
 
     Inputs as for ``diag_scan_fwd`` (device tensors); ``grad_out`` [B,H,T,dv]
     fp32; ``grad_final_state`` [2,B,H,dv,dk] fp32 or None.  ``grad_init_state``
     True (allocate), False/None (skip) or a [2,B,H,dv,dk] fp32 tensor.
     Returns a dict: q, k [B,H,T,dk]; v, beta [B,H,T,dv]; d [B,H,T]; A [H];
-    init_state [2,B,H,dv,dk] or None (all fp32).
+    init_state [2,B,H,dv,dk] or None (all fp32).  ``workspace``: a uint8
+    device tensor of at least ``diag_scan_bwd_workspace`` bytes, or None (one
+    is taken from torch's caching allocator for the call).
     """
     B, H, T, dk = q.shape
     dv = v.shape[-1]
@@ -195,12 +208,17 @@ def diag_scan_bwd(q, k, v, beta, d, A, grad_out, I_prior=1.0, I0=None, mu0=None,
     if grad_init_state is not None:
         _check(grad_init_state, "grad_init_state", torch.float32, (2, B, H, dv, dk))
     g["init_state"] = grad_init_state
+    ws_bytes = diag_scan_bwd_workspace(B, H, T, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
+    elif workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError(f"workspace must hold {ws_bytes} bytes")
     st = lib.kdn_diag_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
                                float(I_prior), _ptr(I0), _ptr(mu0), _ptr(grad_out),
                                _ptr(grad_final_state), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]),
                                _ptr(g["beta"]), _ptr(g["d"]), _ptr(g["A"]), _ptr(grad_init_state),
                                B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
-                               _stream(stream))
+                               _ptr(workspace), ws_bytes, _stream(stream))
     if st != KDN_OK:
         raise KdnError(st, "kdn_diag_scan_bwd")
     return g

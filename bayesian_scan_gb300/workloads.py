@@ -84,6 +84,14 @@ DECODE = {
                          ("uniform", 0.5, 4.0), 0, 0, False, 1005),
 }
 WORKLOADS.update(DECODE)
+# training: the backward pass of the 750M-shaped layer (same inputs, same
+# seed); the gradient flowing into the outputs is drawn by draw_cotangents
+# from the next seed
+TRAIN = {
+    "layer750m_bwd": Workload("layer750m_bwd", 8, 16, 4096, 128, 128, torch.bfloat16,
+                              ("uniform", 0.5, 4.0), 0, 0, False, 1002),
+}
+WORKLOADS.update(TRAIN)
 
 # the five scan configurations in the order the configuration list gives them
 ORDER = ["small", "heads32_t2048_d64", "layer750m", "layer1p3b", "longctx"]

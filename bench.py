@@ -14,6 +14,8 @@ collective; weak scaling); the timing is the max over ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+    python bench.py --workload layer750m_bwd   # the backward pass (training)
+    python bench.py --workload decode2k        # batched one-token decoding
 
 Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
 Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
@@ -517,6 +519,191 @@ def measure_e2e(args, w, host, dev, dist):
                     "kdn_diag_scan_fwd_host / kdn_mobius_scan_host (pipelined H2D, kernels, D2H; sync)"}
 
 
+# backward: per state element and token, the adjoint step and the gradient
+# sums (24 FLOP) plus one evaluation of the forward state it needs (6 FLOP);
+# the kernel's second evaluation of the forward (checkpoint replay) is not
+# counted
+BWD_FLOP_PER_ELEMENT_TOKEN = 30
+
+
+def bwd_inputs(w, dev):
+    import torch
+
+    from bayesian_scan_gb300 import workloads
+    host = workloads.make(w, with_mobius=False)
+    gout, _ = workloads.draw_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed + 1)
+    host["gout"] = gout
+    return host
+
+
+def oracle_bwd_sample(w, host, n_heads: int, t_tokens: int):
+    """The fp64 reverse-mode oracle on the first n_heads heads over the first
+    t_tokens tokens.  Returns (seconds, token-heads, threads)."""
+    import oracle
+    B, H = w.B, w.H
+    sl = lambda x: x.reshape(B * H, *x.shape[2:])[:n_heads, :t_tokens].unsqueeze(0)
+    q, k, v, beta, d, gout = (sl(host[n]) for n in ("q", "k", "v", "beta", "d", "gout"))
+    A = host["A"].repeat(B)[:n_heads].contiguous()
+    oracle.load()
+    t0 = time.perf_counter()
+    oracle.diag_scan_bwd(q, k, v, beta, d, A, host["I_prior"], dout=gout)
+    return time.perf_counter() - t0, n_heads * t_tokens, min(oracle.max_threads(), n_heads)
+
+
+def calibrate_oracle_bwd(w, host, budget_s: float):
+    import oracle
+    threads = oracle.max_threads()
+    dt, _, _ = oracle_bwd_sample(w, host, 1, 64)
+    per_token = dt / 64
+    n_heads = min(w.B * w.H, threads)
+    # every state of a sampled head is kept: bound the sample's memory to ~2 GB
+    mem_tokens = int(2e9 / (16 * w.dv * w.dk * n_heads))
+    t = int(budget_s / max(per_token, 1e-12))
+    return n_heads, max(16, min(w.T, t, mem_tokens))
+
+
+def run_backward(args, w, dist):
+    """Training step of the scan: one kdn_diag_scan_bwd over the workload
+    (the gradient flowing into the outputs given, no final-state gradient);
+    `value` is token-heads per second, the roofline the FP32 ALUs."""
+    import torch
+
+    from bayesian_scan_gb300 import kdn
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w_rank = w if dist.rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * dist.rank})
+    host = bwd_inputs(w_rank, dev)
+    names = ("q", "k", "v", "beta", "d", "A")
+    x = {n: host[n].to(dev) for n in names + ("gout",)}
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(kdn.diag_scan_bwd_workspace(B, H, T, dk, dv), device=dev, dtype=torch.uint8)
+
+    def step():
+        return kdn.diag_scan_bwd(*(x[n] for n in names), x["gout"], I_prior=w.I_prior,
+                                 grad_init_state=False, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error after warm-up: {kdn.status_string(st)}")
+    K = args.steps
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(dist.local_rank))
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        start.record(stream)
+        for _ in range(K):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {kdn.status_string(st)}")
+    ms = start.elapsed_time(stop)
+    max_ms = dist.max(ms)
+    tokens = B * H * T
+    value = dist.world * tokens * K / (max_ms / 1e3)
+    peaks = measured_peaks()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK))
+    alu_peak = nsm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved = BWD_FLOP_PER_ELEMENT_TOKEN * dv * dk * tokens / (ms / K / 1e3) / 1e12
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    line = {
+        "metric": "scan backward tokens/s (B·H·T per s) and % of FP32 roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "T": T, "d_k": dk, "d_v": dv,
+                   "inputs": "bf16" if es == 2 else "fp32", "grad_out": "fp32 N(0,1)",
+                   "grad_final_state": "none", "l2": "inputs larger than the 129 MB L2, no flush"},
+        "roofline": {"kernel": "diag_bwd_kernel (whole kdn_diag_scan_bwd call)", "bound": "alu",
+                     "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": None,
+                     "flop_per_element_token": BWD_FLOP_PER_ELEMENT_TOKEN,
+                     "peak_source": f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz"
+                                    " (recipe unit counts and max SM clock)"},
+        "gpu_launches": 3 * K,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_e2e:
+        pin = {n: host[n].pin_memory() for n in names + ("gout",)}
+        xs = {n: torch.empty_like(x[n]) for n in names + ("gout",)}
+        outs = {"q": (B, H, T, dk), "k": (B, H, T, dk), "v": (B, H, T, dv), "beta": (B, H, T, dv),
+                "d": (B, H, T), "A": (H,)}
+        res = {n: torch.empty(shp).pin_memory() for n, shp in outs.items()}
+
+        def e2e_step():
+            for n in xs:
+                xs[n].copy_(pin[n], non_blocking=True)
+            g = kdn.diag_scan_bwd(*(xs[n] for n in names), xs["gout"], I_prior=w.I_prior,
+                                  grad_init_state=False, workspace=ws, stream=stream)
+            for n in res:
+                res[n].copy_(g[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(1, min(K, 5))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        dt = dist.max(time.perf_counter() - t0)
+        line["e2e"] = {"value": dist.world * tokens * n_e2e / dt, "unit": "tokens/s", "steps": n_e2e,
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                       "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in res.values()),
+                       "path": "page-locked inputs and output gradient -> device copies -> "
+                               "kdn.diag_scan_bwd -> page-locked gradients"}
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        n_heads, t_tokens = calibrate_oracle_bwd(w, host, 10.0)
+        dt, units, reps, cores = 0.0, 0, 0, 1
+        while dt < 10.0 and reps < 100:
+            d1, u1, cores = oracle_bwd_sample(w, host, n_heads, t_tokens)
+            dt, units, reps = dt + d1, units + u1, reps + 1
+        line["cpu_baseline"] = {
+            "value": units / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x ({n_heads} heads x {t_tokens} tokens) of the same inputs (all "
+                      f"{dv}x{dk} state rows), fp64 reverse-mode oracle, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_bwd(args, w, dist):
+    """Reference arm of the backward workload: the fp64 reverse-mode oracle."""
+    if dist.rank != 0:
+        return 0
+    host = bwd_inputs(w, None)
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    n_heads, t_tokens = calibrate_oracle_bwd(w, host, per_step)
+    for _ in range(args.warmup):
+        oracle_bwd_sample(w, host, n_heads, t_tokens)
+    tot_t, tot_units, cores = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, units, cores = oracle_bwd_sample(w, host, n_heads, t_tokens)
+        tot_t += dt
+        tot_units += units
+    value = tot_units / tot_t
+    sample = (f"per step: {n_heads} heads x {t_tokens} tokens of the {w.name} workload "
+              f"(all {w.dv}x{w.dk} state rows), fp64 reverse-mode oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": "scan backward tokens/s (B·H·T per s) and % of FP32 roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.dk, "d_v": w.dv},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from bayesian_scan_gb300 import workloads
@@ -531,6 +718,10 @@ def main():
                                       "cpu_baseline"}), flush=True)
                 return 0
             return run_decode(args, w, dist)
+        if w.name in workloads.TRAIN:
+            if args.impl == "reference":
+                return run_reference_bwd(args, w, dist)
+            return run_backward(args, w, dist)
         if args.impl == "reference":
             return run_reference(args, w, dist)
         return run_ours(args, w, dist)

@@ -125,12 +125,17 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
  *   element-aligned; grad_d, grad_A: 4-byte aligned).  With T = 0 only
  *   grad_init_state (= grad_final_state) and grad_A (= 0) are written.
  *
- * Scratch: one stream-ordered allocation (cudaMallocAsync, freed on the
- * stream before return; KDN_ERR_ALLOC if it cannot be had) of about
+ * Scratch ("workspace"): kdn_diag_scan_bwd_workspace gives its size, about
  * B*H*T*dv*dk + 8*B*H*T*dv bytes (every 8th token's state, and per-column-
- * block row sums).  Each CTA owns all of its SM's tensor memory while it
- * runs.  Arithmetic: fp32 (the information form eta = I mu, J = I - I_prior);
- * results are deterministic (fixed summation order).
+ * block row sums).  With workspace == NULL the call takes it from the
+ * stream-ordered allocator (cudaMallocAsync, freed on the stream before
+ * return; KDN_ERR_ALLOC if it cannot be had); otherwise workspace is a
+ * 256-byte aligned device buffer of at least that many bytes, owned by the
+ * caller and in use until the call's work on the stream completes
+ * (KDN_ERR_INVALID_ARG if smaller or unaligned).  Each CTA owns all of its
+ * SM's tensor memory while it runs.  Arithmetic: fp32 (the information form
+ * eta = I mu, J = I - I_prior); results are deterministic (fixed summation
+ * order).
  */
 KDN_API kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v,
                              const void* beta, const void* d, const float* A,
@@ -140,7 +145,12 @@ KDN_API kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v
                              float* grad_beta, float* grad_d, float* grad_A,
                              float* grad_init_state,
                              int B, int H, int T, int dk, int dv,
-                             kdn_dtype in_dtype, void* stream);
+                             kdn_dtype in_dtype, void* workspace,
+                             long long workspace_bytes, void* stream);
+
+/* Bytes of workspace kdn_diag_scan_bwd needs for these sizes (no GPU call). */
+KDN_API kdn_status kdn_diag_scan_bwd_workspace(int B, int H, int T, int dk, int dv,
+                                       long long* workspace_bytes);
 
 /*
  * kdn_mobius_scan -- lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t)

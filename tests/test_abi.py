@@ -148,11 +148,11 @@ def test_host_mobius_rejects(lib):
 
 def _bwd(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, I0=None, mu0=None, go=FAKE,
          gfs=None, gq=FAKE, gk=FAKE, gv=FAKE, gb=FAKE, gd=FAKE, gA=FAKE, gis=None, B=1, H=1, T=8,
-         dk=16, dv=16, dtype=1):
+         dk=16, dv=16, dtype=1, ws=None, ws_bytes=0):
     vp = lambda x: None if x is None else ctypes.c_void_p(x)
     return lib.kdn_diag_scan_bwd(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), 1.0, vp(I0), vp(mu0),
                                  vp(go), vp(gfs), vp(gq), vp(gk), vp(gv), vp(gb), vp(gd), vp(gA),
-                                 vp(gis), B, H, T, dk, dv, dtype, None)
+                                 vp(gis), B, H, T, dk, dv, dtype, vp(ws), ws_bytes, None)
 
 
 @pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d", "A", "go", "gq", "gk", "gv", "gb", "gd"])
@@ -166,6 +166,7 @@ def test_bwd_null_pointer(lib, field):
     (dict(gis=FAKE + 4), -1), (dict(gfs=FAKE + 8), -1), (dict(I0=FAKE + 4), -1),
     (dict(gd=FAKE + 2), -1), (dict(gA=FAKE + 1), -1), (dict(d=FAKE + 1), -1),
     (dict(B=1 << 20, H=1 << 20, T=1 << 20), -1),
+    (dict(ws=FAKE + 16, ws_bytes=1 << 30), -1), (dict(ws=FAKE, ws_bytes=1024), -1),
 ])
 def test_bwd_rejects(lib, kw, status):
     assert _bwd(lib, **kw) == status
@@ -175,3 +176,13 @@ def test_bwd_empty_without_state_outputs_is_a_no_op(lib):
     # T = 0 and nothing to write: OK without touching any buffer
     assert _bwd(lib, q=None, k=None, v=None, beta=None, d=None, A=None, go=None, gq=None, gk=None,
                 gv=None, gb=None, gd=None, gA=None, T=0) == 0
+
+
+def test_bwd_workspace_size(lib):
+    n = ctypes.c_longlong(-1)
+    assert lib.kdn_diag_scan_bwd_workspace(8, 16, 4096, 128, 128, ctypes.byref(n)) == 0
+    # every 8th token's state of all heads dominates: B*H*T/8 * 2*dv*dk*4 bytes
+    assert n.value >= 8 * 16 * 512 * 2 * 128 * 128 * 4
+    assert lib.kdn_diag_scan_bwd_workspace(1, 1, 0, 16, 16, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.kdn_diag_scan_bwd_workspace(1, 1, 8, 24, 16, ctypes.byref(n)) == -2
+    assert lib.kdn_diag_scan_bwd_workspace(0, 1, 8, 16, 16, ctypes.byref(n)) == -1

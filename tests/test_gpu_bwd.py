@@ -94,3 +94,30 @@ def test_bwd_chain_across_a_split():
         assert e < 1e-4, (n, e)
     assert parity.rel_err(g1["A"] + g2["A"], full["A"]) < 1e-4
     assert parity.rel_err(g1["init_state"], full["init_state"]) < 1e-4
+
+
+def test_bwd_library_workspace_and_caller_workspace_agree():
+    # workspace NULL: the call takes stream-ordered scratch itself
+    import ctypes
+    from bayesian_scan_gb300 import kdn
+    B, H, T, dk, dv = 1, 2, 29, 64, 32
+    inp, gout, gfs, I0, mu0 = make(B, H, T, dk, dv, torch.bfloat16, seed=33, state=True)
+    ref = parity.gpu_bwd(inp, gout, gfs, I0, mu0)
+    dev = "cuda"
+    x = {n: inp[n].to(dev) for n in ("q", "k", "v", "beta", "d", "A")}
+    go, gf, i0, m0 = gout.to(dev), gfs.to(dev), I0.to(dev), mu0.to(dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    out = dict(q=torch.empty(B, H, T, dk, **f32), k=torch.empty(B, H, T, dk, **f32),
+               v=torch.empty(B, H, T, dv, **f32), beta=torch.empty(B, H, T, dv, **f32),
+               d=torch.empty(B, H, T, **f32), A=torch.empty(H, **f32),
+               init_state=torch.empty(2, B, H, dv, dk, **f32))
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = kdn.lib.kdn_diag_scan_bwd(p(x["q"]), p(x["k"]), p(x["v"]), p(x["beta"]), p(x["d"]),
+                                   p(x["A"]), 1.0, p(i0), p(m0), p(go), p(gf), p(out["q"]),
+                                   p(out["k"]), p(out["v"]), p(out["beta"]), p(out["d"]),
+                                   p(out["A"]), p(out["init_state"]), B, H, T, dk, dv, 1, None, 0,
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    for n in out:
+        assert torch.equal(out[n].cpu(), ref[n]), n

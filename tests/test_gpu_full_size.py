@@ -72,3 +72,34 @@ def test_full_size_properties_everywhere():
     torch.cuda.synchronize()
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(fs).all())
     assert float(fs[1].min()) >= inp["I_prior"] * (1 - 1e-6)
+
+
+def test_full_size_backward_sampled_heads():
+    """kdn_diag_scan_bwd over the whole 750M-shaped layer (the bench's
+    backward configuration); the oracle recomputes two whole heads (heads
+    are independent; the gradients of one head depend on that head alone),
+    and dA is checked against the per-token gradients it sums."""
+    from bayesian_scan_gb300 import kdn
+    w = workloads.get("layer750m_bwd")
+    inp = workloads.make(w, with_mobius=False)
+    gout, _ = workloads.draw_cotangents(w.B, w.H, w.T, w.dk, w.dv, seed=w.seed + 1)
+    x = [inp[n].to("cuda") for n in ("q", "k", "v", "beta", "d", "A")]
+    g = kdn.diag_scan_bwd(*x, gout.to("cuda"), I_prior=inp["I_prior"], grad_init_state=False)
+    torch.cuda.synchronize()
+    assert kdn.get_device_error() == 0
+    for n in ("q", "k", "v", "beta", "d", "A"):
+        assert bool(torch.isfinite(g[n]).all()), n
+    # dA_h = sum_b sum_t (d_t / A_h) dd_t   (dd = -A alpha dL/dalpha, dA = -sum d alpha dL/dalpha)
+    dd, d = g["d"].double().cpu(), inp["d"].double()
+    ref_dA = (d * dd).sum(dim=(0, 2)) / inp["A"].double()
+    assert parity.rel_err(g["A"].cpu(), ref_dA) < 1e-4
+    H = w.H
+    for bh in (5, w.B * H - 1):
+        b, h = divmod(bh, H)
+        sl = lambda t: t[b:b + 1, h:h + 1]
+        r = oracle.diag_scan_bwd(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["beta"]),
+                                 sl(inp["d"]), inp["A"][h:h + 1], inp["I_prior"], dout=sl(gout))
+        for n, o in parity.BWD_NAMES.items():
+            if n == "A":
+                continue
+            assert parity.rel_err(g[n][b:b + 1, h:h + 1].cpu(), r[o]) <= parity.TOL_BWD, (n, bh)
