@@ -90,6 +90,10 @@ WORKLOADS.update(DECODE)
 TRAIN = {
     "layer750m_bwd": Workload("layer750m_bwd", 8, 16, 4096, 128, 128, torch.bfloat16,
                               ("uniform", 0.5, 4.0), 0, 0, False, 1002),
+    # a one-wave case of the same head shape (32 heads x 1024 tokens) for
+    # profiling captures
+    "heads32_t1024_bwd": Workload("heads32_t1024_bwd", 2, 16, 1024, 128, 128, torch.bfloat16,
+                                  ("uniform", 0.5, 4.0), 0, 0, False, 1006),
 }
 WORKLOADS.update(TRAIN)
 

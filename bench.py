@@ -84,11 +84,22 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.first = []
         try:
             self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            # wait for the first sample: nvidia-smi's start-up (NVML
+            # initialisation) can hold up kernel launches of this process for
+            # hundreds of ms, which must not fall inside the timed region
+            import select
+            ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+            if ready:
+                line = self.proc.stdout.readline()
+                if line.strip():
+                    self.first.append(line)
         return self
 
     def __exit__(self, *exc):
@@ -100,7 +111,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self.lines = [ln for ln in self.first + out.splitlines() if ln.strip()]
         return False
 
     def summary(self):
