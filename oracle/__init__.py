@@ -71,6 +71,9 @@ def _declare(lib):
     lib.oracle_diag_scan_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double, dp, dp,
                                          dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                          L, L, L, L, L]
+    lib.oracle_lin_scan.restype = ctypes.c_int
+    lib.oracle_lin_scan.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp,
+                                    L, L, L, L, L]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
@@ -125,6 +128,29 @@ def diag_scan(q, k, v, beta, d, A, I_prior, I0=None, mu0=None, lib=None):
     if rc != 0:
         raise RuntimeError(f"oracle_diag_scan failed ({rc})")
     return out, mu_T, I_T
+
+
+def lin_scan(q, k, v, beta, d, A, I_prior, mu0=None, lib=None):
+    """Oracle of the non-metaplastic limit (importance held at I_prior).
+
+    Shapes as ``diag_scan``; mu0 [B,H,dv,dk] or None.  Returns (out
+    [B,H,T,dv], mu_T [B,H,dv,dk]) as fp64 numpy arrays.
+    """
+    lib = lib or load()
+    q, k, v, beta, d, A = (_f64(x) for x in (q, k, v, beta, d, A))
+    mu0 = _f64(mu0)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == (B, H, T, dk) and beta.shape == v.shape == (B, H, T, dv)
+    assert d.shape == (B, H, T) and A.shape == (H,)
+    assert mu0 is None or mu0.shape == (B, H, dv, dk)
+    out = np.empty((B, H, T, dv))
+    mu_T = np.empty((B, H, dv, dk))
+    rc = lib.oracle_lin_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                             float(I_prior), _ptr(mu0), _ptr(out), _ptr(mu_T), B, H, T, dk, dv)
+    if rc != 0:
+        raise RuntimeError(f"oracle_lin_scan failed ({rc})")
+    return out, mu_T
 
 
 def diag_scan_bwd(q, k, v, beta, d, A, I_prior, I0=None, mu0=None, dout=None,

@@ -48,6 +48,14 @@
  *      summed over b by the caller), dL/dI_0 and dL/dmu_0.  I_prior is a
  *      fixed hyperparameter here and gets no gradient.
  *
+ *  (4) The non-metaplastic limit of (1) ("Learning to Remember, Learn, and
+ *      Forget in Attention-Based Models", Metodologia 4, Unificazione
+ *      Teorica: Mamba2 is the case where the importance stays at I_prior).
+ *      oracle_lin_scan holds I_t = I_{t-1} = I_prior in the mean update of
+ *      (1), which leaves
+ *          mu_t = alpha_t mu_{t-1} + (1 / I_prior) . [(beta_t . v_t) (x) k_t]
+ *      with the same readout o_t[i] = sum_j mu_t[i][j] q_t[j].
+ *
  * Parity pins (tests/test_oracle_pins.py) tie every term of these loops to
  * closed forms, special cases and brute force; see that file.
  *
@@ -144,6 +152,52 @@ int oracle_diag_scan(const double* q, const double* k, const double* v,
         }
         free(mu);
         free(I);
+    }
+    return failed ? -2 : 0;
+}
+
+/* The non-metaplastic limit ((4) in the header).  mu0 and mu_T may be NULL
+ * (mu_0 = 0; no final state). */
+int oracle_lin_scan(const double* q, const double* k, const double* v,
+                    const double* beta, const double* d, const double* A,
+                    double I_prior, const double* mu0, double* out, double* mu_T,
+                    long B, long H, long T, long dk, long dv) {
+    if (B < 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return -1;
+    long BH = B * H;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long bh = 0; bh < BH; ++bh) {
+        long h = bh % H;
+        double* mu = (double*)malloc(sizeof(double) * dv * dk);
+        if (!mu) {
+            failed = 1;
+            continue;
+        }
+        for (long e = 0; e < dv * dk; ++e) mu[e] = mu0 ? mu0[bh * dv * dk + e] : 0.0;
+        for (long t = 0; t < T; ++t) {
+            const double* qt = q + (bh * T + t) * dk;
+            const double* kt = k + (bh * T + t) * dk;
+            const double* vt = v + (bh * T + t) * dv;
+            const double* bt = beta + (bh * T + t) * dv;
+            double alpha = exp(-A[h] * d[bh * T + t]);
+            for (long i = 0; i < dv; ++i)
+                for (long j = 0; j < dk; ++j) {
+                    long e = i * dk + j;
+                    /* mu_t = alpha mu_{t-1} + (1/I_prior) (beta_i v_i) k_j */
+                    mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((bt[i] * vt[i]) * kt[j]);
+                }
+            double* ot = out + (bh * T + t) * dv;
+            for (long i = 0; i < dv; ++i) {
+                double s = 0.0;
+                for (long j = 0; j < dk; ++j) s += mu[i * dk + j] * qt[j];
+                ot[i] = s;
+            }
+        }
+        if (mu_T)
+            for (long e = 0; e < dv * dk; ++e) mu_T[bh * dv * dk + e] = mu[e];
+        free(mu);
     }
     return failed ? -2 : 0;
 }

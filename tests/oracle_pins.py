@@ -246,6 +246,75 @@ def pin_resume(lib):
 
 
 # ----------------------------------------------------------------------------
+# Non-metaplastic limit pins
+
+def _lin(lib, x):
+    return oracle.lin_scan(x["q"], x["k"], x["v"], x["beta"], x["d"], x["A"], x["I_prior"],
+                           x["mu0"], lib=lib)
+
+
+def pin_lin_closed_form(lib):
+    """Decayed linear attention written out: o_t = sum_{s<=t} L_ts (q_t . k_s)
+    (beta_s . v_s) / I_prior + L_t0 mu_0 q_t, L_ts = exp(-A sum_{r=s+1..t} d_r),
+    and mu_T = sum_s L_Ts (beta_s . v_s) k_s^T / I_prior + L_T0 mu_0 (O(T^2)
+    brute force, every head and batch)."""
+    x = _inputs(B=2, H=2, T=17, dk=3, dv=5, with_state=True)
+    o, muT = _lin(lib, x)
+    B, H, T, _ = x["q"].shape
+    for b in range(B):
+        for h in range(H):
+            cum = np.concatenate([[0.0], np.cumsum(x["A"][h] * x["d"][b, h])])
+            bv = x["beta"][b, h] * x["v"][b, h]                          # [T, dv]
+            for t in range(T):
+                L = np.exp(-(cum[t + 1] - cum[1:t + 2]))                  # L_{t,s}, s = 0..t
+                qk = x["k"][b, h, :t + 1] @ x["q"][b, h, t]               # [s]
+                ref = (L * qk) @ bv[:t + 1] / x["I_prior"]
+                ref = ref + np.exp(-cum[t + 1]) * (x["mu0"][b, h] @ x["q"][b, h, t])
+                assert _rel(o[b, h, t], ref) < 1e-12, (b, h, t)
+            L = np.exp(-(cum[T] - cum[1:]))
+            refm = (bv * L[:, None]).T @ x["k"][b, h] / x["I_prior"] + np.exp(-cum[T]) * x["mu0"][b, h]
+            assert _rel(muT[b, h], refm) < 1e-12
+
+
+def pin_lin_is_the_metaplastic_limit(lib):
+    """The metaplastic scan with I_0 = I_prior = s tends to the non-metaplastic
+    one as s grows (the importance stays at I_prior): relative distance of
+    the readouts O(1/s), falling ~100x per 100x in s."""
+    x = _inputs(B=1, H=2, T=20, dk=3, dv=4)
+    dists = []
+    for s_ in (1e4, 1e6):
+        y = dict(x, I_prior=s_, I0=np.full((1, 2, 4, 3), s_), mu0=None)
+        o_d, _, _ = _run(lib, y)
+        o_l, _ = _lin(lib, dict(x, I_prior=s_, mu0=None))
+        dists.append(_rel(o_d, o_l))
+    assert dists[1] < 1e-5 and 30 < dists[0] / dists[1] < 300, dists
+
+
+def pin_lin_no_forgetting(lib):
+    """A = 0: mu_T = mu_0 + sum_s (beta_s . v_s) k_s^T / I_prior (cumulative sums)."""
+    x = _inputs(B=1, H=2, T=11, dk=4, dv=3, A=(0.0, 0.0), with_state=True)
+    _, muT = _lin(lib, x)
+    bv = x["beta"] * x["v"]
+    ref = x["mu0"] + np.einsum("bhti,bhtj->bhij", bv, x["k"]) / x["I_prior"]
+    assert _rel(muT, ref) < 1e-13
+
+
+def pin_lin_resume(lib):
+    """One call equals two calls carrying mu."""
+    x = _inputs(B=2, H=2, T=15, with_state=True)
+    o, muT = _lin(lib, x)
+    h = 6
+    x1, x2 = dict(x), dict(x)
+    for n in ("q", "k", "v", "beta", "d"):
+        x1[n] = x[n][:, :, :h]
+        x2[n] = x[n][:, :, h:]
+    o1, mu1 = _lin(lib, x1)
+    x2["mu0"] = mu1
+    o2, mu2 = _lin(lib, x2)
+    assert _rel(np.concatenate([o1, o2], axis=2), o) < 1e-13 and _rel(mu2, muT) < 1e-13
+
+
+# ----------------------------------------------------------------------------
 # Backward-pass pins: the reverse-mode oracle against derivatives obtained
 # without it
 
@@ -445,4 +514,6 @@ DIAG_PINS = [pin_information_form, pin_eta_identity, pin_alpha_one_posterior_mea
 MOBIUS_PINS = [pin_mobius_bracketings, pin_mobius_matrix_power, pin_mobius_affine,
                pin_mobius_product, pin_mobius_resume]
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_autograd, pin_bwd_chain]
-ALL_PINS = DIAG_PINS + MOBIUS_PINS + BWD_PINS
+LIN_PINS = [pin_lin_closed_form, pin_lin_is_the_metaplastic_limit, pin_lin_no_forgetting,
+            pin_lin_resume]
+ALL_PINS = DIAG_PINS + MOBIUS_PINS + BWD_PINS + LIN_PINS

@@ -1,8 +1,9 @@
 """The pins catch plausible mistakes in the oracle (CPU only).
 
 Each case plants one mistake in a copy of ``oracle/kdn_oracle.c`` (a dropped
-term, a sign, a swapped operand or index, an off-by-one step; ``bwd_*`` cases
-in the backward function), builds the copy
+term, a sign, a swapped operand or index, an off-by-one step) in one of its
+functions (chosen by the case's prefix: ``bwd_``, ``lin_``, ``mobius_``, else
+the diagonal scan), builds the copy
 with gcc and requires that at least one pin of ``oracle_pins`` fails on it.
 The real oracle is never modified.
 """
@@ -49,6 +50,15 @@ MUTANTS = {
     "bwd_final_importance_ignored": ("gI[e] = dI_T ? dI_T[bh * S + e] : 0.0;", "gI[e] = 0.0;"),
     "bwd_forward_drop_prior_leak": ("+ (1.0 - alpha) * I_prior", ""),
     "bwd_importance_carry_without_alpha": ("g_Ip += g_In * alpha;", "g_Ip += g_In;"),
+    "lin_gate_sign": ("mu[e] = alpha * mu[e] + (1.0 / I_prior)", "mu[e] = (1.0 / alpha) * mu[e] + (1.0 / I_prior)"),
+    "lin_drop_prior_scale": ("mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((bt[i] * vt[i]) * kt[j]);",
+                             "mu[e] = alpha * mu[e] + ((bt[i] * vt[i]) * kt[j]);"),
+    "lin_write_uses_q": ("mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((bt[i] * vt[i]) * kt[j]);",
+                         "mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((bt[i] * vt[i]) * qt[j]);"),
+    "lin_missing_beta": ("mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((bt[i] * vt[i]) * kt[j]);",
+                         "mu[e] = alpha * mu[e] + (1.0 / I_prior) * ((vt[i]) * kt[j]);"),
+    "lin_ignores_mu0": ("for (long e = 0; e < dv * dk; ++e) mu[e] = mu0 ? mu0[bh * dv * dk + e] : 0.0;",
+                        "for (long e = 0; e < dv * dk; ++e) mu[e] = 0.0;"),
     "mobius_swap_b_c": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
                         "lam = (a[e] * lam + c[e]) / (b[e] * lam + d[e]);"),
     "mobius_swap_c_d": ("lam = (a[e] * lam + b[e]) / (c[e] * lam + d[e]);",
@@ -64,15 +74,17 @@ MUTANTS = {
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    # the backward restates the forward loop: bwd_* mutants edit the backward
-    # function, the others the forward functions before it
-    cut = src.index("int oracle_diag_scan_bwd(")
-    head, tail = src[:cut], src[cut:]
-    part = tail if name.startswith("bwd_") else head
+    # several functions restate the same update: a mutant edits one function,
+    # chosen by its name's prefix
+    func = {"bwd": "oracle_diag_scan_bwd", "lin": "oracle_lin_scan",
+            "mobius": "oracle_mobius_scan"}.get(name.split("_")[0], "oracle_diag_scan")
+    start = src.index(f"int {func}(")
+    nxt = src.find("\nint oracle_", start + 1)
+    end = len(src) if nxt < 0 else nxt
+    part = src[start:end]
     assert part.count(old) == 1, f"mutation site for {name} not unique"
-    part = part.replace(old, new)
     mut = tmp_path / "mutant.c"
-    mut.write_text(head + part if name.startswith("bwd_") else part + tail)
+    mut.write_text(src[:start] + part.replace(old, new) + src[end:])
     so = str(tmp_path / "libmutant.so")
     oracle.build(force=True, src=str(mut), out=so)
     lib = oracle.load(so)
