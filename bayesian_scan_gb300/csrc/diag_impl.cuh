@@ -233,7 +233,7 @@ __device__ __forceinline__ float scale_step(float x, float& W, int& R) {
     return r == 0 ? 1.f : pow2i(-r);
 }
 
-template <int DK, typename TIn, bool AGG>
+template <int DK, typename TIn, bool AGG, bool LIN>
 __global__ void __launch_bounds__(Geo<DK>::NTHREADS, (DK >= 128 ? 1 : 2))
 diag_scan_kernel(const Params p) {
     using G = Geo<DK>;
@@ -332,7 +332,7 @@ diag_scan_kernel(const Params p) {
                 float* base = par(s, h) + tt * PF;
                 const float2 kv = load2(raw_k(s, h) + tt * DK + j);
                 *reinterpret_cast<float2*>(base + pos) = kv;
-                *reinterpret_cast<float2*>(base + DK + pos) = make_float2(kv.x * kv.x, kv.y * kv.y);
+                if (!LIN) *reinterpret_cast<float2*>(base + DK + pos) = make_float2(kv.x * kv.x, kv.y * kv.y);
                 if (!AGG) *reinterpret_cast<float2*>(base + 2 * DK + pos) = load2(raw_q(s, h) + tt * DK + j);
             }
         }
@@ -476,7 +476,7 @@ diag_scan_kernel(const Params p) {
                 for (int r = 0; r < RT; ++r)
 #pragma unroll
                     for (int c2 = 0; c2 < CW / 2; ++c2) {
-                        J[r][c2] = __fmul2_rn(J[r][c2], f22);
+                        if (!LIN) J[r][c2] = __fmul2_rn(J[r][c2], f22);
                         E[r][c2] = __fmul2_rn(E[r][c2], f22);
                     }
             }
@@ -500,6 +500,40 @@ diag_scan_kernel(const Params p) {
             float2 acc[RT];
 #pragma unroll
             for (int r = 0; r < RT; ++r) acc[r] = make_float2(0.f, 0.f);
+            if constexpr (LIN) {
+                // importance held at I_prior: Ew <- Ew + (W beta_i v_i) k_j and
+                // o_i = sum_j q_j Ew_ij / (W I_prior) (one scale per token)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float2 kf[4], qv[4];
+#pragma unroll
+                    for (int h4 = 0; h4 < 2; ++h4) {
+                        const int f4 = ((2 * half + h4) * M + cg) * 4;
+                        const float4 a = *reinterpret_cast<const float4*>(pt + f4);
+                        kf[2 * h4] = make_float2(a.x, a.y);
+                        kf[2 * h4 + 1] = make_float2(a.z, a.w);
+                        if (!AGG) {
+                            const float4 q = *reinterpret_cast<const float4*>(pt + 2 * DK + f4);
+                            qv[2 * h4] = make_float2(q.x, q.y);
+                            qv[2 * h4 + 1] = make_float2(q.z, q.w);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < RT; ++r)
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const int c2 = half * 4 + c4;
+                            E[r][c2] = __ffma2_rn(SBV[r], kf[c4], E[r][c2]);
+                            if (!AGG) acc[r] = __ffma2_rn(qv[c4], E[r][c2], acc[r]);
+                        }
+                }
+                if (!AGG) {
+                    // the flush multiplies by sigma: store sum / (sigma W I_prior)
+                    const float rz = 1.f / sc.z;
+#pragma unroll
+                    for (int r = 0; r < RT; ++r) acc[r] = __fmul2_rn(acc[r], f2(rz));
+                }
+            } else {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 // this lane's 8 columns of the half: float4 numbers (2*half+h4)*M + cg
@@ -550,6 +584,7 @@ diag_scan_kernel(const Params p) {
                     }
                 }
             }
+            }
             if (!AGG) {
                 const int slot = tt & (RB - 1);
                 *reinterpret_cast<float4*>(red + slot * RTS + rs * RSS + 4 * cg) =
@@ -585,6 +620,17 @@ diag_scan_kernel(const Params p) {
             }
         // the head's scale state after the part: W of its last token, total R
         if (i0 == 0 && cg == 0) p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, r_state[hl]};
+    } else if (LIN && p.final_state && part == static_cast<int>(gridDim.y) - 1) {
+        // mu_T = Ew / (W I_prior)
+        float* fm = p.final_state + bh * S;
+        const float rw = 1.f / (W * Ip);
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 2; ++c2) {
+                const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
+                *reinterpret_cast<float2*>(fm + off) = __fmul2_rn(E[r][c2], f2(rw));
+            }
     } else if (p.final_state && part == static_cast<int>(gridDim.y) - 1) {
         // mu_T = eta / (I_prior + J) = Ew / (Jw + W I_prior);  I_T = Jw / W + I_prior
         float* fm = p.final_state + bh * S;
@@ -680,11 +726,11 @@ cudaError_t agg_tc_prepare() {
     return cudaSuccess;
 }
 
-template <int DK, typename TIn, bool AGG>
+template <int DK, typename TIn, bool AGG, bool LIN>
 cudaError_t prepare(int dev, int smem, int* occ) {
     static Cache cache;
     static int smem_set[64] = {};
-    auto kern = diag_scan_kernel<DK, TIn, AGG>;
+    auto kern = diag_scan_kernel<DK, TIn, AGG, LIN>;
     cudaError_t e = cudaSuccess;
     if (dev < 0 || dev >= 64) dev = 0;
     if (smem > smem_set[dev]) {
@@ -721,7 +767,7 @@ struct Plan {
     int kernels = 0;
 };
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, bool LIN>
 kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     constexpr int ES = sizeof(TIn);
     const int dv = a.dv;
@@ -739,9 +785,9 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return from_cuda(e);
     int occ = 1, occ_agg = 1;
-    e = prepare<DK, TIn, false>(dev, pl->smem, &occ);
+    e = prepare<DK, TIn, false, LIN>(dev, pl->smem, &occ);
     if (e != cudaSuccess) return from_cuda(e);
-    e = prepare<DK, TIn, true>(dev, pl->smem, &occ_agg);
+    e = prepare<DK, TIn, true, LIN>(dev, pl->smem, &occ_agg);
     if (e != cudaSuccess) return from_cuda(e);
     // token split: enough parts to give every CTA slot work
     const long long slots = static_cast<long long>(sm_count()) * occ;
@@ -796,11 +842,11 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     return KDN_OK;
 }
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, bool LIN>
 kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
     constexpr int ES = sizeof(TIn);
     Plan pl;
-    kdn_status ps = plan_dk<DK, TIn>(a, &pl);
+    kdn_status ps = plan_dk<DK, TIn, LIN>(a, &pl);
     if (ps != KDN_OK) return ps;
     const int dv = a.dv, TC = pl.TC, smem = pl.smem, P = pl.P;
     const long long BH = static_cast<long long>(a.B) * a.H;
@@ -842,7 +888,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                 e = cudaGetLastError();
             }
         } else {
-            diag_scan_kernel<DK, TIn, true>
+            diag_scan_kernel<DK, TIn, true, LIN>
                 <<<dim3(static_cast<unsigned>(ctas), P - 1), Geo<DK>::NTHREADS, smem, st>>>(prm);
             e = cudaGetLastError();
         }
@@ -854,7 +900,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         }
     }
     if (e == cudaSuccess) {
-        diag_scan_kernel<DK, TIn, false>
+        diag_scan_kernel<DK, TIn, false, LIN>
             <<<dim3(static_cast<unsigned>(ctas), P), Geo<DK>::NTHREADS, smem, st>>>(prm);
         e = cudaGetLastError();
     }
@@ -868,23 +914,28 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
 template <typename TIn>
 kdn_status plan_any(const DiagArgs& a, Plan* pl) {
     switch (a.dk) {
-        case 16: return plan_dk<16, TIn>(a, pl);
-        case 32: return plan_dk<32, TIn>(a, pl);
-        case 64: return plan_dk<64, TIn>(a, pl);
-        case 128: return plan_dk<128, TIn>(a, pl);
+        case 16: return plan_dk<16, TIn, false>(a, pl);
+        case 32: return plan_dk<32, TIn, false>(a, pl);
+        case 64: return plan_dk<64, TIn, false>(a, pl);
+        case 128: return plan_dk<128, TIn, false>(a, pl);
+        default: return KDN_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename TIn, bool LIN>
+kdn_status launch_lin(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
+    switch (a.dk) {
+        case 16: return launch_dk<16, TIn, LIN>(a, st, wait_ns);
+        case 32: return launch_dk<32, TIn, LIN>(a, st, wait_ns);
+        case 64: return launch_dk<64, TIn, LIN>(a, st, wait_ns);
+        case 128: return launch_dk<128, TIn, LIN>(a, st, wait_ns);
         default: return KDN_ERR_UNSUPPORTED;
     }
 }
 
 template <typename TIn>
 kdn_status launch_any(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
-    switch (a.dk) {
-        case 16: return launch_dk<16, TIn>(a, st, wait_ns);
-        case 32: return launch_dk<32, TIn>(a, st, wait_ns);
-        case 64: return launch_dk<64, TIn>(a, st, wait_ns);
-        case 128: return launch_dk<128, TIn>(a, st, wait_ns);
-        default: return KDN_ERR_UNSUPPORTED;
-    }
+    return a.lin ? launch_lin<TIn, true>(a, st, wait_ns) : launch_lin<TIn, false>(a, st, wait_ns);
 }
 
 }  // namespace

@@ -73,6 +73,29 @@ kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v, const 
     return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
 }
 
+kdn_status kdn_lin_scan_fwd(const void* q, const void* k, const void* v, const void* beta,
+                            const void* d, const float* A, float I_prior, const float* mu0,
+                            float* out, float* final_mu, int B, int H, int T, int dk, int dv,
+                            kdn_dtype in_dtype, void* stream) {
+    if (B < 1 || H < 1 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !beta || !d || !A || !out)) return KDN_ERR_INVALID_ARG;
+    if (in_dtype != KDN_F32 && in_dtype != KDN_BF16) return KDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long dmax = dk > dv ? dk : dv;
+    if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / dmax) return KDN_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, beta, out, mu0, final_mu};
+    for (const void* p : ptrs16)
+        if (p && !aligned(p, 16)) return KDN_ERR_INVALID_ARG;
+    if ((A && !aligned(A, 4)) || (d && !aligned(d, in_dtype == KDN_BF16 ? 2 : 4)))
+        return KDN_ERR_INVALID_ARG;
+    DiagArgs a{q, k, v, beta, d, A, I_prior, nullptr, mu0, out, final_mu, B, H, T, dk, dv, in_dtype};
+    a.lin = true;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long wait_ns = g_wait_ns.load();
+    return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
+}
+
 kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v, const void* beta,
                              const void* d, const float* A, float I_prior, const float* I0,
                              const float* mu0, const float* grad_out, const float* grad_final_state,

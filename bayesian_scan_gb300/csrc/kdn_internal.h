@@ -26,6 +26,9 @@ struct DiagArgs {
     // i.e. [B,H,T,...]); lets a call use a token range of longer tensors
     long long out_ld = 0;
     long long d_ld = 0;
+    // the non-metaplastic limit: importance held at I_prior (I0 unused,
+    // final_state is mu_T alone, [B,H,dv,dk])
+    bool lin = false;
 };
 
 // Per-dtype launchers (diag_bf16.cu / diag_f32.cu).

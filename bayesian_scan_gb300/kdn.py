@@ -51,6 +51,9 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_lin_scan_fwd.restype = i
+    lib.kdn_lin_scan_fwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp,
+                                     i, i, i, i, i, i, vp]
     lib.kdn_diag_scan_bwd.restype = i
     lib.kdn_diag_scan_bwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
                                       fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp, ll, vp]
@@ -155,6 +158,45 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     if st != KDN_OK:
         raise KdnError(st, "kdn_diag_scan_fwd")
     return out, final_state
+
+
+def lin_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, mu0=None, out=None, final_mu=True,
+                 stream=None):
+    """The non-metaplastic limit (importance held at I_prior; see
+    ``kdn_lin_scan_fwd``).  Device tensors as for ``diag_scan_fwd``; mu0
+    [B,H,dv,dk] fp32 or None; ``final_mu`` True (allocate), False/None or a
+    [B,H,dv,dk] fp32 tensor.  Returns (out, final_mu or None)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    if not q.is_cuda:
+        raise ValueError("lin_scan_fwd takes device tensors")
+    _check(q, "q", dt)
+    _check(k, "k", dt, (B, H, T, dk))
+    _check(v, "v", dt, (B, H, T, dv))
+    _check(beta, "beta", dt, (B, H, T, dv))
+    _check(d, "d", dt, (B, H, T))
+    _check(A, "A", torch.float32, (H,))
+    if mu0 is not None:
+        _check(mu0, "mu0", torch.float32, (B, H, dv, dk))
+    if out is None:
+        out = torch.empty(B, H, T, dv, device=q.device, dtype=torch.float32)
+    _check(out, "out", torch.float32, (B, H, T, dv))
+    if final_mu is True:
+        final_mu = torch.empty(B, H, dv, dk, device=q.device, dtype=torch.float32)
+    elif final_mu is False:
+        final_mu = None
+    if final_mu is not None:
+        _check(final_mu, "final_mu", torch.float32, (B, H, dv, dk))
+    st = lib.kdn_lin_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                              float(I_prior), _ptr(mu0), _ptr(out), _ptr(final_mu),
+                              B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
+                              _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_lin_scan_fwd")
+    return out, final_mu
 
 
 def diag_scan_bwd_workspace(B, H, T, dk, dv) -> int:

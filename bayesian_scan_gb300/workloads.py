@@ -96,6 +96,15 @@ TRAIN = {
                                   ("uniform", 0.5, 4.0), 0, 0, False, 1006),
 }
 WORKLOADS.update(TRAIN)
+# the non-metaplastic limit (importance held at I_prior) on the layer shapes
+# and the long context: same inputs and seeds as the metaplastic workloads
+LIN = {
+    "layer750m_lin": Workload("layer750m_lin", 8, 16, 4096, 128, 128, torch.bfloat16,
+                              ("uniform", 0.5, 4.0), 0, 0, False, 1002),
+    "longctx_lin": Workload("longctx_lin", 1, 16, 65536, 128, 128, torch.bfloat16,
+                            ("uniform", 0.1, 1.0), 0, 0, False, 1004),
+}
+WORKLOADS.update(LIN)
 
 # the five scan configurations in the order the configuration list gives them
 ORDER = ["small", "heads32_t2048_d64", "layer750m", "layer1p3b", "longctx"]

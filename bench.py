@@ -16,6 +16,7 @@ collective; weak scaling); the timing is the max over ranks.
     python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
     python bench.py --workload layer750m_bwd   # the backward pass (training)
     python bench.py --workload decode2k        # batched one-token decoding
+    python bench.py --workload layer750m_lin   # the non-metaplastic limit
 
 Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
 Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
@@ -685,6 +686,129 @@ def run_backward(args, w, dist):
     return 0
 
 
+# non-metaplastic limit: per state element and token one FMA for the write
+# (in the scaled form Ew += (W beta_i v_i) k_j) and one for the readout
+LIN_FLOP_PER_ELEMENT_TOKEN = 4
+
+
+def run_lin(args, w, dist):
+    """The non-metaplastic scan (kdn_lin_scan_fwd) over the workload; `value`
+    is token-heads per second, the roofline the FP32 ALUs."""
+    import torch
+
+    from bayesian_scan_gb300 import kdn, workloads
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w_rank = w if dist.rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * dist.rank})
+    host = workloads.make(w_rank, with_mobius=False)
+    names = ("q", "k", "v", "beta", "d", "A")
+    x = {n: host[n].to(dev) for n in names}
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    out = torch.empty(B, H, T, dv, device=dev)
+    fmu = torch.empty(B, H, dv, dk, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kdn.lin_scan_fwd(*(x[n] for n in names), I_prior=w.I_prior, out=out, final_mu=fmu,
+                         stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for(dist.local_rank))
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        start.record(stream)
+        for _ in range(K):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    st = kdn.get_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {kdn.status_string(st)}")
+    ms = start.elapsed_time(stop)
+    max_ms = dist.max(ms)
+    tokens = B * H * T
+    value = dist.world * tokens * K / (max_ms / 1e3)
+    peaks = measured_peaks()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_FALLBACK))
+    alu_peak = nsm * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved = LIN_FLOP_PER_ELEMENT_TOKEN * dv * dk * tokens / (ms / K / 1e3) / 1e12
+    plan = kdn.diag_scan_plan(B, H, T, dk, dv, w.dtype)
+    line = {
+        "metric": "non-metaplastic scan tokens/s (B·H·T per s) and % of FP32 roofline, fwd",
+        "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "T": T, "d_k": dk, "d_v": dv,
+                   "inputs": "bf16" if w.dtype == torch.bfloat16 else "fp32",
+                   "state": "fp32 mu (importance held at I_prior)",
+                   "l2": "inputs larger than the 129 MB L2, no flush"},
+        "roofline": {"kernel": "diag_scan_kernel<..., LIN> (whole kdn_lin_scan_fwd call)",
+                     "bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": None,
+                     "flop_per_element_token": LIN_FLOP_PER_ELEMENT_TOKEN,
+                     "peak_source": f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz"
+                                    " (recipe unit counts and max SM clock)"},
+        "gpu_launches": K * plan["kernels"],
+        "clocks": sampler.summary(),
+    }
+    if not args.no_e2e:
+        pin = {n: host[n].pin_memory() for n in names}
+        xs = {n: torch.empty_like(x[n]) for n in names}
+        out_h = torch.empty(B, H, T, dv).pin_memory()
+
+        def e2e_step():
+            for n in names:
+                xs[n].copy_(pin[n], non_blocking=True)
+            kdn.lin_scan_fwd(*(xs[n] for n in names), I_prior=w.I_prior, out=out, final_mu=fmu,
+                             stream=stream)
+            out_h.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(1, min(K, 20))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        dt = dist.max(time.perf_counter() - t0)
+        line["e2e"] = {"value": dist.world * tokens * n_e2e / dt, "unit": "tokens/s", "steps": n_e2e,
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                       "d2h_bytes_per_step": out_h.numel() * 4,
+                       "path": "page-locked inputs -> device copies -> kdn.lin_scan_fwd -> "
+                               "page-locked output"}
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n_heads = min(B * H, oracle.max_threads())
+        sl = lambda t_: t_.reshape(B * H, *t_.shape[2:])[:n_heads].unsqueeze(0)
+        args_o = [sl(host[n]) for n in ("q", "k", "v", "beta", "d")]
+        A_o = host["A"].repeat(B)[:n_heads].contiguous()
+        t_tok = T
+        t0 = time.perf_counter()
+        oracle.lin_scan(*(a_[:, :, :64] for a_ in args_o), A_o, w.I_prior)
+        per_tok = (time.perf_counter() - t0) / 64
+        t_tok = max(64, min(T, int(10.0 / max(per_tok, 1e-9))))
+        dt, reps = 0.0, 0
+        while dt < 10.0 and reps < 100:
+            t0 = time.perf_counter()
+            oracle.lin_scan(*(a_[:, :, :t_tok] for a_ in args_o), A_o, w.I_prior)
+            dt += time.perf_counter() - t0
+            reps += 1
+        line["cpu_baseline"] = {"value": reps * n_heads * t_tok / dt, "unit": "tokens/s",
+                                "cores": n_heads, "kind": "oracle",
+                                "sample": f"{reps} x ({n_heads} heads x {t_tok} tokens) of the same "
+                                          f"inputs (all {dv}x{dk} state rows), fp64 oracle, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference_bwd(args, w, dist):
     """Reference arm of the backward workload: the fp64 reverse-mode oracle."""
     if dist.rank != 0:
@@ -729,6 +853,14 @@ def main():
                                       "cpu_baseline"}), flush=True)
                 return 0
             return run_decode(args, w, dist)
+        if w.name in workloads.LIN:
+            if args.impl == "reference":
+                if dist.rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                                      "oracle on the metaplastic scan workloads; the non-metaplastic "
+                                      "scan's oracle is timed by our arm's cpu_baseline"}), flush=True)
+                return 0
+            return run_lin(args, w, dist)
         if w.name in workloads.TRAIN:
             if args.impl == "reference":
                 return run_reference_bwd(args, w, dist)

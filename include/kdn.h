@@ -100,6 +100,33 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
                              kdn_dtype in_dtype, void* stream);
 
 /*
+ * kdn_lin_scan_fwd -- the non-metaplastic limit of kdn_diag_scan_fwd: the
+ * importance is held at I_prior ("Learning to Remember, Learn, and Forget in
+ * Attention-Based Models", Metodologia 4, Unificazione Teorica: Mamba2 is the
+ * case I_t = I_prior), so per head and token
+ *     mu_t = alpha_t mu_{t-1} + (beta_t . v_t) (x) k_t / I_prior,
+ *     o_t[i] = sum_j mu_t[i][j] q_t[j],        alpha_t = exp(-A d_t)
+ * (decayed linear attention with a per-token scalar decay).
+ *
+ *   q, k, v, beta, d, A, I_prior   as for kdn_diag_scan_fwd
+ *   mu0       [B,H,dv,dk] fp32 or NULL (mu_0 = 0)
+ *   out       [B,H,T,dv] fp32
+ *   final_mu  [B,H,dv,dk] fp32 or NULL   mu_T (feeding it back as mu0 of a
+ *             call on the following tokens gives one call's result)
+ *   Sizes, alignment and errors as for kdn_diag_scan_fwd.
+ *
+ * Same kernels as the diagonal scan with the importance update and the
+ * per-element division taken out (two FP32 FMA per state element and token:
+ * the write and the readout); long sequences with few heads are split into
+ * token parts the same way.
+ */
+KDN_API kdn_status kdn_lin_scan_fwd(const void* q, const void* k, const void* v,
+                            const void* beta, const void* d, const float* A,
+                            float I_prior, const float* mu0, float* out,
+                            float* final_mu, int B, int H, int T, int dk, int dv,
+                            kdn_dtype in_dtype, void* stream);
+
+/*
  * kdn_diag_scan_bwd -- backward pass of kdn_diag_scan_fwd (the pages' kernels
  * serve training on GPUs: "Learning to Remember, Learn, and Forget in
  * Attention-Based Models", Contributi Chiave).  For the scalar

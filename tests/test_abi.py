@@ -186,3 +186,24 @@ def test_bwd_workspace_size(lib):
     assert lib.kdn_diag_scan_bwd_workspace(1, 1, 0, 16, 16, ctypes.byref(n)) == 0 and n.value == 0
     assert lib.kdn_diag_scan_bwd_workspace(1, 1, 8, 24, 16, ctypes.byref(n)) == -2
     assert lib.kdn_diag_scan_bwd_workspace(0, 1, 8, 16, 16, ctypes.byref(n)) == -1
+
+
+def _lin(lib, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, mu0=None, out=FAKE, fm=None,
+         B=1, H=1, T=8, dk=16, dv=16, dtype=1):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_lin_scan_fwd(vp(q), vp(k), vp(v), vp(beta), vp(d), vp(A), 1.0, vp(mu0), vp(out),
+                                vp(fm), B, H, T, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d", "A", "out"])
+def test_lin_null_pointer(lib, field):
+    assert _lin(lib, **{field: None}) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), -1), (dict(T=-1), -1), (dict(dk=8), -2), (dict(dv=48), -2), (dict(dtype=2), -2),
+    (dict(q=FAKE + 8), -1), (dict(out=FAKE + 4), -1), (dict(mu0=FAKE + 8), -1),
+    (dict(fm=FAKE + 2), -1), (dict(A=FAKE + 2), -1), (dict(d=FAKE + 1), -1),
+])
+def test_lin_rejects(lib, kw, status):
+    assert _lin(lib, **kw) == status
