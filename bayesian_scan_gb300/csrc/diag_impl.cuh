@@ -693,6 +693,8 @@ __global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* 
 
 // the aggregate pass on the tensor cores (uses AggScale, LOG2E, g_diag_error)
 #include "diag_agg_tc.cuh"
+// the non-metaplastic full pass on the tensor cores (d = 128, bf16)
+#include "lin_tc.cuh"
 
 namespace kdn {
 namespace diag {
@@ -805,7 +807,7 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     // per extra (head, part) (aggregate, carry and start-state traffic) and
     // 23 for the two extra launches (fitted to GB300 timings of the 750M-shaped
     // layer); taken when it saves more than 2 %.
-    if (P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas < slots && a.T >= 32 * TC) {
+    if (!LIN && P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas < slots && a.T >= 32 * TC) {
         auto est = [&](int parts, int plen) {
             const long long waves = (pl->ctas * parts + slots - 1) / slots;
             return static_cast<double>(waves) * plen +
@@ -899,7 +901,31 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
             e = cudaGetLastError();
         }
     }
-    if (e == cudaSuccess) {
+    bool tc_full = false;
+    if constexpr (LIN && DK == lintc::LD && std::is_same<TIn, __nv_bfloat16>::value) {
+        if (e == cudaSuccess && dv == lintc::LD) {
+            // full pass on the tensor cores: one CTA per (head, part)
+            tc_full = true;
+            static bool attr[64] = {};
+            int dev = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess && dev >= 0 && dev < 64 && !attr[dev]) {
+                e = cudaFuncSetAttribute(lintc::lin_tc_kernel<lintc::LD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, lintc::LSMEM);
+                if (e == cudaSuccess) attr[dev] = true;
+            }
+            if (e == cudaSuccess) {
+                lintc::LinArgs la{static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+                                  static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.beta),
+                                  static_cast<const __nv_bfloat16*>(a.d), a.A, a.I_prior, a.mu0, prm.agg,
+                                  a.out, a.final_state, BH, a.H, a.T, pl.part_len, wait_ns};
+                lintc::lin_tc_kernel<lintc::LD>
+                    <<<dim3(static_cast<unsigned>(BH), P), lintc::LTHREADS, lintc::LSMEM, st>>>(la);
+                e = cudaGetLastError();
+            }
+        }
+    }
+    if (e == cudaSuccess && !tc_full) {
         diag_scan_kernel<DK, TIn, false, LIN>
             <<<dim3(static_cast<unsigned>(ctas), P), Geo<DK>::NTHREADS, smem, st>>>(prm);
         e = cudaGetLastError();

@@ -1,0 +1,387 @@
+// lin_tc.cuh -- the non-metaplastic limit on the tensor cores, for d_k = d_v
+// = 128 and bf16 inputs ("Learning to Remember, Learn, and Forget in
+// Attention-Based Models", Metodologia 4: with the importance held at I_prior
+// the update is decayed linear attention).  Included by diag_impl.cuh.
+//
+// What is computed, per head: with S = I_prior mu (d_v x d_k, fp32),
+//     S_t = alpha_t S_{t-1} + (beta_t . v_t) k_t^T,   o_t = S_t q_t / I_prior.
+// How: chunks of C = 32 tokens.  With g_t = sum_{r <= t} log alpha_r inside a
+// chunk (g_t <= 0), the chunk's outputs and end state are
+//     o_t = [ sum_{s <= t} e^{g_t - g_s} (q_t . k_s) Vb_s  +  e^{g_t} S q_t ] / I_prior
+//     S'  = e^{g_C} S + sum_s e^{g_C - g_s} Vb_s k_s^T,      Vb_s = beta_s . v_s,
+// five matrix products per chunk, all with M = 128 rows on the tensor cores
+// (tcgen05.mma kind::f16, bf16 operands staged in shared memory as K-major
+// 8 x 16-byte core matrices, fp32 accumulators in tensor memory):
+//     P^T  [s x t] = K Q^T            (K padded to 128 rows; rows >= 32 unused)
+//     Oi^T [i x t] = S Q^T            (S as hi + lo bf16 halves: 2 products)
+//     Oa^T [i x t] = Vb^T P^T         (Vb and P as hi + lo halves: 3 products)
+//     S   [i x j] += (w . Vb)^T K     (w_s = e^{g_C - g_s}; hi + lo: 2 products)
+// The hi + lo splits keep every operand to ~2^-16 relative (one bf16 product
+// alone loses ~2^-9, which fails the 2e-3 bar on o); q, k are bf16 inputs and
+// exact.  S lives in tensor memory for the whole sequence; once per chunk it
+// is read to registers, written to shared memory as the hi/lo operand of the
+// Oi product, and scaled by e^{g_C} in place before the state product adds
+// the chunk.  The P product is issued as soon as the Q and K tiles exist;
+// warps 0 and 4 turn its result into the masked, decayed hi/lo operand of the
+// Oa product while the other warps build the remaining tiles.  Inputs of the
+// next chunk arrive by 1-D bulk copies while the current chunk computes.  All
+// waits are bounded.
+
+namespace kdn {
+namespace lintc {
+namespace {
+
+constexpr int LD = 128;            // d_k = d_v
+constexpr int LC = 32;             // tokens per chunk
+constexpr int LTHREADS = 256;
+constexpr uint32_t LTMEM_COLS = 256;
+constexpr uint32_t COL_S = 0, COL_OA = 128, COL_OI = 160, COL_P = 192;
+// shared memory (bytes); K-major operand tiles: element (row r, k) at
+// (r / 8) * SBO + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2
+constexpr int RAW1 = LC * LD * 2;                 // one input array of a chunk
+constexpr int RAW_STAGE = 4 * RAW1;               // q, k, v, beta
+constexpr int OFF_RAW = 0;
+constexpr int OFF_KB = OFF_RAW + 2 * RAW_STAGE;   // [s x j], read as 128 rows by the P product
+constexpr int OFF_QB = OFF_KB + LC * LD * 2;      // [t x j]
+constexpr int OFF_KT = OFF_QB + LC * LD * 2;      // [j x s]
+constexpr int OFF_VH = OFF_KT + LD * LC * 2;      // [i x s] hi, lo
+constexpr int OFF_AW = OFF_VH + 2 * LD * LC * 2;  // [i x s] hi, lo
+constexpr int OFF_P = OFF_AW + 2 * LD * LC * 2;   // [t x s] hi, lo
+constexpr int OFF_S = OFF_P + 2 * LC * LC * 2;    // [i x j] hi, lo
+constexpr int OFF_MISC = OFF_S + 2 * LD * LD * 2;
+constexpr int SBO_J = (LD / 8) * 128;             // K = 128 (j)
+constexpr int SBO_C = (LC / 8) * 128;             // K = 32 (s)
+constexpr int LSMEM = OFF_MISC + 512;
+static_assert(OFF_KB + (LD / 8) * SBO_J <= LSMEM, "the P product's 128-row read of K stays in shared memory");
+static_assert(LSMEM <= 227 * 1024, "shared memory");
+
+struct LinArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* beta;
+    const __nv_bfloat16* d;
+    const float* A;
+    float Ip;
+    const float* mu0;      // part 0's initial mean, or null
+    const float* agg;      // start states of parts 1.. (carry pass output), or null
+    float* out;
+    float* final_mu;       // or null
+    long long BH;
+    int H, T, part_len;
+    long long wait_ns;
+};
+
+// hi + lo bf16 halves of a pair (x0, x1), packed two per 32-bit word: hi is
+// x truncated to bf16 (exact, an integer mask), lo the rest x - hi (exact in
+// fp32, below 2^-7 |x|) rounded to bf16, so hi + lo is within 2^-16 |x|.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const uint32_t b0 = __float_as_uint(x0) & 0xffff0000u, b1 = __float_as_uint(x1) & 0xffff0000u;
+    hi = (b0 >> 16) | b1;
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(b0), x1 - __uint_as_float(b1));
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int D_>
+__global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
+    static_assert(D_ == LD, "d_k = d_v = 128");
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* s_g = reinterpret_cast<float*>(smem + OFF_MISC);          // [LC] g_t
+    float* s_eg = s_g + LC;                                          // [LC] e^{g_t}
+    float* s_w = s_eg + LC;                                          // [LC] e^{g_C - g_t}
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_w + LC);      // [2]
+    uint64_t* bar_p = raw_full + 2;
+    uint64_t* bar_o = bar_p + 1;
+    uint32_t* holder = reinterpret_cast<uint32_t*>(bar_o + 1);
+    float* s_egl = reinterpret_cast<float*>(holder + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long bh = blockIdx.x;
+    const int part = blockIdx.y;
+    const int T = p.T;
+    const int tb = min(T, part * p.part_len);
+    const int te = min(T, tb + p.part_len);
+    const int nch = (te - tb + LC - 1) / LC;
+    const long long S2 = static_cast<long long>(LD) * LD;
+    const float Ah = p.A[bh % p.H];
+    bool ok = true;
+
+    auto issue = [&](int c) {   // thread 0: raw inputs of chunk c into stage c & 1
+        const int st = c & 1;
+        const int t0 = tb + c * LC, n = min(LC, te - t0);
+        const uint32_t bytes = static_cast<uint32_t>(n * LD * 2);
+        const long long off = (bh * T + t0) * LD;
+        unsigned char* dst = smem + OFF_RAW + st * RAW_STAGE;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&raw_full[st], 4 * bytes);
+        bulk_g2s(dst, p.q + off, bytes, &raw_full[st]);
+        bulk_g2s(dst + RAW1, p.k + off, bytes, &raw_full[st]);
+        bulk_g2s(dst + 2 * RAW1, p.v + off, bytes, &raw_full[st]);
+        bulk_g2s(dst + 3 * RAW1, p.beta + off, bytes, &raw_full[st]);
+    };
+
+    if (tid == 0) {
+        mbar_init(&raw_full[0], 1);
+        mbar_init(&raw_full[1], 1);
+        mbar_init(bar_p, 1);
+        mbar_init(bar_o, 1);
+        mbar_init_fence();
+        if (nch > 0) issue(0);
+    }
+    if (warp == 0) tmem_alloc(holder, LTMEM_COLS);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *holder;
+    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+    const int row = 32 * q4 + lane;          // its TMEM lane = state row i
+    const int cbase = (warp >> 2) * 64;      // its half of the state's columns
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+
+    // ---- initial state S = I_prior mu_start into tensor memory ---------------
+    {
+        const float* src = nullptr;
+        float scale = p.Ip;
+        if (part > 0) {
+            src = p.agg + (static_cast<long long>(part - 1) * p.BH + bh) * 2 * S2 + S2;   // eta part
+            scale = 1.f;
+        } else if (p.mu0) {
+            src = p.mu0 + bh * S2;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (src) x = *reinterpret_cast<const float4*>(src + static_cast<long long>(row) * LD + cbase + 32 * h + j);
+                v[j] = x.x * scale;
+                v[j + 1] = x.y * scale;
+                v[j + 2] = x.z * scale;
+                v[j + 3] = x.w * scale;
+            }
+            tmem_st32(tl + COL_S + cbase + 32 * h, v);
+        }
+        tmem_wait_st();
+    }
+    // operand rows the P product reads past K's 32 rows hold other data;
+    // zero the K rows of a short chunk below
+
+    __nv_bfloat16 dreg = __float2bfloat16_rn(0.f);   // d of token (chunk start + lane), warp 0
+    if (warp == 0 && nch > 0 && lane < min(LC, te - tb)) dreg = p.d[bh * T + tb + lane];
+    constexpr uint32_t IDESC_T = umma_idesc_bf16_f32(128, LC);    // N = 32 tokens
+    constexpr uint32_t IDESC_J = umma_idesc_bf16_f32(128, LD);    // N = 128 key columns
+
+    for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        const int t0 = tb + c * LC, n = min(LC, te - t0);
+        if (!mbar_wait(&raw_full[st], (c >> 1) & 1, p.wait_ns)) ok = false;
+        // ---- decay exponents of the chunk (warp 0) ----
+        if (warp == 0) {
+            float a = lane < n ? -Ah * __bfloat162float(dreg) : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, a, o);
+                if (lane >= o) a += y;
+            }
+            const float gl = __shfl_sync(0xffffffffu, a, 31);
+            s_g[lane] = a;
+            s_eg[lane] = expf(a);
+            s_w[lane] = expf(gl - a);
+            if (lane == 0) *s_egl = expf(gl);
+            if (c + 1 < nch) {
+                const int n1 = min(LC, te - (t0 + LC));
+                if (lane < n1) dreg = p.d[bh * T + t0 + LC + lane];
+            }
+        }
+        __syncthreads();   // exponents ready; every thread is past chunk c-1
+        if (tid == 0 && c + 1 < nch) issue(c + 1);
+
+        const unsigned char* rq = smem + OFF_RAW + st * RAW_STAGE;
+        const unsigned char* rk = rq + RAW1;
+        const unsigned char* rv = rq + 2 * RAW1;
+        const unsigned char* rbt = rq + 3 * RAW1;
+        const uint32_t sbase = smem_addr(smem);
+        auto dj = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_J); };
+        auto dc = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_C); };
+        // ---- Q and K tiles [token x j] (16-byte pieces; a warp stores 512
+        // contiguous bytes), then the P product ----
+        for (int pc = tid; pc < LC * (LD / 8); pc += LTHREADS) {
+            const int t8 = pc & 7, jq = (pc >> 3) & 3, rest = pc >> 5;
+            const int t = 8 * (rest & 3) + t8, jc = 4 * (rest >> 2) + jq;
+            const int off = (t >> 3) * SBO_J + jc * 128 + t8 * 16;
+            uint4 qv = make_uint4(0u, 0u, 0u, 0u), kv = qv;
+            if (t < n) {
+                qv = *reinterpret_cast<const uint4*>(rq + t * LD * 2 + jc * 16);
+                kv = *reinterpret_cast<const uint4*>(rk + t * LD * 2 + jc * 16);
+            }
+            *reinterpret_cast<uint4*>(smem + OFF_QB + off) = qv;
+            *reinterpret_cast<uint4*>(smem + OFF_KB + off) = kv;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();   // Q, K tiles written
+        if (tid == 0) {
+            tc_fence_after_sync();
+            // P^T [s x t] = K Q^T
+#pragma unroll
+            for (int ks = 0; ks < LD / 16; ++ks)
+                umma_bf16(tmem + COL_P, dj(OFF_KB, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
+            umma_commit(bar_p);
+        }
+        // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (warps 1-7;
+        // lanes run over consecutive rows, so gathers and stores are
+        // conflict-free) ----
+        if (warp != 0 && warp != 4) {
+            const int bt = tid - (warp < 4 ? 32 : 64);   // 0 .. 191 over warps 1-3, 5-7
+            for (int pc = bt; pc < LD * (LC / 8); pc += LTHREADS - 64) {
+                const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
+                uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t kb[2];
+                    float x[2], xw[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int s_ = 8 * sc + 2 * e + u;
+                        const bool in = s_ < n;
+                        const unsigned short kbits = in ? *reinterpret_cast<const unsigned short*>(rk + (s_ * LD + r) * 2) : 0;
+                        const unsigned short bb = in ? *reinterpret_cast<const unsigned short*>(rbt + (s_ * LD + r) * 2) : 0;
+                        const unsigned short vb = in ? *reinterpret_cast<const unsigned short*>(rv + (s_ * LD + r) * 2) : 0;
+                        x[u] = __uint_as_float(static_cast<uint32_t>(bb) << 16) *
+                               __uint_as_float(static_cast<uint32_t>(vb) << 16);
+                        xw[u] = s_w[s_] * x[u];
+                        kb[u] = kbits;
+                    }
+                    kt[e] = kb[0] | (kb[1] << 16);
+                    split_pair(x[0], x[1], vh[e], vl[e]);
+                    split_pair(xw[0], xw[1], ah[e], al[e]);
+                }
+                const int off = (r >> 3) * SBO_C + sc * 128 + (r & 7) * 16;
+                *reinterpret_cast<uint4*>(smem + OFF_KT + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_VH + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_VH + LD * LC * 2 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_AW + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_AW + LD * LC * 2 + off) = make_uint4(al[0], al[1], al[2], al[3]);
+            }
+        } else {
+            // ---- warps 0 and 4 (TMEM lanes 0-31): the masked, decayed P back
+            // as the hi/lo operand of the Oa product, 16 tokens t each ----
+            if (!mbar_wait(bar_p, c & 1, p.wait_ns)) ok = false;
+            tc_fence_after_sync();
+            float pv[32];
+            tmem_ld32(tmem + COL_P, pv);   // lane s: P^T[s][t], t = 0..31
+            const int s_ = lane, tbase = warp == 0 ? 0 : LC / 2;
+            const float gs = s_g[s_];
+            float ph[LC / 2];   // this warp's half of the tokens (static indices)
+#pragma unroll
+            for (int u = 0; u < LC / 2; ++u) ph[u] = warp == 0 ? pv[u] : pv[LC / 2 + u];
+#pragma unroll
+            for (int tt = 0; tt < LC / 2; tt += 2) {
+                float x[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = tbase + tt + u;
+                    x[u] = (s_ <= t && t < n && s_ < n) ? ph[tt + u] * expf(s_g[t] - gs) : 0.f;
+                }
+                uint32_t hi, lo;
+                split_pair(x[0], x[1], hi, lo);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = tbase + tt + u;
+                    const int off = (t >> 3) * SBO_C + (s_ >> 3) * 128 + (t & 7) * 16 + (s_ & 7) * 2;
+                    *reinterpret_cast<unsigned short*>(smem + OFF_P + off) =
+                        static_cast<unsigned short>(u ? hi >> 16 : hi & 0xffffu);
+                    *reinterpret_cast<unsigned short*>(smem + OFF_P + LC * LC * 2 + off) =
+                        static_cast<unsigned short>(u ? lo >> 16 : lo & 0xffffu);
+                }
+            }
+        }
+        // ---- S: hi/lo operand of the Oi product, then S *= e^{g_C} in place ----
+        {
+            const float egl = *s_egl;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                tmem_ld32(tl + COL_S + cbase + 32 * h, v);
+#pragma unroll
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split_pair(v[8 * j8 + 2 * e], v[8 * j8 + 2 * e + 1], hi[e], lo[e]);
+                    const int jc = (cbase + 32 * h) / 8 + j8;
+                    const int off = (row >> 3) * SBO_J + jc * 128 + (row & 7) * 16;
+                    *reinterpret_cast<uint4*>(smem + OFF_S + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(smem + OFF_S + LD * LD * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= egl;
+                tmem_st32(tl + COL_S + cbase + 32 * h, v);
+            }
+            tmem_wait_st();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before_sync();
+        __syncthreads();   // all operands in shared memory, S scaled, P read
+        if (tid == 0) {
+            tc_fence_after_sync();
+            // Oi^T [i x t] = (S hi + S lo) Q^T
+#pragma unroll
+            for (int ks = 0; ks < LD / 16; ++ks) {
+                umma_bf16(tmem + COL_OI, dj(OFF_S, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
+                umma_bf16(tmem + COL_OI, dj(OFF_S + LD * LD * 2, ks), dj(OFF_QB, ks), IDESC_T, 1u);
+            }
+            // S [i x j] += (w Vb hi + w Vb lo)^T K
+#pragma unroll
+            for (int ks = 0; ks < LC / 16; ++ks) {
+                umma_bf16(tmem + COL_S, dc(OFF_AW, ks), dc(OFF_KT, ks), IDESC_J, 1u);
+                umma_bf16(tmem + COL_S, dc(OFF_AW + LD * LC * 2, ks), dc(OFF_KT, ks), IDESC_J, 1u);
+            }
+            // Oa^T [i x t] = Vb hi P hi + Vb hi P lo + Vb lo P hi
+#pragma unroll
+            for (int ks = 0; ks < LC / 16; ++ks) {
+                umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P, ks), IDESC_T, ks > 0 ? 1u : 0u);
+                umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P + LC * LC * 2, ks), IDESC_T, 1u);
+                umma_bf16(tmem + COL_OA, dc(OFF_VH + LD * LC * 2, ks), dc(OFF_P, ks), IDESC_T, 1u);
+            }
+            umma_commit(bar_o);
+        }
+        if (!mbar_wait(bar_o, c & 1, p.wait_ns)) ok = false;
+        tc_fence_after_sync();
+        // ---- outputs: o_t[i] = (Oa + e^{g_t} Oi) / I_prior (warps 0-3) ----
+        if (warp < 4) {
+            float oa[32], oi[32];
+            tmem_ld32(tl + COL_OA, oa);
+            tmem_ld32(tl + COL_OI, oi);
+            const float rI = 1.f / p.Ip;
+            float* dst = p.out + (bh * T + t0) * LD + row;
+#pragma unroll
+            for (int t = 0; t < LC; ++t)
+                if (t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[t] * oi[t]) * rI;
+        }
+        tc_fence_before_sync();
+        __syncthreads();   // accumulators read; shared operands free
+    }
+
+    // ---- end state mu_T = S / I_prior ----------------------------------------
+    if (p.final_mu && part == static_cast<int>(gridDim.y) - 1) {
+        tc_fence_after_sync();
+        const float rI = 1.f / p.Ip;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tl + COL_S + cbase + 32 * h, v);
+            float* dst = p.final_mu + bh * S2 + static_cast<long long>(row) * LD + cbase + 32 * h;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(v[j] * rI, v[j + 1] * rI, v[j + 2] * rI, v[j + 3] * rI);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, LTMEM_COLS);
+    if (!ok) record_error(&kdn::diag::g_diag_error, KDN_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace lintc
+}  // namespace kdn

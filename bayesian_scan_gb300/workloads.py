@@ -103,6 +103,9 @@ LIN = {
                               ("uniform", 0.5, 4.0), 0, 0, False, 1002),
     "longctx_lin": Workload("longctx_lin", 1, 16, 65536, 128, 128, torch.bfloat16,
                             ("uniform", 0.1, 1.0), 0, 0, False, 1004),
+    # one wave of the 750M layer's heads over 512 tokens, for profiling captures
+    "heads128_t512_lin": Workload("heads128_t512_lin", 8, 16, 512, 128, 128, torch.bfloat16,
+                                  ("uniform", 0.5, 4.0), 0, 0, False, 1007),
 }
 WORKLOADS.update(LIN)
 

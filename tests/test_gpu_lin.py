@@ -93,3 +93,18 @@ def test_lin_is_the_metaplastic_limit_on_the_gpu():
     o_d, _ = kdn.diag_scan_fwd(*x, I_prior=1e6)
     torch.cuda.synchronize()
     assert parity.rel_err(o_d.cpu(), o_l) < 1e-4
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 64, 100, 517])
+def test_lin_tensor_core_path(T):
+    # d_k = d_v = 128 with bf16 inputs runs the chunked tensor-core kernel
+    # (32-token chunks): chunk boundaries, a given initial mean, all heads
+    g = torch.Generator().manual_seed(T)
+    inp = make(2, 3, T, 128, 128, seed=40 + T)
+    check(inp, mu0=torch.randn(2, 3, 128, 128, generator=g))
+
+
+@pytest.mark.parametrize("I_prior,law", [(1e-2, ("const", 1.0)), (1e3, ("uniform", 0.5, 4.0)),
+                                         (1.0, ("const", 0.0)), (1.0, ("const", 30.0))])
+def test_lin_tensor_core_scales(I_prior, law):
+    check(make(1, 4, 96, 128, 128, law=law, seed=50, I_prior=I_prior))
