@@ -92,12 +92,15 @@ class ClockSampler:
         except OSError:
             self.proc = None
         if self.proc is not None:
-            # wait for the first sample: nvidia-smi's start-up (NVML
+            # wait for two samples: nvidia-smi's start-up (NVML
             # initialisation) can hold up kernel launches of this process for
-            # hundreds of ms, which must not fall inside the timed region
+            # up to a few hundred ms, which must not fall inside the timed
+            # region
             import select
-            ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
-            if ready:
+            for _ in range(2):
+                ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+                if not ready:
+                    break
                 line = self.proc.stdout.readline()
                 if line.strip():
                     self.first.append(line)
