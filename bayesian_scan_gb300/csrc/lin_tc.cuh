@@ -22,8 +22,9 @@
 // is read to registers, written to shared memory as the hi/lo operand of the
 // Oi product, and scaled by e^{g_C} in place before the state product adds
 // the chunk.  The P product is issued as soon as the Q and K tiles exist;
-// warps 0 and 4 turn its result into the masked, decayed hi/lo operand of the
-// Oa product while the other warps build the remaining tiles.  Inputs of the
+// warp 0 copies its result to shared memory while the other warps build the
+// remaining tiles, and all warps turn it into the masked, decayed hi/lo
+// operand of the Oa product while the Oi and state products run.  Inputs of the
 // next chunk arrive by 1-D bulk copies while the current chunk computes.  All
 // waits are bounded.
 
@@ -48,7 +49,9 @@ constexpr int OFF_VH = OFF_KT + LD * LC * 2;      // [i x s] hi, lo
 constexpr int OFF_AW = OFF_VH + 2 * LD * LC * 2;  // [i x s] hi, lo
 constexpr int OFF_P = OFF_AW + 2 * LD * LC * 2;   // [t x s] hi, lo
 constexpr int OFF_S = OFF_P + 2 * LC * LC * 2;    // [i x j] hi, lo
-constexpr int OFF_MISC = OFF_S + 2 * LD * LD * 2;
+constexpr int OFF_PRAW = OFF_S + 2 * LD * LD * 2;  // [t][s] fp32, row stride 36
+constexpr int PRAW_LD = 36;
+constexpr int OFF_MISC = OFF_PRAW + LC * PRAW_LD * 4;
 constexpr int SBO_J = (LD / 8) * 128;             // K = 128 (j)
 constexpr int SBO_C = (LC / 8) * 128;             // K = 32 (s)
 constexpr int LSMEM = OFF_MISC + 512;
@@ -80,6 +83,24 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     hi = (b0 >> 16) | b1;
     const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(b0), x1 - __uint_as_float(b1));
     lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (waits for them)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+          "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15])
+                 :
+                 : "memory");
 }
 
 template <int D_>
@@ -231,9 +252,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (warps 1-7;
         // lanes run over consecutive rows, so gathers and stores are
         // conflict-free) ----
-        if (warp != 0 && warp != 4) {
-            const int bt = tid - (warp < 4 ? 32 : 64);   // 0 .. 191 over warps 1-3, 5-7
-            for (int pc = bt; pc < LD * (LC / 8); pc += LTHREADS - 64) {
+        if (warp != 0) {
+            for (int pc = tid - 32; pc < LD * (LC / 8); pc += LTHREADS - 32) {
                 const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
                 uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
 #pragma unroll
@@ -264,37 +284,14 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 *reinterpret_cast<uint4*>(smem + OFF_AW + LD * LC * 2 + off) = make_uint4(al[0], al[1], al[2], al[3]);
             }
         } else {
-            // ---- warps 0 and 4 (TMEM lanes 0-31): the masked, decayed P back
-            // as the hi/lo operand of the Oa product, 16 tokens t each ----
+            // ---- warp 0 (TMEM lanes 0-31): P^T to shared memory as fp32 ----
             if (!mbar_wait(bar_p, c & 1, p.wait_ns)) ok = false;
             tc_fence_after_sync();
             float pv[32];
             tmem_ld32(tmem + COL_P, pv);   // lane s: P^T[s][t], t = 0..31
-            const int s_ = lane, tbase = warp == 0 ? 0 : LC / 2;
-            const float gs = s_g[s_];
-            float ph[LC / 2];   // this warp's half of the tokens (static indices)
+            float* praw = reinterpret_cast<float*>(smem + OFF_PRAW);
 #pragma unroll
-            for (int u = 0; u < LC / 2; ++u) ph[u] = warp == 0 ? pv[u] : pv[LC / 2 + u];
-#pragma unroll
-            for (int tt = 0; tt < LC / 2; tt += 2) {
-                float x[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = tbase + tt + u;
-                    x[u] = (s_ <= t && t < n && s_ < n) ? ph[tt + u] * expf(s_g[t] - gs) : 0.f;
-                }
-                uint32_t hi, lo;
-                split_pair(x[0], x[1], hi, lo);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = tbase + tt + u;
-                    const int off = (t >> 3) * SBO_C + (s_ >> 3) * 128 + (t & 7) * 16 + (s_ & 7) * 2;
-                    *reinterpret_cast<unsigned short*>(smem + OFF_P + off) =
-                        static_cast<unsigned short>(u ? hi >> 16 : hi & 0xffffu);
-                    *reinterpret_cast<unsigned short*>(smem + OFF_P + LC * LC * 2 + off) =
-                        static_cast<unsigned short>(u ? lo >> 16 : lo & 0xffffu);
-                }
-            }
+            for (int t = 0; t < LC; ++t) praw[t * PRAW_LD + lane] = pv[t];
         }
         // ---- S: hi/lo operand of the Oi product, then S *= e^{g_C} in place ----
         {
@@ -321,7 +318,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before_sync();
-        __syncthreads();   // all operands in shared memory, S scaled, P read
+        __syncthreads();   // operands in shared memory, S scaled, P^T in praw
         if (tid == 0) {
             tc_fence_after_sync();
             // Oi^T [i x t] = (S hi + S lo) Q^T
@@ -336,6 +333,33 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 umma_bf16(tmem + COL_S, dc(OFF_AW, ks), dc(OFF_KT, ks), IDESC_J, 1u);
                 umma_bf16(tmem + COL_S, dc(OFF_AW + LD * LC * 2, ks), dc(OFF_KT, ks), IDESC_J, 1u);
             }
+        }
+        // ---- the masked, decayed P as the hi/lo operand of the Oa product:
+        // 4 elements per thread (t = tid / 8, s = 4 (tid % 8) ..), while the
+        // two products above run ----
+        {
+            const float* praw = reinterpret_cast<const float*>(smem + OFF_PRAW);
+            const int t = tid >> 3, s0 = 4 * (tid & 7);
+            const float4 pr = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0);
+            const float pvv[4] = {pr.x, pr.y, pr.z, pr.w};
+            const float gt = s_g[t];
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s_ = s0 + u;
+                x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * expf(gt - s_g[s_]) : 0.f;
+            }
+            uint32_t h0, l0, h1, l1;
+            split_pair(x[0], x[1], h0, l0);
+            split_pair(x[2], x[3], h1, l1);
+            const int off = (t >> 3) * SBO_C + (s0 >> 3) * 128 + (t & 7) * 16 + (s0 & 7) * 2;
+            *reinterpret_cast<uint2*>(smem + OFF_P + off) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(smem + OFF_P + LC * LC * 2 + off) = make_uint2(l0, l1);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();   // P operand ready
+        if (tid == 0) {
+            tc_fence_after_sync();
             // Oa^T [i x t] = Vb hi P hi + Vb hi P lo + Vb lo P hi
 #pragma unroll
             for (int ks = 0; ks < LC / 16; ++ks) {
@@ -347,16 +371,18 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         if (!mbar_wait(bar_o, c & 1, p.wait_ns)) ok = false;
         tc_fence_after_sync();
-        // ---- outputs: o_t[i] = (Oa + e^{g_t} Oi) / I_prior (warps 0-3) ----
-        if (warp < 4) {
-            float oa[32], oi[32];
-            tmem_ld32(tl + COL_OA, oa);
-            tmem_ld32(tl + COL_OI, oi);
+        // ---- outputs: o_t[i] = (Oa + e^{g_t} Oi) / I_prior; the warps of a
+        // lane quarter take 16 tokens each ----
+        {
+            const int tb16 = (warp >> 2) * (LC / 2);
+            float oa[16], oi[16];
+            tmem_ld16(tl + COL_OA + tb16, oa);
+            tmem_ld16(tl + COL_OI + tb16, oi);
             const float rI = 1.f / p.Ip;
-            float* dst = p.out + (bh * T + t0) * LD + row;
+            float* dst = p.out + (bh * T + t0 + tb16) * LD + row;
 #pragma unroll
-            for (int t = 0; t < LC; ++t)
-                if (t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[t] * oi[t]) * rI;
+            for (int t = 0; t < LC / 2; ++t)
+                if (tb16 + t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[tb16 + t] * oi[t]) * rI;
         }
         tc_fence_before_sync();
         __syncthreads();   // accumulators read; shared operands free

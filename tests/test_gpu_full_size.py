@@ -103,3 +103,28 @@ def test_full_size_backward_sampled_heads():
             if n == "A":
                 continue
             assert parity.rel_err(g[n][b:b + 1, h:h + 1].cpu(), r[o]) <= parity.TOL_BWD, (n, bh)
+
+
+@pytest.mark.parametrize("name", ["layer750m_lin", "longctx_lin"])
+def test_full_size_lin_sampled(name):
+    """kdn_lin_scan_fwd at the bench sizes (the tensor-core path; the long
+    context with its token split): rows of the state are independent, so the
+    oracle recomputes sampled rows of sampled heads over the whole sequence."""
+    from bayesian_scan_gb300 import kdn
+    w = workloads.get(name)
+    inp = workloads.make(w, with_mobius=False)
+    x = [inp[n].to("cuda") for n in ("q", "k", "v", "beta", "d", "A")]
+    o, mu = kdn.lin_scan_fwd(*x, I_prior=inp["I_prior"])
+    torch.cuda.synchronize()
+    assert kdn.get_device_error() == 0
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(mu).all())
+    rng = np.random.default_rng(sum(map(ord, name)))
+    heads, rows = _sample(w, rng)
+    for bh in heads:
+        b, h = divmod(bh, w.H)
+        sl = lambda t: t[b:b + 1, h:h + 1]
+        ro, rmu = oracle.lin_scan(sl(inp["q"]), sl(inp["k"]), sl(inp["v"])[..., rows],
+                                  sl(inp["beta"])[..., rows], sl(inp["d"]), inp["A"][h:h + 1],
+                                  inp["I_prior"])
+        assert parity.rel_err(o[b, h][:, rows].cpu(), ro[0, 0]) <= parity.TOL_DIAG, (name, bh)
+        assert parity.rel_err(mu[b, h][rows].cpu(), rmu[0, 0]) <= parity.TOL_DIAG, (name, bh)
