@@ -11,7 +11,9 @@
 //     S'  = e^{g_C} S + sum_s e^{g_C - g_s} Vb_s k_s^T,      Vb_s = beta_s . v_s,
 // five matrix products per chunk, all with M = 128 rows on the tensor cores
 // (tcgen05.mma kind::f16, bf16 operands staged in shared memory as K-major
-// 8 x 16-byte core matrices, fp32 accumulators in tensor memory):
+// 8 x 16-byte core matrices, fp32 accumulators in tensor memory; three
+// threads issue them, since one thread issues only about one MMA per 70
+// cycles):
 //     P^T  [s x t] = K Q^T            (K padded to 128 rows; rows >= 32 unused)
 //     Oi^T [i x t] = S Q^T            (S as hi + lo bf16 halves: 2 products)
 //     Oa^T [i x t] = Vb^T P^T         (Vb and P as hi + lo halves: 3 products)
@@ -23,8 +25,9 @@
 // Oi product, and scaled by e^{g_C} in place before the state product adds
 // the chunk.  The P product is issued as soon as the Q and K tiles exist;
 // warp 0 copies its result to shared memory while the other warps build the
-// remaining tiles, and all warps turn it into the masked, decayed hi/lo
-// operand of the Oa product while the Oi and state products run.  Inputs of the
+// remaining tiles, and warps 1-4 turn it into the masked, decayed hi/lo
+// operand of the Oa product while thread 0 issues the Oi and state products;
+// warp 7 keeps the input copies and the decay exponents one chunk ahead.  Inputs of the
 // next chunk arrive by 1-D bulk copies while the current chunk computes.  All
 // waits are bounded.
 
@@ -36,7 +39,8 @@ constexpr int LD = 128;            // d_k = d_v
 constexpr int LC = 32;             // tokens per chunk
 constexpr int LTHREADS = 256;
 constexpr uint32_t LTMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_OA = 128, COL_OI = 160, COL_P = 192;
+constexpr uint32_t COL_S = 0, COL_OA = 128, COL_OI = 160, COL_P = 192, COL_OL = 224;
+constexpr float LOG2E_L = 1.4426950408889634f;
 // shared memory (bytes); K-major operand tiles: element (row r, k) at
 // (r / 8) * SBO + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2
 constexpr int RAW1 = LC * LD * 2;                 // one input array of a chunk
@@ -54,7 +58,7 @@ constexpr int PRAW_LD = 36;
 constexpr int OFF_MISC = OFF_PRAW + LC * PRAW_LD * 4;
 constexpr int SBO_J = (LD / 8) * 128;             // K = 128 (j)
 constexpr int SBO_C = (LC / 8) * 128;             // K = 32 (s)
-constexpr int LSMEM = OFF_MISC + 512;
+constexpr int LSMEM = OFF_MISC + 1024;
 static_assert(OFF_KB + (LD / 8) * SBO_J <= LSMEM, "the P product's 128-row read of K stays in shared memory");
 static_assert(LSMEM <= 227 * 1024, "shared memory");
 
@@ -107,14 +111,13 @@ template <int D_>
 __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     static_assert(D_ == LD, "d_k = d_v = 128");
     extern __shared__ __align__(128) unsigned char smem[];
-    float* s_g = reinterpret_cast<float*>(smem + OFF_MISC);          // [LC] g_t
-    float* s_eg = s_g + LC;                                          // [LC] e^{g_t}
-    float* s_w = s_eg + LC;                                          // [LC] e^{g_C - g_t}
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_w + LC);      // [2]
+    // per chunk (double-buffered by chunk parity): g_t, e^{g_t}, e^{g_C - g_t}, e^{g_C}
+    float* s_gall = reinterpret_cast<float*>(smem + OFF_MISC);       // [2][3][LC]
+    float* s_eglall = s_gall + 2 * 3 * LC;                           // [2] (+2 pad)
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_eglall + 4);  // [2]
     uint64_t* bar_p = raw_full + 2;
     uint64_t* bar_o = bar_p + 1;
     uint32_t* holder = reinterpret_cast<uint32_t*>(bar_o + 1);
-    float* s_egl = reinterpret_cast<float*>(holder + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long bh = blockIdx.x;
@@ -145,9 +148,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         mbar_init(&raw_full[0], 1);
         mbar_init(&raw_full[1], 1);
         mbar_init(bar_p, 1);
-        mbar_init(bar_o, 1);
+        mbar_init(bar_o, 3);   // three issuing threads commit per chunk
         mbar_init_fence();
-        if (nch > 0) issue(0);
     }
     if (warp == 0) tmem_alloc(holder, LTMEM_COLS);
     tc_fence_before_sync();
@@ -188,36 +190,46 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     // operand rows the P product reads past K's 32 rows hold other data;
     // zero the K rows of a short chunk below
 
-    __nv_bfloat16 dreg = __float2bfloat16_rn(0.f);   // d of token (chunk start + lane), warp 0
-    if (warp == 0 && nch > 0 && lane < min(LC, te - tb)) dreg = p.d[bh * T + tb + lane];
     constexpr uint32_t IDESC_T = umma_idesc_bf16_f32(128, LC);    // N = 32 tokens
     constexpr uint32_t IDESC_J = umma_idesc_bf16_f32(128, LD);    // N = 128 key columns
+    // Warp 7 keeps the raw-input copies and the decay exponents one chunk
+    // ahead (warp 0 issues the MMAs): exponents of chunk c from d of its tokens
+    // (dnext), into buffer c & 1.
+    __nv_bfloat16 dnext = __float2bfloat16_rn(0.f);
+    auto exponents = [&](int c) {   // warp 7
+        const int t0 = tb + c * LC, n = min(LC, te - t0);
+        float a = lane < n ? -Ah * __bfloat162float(dnext) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, a, o);
+            if (lane >= o) a += y;
+        }
+        const float gl = __shfl_sync(0xffffffffu, a, 31);
+        float* g = s_gall + (c & 1) * 3 * LC;
+        g[lane] = a;
+        g[LC + lane] = expf(a);
+        g[2 * LC + lane] = expf(gl - a);
+        if (lane == 0) s_eglall[c & 1] = expf(gl);
+        // d of the chunk after
+        const int n2 = min(LC, te - (t0 + LC));
+        dnext = __float2bfloat16_rn(0.f);
+        if (lane < n2) dnext = p.d[bh * T + t0 + LC + lane];
+    };
+    if (warp == 7 && nch > 0) {
+        if (lane == 0) issue(0);
+        if (lane < min(LC, te - tb)) dnext = p.d[bh * T + tb + lane];
+        exponents(0);
+    }
+    __syncthreads();   // chunk 0's exponents
 
     for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
         const int t0 = tb + c * LC, n = min(LC, te - t0);
+        const float* s_g = s_gall + st * 3 * LC;
+        const float* s_eg = s_g + LC;
+        const float* s_w = s_g + 2 * LC;
+        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1);   // stage (c+1)&1 is free
         if (!mbar_wait(&raw_full[st], (c >> 1) & 1, p.wait_ns)) ok = false;
-        // ---- decay exponents of the chunk (warp 0) ----
-        if (warp == 0) {
-            float a = lane < n ? -Ah * __bfloat162float(dreg) : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, a, o);
-                if (lane >= o) a += y;
-            }
-            const float gl = __shfl_sync(0xffffffffu, a, 31);
-            s_g[lane] = a;
-            s_eg[lane] = expf(a);
-            s_w[lane] = expf(gl - a);
-            if (lane == 0) *s_egl = expf(gl);
-            if (c + 1 < nch) {
-                const int n1 = min(LC, te - (t0 + LC));
-                if (lane < n1) dreg = p.d[bh * T + t0 + LC + lane];
-            }
-        }
-        __syncthreads();   // exponents ready; every thread is past chunk c-1
-        if (tid == 0 && c + 1 < nch) issue(c + 1);
-
         const unsigned char* rq = smem + OFF_RAW + st * RAW_STAGE;
         const unsigned char* rk = rq + RAW1;
         const unsigned char* rv = rq + 2 * RAW1;
@@ -249,11 +261,10 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 umma_bf16(tmem + COL_P, dj(OFF_KB, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
             umma_commit(bar_p);
         }
-        // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (warps 1-7;
-        // lanes run over consecutive rows, so gathers and stores are
-        // conflict-free) ----
-        if (warp != 0) {
-            for (int pc = tid - 32; pc < LD * (LC / 8); pc += LTHREADS - 32) {
+        // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (lanes run
+        // over consecutive rows, so gathers and stores are conflict-free) ----
+        {
+            for (int pc = tid; pc < LD * (LC / 8); pc += LTHREADS) {
                 const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
                 uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
 #pragma unroll
@@ -283,7 +294,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 *reinterpret_cast<uint4*>(smem + OFF_AW + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
                 *reinterpret_cast<uint4*>(smem + OFF_AW + LD * LC * 2 + off) = make_uint4(al[0], al[1], al[2], al[3]);
             }
-        } else {
+        }
+        if (warp == 0) {
             // ---- warp 0 (TMEM lanes 0-31): P^T to shared memory as fp32 ----
             if (!mbar_wait(bar_p, c & 1, p.wait_ns)) ok = false;
             tc_fence_after_sync();
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         // ---- S: hi/lo operand of the Oi product, then S *= e^{g_C} in place ----
         {
-            const float egl = *s_egl;
+            const float egl = s_eglall[st];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float v[32];
@@ -321,63 +333,82 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         __syncthreads();   // operands in shared memory, S scaled, P^T in praw
         if (tid == 0) {
             tc_fence_after_sync();
-            // Oi^T [i x t] = (S hi + S lo) Q^T
+            // Oi^T [i x t] = S hi Q^T (the S lo half goes to its own
+            // accumulator from a second issuing thread)
 #pragma unroll
-            for (int ks = 0; ks < LD / 16; ++ks) {
+            for (int ks = 0; ks < LD / 16; ++ks)
                 umma_bf16(tmem + COL_OI, dj(OFF_S, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
-                umma_bf16(tmem + COL_OI, dj(OFF_S + LD * LD * 2, ks), dj(OFF_QB, ks), IDESC_T, 1u);
-            }
             // S [i x j] += (w Vb hi + w Vb lo)^T K
 #pragma unroll
             for (int ks = 0; ks < LC / 16; ++ks) {
                 umma_bf16(tmem + COL_S, dc(OFF_AW, ks), dc(OFF_KT, ks), IDESC_J, 1u);
                 umma_bf16(tmem + COL_S, dc(OFF_AW + LD * LC * 2, ks), dc(OFF_KT, ks), IDESC_J, 1u);
             }
-        }
-        // ---- the masked, decayed P as the hi/lo operand of the Oa product:
-        // 4 elements per thread (t = tid / 8, s = 4 (tid % 8) ..), while the
-        // two products above run ----
-        {
-            const float* praw = reinterpret_cast<const float*>(smem + OFF_PRAW);
-            const int t = tid >> 3, s0 = 4 * (tid & 7);
-            const float4 pr = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0);
-            const float pvv[4] = {pr.x, pr.y, pr.z, pr.w};
-            const float gt = s_g[t];
-            float x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s_ = s0 + u;
-                x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * expf(gt - s_g[s_]) : 0.f;
-            }
-            uint32_t h0, l0, h1, l1;
-            split_pair(x[0], x[1], h0, l0);
-            split_pair(x[2], x[3], h1, l1);
-            const int off = (t >> 3) * SBO_C + (s0 >> 3) * 128 + (t & 7) * 16 + (s0 & 7) * 2;
-            *reinterpret_cast<uint2*>(smem + OFF_P + off) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2*>(smem + OFF_P + LC * LC * 2 + off) = make_uint2(l0, l1);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();   // P operand ready
-        if (tid == 0) {
-            tc_fence_after_sync();
-            // Oa^T [i x t] = Vb hi P hi + Vb hi P lo + Vb lo P hi
-#pragma unroll
-            for (int ks = 0; ks < LC / 16; ++ks) {
-                umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P, ks), IDESC_T, ks > 0 ? 1u : 0u);
-                umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P + LC * LC * 2, ks), IDESC_T, 1u);
-                umma_bf16(tmem + COL_OA, dc(OFF_VH + LD * LC * 2, ks), dc(OFF_P, ks), IDESC_T, 1u);
-            }
             umma_commit(bar_o);
         }
+        if (tid == 160) {   // warp 5: S lo Q^T into its own accumulator
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < LD / 16; ++ks)
+                umma_bf16(tmem + COL_OL, dj(OFF_S + LD * LD * 2, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
+            umma_commit(bar_o);
+        }
+        // ---- the masked, decayed P as the hi/lo operand of the Oa product,
+        // on warps 1-4 (8 elements, one core-matrix row each) while thread 0
+        // issues the two products above ----
+        if (warp >= 1 && warp <= 4) {
+            const float* praw = reinterpret_cast<const float*>(smem + OFF_PRAW);
+            const int idx = tid - 32, t = idx >> 2, s0 = 8 * (idx & 3);
+            const float4 pa = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0);
+            const float4 pb = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0 + 4);
+            const float pvv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+            const float gt = s_g[t];
+            const float4 ga = *reinterpret_cast<const float4*>(s_g + s0);
+            const float4 gb = *reinterpret_cast<const float4*>(s_g + s0 + 4);
+            const float gsv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s_ = s0 + u;
+                x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * exp2f((gt - gsv[u]) * LOG2E_L) : 0.f;
+            }
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+            const int off = (t >> 3) * SBO_C + (s0 >> 3) * 128 + (t & 7) * 16;
+            *reinterpret_cast<uint4*>(smem + OFF_P + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + OFF_P + LC * LC * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        if (warp >= 1 && warp <= 4) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // P operand ready (warps 1-4)
+            if (tid == 32) {
+                // a second issuing thread, so that this product does not wait
+                // behind thread 0's issue of the two products above
+                tc_fence_after_sync();
+                // Oa^T [i x t] = Vb hi P hi + Vb hi P lo + Vb lo P hi
+#pragma unroll
+                for (int ks = 0; ks < LC / 16; ++ks) {
+                    umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P, ks), IDESC_T, ks > 0 ? 1u : 0u);
+                    umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P + LC * LC * 2, ks), IDESC_T, 1u);
+                    umma_bf16(tmem + COL_OA, dc(OFF_VH + LD * LC * 2, ks), dc(OFF_P, ks), IDESC_T, 1u);
+                }
+                umma_commit(bar_o);
+            }
+        }
+        if (warp == 7 && c + 1 < nch) exponents(c + 1);   // buffer (c+1)&1 is unused in chunk c
         if (!mbar_wait(bar_o, c & 1, p.wait_ns)) ok = false;
         tc_fence_after_sync();
         // ---- outputs: o_t[i] = (Oa + e^{g_t} Oi) / I_prior; the warps of a
         // lane quarter take 16 tokens each ----
         {
             const int tb16 = (warp >> 2) * (LC / 2);
-            float oa[16], oi[16];
+            float oa[16], oi[16], ol[16];
             tmem_ld16(tl + COL_OA + tb16, oa);
             tmem_ld16(tl + COL_OI + tb16, oi);
+            tmem_ld16(tl + COL_OL + tb16, ol);
+#pragma unroll
+            for (int t = 0; t < LC / 2; ++t) oi[t] += ol[t];
             const float rI = 1.f / p.Ip;
             float* dst = p.out + (bh * T + t0 + tb16) * LD + row;
 #pragma unroll
@@ -385,7 +416,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 if (tb16 + t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[tb16 + t] * oi[t]) * rI;
         }
         tc_fence_before_sync();
-        __syncthreads();   // accumulators read; shared operands free
+        __syncthreads();   // accumulators read; shared operands free; next exponents ready
     }
 
     // ---- end state mu_T = S / I_prior ----------------------------------------
