@@ -5,60 +5,63 @@
 //
 // What is computed, per head: with S = I_prior mu (d_v x d_k, fp32),
 //     S_t = alpha_t S_{t-1} + (beta_t . v_t) k_t^T,   o_t = S_t q_t / I_prior.
-// How: chunks of C = 32 tokens.  With g_t = sum_{r <= t} log alpha_r inside a
+// How: chunks of C = 64 tokens.  With g_t = sum_{r <= t} log alpha_r inside a
 // chunk (g_t <= 0), the chunk's outputs and end state are
 //     o_t = [ sum_{s <= t} e^{g_t - g_s} (q_t . k_s) Vb_s  +  e^{g_t} S q_t ] / I_prior
 //     S'  = e^{g_C} S + sum_s e^{g_C - g_s} Vb_s k_s^T,      Vb_s = beta_s . v_s,
 // five matrix products per chunk, all with M = 128 rows on the tensor cores
 // (tcgen05.mma kind::f16, bf16 operands staged in shared memory as K-major
-// 8 x 16-byte core matrices, fp32 accumulators in tensor memory; three
-// threads issue them, since one thread issues only about one MMA per 70
-// cycles):
-//     P^T  [s x t] = K Q^T            (K padded to 128 rows; rows >= 32 unused)
-//     Oi^T [i x t] = S Q^T            (S as hi + lo bf16 halves: 2 products)
+// 8 x 16-byte core matrices, fp32 accumulators in tensor memory):
+//     P^T  [s x t] = K Q^T            (K padded to 128 rows; rows >= 64 unused)
+//     Oi^T [i x t] = S Q^T            (S as hi + lo bf16 halves, read from
+//                                      tensor memory as the A operand: 2 products)
 //     Oa^T [i x t] = Vb^T P^T         (Vb and P as hi + lo halves: 3 products)
 //     S   [i x j] += (w . Vb)^T K     (w_s = e^{g_C - g_s}; hi + lo: 2 products)
 // The hi + lo splits keep every operand to ~2^-16 relative (one bf16 product
 // alone loses ~2^-9, which fails the 2e-3 bar on o); q, k are bf16 inputs and
-// exact.  S lives in tensor memory for the whole sequence; once per chunk it
-// is read to registers, written to shared memory as the hi/lo operand of the
-// Oi product, and scaled by e^{g_C} in place before the state product adds
-// the chunk.  The P product is issued as soon as the Q and K tiles exist;
-// warp 0 copies its result to shared memory while the other warps build the
-// remaining tiles, and warps 1-4 turn it into the masked, decayed hi/lo
-// operand of the Oa product while thread 0 issues the Oi and state products;
-// warp 7 keeps the input copies and the decay exponents one chunk ahead.  Inputs of the
-// next chunk arrive by 1-D bulk copies while the current chunk computes.  All
-// waits are bounded.
+// exact.  S lives in tensor memory for the whole sequence; once per chunk each
+// warp reads its lanes and columns, writes the hi/lo halves back into tensor
+// memory as packed bf16 pairs (the Oi product reads its A operand there, which
+// leaves shared memory room for 64-token chunks) and scales S by e^{g_C} in
+// place before the state product adds the chunk.  The P product is issued as
+// soon as the Q and K tiles exist; warps 0, 1, 4, 5 copy its result to shared
+// memory while all warps build the remaining tiles, and warps 1-4 turn it
+// into the masked, decayed hi/lo operand of the Oa product while thread 0
+// issues the Oi and state products; thread 32 issues the Oa product (a
+// single thread gets only about one MMA accepted per 70 cycles).  Warp 7
+// issues the 1-D bulk copies of the next chunk's inputs as soon as the
+// current ones are consumed and computes the decay exponents one chunk ahead.
+// All waits are bounded.
 
 namespace kdn {
 namespace lintc {
 namespace {
 
 constexpr int LD = 128;            // d_k = d_v
-constexpr int LC = 32;             // tokens per chunk
+constexpr int LC = 64;             // tokens per chunk
 constexpr int LTHREADS = 256;
-constexpr uint32_t LTMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_OA = 128, COL_OI = 160, COL_P = 192, COL_OL = 224;
+constexpr uint32_t LTMEM_COLS = 512;
+// tensor memory columns: S (fp32), its hi / lo bf16 halves as packed pairs
+// (the A operand of the Oi product), the Oa and Oi accumulators, P^T
+constexpr uint32_t COL_S = 0, COL_SH = 128, COL_SL = 192, COL_OA = 256, COL_OI = 320, COL_P = 384;
 constexpr float LOG2E_L = 1.4426950408889634f;
 // shared memory (bytes); K-major operand tiles: element (row r, k) at
 // (r / 8) * SBO + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2
 constexpr int RAW1 = LC * LD * 2;                 // one input array of a chunk
-constexpr int RAW_STAGE = 4 * RAW1;               // q, k, v, beta
+constexpr int RAW_STAGE = 4 * RAW1;               // q, k, v, beta (one stage)
 constexpr int OFF_RAW = 0;
-constexpr int OFF_KB = OFF_RAW + 2 * RAW_STAGE;   // [s x j], read as 128 rows by the P product
+constexpr int OFF_KB = OFF_RAW + RAW_STAGE;       // [s x j], read as 128 rows by the P product
 constexpr int OFF_QB = OFF_KB + LC * LD * 2;      // [t x j]
 constexpr int OFF_KT = OFF_QB + LC * LD * 2;      // [j x s]
 constexpr int OFF_VH = OFF_KT + LD * LC * 2;      // [i x s] hi, lo
 constexpr int OFF_AW = OFF_VH + 2 * LD * LC * 2;  // [i x s] hi, lo
 constexpr int OFF_P = OFF_AW + 2 * LD * LC * 2;   // [t x s] hi, lo
-constexpr int OFF_S = OFF_P + 2 * LC * LC * 2;    // [i x j] hi, lo
-constexpr int OFF_PRAW = OFF_S + 2 * LD * LD * 2;  // [t][s] fp32, row stride 36
-constexpr int PRAW_LD = 36;
+constexpr int OFF_PRAW = OFF_P + 2 * LC * LC * 2; // [t][s] fp32 copy of P^T
+constexpr int PRAW_LD = LC + 4;
 constexpr int OFF_MISC = OFF_PRAW + LC * PRAW_LD * 4;
 constexpr int SBO_J = (LD / 8) * 128;             // K = 128 (j)
-constexpr int SBO_C = (LC / 8) * 128;             // K = 32 (s)
-constexpr int LSMEM = OFF_MISC + 1024;
+constexpr int SBO_C = (LC / 8) * 128;             // K = 64 (s)
+constexpr int LSMEM = OFF_MISC + 2048;
 static_assert(OFF_KB + (LD / 8) * SBO_J <= LSMEM, "the P product's 128-row read of K stays in shared memory");
 static_assert(LSMEM <= 227 * 1024, "shared memory");
 
@@ -89,33 +92,35 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (waits for them)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+// D (TMEM) = A (TMEM, bf16 pairs packed per column, lane = row) * B^T (smem)
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
-          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
-          "=f"(v[14]), "=f"(v[15])
-        : "r"(taddr)
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
-                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
-                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15])
-                 :
-                 : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t v[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
 }
 
 template <int D_>
 __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     static_assert(D_ == LD, "d_k = d_v = 128");
     extern __shared__ __align__(128) unsigned char smem[];
-    // per chunk (double-buffered by chunk parity): g_t, e^{g_t}, e^{g_C - g_t}, e^{g_C}
+    // per chunk (double-buffered by chunk parity): g_t, e^{g_t}, e^{g_C - g_t}, then e^{g_C}
     float* s_gall = reinterpret_cast<float*>(smem + OFF_MISC);       // [2][3][LC]
     float* s_eglall = s_gall + 2 * 3 * LC;                           // [2] (+2 pad)
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_eglall + 4);  // [2]
-    uint64_t* bar_p = raw_full + 2;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_eglall + 4);
+    uint64_t* bar_p = raw_full + 1;
     uint64_t* bar_o = bar_p + 1;
     uint32_t* holder = reinterpret_cast<uint32_t*>(bar_o + 1);
 
@@ -130,25 +135,23 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     const float Ah = p.A[bh % p.H];
     bool ok = true;
 
-    auto issue = [&](int c) {   // thread 0: raw inputs of chunk c into stage c & 1
-        const int st = c & 1;
+    auto issue = [&](int c) {   // one thread: raw inputs of chunk c into the stage
         const int t0 = tb + c * LC, n = min(LC, te - t0);
         const uint32_t bytes = static_cast<uint32_t>(n * LD * 2);
         const long long off = (bh * T + t0) * LD;
-        unsigned char* dst = smem + OFF_RAW + st * RAW_STAGE;
+        unsigned char* dst = smem + OFF_RAW;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&raw_full[st], 4 * bytes);
-        bulk_g2s(dst, p.q + off, bytes, &raw_full[st]);
-        bulk_g2s(dst + RAW1, p.k + off, bytes, &raw_full[st]);
-        bulk_g2s(dst + 2 * RAW1, p.v + off, bytes, &raw_full[st]);
-        bulk_g2s(dst + 3 * RAW1, p.beta + off, bytes, &raw_full[st]);
+        mbar_arrive_expect_tx(raw_full, 4 * bytes);
+        bulk_g2s(dst, p.q + off, bytes, raw_full);
+        bulk_g2s(dst + RAW1, p.k + off, bytes, raw_full);
+        bulk_g2s(dst + 2 * RAW1, p.v + off, bytes, raw_full);
+        bulk_g2s(dst + 3 * RAW1, p.beta + off, bytes, raw_full);
     };
 
     if (tid == 0) {
-        mbar_init(&raw_full[0], 1);
-        mbar_init(&raw_full[1], 1);
+        mbar_init(raw_full, 1);
         mbar_init(bar_p, 1);
-        mbar_init(bar_o, 3);   // three issuing threads commit per chunk
+        mbar_init(bar_o, 2);   // two issuing threads commit per chunk
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(holder, LTMEM_COLS);
@@ -187,40 +190,56 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         tmem_wait_st();
     }
-    // operand rows the P product reads past K's 32 rows hold other data;
-    // zero the K rows of a short chunk below
 
-    constexpr uint32_t IDESC_T = umma_idesc_bf16_f32(128, LC);    // N = 32 tokens
+    constexpr uint32_t IDESC_T = umma_idesc_bf16_f32(128, LC);    // N = 64 tokens
     constexpr uint32_t IDESC_J = umma_idesc_bf16_f32(128, LD);    // N = 128 key columns
     // Warp 7 keeps the raw-input copies and the decay exponents one chunk
-    // ahead (warp 0 issues the MMAs): exponents of chunk c from d of its tokens
-    // (dnext), into buffer c & 1.
-    __nv_bfloat16 dnext = __float2bfloat16_rn(0.f);
+    // ahead (threads 0 and 32 issue the MMAs): exponents of chunk c from the
+    // d of its tokens (dn0: token lane, dn1: token 32 + lane), into buffer c & 1.
+    __nv_bfloat16 dn0 = __float2bfloat16_rn(0.f), dn1 = dn0;
+    auto load_d = [&](int c) {
+        const int t0 = tb + c * LC, n = min(LC, te - t0);
+        dn0 = __float2bfloat16_rn(0.f);
+        dn1 = dn0;
+        if (lane < n) dn0 = p.d[bh * T + t0 + lane];
+        if (32 + lane < n) dn1 = p.d[bh * T + t0 + 32 + lane];
+    };
     auto exponents = [&](int c) {   // warp 7
         const int t0 = tb + c * LC, n = min(LC, te - t0);
-        float a = lane < n ? -Ah * __bfloat162float(dnext) : 0.f;
+        float a0 = lane < n ? -Ah * __bfloat162float(dn0) : 0.f;
+        float a1 = 32 + lane < n ? -Ah * __bfloat162float(dn1) : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, a, o);
-            if (lane >= o) a += y;
+            const float y0 = __shfl_up_sync(0xffffffffu, a0, o);
+            const float y1 = __shfl_up_sync(0xffffffffu, a1, o);
+            if (lane >= o) {
+                a0 += y0;
+                a1 += y1;
+            }
         }
-        const float gl = __shfl_sync(0xffffffffu, a, 31);
+        a1 += __shfl_sync(0xffffffffu, a0, 31);
+        const float gl = __shfl_sync(0xffffffffu, a1, 31);
         float* g = s_gall + (c & 1) * 3 * LC;
-        g[lane] = a;
-        g[LC + lane] = expf(a);
-        g[2 * LC + lane] = expf(gl - a);
+        g[lane] = a0;
+        g[32 + lane] = a1;
+        g[LC + lane] = expf(a0);
+        g[LC + 32 + lane] = expf(a1);
+        g[2 * LC + lane] = expf(gl - a0);
+        g[2 * LC + 32 + lane] = expf(gl - a1);
         if (lane == 0) s_eglall[c & 1] = expf(gl);
-        // d of the chunk after
-        const int n2 = min(LC, te - (t0 + LC));
-        dnext = __float2bfloat16_rn(0.f);
-        if (lane < n2) dnext = p.d[bh * T + t0 + LC + lane];
+        if (c + 1 < nch) load_d(c + 1);
     };
     if (warp == 7 && nch > 0) {
         if (lane == 0) issue(0);
-        if (lane < min(LC, te - tb)) dnext = p.d[bh * T + tb + lane];
+        load_d(0);
         exponents(0);
     }
     __syncthreads();   // chunk 0's exponents
+
+    const uint32_t sbase = smem_addr(smem);
+    auto dj = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_J); };
+    auto dc = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_C); };
+    float* praw = reinterpret_cast<float*>(smem + OFF_PRAW);
 
     for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
@@ -228,20 +247,16 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         const float* s_g = s_gall + st * 3 * LC;
         const float* s_eg = s_g + LC;
         const float* s_w = s_g + 2 * LC;
-        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1);   // stage (c+1)&1 is free
-        if (!mbar_wait(&raw_full[st], (c >> 1) & 1, p.wait_ns)) ok = false;
-        const unsigned char* rq = smem + OFF_RAW + st * RAW_STAGE;
+        if (!mbar_wait(raw_full, c & 1, p.wait_ns)) ok = false;
+        const unsigned char* rq = smem + OFF_RAW;
         const unsigned char* rk = rq + RAW1;
         const unsigned char* rv = rq + 2 * RAW1;
         const unsigned char* rbt = rq + 3 * RAW1;
-        const uint32_t sbase = smem_addr(smem);
-        auto dj = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_J); };
-        auto dc = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_C); };
         // ---- Q and K tiles [token x j] (16-byte pieces; a warp stores 512
         // contiguous bytes), then the P product ----
         for (int pc = tid; pc < LC * (LD / 8); pc += LTHREADS) {
             const int t8 = pc & 7, jq = (pc >> 3) & 3, rest = pc >> 5;
-            const int t = 8 * (rest & 3) + t8, jc = 4 * (rest >> 2) + jq;
+            const int t = 8 * (rest & 7) + t8, jc = 4 * (rest >> 3) + jq;
             const int off = (t >> 3) * SBO_J + jc * 128 + t8 * 16;
             uint4 qv = make_uint4(0u, 0u, 0u, 0u), kv = qv;
             if (t < n) {
@@ -263,65 +278,61 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (lanes run
         // over consecutive rows, so gathers and stores are conflict-free) ----
-        {
-            for (int pc = tid; pc < LD * (LC / 8); pc += LTHREADS) {
-                const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
-                uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
+        for (int pc = tid; pc < LD * (LC / 8); pc += LTHREADS) {
+            const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
+            uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint32_t kb[2];
-                    float x[2], xw[2];
+            for (int e = 0; e < 4; ++e) {
+                uint32_t kb[2];
+                float x[2], xw[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int s_ = 8 * sc + 2 * e + u;
-                        const bool in = s_ < n;
-                        const unsigned short kbits = in ? *reinterpret_cast<const unsigned short*>(rk + (s_ * LD + r) * 2) : 0;
-                        const unsigned short bb = in ? *reinterpret_cast<const unsigned short*>(rbt + (s_ * LD + r) * 2) : 0;
-                        const unsigned short vb = in ? *reinterpret_cast<const unsigned short*>(rv + (s_ * LD + r) * 2) : 0;
-                        x[u] = __uint_as_float(static_cast<uint32_t>(bb) << 16) *
-                               __uint_as_float(static_cast<uint32_t>(vb) << 16);
-                        xw[u] = s_w[s_] * x[u];
-                        kb[u] = kbits;
-                    }
-                    kt[e] = kb[0] | (kb[1] << 16);
-                    split_pair(x[0], x[1], vh[e], vl[e]);
-                    split_pair(xw[0], xw[1], ah[e], al[e]);
+                for (int u = 0; u < 2; ++u) {
+                    const int s_ = 8 * sc + 2 * e + u;
+                    const bool in = s_ < n;
+                    const unsigned short kbits = in ? *reinterpret_cast<const unsigned short*>(rk + (s_ * LD + r) * 2) : 0;
+                    const unsigned short bb = in ? *reinterpret_cast<const unsigned short*>(rbt + (s_ * LD + r) * 2) : 0;
+                    const unsigned short vb = in ? *reinterpret_cast<const unsigned short*>(rv + (s_ * LD + r) * 2) : 0;
+                    x[u] = __uint_as_float(static_cast<uint32_t>(bb) << 16) *
+                           __uint_as_float(static_cast<uint32_t>(vb) << 16);
+                    xw[u] = s_w[s_] * x[u];
+                    kb[u] = kbits;
                 }
-                const int off = (r >> 3) * SBO_C + sc * 128 + (r & 7) * 16;
-                *reinterpret_cast<uint4*>(smem + OFF_KT + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_VH + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_VH + LD * LC * 2 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_AW + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_AW + LD * LC * 2 + off) = make_uint4(al[0], al[1], al[2], al[3]);
+                kt[e] = kb[0] | (kb[1] << 16);
+                split_pair(x[0], x[1], vh[e], vl[e]);
+                split_pair(xw[0], xw[1], ah[e], al[e]);
             }
+            const int off = (r >> 3) * SBO_C + sc * 128 + (r & 7) * 16;
+            *reinterpret_cast<uint4*>(smem + OFF_KT + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
+            *reinterpret_cast<uint4*>(smem + OFF_VH + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+            *reinterpret_cast<uint4*>(smem + OFF_VH + LD * LC * 2 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+            *reinterpret_cast<uint4*>(smem + OFF_AW + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+            *reinterpret_cast<uint4*>(smem + OFF_AW + LD * LC * 2 + off) = make_uint4(al[0], al[1], al[2], al[3]);
         }
-        if (warp == 0) {
-            // ---- warp 0 (TMEM lanes 0-31): P^T to shared memory as fp32 ----
+        // ---- P^T (TMEM lanes 0-63) to shared memory as fp32: warps 0, 1, 4,
+        // 5 (the two lane quarters), 32 tokens each ----
+        if (q4 < 2) {
             if (!mbar_wait(bar_p, c & 1, p.wait_ns)) ok = false;
             tc_fence_after_sync();
             float pv[32];
-            tmem_ld32(tmem + COL_P, pv);   // lane s: P^T[s][t], t = 0..31
-            float* praw = reinterpret_cast<float*>(smem + OFF_PRAW);
+            const int tcol = (warp >> 2) * 32;
+            tmem_ld32(tl + COL_P + tcol, pv);   // lane s = row: P^T[s][t]
 #pragma unroll
-            for (int t = 0; t < LC; ++t) praw[t * PRAW_LD + lane] = pv[t];
+            for (int t = 0; t < 32; ++t) praw[(tcol + t) * PRAW_LD + row] = pv[t];
         }
-        // ---- S: hi/lo operand of the Oi product, then S *= e^{g_C} in place ----
+        // ---- S: its hi/lo bf16 halves into tensor memory (the A operand of
+        // the Oi product), then S *= e^{g_C} in place ----
         {
             const float egl = s_eglall[st];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float v[32];
                 tmem_ld32(tl + COL_S + cbase + 32 * h, v);
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int j8 = 0; j8 < 4; ++j8) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) split_pair(v[8 * j8 + 2 * e], v[8 * j8 + 2 * e + 1], hi[e], lo[e]);
-                    const int jc = (cbase + 32 * h) / 8 + j8;
-                    const int off = (row >> 3) * SBO_J + jc * 128 + (row & 7) * 16;
-                    *reinterpret_cast<uint4*>(smem + OFF_S + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(smem + OFF_S + LD * LD * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
+                for (int e = 0; e < 16; ++e) split_pair(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
+                const uint32_t pc0 = (cbase + 32 * h) / 2;   // packed column of this j range
+                tmem_st16u(tl + COL_SH + pc0, hi);
+                tmem_st16u(tl + COL_SL + pc0, lo);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] *= egl;
                 tmem_st32(tl + COL_S + cbase + 32 * h, v);
@@ -330,14 +341,16 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before_sync();
-        __syncthreads();   // operands in shared memory, S scaled, P^T in praw
+        __syncthreads();   // tiles built, raw stage consumed, S split and scaled, P^T copied
+        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1);
         if (tid == 0) {
             tc_fence_after_sync();
-            // Oi^T [i x t] = S hi Q^T (the S lo half goes to its own
-            // accumulator from a second issuing thread)
+            // Oi^T [i x t] = (S hi + S lo) Q^T, S from tensor memory
 #pragma unroll
-            for (int ks = 0; ks < LD / 16; ++ks)
-                umma_bf16(tmem + COL_OI, dj(OFF_S, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < LD / 16; ++ks) {
+                umma_bf16_ta(tmem + COL_OI, tmem + COL_SH + 8 * ks, dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
+                umma_bf16_ta(tmem + COL_OI, tmem + COL_SL + 8 * ks, dj(OFF_QB, ks), IDESC_T, 1u);
+            }
             // S [i x j] += (w Vb hi + w Vb lo)^T K
 #pragma unroll
             for (int ks = 0; ks < LC / 16; ++ks) {
@@ -346,40 +359,33 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
             }
             umma_commit(bar_o);
         }
-        if (tid == 160) {   // warp 5: S lo Q^T into its own accumulator
-            tc_fence_after_sync();
-#pragma unroll
-            for (int ks = 0; ks < LD / 16; ++ks)
-                umma_bf16(tmem + COL_OL, dj(OFF_S + LD * LD * 2, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
-            umma_commit(bar_o);
-        }
         // ---- the masked, decayed P as the hi/lo operand of the Oa product,
-        // on warps 1-4 (8 elements, one core-matrix row each) while thread 0
-        // issues the two products above ----
+        // on warps 1-4 (token t = idx / 2, 32 source tokens each) ----
         if (warp >= 1 && warp <= 4) {
-            const float* praw = reinterpret_cast<const float*>(smem + OFF_PRAW);
-            const int idx = tid - 32, t = idx >> 2, s0 = 8 * (idx & 3);
-            const float4 pa = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0);
-            const float4 pb = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0 + 4);
-            const float pvv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+            const int idx = tid - 32, t = idx >> 1, sb = 32 * (idx & 1);
             const float gt = s_g[t];
-            const float4 ga = *reinterpret_cast<const float4*>(s_g + s0);
-            const float4 gb = *reinterpret_cast<const float4*>(s_g + s0 + 4);
-            const float gsv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-            float x[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int s_ = s0 + u;
-                x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * exp2f((gt - gsv[u]) * LOG2E_L) : 0.f;
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int s0 = sb + 8 * g8;
+                const float4 pa = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0);
+                const float4 pb = *reinterpret_cast<const float4*>(praw + t * PRAW_LD + s0 + 4);
+                const float4 ga = *reinterpret_cast<const float4*>(s_g + s0);
+                const float4 gb = *reinterpret_cast<const float4*>(s_g + s0 + 4);
+                const float pvv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+                const float gsv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int s_ = s0 + u;
+                    x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * exp2f((gt - gsv[u]) * LOG2E_L) : 0.f;
+                }
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+                const int off = (t >> 3) * SBO_C + (s0 >> 3) * 128 + (t & 7) * 16;
+                *reinterpret_cast<uint4*>(smem + OFF_P + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_P + LC * LC * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
-            const int off = (t >> 3) * SBO_C + (s0 >> 3) * 128 + (t & 7) * 16;
-            *reinterpret_cast<uint4*>(smem + OFF_P + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(smem + OFF_P + LC * LC * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        if (warp >= 1 && warp <= 4) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             asm volatile("bar.sync 1, 128;" ::: "memory");   // P operand ready (warps 1-4)
             if (tid == 32) {
@@ -400,20 +406,17 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         if (!mbar_wait(bar_o, c & 1, p.wait_ns)) ok = false;
         tc_fence_after_sync();
         // ---- outputs: o_t[i] = (Oa + e^{g_t} Oi) / I_prior; the warps of a
-        // lane quarter take 16 tokens each ----
+        // lane quarter take 32 tokens each ----
         {
-            const int tb16 = (warp >> 2) * (LC / 2);
-            float oa[16], oi[16], ol[16];
-            tmem_ld16(tl + COL_OA + tb16, oa);
-            tmem_ld16(tl + COL_OI + tb16, oi);
-            tmem_ld16(tl + COL_OL + tb16, ol);
-#pragma unroll
-            for (int t = 0; t < LC / 2; ++t) oi[t] += ol[t];
+            const int tb32 = (warp >> 2) * 32;
+            float oa[32], oi[32];
+            tmem_ld32(tl + COL_OA + tb32, oa);
+            tmem_ld32(tl + COL_OI + tb32, oi);
             const float rI = 1.f / p.Ip;
-            float* dst = p.out + (bh * T + t0 + tb16) * LD + row;
+            float* dst = p.out + (bh * T + t0 + tb32) * LD + row;
 #pragma unroll
-            for (int t = 0; t < LC / 2; ++t)
-                if (tb16 + t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[tb16 + t] * oi[t]) * rI;
+            for (int t = 0; t < 32; ++t)
+                if (tb32 + t < n) dst[static_cast<long long>(t) * LD] = (oa[t] + s_eg[tb32 + t] * oi[t]) * rI;
         }
         tc_fence_before_sync();
         __syncthreads();   // accumulators read; shared operands free; next exponents ready
