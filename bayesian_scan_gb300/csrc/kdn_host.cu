@@ -61,7 +61,7 @@ cudaError_t copy_streams(CopyStreams* cs) {
 
 // The host-buffer calls' device scratch comes from a memory pool of the
 // library's own (one per device, created on first use) that keeps freed
-// memory instead of returning it to the driver at every synchronisation: a
+// memory instead of releasing it to CUDA at every synchronisation: a
 // call then reuses the previous call's buffers.  The pool holds at most the
 // largest scratch one call needed.
 cudaMemPool_t g_pools[kMaxDev] = {};

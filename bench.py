@@ -20,7 +20,7 @@ collective; weak scaling); the timing is the max over ranks.
 
 Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
 Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
-10 FLOP per state element per token (see the design doc for the count), peak =
+10 FLOP per state element per token (I update 4, mean update 3, readout 3), peak =
 SMs x 128 FP32 lanes x 2 FLOP x max SM clock.
 """
 from __future__ import annotations

@@ -243,7 +243,7 @@ KDN_API kdn_status kdn_diag_step(const void* q, const void* k, const void* v, co
  * Device memory for three chunks, the carried states, d, A, I0 and mu0 comes,
  * stream-ordered on `stream`, from a memory pool of the library's own (one
  * per device) that keeps freed memory for the next host-buffer call instead
- * of returning it to the driver: after a call the pool holds up to the
+ * of releasing it to CUDA: after a call the pool holds up to the
  * largest scratch a host-buffer call has needed (about 3 x 5 chunk buffers;
  * 0.35 GB for 128 heads x 4096 tokens at d = 128).  KDN_ERR_ALLOC if the
  * memory cannot be had.
