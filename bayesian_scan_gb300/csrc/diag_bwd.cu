@@ -119,6 +119,22 @@ struct Tile {
     static constexpr int used = holder + 16;
     static constexpr int SMEM = used < MIN_SMEM ? MIN_SMEM : used;
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    // The forward sweep stages F1 tokens at a time (several checkpoint
+    // intervals per barrier pair): raw k, beta, v in a raw buffer, converted
+    // k, k^2, beta, beta v, alpha in the row-partial area (free until the
+    // backward sweep).  F1 is the longest of 32, 16, 8 that fits both.
+    static constexpr int f1_raw(int f) { return align16(f * CWB * ES) + 2 * align16(f * DV * ES); }
+    static constexpr int f1_cvt(int f) { return 2 * align16(f * CWB * 4) + 2 * align16(f * DV * 4) + align16(f * 4); }
+    static constexpr int s_row_bytes = align16(C * 2 * NCQ * DV * 4);
+    static constexpr int F1 = (f1_raw(32) <= RAW && f1_cvt(32) <= s_row_bytes) ? 32
+                              : (f1_raw(16) <= RAW && f1_cvt(16) <= s_row_bytes) ? 16 : C;
+    static constexpr int f1_k = 0, f1_b = align16(F1 * CWB * ES), f1_v = f1_b + align16(F1 * DV * ES);
+    static constexpr int g_k = (F1 == C) ? s_k : s_row;
+    static constexpr int g_kk = (F1 == C) ? s_kk : g_k + align16(F1 * CWB * 4);
+    static constexpr int g_b = (F1 == C) ? s_b : g_kk + align16(F1 * CWB * 4);
+    static constexpr int g_bv = (F1 == C) ? s_bv : g_b + align16(F1 * DV * 4);
+    static constexpr int g_al = (F1 == C) ? s_al : g_bv + align16(F1 * DV * 4);
+    static_assert(F1 % C == 0, "a stage holds whole checkpoint intervals");
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -362,34 +378,98 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
             }
     };
 
-    // ---- forward sweep: checkpoints every C tokens -------------------------
+    // ---- forward sweep: checkpoints every C tokens, staged F1 tokens at a time
+    constexpr int F1 = Tl::F1;
     const float A_h = p.A[bh % p.H];
-    TIn dreg{};   // d of token (chunk start + tid), prefetched
-    if (nC > 0) {
-        issue_chunk<TIn, DV, CWB>(p, raw(0), bh, cb, 0, ntok(0), false, tid);
-        if (tid < ntok(0)) dreg = d_of<TIn>(p, bh, tid);
-    }
-    for (int c = 0; c < nC; ++c) {
-        const int n = ntok(c);
-        {   // checkpoint: the tile's state before chunk c
-            float4* dst = reinterpret_cast<float4*>(ckpt_cta + static_cast<long long>(c) * 32 * NT);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                dst[(2 * r) * NT + tid] = make_float4(J[r][0].x, J[r][0].y, J[r][1].x, J[r][1].y);
-                dst[(2 * r + 1) * NT + tid] = make_float4(E[r][0].x, E[r][0].y, E[r][1].x, E[r][1].y);
-            }
+    TIn dreg{};   // d of token (stage start + tid), prefetched
+    const int nS = (p.T + F1 - 1) / F1;
+    auto f1n = [&](int g) { return min(F1, p.T - g * F1); };
+    auto issue_stage = [&](int g, unsigned char* rb) {   // k column block, beta, v rows of stage g
+        constexpr int ES = Tl::ES, KP = CWB * ES / 16;
+        const int n = f1n(g);
+        const long long tok0 = bh * p.T + static_cast<long long>(g) * F1;
+        const char* kg = static_cast<const char*>(p.k) + (tok0 * p.dk + cb * CWB) * ES;
+        for (int i = tid; i < n * KP; i += NT) {
+            const int ss = i / KP, w = i % KP;
+            cp_async16(rb + Tl::f1_k + i * 16, kg + static_cast<long long>(ss) * p.dk * ES + w * 16);
         }
+        const int rp = n * (DV * ES / 16);
+        const char* bg = static_cast<const char*>(p.beta) + tok0 * DV * ES;
+        const char* vg = static_cast<const char*>(p.v) + tok0 * DV * ES;
+        for (int i = tid; i < rp; i += NT) {
+            cp_async16(rb + Tl::f1_b + i * 16, bg + i * 16);
+            cp_async16(rb + Tl::f1_v + i * 16, vg + i * 16);
+        }
+        cp_async_commit();
+    };
+    const float* gk = reinterpret_cast<const float*>(sm + Tl::g_k);
+    const float* gkk = reinterpret_cast<const float*>(sm + Tl::g_kk);
+    const float* gb = reinterpret_cast<const float*>(sm + Tl::g_b);
+    const float* gbv = reinterpret_cast<const float*>(sm + Tl::g_bv);
+    const float* gal = reinterpret_cast<const float*>(sm + Tl::g_al);
+    if (nS > 0) {
+        issue_stage(0, raw(0));
+        if (tid < f1n(0)) dreg = d_of<TIn>(p, bh, tid);
+    }
+    for (int g = 0; g < nS; ++g) {
+        const int n = f1n(g);
         cp_async_wait_all();
-        __syncthreads();   // chunk c landed; chunk c-1's compute finished
-        convert_chunk<TIn, DV, CWB>(sm, raw(c & 1), n, false, dreg, A_h, tid);
-        if (c + 1 < nC) {
-            issue_chunk<TIn, DV, CWB>(p, raw((c + 1) & 1), bh, cb, c + 1, ntok(c + 1), false, tid);
-            if (tid < ntok(c + 1)) dreg = d_of<TIn>(p, bh, static_cast<long long>(c + 1) * C + tid);
+        __syncthreads();   // stage g landed; stage g-1's compute finished
+        {   // convert: k -> k, k^2; beta, v -> beta, beta v; d -> alpha
+            const unsigned char* rb = raw(g & 1);
+            const TIn* rk = reinterpret_cast<const TIn*>(rb + Tl::f1_k);
+            const TIn* rbt = reinterpret_cast<const TIn*>(rb + Tl::f1_b);
+            const TIn* rv = reinterpret_cast<const TIn*>(rb + Tl::f1_v);
+            float* wk = reinterpret_cast<float*>(sm + Tl::g_k);
+            float* wkk = reinterpret_cast<float*>(sm + Tl::g_kk);
+            float* wb = reinterpret_cast<float*>(sm + Tl::g_b);
+            float* wbv = reinterpret_cast<float*>(sm + Tl::g_bv);
+            for (int i = tid; i < n * CWB; i += NT) {
+                const float kv = to_f<TIn>(rk[i]);
+                wk[i] = kv;
+                wkk[i] = kv * kv;
+            }
+            for (int i = tid; i < n * DV; i += NT) {
+                const float b = to_f<TIn>(rbt[i]);
+                wb[i] = b;
+                wbv[i] = b * to_f<TIn>(rv[i]);
+            }
+            if (tid < n) reinterpret_cast<float*>(sm + Tl::g_al)[tid] = expf(-A_h * to_f<TIn>(dreg));
+        }
+        if (g + 1 < nS) {
+            issue_stage(g + 1, raw((g + 1) & 1));
+            if (tid < f1n(g + 1)) dreg = d_of<TIn>(p, bh, static_cast<long long>(g + 1) * F1 + tid);
         }
         __syncthreads();
 #pragma unroll 1
-        for (int s = 0; s < n; ++s) forward_step(s);
+        for (int s = 0; s < n; ++s) {
+            if ((s & (C - 1)) == 0) {   // checkpoint: the tile's state before chunk (g F1 + s) / C
+                const int c = (g * F1 + s) / C;
+                float4* dst = reinterpret_cast<float4*>(ckpt_cta + static_cast<long long>(c) * 32 * NT);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    dst[(2 * r) * NT + tid] = make_float4(J[r][0].x, J[r][0].y, J[r][1].x, J[r][1].y);
+                    dst[(2 * r + 1) * NT + tid] = make_float4(E[r][0].x, E[r][0].y, E[r][1].x, E[r][1].y);
+                }
+            }
+            const float2 al = f2(gal[s]);
+            const float4 b4 = *reinterpret_cast<const float4*>(gb + s * DV + row0);
+            const float4 v4 = *reinterpret_cast<const float4*>(gbv + s * DV + row0);
+            const float4 k4 = *reinterpret_cast<const float4*>(gk + s * CWB + col0);
+            const float4 kk4 = *reinterpret_cast<const float4*>(gkk + s * CWB + col0);
+            const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
+            const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
+            const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
+                    E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
+                }
+        }
     }
+    cp_async_wait_all();
     // checkpoints written by other threads are read back through cp.async
     __threadfence();
     __syncthreads();
