@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
                 }
             tmem_st32(tlane + static_cast<uint32_t>(s * 32), st);
         };
-#pragma unroll 1
+#pragma unroll 2
         for (int s = 0; s < n; ++s) fwd_store(s);
         tmem_wait_st();
         const float* sdo = reinterpret_cast<const float*>(rb + Tl::r_do);
@@ -599,21 +599,32 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
             adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cv, rsum, dsum);
             alpha_next = sal[n - 1];
         }
-#pragma unroll 1
-        for (int s = n - 2; s >= 0; --s) {
+        // two tokens per iteration with the partial-sum buffers swapped (no
+        // register copies between steps)
+        auto step_back = [&](int s, float (&cvi)[12], float (&rsi)[8], float& dsi, float (&cvo)[12],
+                             float (&rso)[8], float& dso) {
             tmem_ld32_async(tlane + static_cast<uint32_t>(s * 32), cur);
             tmem_wait_ld(cur);
             TokIn in;
             load_in(s, in);
-            float cv2[12], rsum2[8], dsum2;
-            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cv2, rsum2, dsum2);
-            emit(s + 1, cv, rsum, dsum);
+            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cvo, rso, dso);
+            emit(s + 1, cvi, rsi, dsi);
             alpha_next = sal[s];
+        };
+        float cvb[12], rsumb[8], dsumb;
+        int s = n - 2;
+#pragma unroll 1
+        for (; s >= 1; s -= 2) {
+            step_back(s, cv, rsum, dsum, cvb, rsumb, dsumb);
+            step_back(s - 1, cvb, rsumb, dsumb, cv, rsum, dsum);
+        }
+        if (s == 0) {
+            step_back(0, cv, rsum, dsum, cvb, rsumb, dsumb);
 #pragma unroll
-            for (int m = 0; m < 12; ++m) cv[m] = cv2[m];
+            for (int m = 0; m < 12; ++m) cv[m] = cvb[m];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) rsum[m] = rsum2[m];
-            dsum = dsum2;
+            for (int m = 0; m < 8; ++m) rsum[m] = rsumb[m];
+            dsum = dsumb;
         }
         emit(0, cv, rsum, dsum);
         __syncthreads();   // the chunk's partials are complete
@@ -621,13 +632,26 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         {
             const long long tokbase = bh * p.T + t0;
             float* prow = p.prow + (static_cast<long long>(cb) * p.BH * p.T + tokbase) * 2 * DV;
-            for (int i = tid; i < n * 2 * DV; i += NT) {
-                const int ss = i / (2 * DV), rem = i % (2 * DV), qi = rem / DV, row = rem % DV;
-                const float* src = s_row + ss * 2 * NCQ * DV + qi * NCQ * DV + row;
-                float acc = 0.f;
+            // 4 rows per thread and item: all NCQ partials loaded, then a tree sum
+            constexpr int R4 = DV / 4;
+#pragma unroll 2
+            for (int i = tid; i < n * 2 * R4; i += NT) {
+                const int ss = i / (2 * R4), rem = i % (2 * R4), qi = rem / R4, r4 = rem % R4;
+                const float4* src =
+                    reinterpret_cast<const float4*>(s_row + ss * 2 * NCQ * DV + qi * NCQ * DV) + r4;
+                float4 part[NCQ];
 #pragma unroll
-                for (int x = 0; x < NCQ; ++x) acc += src[x * DV];
-                prow[i] = acc;
+                for (int x = 0; x < NCQ; ++x) part[x] = src[x * R4];
+#pragma unroll
+                for (int w = 1; w < NCQ; w *= 2)
+#pragma unroll
+                    for (int x = 0; x + w < NCQ; x += 2 * w) {
+                        part[x].x += part[x + w].x;
+                        part[x].y += part[x + w].y;
+                        part[x].z += part[x + w].z;
+                        part[x].w += part[x + w].w;
+                    }
+                reinterpret_cast<float4*>(prow)[i] = part[0];
             }
             // slot s holds token t0 + s + 1 (none after the last token)
             if (tid < n && t0 + tid + 1 < p.T) {
