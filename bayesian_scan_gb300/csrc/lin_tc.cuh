@@ -252,12 +252,19 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         const unsigned char* rk = rq + RAW1;
         const unsigned char* rv = rq + 2 * RAW1;
         const unsigned char* rbt = rq + 3 * RAW1;
-        // ---- Q and K tiles [token x j] (16-byte pieces; a warp stores 512
-        // contiguous bytes), then the P product ----
-        for (int pc = tid; pc < LC * (LD / 8); pc += LTHREADS) {
-            const int t8 = pc & 7, jq = (pc >> 3) & 3, rest = pc >> 5;
-            const int t = 8 * (rest & 7) + t8, jc = 4 * (rest >> 3) + jq;
-            const int off = (t >> 3) * SBO_J + jc * 128 + t8 * 16;
+        // ---- Q and K tiles [token x j] (16-byte pieces), then the P product.
+        // A warp instruction moves 8 tokens x 4 of their 16-byte pieces,
+        // chosen in a checkerboard (piece (a + 2 b + u) mod 8 of token a for
+        // lane 8 b + a), so that both the row reads (bank group = piece mod 8)
+        // and the core-matrix writes (bank group = token mod 8) hit each bank
+        // group exactly four times ----
+        static_assert(LC * (LD / 8) == 4 * LTHREADS, "four pieces per thread");
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int combo = warp + 8 * it, tg = combo >> 2, u = combo & 3;
+            const int a = lane & 7, b = lane >> 3;
+            const int t = 8 * tg + a, jc = 8 * (u >> 1) + ((a + 2 * b + (u & 1)) & 7);
+            const int off = tg * SBO_J + jc * 128 + a * 16;
             uint4 qv = make_uint4(0u, 0u, 0u, 0u), kv = qv;
             if (t < n) {
                 qv = *reinterpret_cast<const uint4*>(rq + t * LD * 2 + jc * 16);
