@@ -82,6 +82,16 @@ struct LinArgs {
     long long wait_ns;
 };
 
+// 2^x by the hardware approximation (MUFU ex2); results below the normal
+// range flush to zero.  The library exp2f takes a slow path for the large
+// negative arguments that fast decay gives, which cost more than the rest of
+// the P operand's build.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // hi + lo bf16 halves of a pair (x0, x1), packed two per 32-bit word: hi is
 // x truncated to bf16 (exact, an integer mask), lo the rest x - hi (exact in
 // fp32, below 2^-7 |x|) rounded to bf16, so hi + lo is within 2^-16 |x|.
@@ -384,7 +394,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int s_ = s0 + u;
-                    x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * exp2f((gt - gsv[u]) * LOG2E_L) : 0.f;
+                    x[u] = (s_ <= t && t < n && s_ < n) ? pvv[u] * ex2_approx((gt - gsv[u]) * LOG2E_L) : 0.f;
                 }
                 uint32_t hi[4], lo[4];
 #pragma unroll
