@@ -113,13 +113,22 @@ __device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// The same descriptor for an MN-major operand without swizzle: core matrices
+// of 8 K-rows x 16 bytes (8 consecutive M/N elements of one K index);
+// `kstride` = byte distance between core matrices adjacent along K (the
+// leading-dimension field), `mnstride` = along M/N (the stride field), as a
+// one-CTA product against a host reference showed on GB300.
+__device__ __forceinline__ uint64_t umma_desc_mnmajor(uint32_t saddr, uint32_t kstride, uint32_t mnstride) {
+    return umma_desc_kmajor(saddr, kstride, mnstride);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, fp32
-// accumulator, both operands K-major, dense: D format bits [4,6) = 1 (f32),
-// A format [7,10) = 1 (bf16), B format [10,13) = 1 (bf16), N >> 3 in
-// [17,23), M >> 4 in [24,29).
-__host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(m >> 4) << 24);
+// accumulator, dense: D format bits [4,6) = 1 (f32), A format [7,10) = 1
+// (bf16), B format [10,13) = 1 (bf16), A MN-major at bit 15, B MN-major at
+// bit 16 (else K-major), N >> 3 in [17,23), M >> 4 in [24,29).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int m, int n, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // D (TMEM) = A * B^T (+ D when accumulate != 0); issued by one thread.

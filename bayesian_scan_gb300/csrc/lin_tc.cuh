@@ -52,9 +52,8 @@ constexpr int RAW_STAGE = 4 * RAW1;               // q, k, v, beta (one stage)
 constexpr int OFF_RAW = 0;
 constexpr int OFF_KB = OFF_RAW + RAW_STAGE;       // [s x j], read as 128 rows by the P product
 constexpr int OFF_QB = OFF_KB + LC * LD * 2;      // [t x j]
-constexpr int OFF_KT = OFF_QB + LC * LD * 2;      // [j x s]
-constexpr int OFF_VH = OFF_KT + LD * LC * 2;      // [i x s] hi, lo
-constexpr int OFF_AW = OFF_VH + 2 * LD * LC * 2;  // [i x s] hi, lo
+constexpr int OFF_VH = OFF_QB + LC * LD * 2;      // Vb [s x i] hi, lo (MN-major A operand)
+constexpr int OFF_AW = OFF_VH + 2 * LD * LC * 2;  // w . Vb [s x i] hi, lo (MN-major A operand)
 constexpr int OFF_P = OFF_AW + 2 * LD * LC * 2;   // [t x s] hi, lo
 constexpr int OFF_PRAW = OFF_P + 2 * LC * LC * 2; // [t][s] fp32 copy of P^T
 constexpr int PRAW_LD = LC + 4;
@@ -202,7 +201,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     }
 
     constexpr uint32_t IDESC_T = umma_idesc_bf16_f32(128, LC);    // N = 64 tokens
-    constexpr uint32_t IDESC_J = umma_idesc_bf16_f32(128, LD);    // N = 128 key columns
+    constexpr uint32_t IDESC_OA = umma_idesc_bf16_f32(128, LC, true);          // A = Vb^T MN-major
+    constexpr uint32_t IDESC_S = umma_idesc_bf16_f32(128, LD, true, true);     // A = (w Vb)^T, B = K: MN-major
     // Warp 7 keeps the raw-input copies and the decay exponents one chunk
     // ahead (threads 0 and 32 issue the MMAs): exponents of chunk c from the
     // d of its tokens (dn0: token lane, dn1: token 32 + lane), into buffer c & 1.
@@ -249,6 +249,10 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     const uint32_t sbase = smem_addr(smem);
     auto dj = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_J); };
     auto dc = [&](int off, int ks) { return umma_desc_kmajor(sbase + off + ks * 256, 128, SBO_C); };
+    // MN-major [s x (i or j)] tiles in the Q/K tile layout: 16-byte pieces of
+    // 8 consecutive i (or j) of one token, core matrices 128 bytes apart along
+    // i and SBO_J along s; a K = 16 step is two core matrices along s
+    auto dm = [&](int off, int ks) { return umma_desc_mnmajor(sbase + off + ks * 2 * SBO_J, SBO_J, 128); };
     float* praw = reinterpret_cast<float*>(smem + OFF_PRAW);
 
     for (int c = 0; c < nch; ++c) {
@@ -293,33 +297,31 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 umma_bf16(tmem + COL_P, dj(OFF_KB, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
             umma_commit(bar_p);
         }
-        // ---- K^T [j x s]; Vb^T and (w . Vb)^T [i x s], hi and lo (lanes run
-        // over consecutive rows, so gathers and stores are conflict-free) ----
-        for (int pc = tid; pc < LD * (LC / 8); pc += LTHREADS) {
-            const int r = pc % LD, sc = pc / LD;   // row j (or i), tokens 8 sc ..
-            uint32_t kt[4], vh[4], vl[4], ah[4], al[4];
+        // ---- Vb = beta . v and w . Vb [s x i], hi and lo: the A operands of
+        // the Oa and state products, MN-major (read as Vb^T), built piece by
+        // piece from the raw rows in the Q/K tiles' checkerboard (K itself is
+        // the state product's MN-major B operand) ----
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                uint32_t kb[2];
-                float x[2], xw[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int s_ = 8 * sc + 2 * e + u;
-                    const bool in = s_ < n;
-                    const unsigned short kbits = in ? *reinterpret_cast<const unsigned short*>(rk + (s_ * LD + r) * 2) : 0;
-                    const unsigned short bb = in ? *reinterpret_cast<const unsigned short*>(rbt + (s_ * LD + r) * 2) : 0;
-                    const unsigned short vb = in ? *reinterpret_cast<const unsigned short*>(rv + (s_ * LD + r) * 2) : 0;
-                    x[u] = __uint_as_float(static_cast<uint32_t>(bb) << 16) *
-                           __uint_as_float(static_cast<uint32_t>(vb) << 16);
-                    xw[u] = s_w[s_] * x[u];
-                    kb[u] = kbits;
-                }
-                kt[e] = kb[0] | (kb[1] << 16);
-                split_pair(x[0], x[1], vh[e], vl[e]);
-                split_pair(xw[0], xw[1], ah[e], al[e]);
+        for (int it = 0; it < 4; ++it) {
+            const int combo = warp + 8 * it, tg = combo >> 2, u = combo & 3;
+            const int a = lane & 7, b = lane >> 3;
+            const int s_ = 8 * tg + a, ic = 8 * (u >> 1) + ((a + 2 * b + (u & 1)) & 7);
+            const int off = tg * SBO_J + ic * 128 + a * 16;
+            uint4 bq = make_uint4(0u, 0u, 0u, 0u), vq = bq;
+            if (s_ < n) {
+                bq = *reinterpret_cast<const uint4*>(rbt + s_ * LD * 2 + ic * 16);
+                vq = *reinterpret_cast<const uint4*>(rv + s_ * LD * 2 + ic * 16);
             }
-            const int off = (r >> 3) * SBO_C + sc * 128 + (r & 7) * 16;
-            *reinterpret_cast<uint4*>(smem + OFF_KT + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
+            const float ws = s_w[s_];
+            const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w}, vw[4] = {vq.x, vq.y, vq.z, vq.w};
+            uint32_t vh[4], vl[4], ah[4], al[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {   // elements i = 8 ic + 2 e, + 1 (low, high halves)
+                const float x0 = __uint_as_float(bw[e] << 16) * __uint_as_float(vw[e] << 16);
+                const float x1 = __uint_as_float(bw[e] & 0xffff0000u) * __uint_as_float(vw[e] & 0xffff0000u);
+                split_pair(x0, x1, vh[e], vl[e]);
+                split_pair(ws * x0, ws * x1, ah[e], al[e]);
+            }
             *reinterpret_cast<uint4*>(smem + OFF_VH + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
             *reinterpret_cast<uint4*>(smem + OFF_VH + LD * LC * 2 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
             *reinterpret_cast<uint4*>(smem + OFF_AW + off) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
@@ -371,8 +373,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
             // S [i x j] += (w Vb hi + w Vb lo)^T K
 #pragma unroll
             for (int ks = 0; ks < LC / 16; ++ks) {
-                umma_bf16(tmem + COL_S, dc(OFF_AW, ks), dc(OFF_KT, ks), IDESC_J, 1u);
-                umma_bf16(tmem + COL_S, dc(OFF_AW + LD * LC * 2, ks), dc(OFF_KT, ks), IDESC_J, 1u);
+                umma_bf16(tmem + COL_S, dm(OFF_AW, ks), dm(OFF_KB, ks), IDESC_S, 1u);
+                umma_bf16(tmem + COL_S, dm(OFF_AW + LD * LC * 2, ks), dm(OFF_KB, ks), IDESC_S, 1u);
             }
             umma_commit(bar_o);
         }
@@ -412,9 +414,9 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 // Oa^T [i x t] = Vb hi P hi + Vb hi P lo + Vb lo P hi
 #pragma unroll
                 for (int ks = 0; ks < LC / 16; ++ks) {
-                    umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P, ks), IDESC_T, ks > 0 ? 1u : 0u);
-                    umma_bf16(tmem + COL_OA, dc(OFF_VH, ks), dc(OFF_P + LC * LC * 2, ks), IDESC_T, 1u);
-                    umma_bf16(tmem + COL_OA, dc(OFF_VH + LD * LC * 2, ks), dc(OFF_P, ks), IDESC_T, 1u);
+                    umma_bf16(tmem + COL_OA, dm(OFF_VH, ks), dc(OFF_P, ks), IDESC_OA, ks > 0 ? 1u : 0u);
+                    umma_bf16(tmem + COL_OA, dm(OFF_VH, ks), dc(OFF_P + LC * LC * 2, ks), IDESC_OA, 1u);
+                    umma_bf16(tmem + COL_OA, dm(OFF_VH + LD * LC * 2, ks), dc(OFF_P, ks), IDESC_OA, 1u);
                 }
                 umma_commit(bar_o);
             }
