@@ -128,8 +128,9 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     // per chunk (double-buffered by chunk parity): g_t, e^{g_t}, e^{g_C - g_t}, then e^{g_C}
     float* s_gall = reinterpret_cast<float*>(smem + OFF_MISC);       // [2][3][LC]
     float* s_eglall = s_gall + 2 * 3 * LC;                           // [2] (+2 pad)
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(s_eglall + 4);
-    uint64_t* bar_p = raw_full + 1;
+    uint64_t* raw_qk = reinterpret_cast<uint64_t*>(s_eglall + 4);   // q, k of a chunk landed
+    uint64_t* raw_bv = raw_qk + 1;                                     // v, beta of a chunk landed
+    uint64_t* bar_p = raw_bv + 1;
     uint64_t* bar_o = bar_p + 1;
     uint32_t* holder = reinterpret_cast<uint32_t*>(bar_o + 1);
 
@@ -144,21 +145,29 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
     const float Ah = p.A[bh % p.H];
     bool ok = true;
 
-    auto issue = [&](int c) {   // one thread: raw inputs of chunk c into the stage
+    // One thread: raw inputs of chunk c into the stage, in two halves with a
+    // barrier each, so that q and k of the next chunk are fetched as soon as
+    // this chunk's Q and K tiles exist.
+    auto issue = [&](int c, bool qk) {
         const int t0 = tb + c * LC, n = min(LC, te - t0);
         const uint32_t bytes = static_cast<uint32_t>(n * LD * 2);
         const long long off = (bh * T + t0) * LD;
         unsigned char* dst = smem + OFF_RAW;
+        uint64_t* bar = qk ? raw_qk : raw_bv;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(raw_full, 4 * bytes);
-        bulk_g2s(dst, p.q + off, bytes, raw_full);
-        bulk_g2s(dst + RAW1, p.k + off, bytes, raw_full);
-        bulk_g2s(dst + 2 * RAW1, p.v + off, bytes, raw_full);
-        bulk_g2s(dst + 3 * RAW1, p.beta + off, bytes, raw_full);
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        if (qk) {
+            bulk_g2s(dst, p.q + off, bytes, bar);
+            bulk_g2s(dst + RAW1, p.k + off, bytes, bar);
+        } else {
+            bulk_g2s(dst + 2 * RAW1, p.v + off, bytes, bar);
+            bulk_g2s(dst + 3 * RAW1, p.beta + off, bytes, bar);
+        }
     };
 
     if (tid == 0) {
-        mbar_init(raw_full, 1);
+        mbar_init(raw_qk, 1);
+        mbar_init(raw_bv, 1);
         mbar_init(bar_p, 1);
         mbar_init(bar_o, 2);   // two issuing threads commit per chunk
         mbar_init_fence();
@@ -240,7 +249,10 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         if (c + 1 < nch) load_d(c + 1);
     };
     if (warp == 7 && nch > 0) {
-        if (lane == 0) issue(0);
+        if (lane == 0) {
+            issue(0, true);
+            issue(0, false);
+        }
         load_d(0);
         exponents(0);
     }
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         const float* s_g = s_gall + st * 3 * LC;
         const float* s_eg = s_g + LC;
         const float* s_w = s_g + 2 * LC;
-        if (!mbar_wait(raw_full, c & 1, p.wait_ns)) ok = false;
+        if (!mbar_wait(raw_qk, c & 1, p.wait_ns)) ok = false;
         const unsigned char* rq = smem + OFF_RAW;
         const unsigned char* rk = rq + RAW1;
         const unsigned char* rv = rq + 2 * RAW1;
@@ -297,6 +309,8 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
                 umma_bf16(tmem + COL_P, dj(OFF_KB, ks), dj(OFF_QB, ks), IDESC_T, ks > 0 ? 1u : 0u);
             umma_commit(bar_p);
         }
+        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1, true);   // q, k consumed
+        if (!mbar_wait(raw_bv, c & 1, p.wait_ns)) ok = false;
         // ---- Vb = beta . v and w . Vb [s x i], hi and lo: the A operands of
         // the Oa and state products, MN-major (read as Vb^T), built piece by
         // piece from the raw rows in the Q/K tiles' checkerboard (K itself is
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(LTHREADS, 1) lin_tc_kernel(const LinArgs p) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before_sync();
         __syncthreads();   // tiles built, raw stage consumed, S split and scaled, P^T copied
-        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1);
+        if (warp == 7 && lane == 0 && c + 1 < nch) issue(c + 1, false);   // v, beta consumed
         if (tid == 0) {
             tc_fence_after_sync();
             // Oi^T [i x t] = (S hi + S lo) Q^T, S from tensor memory
