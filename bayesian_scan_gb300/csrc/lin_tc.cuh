@@ -10,8 +10,8 @@
 //     o_t = [ sum_{s <= t} e^{g_t - g_s} (q_t . k_s) Vb_s  +  e^{g_t} S q_t ] / I_prior
 //     S'  = e^{g_C} S + sum_s e^{g_C - g_s} Vb_s k_s^T,      Vb_s = beta_s . v_s,
 // five matrix products per chunk, all with M = 128 rows on the tensor cores
-// (tcgen05.mma kind::f16, bf16 operands staged in shared memory as K-major
-// 8 x 16-byte core matrices, fp32 accumulators in tensor memory):
+// (tcgen05.mma kind::f16, bf16 operands staged in shared memory as 8 x
+// 16-byte core matrices, fp32 accumulators in tensor memory):
 //     P^T  [s x t] = K Q^T            (K padded to 128 rows; rows >= 64 unused)
 //     Oi^T [i x t] = S Q^T            (S as hi + lo bf16 halves, read from
 //                                      tensor memory as the A operand: 2 products)
@@ -19,18 +19,25 @@
 //     S   [i x j] += (w . Vb)^T K     (w_s = e^{g_C - g_s}; hi + lo: 2 products)
 // The hi + lo splits keep every operand to ~2^-16 relative (one bf16 product
 // alone loses ~2^-9, which fails the 2e-3 bar on o); q, k are bf16 inputs and
-// exact.  S lives in tensor memory for the whole sequence; once per chunk each
-// warp reads its lanes and columns, writes the hi/lo halves back into tensor
-// memory as packed bf16 pairs (the Oi product reads its A operand there, which
-// leaves shared memory room for 64-token chunks) and scales S by e^{g_C} in
-// place before the state product adds the chunk.  The P product is issued as
-// soon as the Q and K tiles exist; warps 0, 1, 4, 5 copy its result to shared
-// memory while all warps build the remaining tiles, and warps 1-4 turn it
-// into the masked, decayed hi/lo operand of the Oa product while thread 0
-// issues the Oi and state products; thread 32 issues the Oa product (a
-// single thread gets only about one MMA accepted per 70 cycles).  Warp 7
-// issues the 1-D bulk copies of the next chunk's inputs as soon as the
-// current ones are consumed and computes the decay exponents one chunk ahead.
+// exact.  Q and K are copied from the raw rows into K-major tiles ([token x
+// j], 16-byte pieces of 8 consecutive j); the same tile of K is the state
+// product's MN-major B operand, and Vb, w . Vb are built straight from the
+// raw rows of beta and v as MN-major A operands in that layout, so no
+// operand is transposed on the CUDA cores.  S lives in tensor memory for the
+// whole sequence; once per chunk each warp reads its lanes and columns,
+// writes the hi/lo halves back into tensor memory as packed bf16 pairs (the
+// Oi product reads its A operand there, which leaves shared memory room for
+// 64-token chunks) and scales S by e^{g_C} in place before the state product
+// adds the chunk.  The P product is issued as soon as the Q and K tiles
+// exist; warps 0, 1, 4, 5 copy its result to shared memory after the other
+// tiles are built, and warps 1-4 turn it into the masked, decayed hi/lo
+// operand of the Oa product while thread 0 issues the Oi and state products;
+// thread 32 issues the Oa product.  One thread issues a tcgen05.mma about
+// every 47 cycles, so the N = 64 products run at about 52 cycles each and
+// the 36 products after the operand barrier take about 2000 cycles.  Warp 7 issues the 1-D
+// bulk copies of the next chunk's q and k as soon as the Q and K tiles exist
+// and of its v and beta once the operands are built, and computes the decay
+// exponents one chunk ahead.
 // All waits are bounded.
 
 namespace kdn {
