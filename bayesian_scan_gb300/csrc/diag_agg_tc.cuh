@@ -24,15 +24,19 @@
 // 2^-R / W = 2^-L, W in [1, 2), that the CUDA-core aggregate pass leaves for
 // the carry kernel.
 //
-// Per CTA: one (head, part); 256 threads.  Chunks of the part are visited
-// from the last to the first (so the suffix sums accumulate).  The weights
-// w_t of 2048 tokens at a time are prepared by all threads (8 tokens each,
-// fp64 suffix sums across the CTA); per chunk all threads build the 7 operand
-// tiles (128 x 32 bf16 each, core-matrix layout) from the raw chunk (k, beta,
-// v, brought in by 1-D bulk copies two chunks ahead), then one thread issues
-// the 10 MMAs of the chunk and commits them to an mbarrier; operand tiles are
-// double-buffered on that barrier, so a chunk's MMAs run while the next is
-// built.  One CTA barrier per chunk; all waits are bounded by GPU time.
+// Per CTA: one (head, part); 8 KC build threads and one issuing warp.
+// Chunks of the part are visited from the last to the first (so the suffix
+// sums accumulate).  The weights w_t of a super-chunk of tokens are prepared
+// by the build threads (8 tokens each, fp64 suffix sums across them); per
+// chunk the build threads write the 7 operand tiles (128 x KC bf16 each,
+// core-matrix layout) from the raw chunk (k, beta, v, brought in by 1-D bulk
+// copies two chunks ahead) and arrive, one lane per warp, on the chunk's
+// operand barrier; the issuing warp waits there, issues the next copies into
+// the consumed raw stage and the chunk's 5 KC / 16 MMAs, and commits them to
+// an mbarrier.  Operand tiles are double-buffered on that barrier, so the
+// build threads never wait for the products to be issued (a build thread
+// that also issued held its warp, and at the chunk barrier all others, for
+// about 770 cycles a chunk).  All waits are bounded by GPU time.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,20 +54,22 @@ constexpr int AG_NTILE = 7;                        // A_J hi/lo, A_E hi/lo, B_k,
 constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta in [128,256)
 constexpr uint32_t AG_LBO = 128;                   // core matrices: next 8 tokens (K)
 
-// Chunk shapes: KC tokens per chunk, 8 KC threads (one per row pair and
-// group of 8 tokens).  KC = 32: 256 threads, one CTA per SM; KC = 16: 128
-// threads, two CTAs per SM (each holding 256 of the SM's 512 TMEM columns),
-// for grids with at least two CTAs per SM.
+// Chunk shapes: KC tokens per chunk, 8 KC build threads (one per row pair
+// and group of 8 tokens) and one more warp that issues the products and the
+// copies.  KC = 32: 288 threads, one CTA per SM; KC = 16: 160 threads, two
+// CTAs per SM (each holding 256 of the SM's 512 TMEM columns), for grids
+// with at least two CTAs per SM.
 template <int KC>
 struct AggShape {
-    static constexpr int THREADS = 8 * KC;
+    static constexpr int BUILD = 8 * KC;
+    static constexpr int THREADS = BUILD + 32;
     static constexpr int CTAS_PER_SM = KC == 16 ? 2 : 1;
     static constexpr int TILE = AG_D * KC * 2;          // one 128 x KC bf16 operand tile, bytes
     static constexpr int OPS = AG_NTILE * TILE;         // one operand buffer
     static constexpr int RAW = KC * AG_D * 2;           // one raw array (k, beta or v) of a chunk
     static constexpr uint32_t SBO = (KC / 8) * 128;     // core matrices: next 8 rows (M or N)
-    static constexpr int SUP = 8 * THREADS;             // tokens per super-chunk of decay weights
-    static constexpr int SMEM = 2 * OPS + 2 * 3 * RAW + SUP * 4 + 8 * 8 + 4 * 8 + 16;
+    static constexpr int SUP = 8 * BUILD;               // tokens per super-chunk of decay weights
+    static constexpr int SMEM = 2 * OPS + 2 * 3 * RAW + SUP * 4 + 8 * 8 + 6 * 8 + 16;
 };
 
 // 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
@@ -85,6 +91,12 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Named CTA barrier `ID` (0 is __syncthreads) over `n` threads, whole warps.
+template <int ID>
+__device__ __forceinline__ void named_sync(int n) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
+}
+
 struct AggArgs {
     const __nv_bfloat16* k;
     const __nv_bfloat16* beta;
@@ -104,7 +116,7 @@ template <int KC>
 __global__ void __launch_bounds__(AggShape<KC>::THREADS, AggShape<KC>::CTAS_PER_SM)
 diag_agg_tc_kernel(const AggArgs p) {
     using Sh = AggShape<KC>;
-    constexpr int AG_KC = KC, AG_THREADS = Sh::THREADS, AG_TILE = Sh::TILE, AG_OPS = Sh::OPS,
+    constexpr int AG_KC = KC, AG_BUILD = Sh::BUILD, AG_TILE = Sh::TILE, AG_OPS = Sh::OPS,
                   AG_RAW = Sh::RAW, AG_SUP = Sh::SUP;
     constexpr uint32_t AG_SBO = Sh::SBO;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -114,7 +126,8 @@ diag_agg_tc_kernel(const AggArgs p) {
     double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [warps] warp totals
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);
     uint64_t* mma_done = raw_full + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 2);
+    uint64_t* ops_full = mma_done + 2;                          // a chunk's operands built (per build warp)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ops_full + 2);
     float* s_wend = reinterpret_cast<float*>(tmem_holder + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -146,6 +159,7 @@ diag_agg_tc_kernel(const AggArgs p) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&mma_done[i], 1);
+            mbar_init(&ops_full[i], AG_BUILD / 32);
         }
         mbar_init_fence();
         for (int it = 0; it < 2 && it < nch; ++it) issue(it);
@@ -159,21 +173,48 @@ diag_agg_tc_kernel(const AggArgs p) {
     const float Ah = p.A[bh % p.H];
     double Z = 0.0;          // sum of the decay exponents of the tokens after the current super-chunk
     int sup0 = tb;           // first token of the current super-chunk
-    const int pr = tid & 63;                // this thread's operand rows 2 pr, 2 pr + 1
+    const bool builder = tid < AG_BUILD;    // else the issuing warp
+    const int pr = tid & 63;                // a builder's operand rows 2 pr, 2 pr + 1
     const int kg = tid >> 6;                // and its group of 8 tokens of a chunk (AG_KC / 8 groups)
-    static_assert(AG_THREADS == 64 * (AG_KC / 8), "one thread per (row pair, token group)");
-    static_assert(AG_SUP == 8 * AG_THREADS, "a thread prepares 8 weights of a super-chunk");
+    static_assert(AG_BUILD == 64 * (AG_KC / 8), "one build thread per (row pair, token group)");
+    static_assert(AG_SUP == 8 * AG_BUILD, "a build thread prepares 8 weights of a super-chunk");
     constexpr uint32_t IDESC = umma_idesc_bf16_f32(AG_D, AG_D);
 
     for (int it = 0; it < nch; ++it) {
         const int st = it & 1, ob = it & 1;
         const int c = nch - 1 - it;
         const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
+        if (!builder) {
+            // ---- the issuing warp: once every build warp has arrived on the
+            // chunk's operand barrier, the next copies into the consumed raw
+            // stage and the chunk's products ----
+            if (!mbar_wait(&ops_full[ob], (it >> 1) & 1, p.wait_ns)) ok = false;
+            if (lane == 0) {
+                if (it + 2 < nch) issue(it + 2);
+                tc_fence_after_sync();
+                const uint32_t base = smem_addr(ops + ob * AG_OPS);
+#pragma unroll
+                for (int s = 0; s < AG_KC / 16; ++s) {
+                    auto desc = [&](int tile) {
+                        return umma_desc_kmajor(base + tile * AG_TILE + s * 2 * 128, AG_LBO, AG_SBO);
+                    };
+                    const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
+                    umma_bf16(tmem, desc(0), desc(5), IDESC, first);           // J += A_J hi  B_k2 hi
+                    umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);              //    + A_J hi  B_k2 lo
+                    umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);              //    + A_J lo  B_k2 hi
+                    umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, first);    // eta += A_E hi B_k
+                    umma_bf16(tmem + AG_D, desc(3), desc(4), IDESC, 1u);       //      + A_E lo B_k
+                }
+                umma_commit(&mma_done[ob]);
+            }
+            __syncwarp();
+            continue;
+        }
         if (it == 0 || ((c + 1) % (AG_SUP / AG_KC)) == 0) {
             // ---- decay weights of this chunk's super-chunk: chunks
             // [SC, SC + AG_SUP / AG_KC) of the part, SC a multiple of it, so
-            // super-chunks hold whole chunks.  Every thread passed the barrier
-            // after the last build that read wsup.
+            // super-chunks hold whole chunks.  The builders' barrier 1 below
+            // orders every build that read wsup before its rewrite.
             sup0 = tb + (c / (AG_SUP / AG_KC)) * AG_SUP;
             const int s1 = min(te, sup0 + AG_SUP);
             const int u0 = sup0 + 8 * tid;
@@ -192,11 +233,11 @@ diag_agg_tc_kernel(const AggArgs p) {
                 if (lane + off < 32) suf += y;
             }
             if (lane == 0) wtot[warp] = suf;
-            __syncthreads();
+            named_sync<1>(AG_BUILD);
             double later = suf - loc;
             double all = 0.0;
 #pragma unroll
-            for (int w = 0; w < AG_THREADS / 32; ++w) {
+            for (int w = 0; w < AG_BUILD / 32; ++w) {
                 const double tw = wtot[w];
                 all += tw;
                 if (w > warp) later += tw;
@@ -208,7 +249,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                 later += x[u];
             }
             Z += all;
-            __syncthreads();   // weights ready; wtot may be reused
+            named_sync<1>(AG_BUILD);   // weights ready; wtot may be reused
         }
         if (!mbar_wait(&raw_full[st], (it >> 1) & 1, p.wait_ns)) ok = false;
         // the operand buffer was last read by the MMAs of iteration it - 2
@@ -264,26 +305,8 @@ diag_agg_tc_kernel(const AggArgs p) {
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();   // operands written, raw stage consumed
-
-        if (tid == 0) {
-            if (it + 2 < nch) issue(it + 2);
-            tc_fence_after_sync();
-            const uint32_t base = smem_addr(ops + ob * AG_OPS);
-#pragma unroll
-            for (int s = 0; s < AG_KC / 16; ++s) {
-                auto desc = [&](int tile) {
-                    return umma_desc_kmajor(base + tile * AG_TILE + s * 2 * 128, AG_LBO, AG_SBO);
-                };
-                const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
-                umma_bf16(tmem, desc(0), desc(5), IDESC, first);           // J += A_J hi  B_k2 hi
-                umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);              //    + A_J hi  B_k2 lo
-                umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);              //    + A_J lo  B_k2 hi
-                umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, first);    // eta += A_E hi B_k
-                umma_bf16(tmem + AG_D, desc(3), desc(4), IDESC, 1u);       //      + A_E lo B_k
-            }
-            umma_commit(&mma_done[ob]);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ops_full[ob]);   // operands written, raw stage consumed
     }
 
     // ---- end state and scale of the part -------------------------------------
@@ -309,11 +332,11 @@ diag_agg_tc_kernel(const AggArgs p) {
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    {
+    if (builder) {
         const float W = *s_wend;
-        // warp w reads TMEM lanes 32 (w % 4) .. + 31; the warps of a lane
-        // quarter share its 256 columns (J, then eta)
-        constexpr int QW = AG_THREADS / 128;                 // warps per lane quarter
+        // build warp w reads TMEM lanes 32 (w % 4) .. + 31; the warps of a
+        // lane quarter share its 256 columns (J, then eta)
+        constexpr int QW = AG_BUILD / 128;                   // warps per lane quarter
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const int c_begin = (warp >> 2) * (2 * AG_D / QW), c_end = c_begin + 2 * AG_D / QW;

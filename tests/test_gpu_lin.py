@@ -98,7 +98,7 @@ def test_lin_is_the_metaplastic_limit_on_the_gpu():
 @pytest.mark.parametrize("T", [1, 31, 32, 33, 64, 100, 517])
 def test_lin_tensor_core_path(T):
     # d_k = d_v = 128 with bf16 inputs runs the chunked tensor-core kernel
-    # (32-token chunks): chunk boundaries, a given initial mean, all heads
+    # (64-token chunks): chunk boundaries, a given initial mean, all heads
     g = torch.Generator().manual_seed(T)
     inp = make(2, 3, T, 128, 128, seed=40 + T)
     check(inp, mu0=torch.randn(2, 3, 128, 128, generator=g))
