@@ -151,6 +151,18 @@ __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// 4 consecutive inputs (16-byte aligned for fp32, 8-byte for bf16) as fp32
+template <typename TIn>
+__device__ __forceinline__ float4 load4(const TIn* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -724,16 +736,28 @@ __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
     const long long tok = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (tok >= BHT) return;
-    for (int i = lane; i < dv; i += 32) {
-        float sb = 0.f, se = 0.f;
-        for (int cb = 0; cb < ncb; ++cb) {
-            const float* pr = prow + (static_cast<long long>(cb) * BHT + tok) * 2 * dv;
-            sb += pr[i];
-            se += pr[dv + i];
+    // 4 rows per lane: every partial is one 16-byte load, all issued before
+    // the sums (at most 4 column blocks)
+    for (int i4 = lane; i4 < dv / 4; i4 += 32) {
+        float4 pb[4], pe[4];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            if (cb < ncb) {
+                const float4* pr = reinterpret_cast<const float4*>(prow + (static_cast<long long>(cb) * BHT + tok) * 2 * dv);
+                pb[cb] = pr[i4];
+                pe[cb] = pr[dv / 4 + i4];
+            } else {
+                pb[cb] = pe[cb] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        const float b = to_f<TIn>(beta[tok * dv + i]), vv = to_f<TIn>(v[tok * dv + i]);
-        dbeta[tok * dv + i] = sb + vv * se;
-        dv_out[tok * dv + i] = b * se;
+        const float4 b4 = load4<TIn>(beta + tok * dv + 4 * i4), v4 = load4<TIn>(v + tok * dv + 4 * i4);
+        const float4 sb = make_float4((pb[0].x + pb[1].x) + (pb[2].x + pb[3].x), (pb[0].y + pb[1].y) + (pb[2].y + pb[3].y),
+                                      (pb[0].z + pb[1].z) + (pb[2].z + pb[3].z), (pb[0].w + pb[1].w) + (pb[2].w + pb[3].w));
+        const float4 se = make_float4((pe[0].x + pe[1].x) + (pe[2].x + pe[3].x), (pe[0].y + pe[1].y) + (pe[2].y + pe[3].y),
+                                      (pe[0].z + pe[1].z) + (pe[2].z + pe[3].z), (pe[0].w + pe[1].w) + (pe[2].w + pe[3].w));
+        reinterpret_cast<float4*>(dbeta + tok * dv)[i4] =
+            make_float4(sb.x + v4.x * se.x, sb.y + v4.y * se.y, sb.z + v4.z * se.z, sb.w + v4.w * se.w);
+        reinterpret_cast<float4*>(dv_out + tok * dv)[i4] = make_float4(b4.x * se.x, b4.y * se.y, b4.z * se.z, b4.w * se.w);
     }
     if (lane == 0) {
         float g_alpha = 0.f;
