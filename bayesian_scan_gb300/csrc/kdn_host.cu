@@ -148,7 +148,130 @@ struct Status {
 
 }  // namespace
 
+// Batches: with four or more, the call is cut into about eight groups of
+// whole batches (every head of a group, all its tokens, in one launch that
+// fills the GPU through the token split).  A group's inputs are contiguous
+// in host memory, so they travel as 1-D copies on one stream in group
+// order: group 0 has the link to itself and the copies run back to back,
+// where token chunks need pitched copies spread over several streams and
+// let the first chunk share the link with the next two.  No state is
+// carried between groups.  The outputs are staged on the device and copied
+// out per group: written by the scan through the host mapping while the
+// next groups' inputs come in, they held each group's scan to ~0.5 ms
+// against ~0.36 ms (GB300, 750M-shaped layer: 3.7 ms per call against 4.2).
+kdn_status diag_host_batches(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
+    const int B = h.B, H = h.H, T = h.T, dk = h.dk, dv = h.dv;
+    const size_t es = h.dtype == KDN_BF16 ? 2 : 4;
+    const size_t S = static_cast<size_t>(dv) * dk;
+    const int gb = (B + 7) / 8;                 // batches per group
+    const int ng = (B + gb - 1) / gb;
+    const size_t gbh = static_cast<size_t>(gb) * H;   // heads per (full) group
+
+    CopyStreams cs;
+    cudaError_t e = copy_streams(&cs);
+    if (e != cudaSuccess) return from_cuda(e);
+    ChunkEvents ev;
+    e = ev.create();
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // device layout: kBufs group buffer sets, then A
+    const size_t qk_b = align256(gbh * T * dk * es);
+    const size_t vb_b = align256(gbh * T * dv * es);
+    const size_t d_b = align256(gbh * T * es);
+    const size_t o_b = align256(gbh * T * dv * 4);
+    const size_t init_b = align256(gbh * S * 4);
+    const size_t fs_b = align256(2 * gbh * S * 4);
+    const size_t set_b = 2 * qk_b + 2 * vb_b + d_b + o_b + (h.I0 ? init_b : 0) + (h.mu0 ? init_b : 0) + fs_b;
+    const size_t a_b = align256(static_cast<size_t>(H) * 4);
+    cudaMemPool_t pool = nullptr;
+    e = host_pool(&pool);
+    if (e != cudaSuccess) return from_cuda(e);
+    char* base = nullptr;
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), kBufs * set_b + a_b, pool, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    float* A_d = reinterpret_cast<float*>(base + kBufs * set_b);
+
+    Status s;
+    s.cuda(cudaMemcpyAsync(A_d, h.A, static_cast<size_t>(H) * 4, cudaMemcpyHostToDevice, st));
+    s.cuda(cudaEventRecord(ev.start, st));
+    for (cudaStream_t x : {cs.in[0], cs.out}) s.cuda(cudaStreamWaitEvent(x, ev.start, 0));
+
+    const size_t BHs = static_cast<size_t>(B) * H;
+    for (int g = 0; g < ng && s.ok(); ++g) {
+        const int b = g % kBufs;
+        const int nb = (B - g * gb < gb) ? B - g * gb : gb;
+        const size_t bh0 = static_cast<size_t>(g) * gbh, nbh = static_cast<size_t>(nb) * H;
+        char* set = base + b * set_b;
+        char* dq = set;
+        char* dkp = dq + qk_b;
+        char* dvp = dkp + qk_b;
+        char* dbp = dvp + vb_b;
+        char* dd = dbp + vb_b;
+        float* dout = reinterpret_cast<float*>(dd + d_b);
+        char* tail = dd + d_b + o_b;
+        float* I0_d = h.I0 ? reinterpret_cast<float*>(tail) : nullptr;
+        float* mu0_d = h.mu0 ? reinterpret_cast<float*>(tail + (h.I0 ? init_b : 0)) : nullptr;
+        float* fs_d = reinterpret_cast<float*>(tail + (h.I0 ? init_b : 0) + (h.mu0 ? init_b : 0));
+        // buffer b was last read by the scan of group g - kBufs and its final
+        // state by that group's copy out
+        if (g >= kBufs) {
+            s.cuda(cudaStreamWaitEvent(cs.in[0], ev.comp[b], 0));
+            s.cuda(cudaStreamWaitEvent(cs.in[0], ev.out[b], 0));
+        }
+        auto in1d = [&](void* dst, const void* src, size_t off, size_t bytes) {
+            s.cuda(cudaMemcpyAsync(dst, static_cast<const char*>(src) + off, bytes, cudaMemcpyHostToDevice, cs.in[0]));
+        };
+        in1d(dq, h.q, bh0 * T * dk * es, nbh * T * dk * es);
+        in1d(dkp, h.k, bh0 * T * dk * es, nbh * T * dk * es);
+        in1d(dd, h.d, bh0 * T * es, nbh * T * es);
+        in1d(dvp, h.v, bh0 * T * dv * es, nbh * T * dv * es);
+        in1d(dbp, h.beta, bh0 * T * dv * es, nbh * T * dv * es);
+        if (I0_d) in1d(I0_d, h.I0, bh0 * S * 4, nbh * S * 4);
+        if (mu0_d) in1d(mu0_d, h.mu0, bh0 * S * 4, nbh * S * 4);
+        s.cuda(cudaEventRecord(ev.in[b][0], cs.in[0]));
+        s.cuda(cudaStreamWaitEvent(st, ev.in[b][0], 0));
+        if (g >= kBufs) s.cuda(cudaStreamWaitEvent(st, ev.out[b], 0));
+        DiagArgs a = h;
+        a.B = nb;
+        a.q = dq;
+        a.k = dkp;
+        a.v = dvp;
+        a.beta = dbp;
+        a.d = dd;
+        a.d_ld = 0;
+        a.A = A_d;
+        a.I0 = I0_d;
+        a.mu0 = mu0_d;
+        a.out = dout;
+        a.out_ld = 0;
+        a.final_state = h.final_state ? fs_d : nullptr;
+        if (s.ok()) s.kdn(a.dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns));
+        s.cuda(cudaEventRecord(ev.comp[b], st));
+        // outputs of group g: out, then mu_T and I_T into their halves of
+        // final_state
+        s.cuda(cudaStreamWaitEvent(cs.out, ev.comp[b], 0));
+        s.cuda(cudaMemcpyAsync(h.out + bh0 * T * dv, dout, nbh * T * dv * 4, cudaMemcpyDeviceToHost, cs.out));
+        if (h.final_state) {
+            s.cuda(cudaMemcpyAsync(h.final_state + bh0 * S, fs_d, nbh * S * 4, cudaMemcpyDeviceToHost, cs.out));
+            s.cuda(cudaMemcpyAsync(h.final_state + BHs * S + bh0 * S, fs_d + nbh * S, nbh * S * 4,
+                                   cudaMemcpyDeviceToHost, cs.out));
+        }
+        s.cuda(cudaEventRecord(ev.out[b], cs.out));
+    }
+    // every copy is ordered before the release and the final synchronisation
+    for (int b = 0; b < kBufs; ++b) {
+        if (ng > b) {
+            cudaStreamWaitEvent(st, ev.in[b][0], 0);
+            cudaStreamWaitEvent(st, ev.out[b], 0);
+        }
+    }
+    s.cuda(cudaFreeAsync(base, st));
+    s.cuda(cudaStreamSynchronize(st));
+    return s.result();
+}
+
 kdn_status diag_host(const DiagArgs& h, cudaStream_t st, long long wait_ns) {
+    if (h.B >= 4 && h.T > 0 && !h.lin && h.d_ld == 0 && h.out_ld == 0) return diag_host_batches(h, st, wait_ns);
     const int B = h.B, H = h.H, T = h.T, dk = h.dk, dv = h.dv;
     const size_t es = h.dtype == KDN_BF16 ? 2 : 4;
     const long long BH = static_cast<long long>(B) * H;

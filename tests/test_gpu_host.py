@@ -94,6 +94,42 @@ def test_host_diag_output_buffers(where):
     assert parity.rel_err(o, ro) <= parity.TOL_DIAG
 
 
+def test_host_diag_batch_groups_match_oracle():
+    # four or more batches run as groups of whole batches (here 5 groups of
+    # one batch: the three group buffers are reused), with an initial state
+    inp = draw(5, 2, 300, 32, 32, seed=21)
+    g = torch.Generator().manual_seed(22)
+    I0 = 0.5 + torch.rand(5, 2, 32, 32, generator=g)
+    mu0 = torch.randn(5, 2, 32, 32, generator=g)
+    o, fs = host_diag(inp, I0, mu0)
+    ro, rmu, rI = parity.oracle_diag(inp, I0, mu0)
+    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
+    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
+    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+
+
+def test_host_diag_batch_groups_uneven_and_pageable():
+    # 9 batches in groups of 2 (the last holds one); pageable buffers, so the
+    # outputs are staged and copied out
+    inp = draw(9, 2, 129, 16, 16, torch.float32, seed=23)
+    o, fs = host_diag(inp, pin=False)
+    ro, rmu, rI = parity.oracle_diag(inp)
+    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
+    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
+    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+
+
+def test_host_diag_batch_groups_agree_with_device_call():
+    # the 750M-shaped pattern (8 batches of 16 heads, d = 128) at 1000 tokens:
+    # each group's call plans its own token split, so agreement is to rounding
+    inp = draw(8, 16, 1000, 128, 128, seed=24)
+    o_h, fs_h = host_diag(inp)
+    o_d, fs_d = parity.gpu_diag(inp)
+    assert parity.rel_err(o_h, o_d) < 1e-4
+    assert parity.rel_err(fs_h[0], fs_d[0]) < 1e-4
+    assert parity.rel_err(fs_h[1], fs_d[1]) < 1e-4
+
+
 def test_host_diag_zero_length_returns_initial_state():
     inp = draw(1, 2, 0, 16, 16)
     g = torch.Generator().manual_seed(2)
