@@ -4,11 +4,13 @@
 // The work is cut into chunks that are pipelined over six streams: the
 // caller's stream runs the kernels, four internal streams copy later chunks'
 // inputs in while chunk c is scanned, another copies chunk c-1's outputs
-// out (or the scan writes them straight into page-locked host memory).  The diagonal scan is cut along the tokens (every head of a chunk
-// runs in one launch, so the GPU stays full) and carries the state from one
-// chunk to the next on the device through the scan's own final-state /
-// initial-state interface; the Moebius scan is cut along the sequences,
-// which are independent.  Host buffers should be page-locked for the copies
+// out (or the scan writes them straight into page-locked host memory).  The
+// diagonal scan is cut into groups of whole batches when it has four or
+// more (independent, contiguous in host memory; see diag_host_batches),
+// else along the tokens (every head of a chunk runs in one launch, so the
+// GPU stays full), carrying the state from one chunk to the next on the
+// device through the scan's own final-state / initial-state interface; the
+// Moebius scan is cut along the sequences, which are independent.  Host buffers should be page-locked for the copies
 // to run asynchronously; pageable memory works, with the copies serialised.
 #include <cuda_runtime.h>
 
