@@ -232,21 +232,25 @@ KDN_API kdn_status kdn_diag_step(const void* q, const void* k, const void* v, co
  * results; pointers need only their element alignment.  The call returns when
  * the results are in host memory.
  *
- * The tokens are cut into about eight chunks (at least 512 tokens each) that
- * are pipelined over three device buffers: later chunks' inputs are copied
- * to the device on two internal streams while chunk c is scanned on
- * `stream`; outputs go straight into page-locked 16-byte aligned host memory
- * from the scan, or are copied back on a third internal stream; the state
- * passes from chunk to chunk on the device.  Page-locked host buffers (cudaHostAlloc,
- * cudaHostRegister, pinned framework tensors) let the copies overlap the
- * scan; pageable buffers give the same results with serialised copies.
- * Device memory for three chunks, the carried states, d, A, I0 and mu0 comes,
+ * With B >= 4 the call is cut into about eight groups of whole batches,
+ * pipelined over three device buffers: a group's inputs (contiguous in host
+ * memory) are copied in on an internal stream, in group order, while
+ * earlier groups are scanned on `stream`, and each group's out and final
+ * state are copied back on another internal stream.  With B < 4 the tokens
+ * are cut into about eight chunks (at least 512 tokens each) instead: later
+ * chunks' inputs come in on internal streams while chunk c is scanned,
+ * outputs go straight into page-locked 16-byte aligned host memory from the
+ * scan (or are copied back), and the state passes from chunk to chunk on
+ * the device.  Page-locked host buffers (cudaHostAlloc, cudaHostRegister,
+ * pinned framework tensors) let the copies overlap the scan; pageable
+ * buffers give the same results with serialised copies.  Device memory for
+ * three groups or chunks (and, for chunks, the carried states and d) comes,
  * stream-ordered on `stream`, from a memory pool of the library's own (one
  * per device) that keeps freed memory for the next host-buffer call instead
- * of releasing it to CUDA: after a call the pool holds up to the
- * largest scratch a host-buffer call has needed (about 3 x 5 chunk buffers;
- * 0.35 GB for 128 heads x 4096 tokens at d = 128).  KDN_ERR_ALLOC if the
- * memory cannot be had.
+ * of releasing it to CUDA: after a call the pool holds up to the largest
+ * scratch a host-buffer call has needed (about three groups' inputs,
+ * outputs and states; 0.5 GB for 8 x 16 heads x 4096 tokens at d = 128).
+ * KDN_ERR_ALLOC if the memory cannot be had.
  */
 KDN_API kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v,
                                           const void* beta, const void* d, const float* A,
