@@ -249,7 +249,7 @@ KDN_API kdn_status kdn_diag_step(const void* q, const void* k, const void* v, co
  * per device) that keeps freed memory for the next host-buffer call instead
  * of releasing it to CUDA: after a call the pool holds up to the largest
  * scratch a host-buffer call has needed (about three groups' inputs,
- * outputs and states; 0.5 GB for 8 x 16 heads x 4096 tokens at d = 128).
+ * outputs and states; 0.31 GB for 8 x 16 heads x 4096 tokens at d = 128).
  * KDN_ERR_ALLOC if the memory cannot be had.
  */
 KDN_API kdn_status kdn_diag_scan_fwd_host(const void* q, const void* k, const void* v,
