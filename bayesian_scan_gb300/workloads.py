@@ -94,6 +94,12 @@ TRAIN = {
     # profiling captures
     "heads32_t1024_bwd": Workload("heads32_t1024_bwd", 2, 16, 1024, 128, 128, torch.bfloat16,
                                   ("uniform", 0.5, 4.0), 0, 0, False, 1006),
+    # the backward pass of the 1.3B-shaped layer and of the long context
+    # (same inputs and seeds as their forward workloads)
+    "layer1p3b_bwd": Workload("layer1p3b_bwd", 16, 32, 4096, 64, 64, torch.bfloat16,
+                              ("uniform", 0.5, 4.0), 0, 0, False, 1003),
+    "longctx_bwd": Workload("longctx_bwd", 1, 16, 65536, 128, 128, torch.bfloat16,
+                            ("uniform", 0.1, 1.0), 0, 0, False, 1004),
 }
 WORKLOADS.update(TRAIN)
 # the non-metaplastic limit (importance held at I_prior) on the layer shapes
