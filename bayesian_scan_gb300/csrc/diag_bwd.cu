@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
 // Per (head, token): adds the column blocks' partials and forms dbeta, dv,
 // dd = -A alpha dL/dalpha and the token's dA term -d alpha dL/dalpha.  One
 // warp per token.
-template <typename TIn>
+template <typename TIn, int NCBM>
 __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
     const TIn* __restrict__ v, const TIn* __restrict__ beta, const TIn* __restrict__ d,
     const float* __restrict__ A, const float* __restrict__ prow, const float* __restrict__ pD,
@@ -737,11 +737,11 @@ __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
     const int lane = threadIdx.x & 31;
     if (tok >= BHT) return;
     // 4 rows per lane: every partial is one 16-byte load, all issued before
-    // the sums (at most 4 column blocks)
+    // the sums (at most NCBM column blocks: 4, or 8 for 16-column blocks)
     for (int i4 = lane; i4 < dv / 4; i4 += 32) {
-        float4 pb[4], pe[4];
+        float4 pb[NCBM], pe[NCBM];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < NCBM; ++cb) {
             if (cb < ncb) {
                 const float4* pr = reinterpret_cast<const float4*>(prow + (static_cast<long long>(cb) * BHT + tok) * 2 * dv);
                 pb[cb] = pr[i4];
@@ -750,11 +750,15 @@ __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
                 pb[cb] = pe[cb] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+#pragma unroll
+        for (int w = 1; w < NCBM; w *= 2)
+#pragma unroll
+            for (int x = 0; x + w < NCBM; x += 2 * w) {
+                pb[x].x += pb[x + w].x; pb[x].y += pb[x + w].y; pb[x].z += pb[x + w].z; pb[x].w += pb[x + w].w;
+                pe[x].x += pe[x + w].x; pe[x].y += pe[x + w].y; pe[x].z += pe[x + w].z; pe[x].w += pe[x + w].w;
+            }
         const float4 b4 = load4<TIn>(beta + tok * dv + 4 * i4), v4 = load4<TIn>(v + tok * dv + 4 * i4);
-        const float4 sb = make_float4((pb[0].x + pb[1].x) + (pb[2].x + pb[3].x), (pb[0].y + pb[1].y) + (pb[2].y + pb[3].y),
-                                      (pb[0].z + pb[1].z) + (pb[2].z + pb[3].z), (pb[0].w + pb[1].w) + (pb[2].w + pb[3].w));
-        const float4 se = make_float4((pe[0].x + pe[1].x) + (pe[2].x + pe[3].x), (pe[0].y + pe[1].y) + (pe[2].y + pe[3].y),
-                                      (pe[0].z + pe[1].z) + (pe[2].z + pe[3].z), (pe[0].w + pe[1].w) + (pe[2].w + pe[3].w));
+        const float4 sb = pb[0], se = pe[0];
         reinterpret_cast<float4*>(dbeta + tok * dv)[i4] =
             make_float4(sb.x + v4.x * se.x, sb.y + v4.y * se.y, sb.z + v4.z * se.z, sb.w + v4.w * se.w);
         reinterpret_cast<float4*>(dv_out + tok * dv)[i4] = make_float4(b4.x * se.x, b4.y * se.y, b4.z * se.z, b4.w * se.w);
@@ -823,9 +827,17 @@ struct Scratch {
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Key columns per CTA: all of d_k below 32; else 32, or 16 when 32-column
+// blocks would leave more than half of the SMs idle (few heads: 16-column
+// blocks double the CTAs; the row partials to add up double too).
+inline int bwd_cwb(long long BH, int dk) {
+    if (dk < 32) return dk;
+    return BH * (dk / 32) * 2 <= sm_count() ? 16 : 32;
+}
+
 inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
     const long long BH = static_cast<long long>(B) * H;
-    const int cwb = dk < 32 ? dk : 32;
+    const int cwb = bwd_cwb(BH, dk);
     const int ncb = dk / cwb;
     const int nta = (dv / 4) * (cwb / 4);
     const int nt = nta < 32 ? 32 : nta;
@@ -842,7 +854,7 @@ inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
 template <typename TIn>
 kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     const long long BH = static_cast<long long>(a.B) * a.H;
-    const int cwb = a.dk < 32 ? a.dk : 32;
+    const int cwb = bwd_cwb(BH, a.dk);
     const int ncb = a.dk / cwb;
     const int nC = (a.T + C - 1) / C;
     const Scratch sc = scratch_of(a.B, a.H, a.T, a.dk, a.dv);
@@ -867,7 +879,8 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     e = cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
     if (e == cudaSuccess && a.T > 0) {
         const long long BHT = BH * a.T;
-        diag_bwd_finalize_kernel<TIn><<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
+        auto fin = ncb <= 4 ? diag_bwd_finalize_kernel<TIn, 4> : diag_bwd_finalize_kernel<TIn, 8>;
+        fin<<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
             static_cast<const TIn*>(a.v), static_cast<const TIn*>(a.beta), static_cast<const TIn*>(a.d),
             a.A, p.prow, p.pD, a.grad_v, a.grad_beta, a.grad_d, eA, BHT, a.T, a.H, a.dv, ncb);
         e = cudaGetLastError();
