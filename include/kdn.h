@@ -154,7 +154,9 @@ KDN_API kdn_status kdn_lin_scan_fwd(const void* q, const void* k, const void* v,
  *
  * Scratch ("workspace"): kdn_diag_scan_bwd_workspace gives its size, about
  * B*H*T*dv*dk + 8*B*H*T*dv bytes (every 8th token's state, and per-column-
- * block row sums).  With workspace == NULL the call takes it from the
+ * block row sums; 16*B*H*T*dv for the latter when so few heads that the call
+ * takes 16-column blocks, B*H*dk/32*2 <= the current device's SM count).
+ * With workspace == NULL the call takes it from the
  * stream-ordered allocator (cudaMallocAsync, freed on the stream before
  * return; KDN_ERR_ALLOC if it cannot be had); otherwise workspace is a
  * 256-byte aligned device buffer of at least that many bytes, owned by the
@@ -175,7 +177,8 @@ KDN_API kdn_status kdn_diag_scan_bwd(const void* q, const void* k, const void* v
                              kdn_dtype in_dtype, void* workspace,
                              long long workspace_bytes, void* stream);
 
-/* Bytes of workspace kdn_diag_scan_bwd needs for these sizes (no GPU call). */
+/* Bytes of workspace kdn_diag_scan_bwd needs for these sizes on the current
+ * device (no GPU work; it reads the device's SM count). */
 KDN_API kdn_status kdn_diag_scan_bwd_workspace(int B, int H, int T, int dk, int dv,
                                        long long* workspace_bytes);
 
