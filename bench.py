@@ -46,8 +46,8 @@ MOBIUS_BYTES_PER_STEP = 20
 # (all its kernels: tensor-core aggregates, carry, full pass) per workload,
 # from the ncu capture of the current kernels summarised in profiles/
 # (launches_layer750m.md); workloads without such a capture report null.
-DIAG_TRAFFIC_BYTES = {"layer750m": (350_351_616 + 68_281_088) + (100_694_784 + 36_312_064)
-                      + (638_839_296 + 241_371_904)}
+DIAG_TRAFFIC_BYTES = {"layer750m": (350_416_896 + 67_866_880) + (100_696_320 + 36_271_104)
+                      + (638_855_424 + 241_288_448)}
 
 
 def parse_args():
