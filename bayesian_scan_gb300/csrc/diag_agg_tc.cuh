@@ -10,7 +10,7 @@
 // plus the part's total decay prod alpha = 2^-L.  Both sums are dense
 // contractions over the part's tokens, [d_v x T_p] x [T_p x d_k]: here they
 // run as tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor
-// memory), K = 32 tokens per chunk.
+// memory), K = 16 or 32 tokens per chunk.
 //
 // Precision.  k is a bf16 input, so k is exact in bf16 and k^2 (at most 16
 // significant bits) is exactly hi + lo of two bf16.  The weighted row
