@@ -14,9 +14,13 @@ collective; weak scaling); the timing is the max over ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
-    python bench.py --workload layer750m_bwd   # the backward pass (training)
+    python bench.py --workload layer750m_bwd   # the backward pass (training);
+                                               # also layer1p3b_bwd, longctx_bwd,
+                                               # heads32_t1024_bwd (one wave, for ncu)
     python bench.py --workload decode2k        # batched one-token decoding
-    python bench.py --workload layer750m_lin   # the non-metaplastic limit
+    python bench.py --workload layer750m_lin   # the non-metaplastic limit; also
+                                               # longctx_lin, heads128_t512_lin
+    python bench.py --workload layer1p3b       # or longctx: the other scan shapes
 
 Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
 Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
