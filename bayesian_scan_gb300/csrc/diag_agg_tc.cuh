@@ -112,7 +112,10 @@ struct AggArgs {
     long long wait_ns;
 };
 
-template <int KC>
+// ETA_ONLY: the non-metaplastic limit needs only Delta eta (its carry and
+// full pass ignore the J half): 3 operand tiles and 2 products a K step
+// instead of 7 and 5, and J written as zeros.
+template <int KC, bool ETA_ONLY = false>
 __global__ void __launch_bounds__(AggShape<KC>::THREADS, AggShape<KC>::CTAS_PER_SM)
 diag_agg_tc_kernel(const AggArgs p) {
     using Sh = AggShape<KC>;
@@ -199,9 +202,11 @@ diag_agg_tc_kernel(const AggArgs p) {
                         return umma_desc_kmajor(base + tile * AG_TILE + s * 2 * 128, AG_LBO, AG_SBO);
                     };
                     const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
-                    umma_bf16(tmem, desc(0), desc(5), IDESC, first);           // J += A_J hi  B_k2 hi
-                    umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);              //    + A_J hi  B_k2 lo
-                    umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);              //    + A_J lo  B_k2 hi
+                    if (!ETA_ONLY) {
+                        umma_bf16(tmem, desc(0), desc(5), IDESC, first);       // J += A_J hi  B_k2 hi
+                        umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_J hi  B_k2 lo
+                        umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);          //    + A_J lo  B_k2 hi
+                    }
                     umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, first);    // eta += A_E hi B_k
                     umma_bf16(tmem + AG_D, desc(3), desc(4), IDESC, 1u);       //      + A_E lo B_k
                 }
@@ -287,10 +292,10 @@ diag_agg_tc_kernel(const AggArgs p) {
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    split2(aj[r][0], aj[r][1], t[0][r][u2], t[1][r][u2]);
+                    if (!ETA_ONLY) split2(aj[r][0], aj[r][1], t[0][r][u2], t[1][r][u2]);
                     split2(ae[r][0], ae[r][1], t[2][r][u2], t[3][r][u2]);
                     t[4][r][u2] = kbits[r][0] | (kbits[r][1] << 16);
-                    split2(kf[r][0] * kf[r][0], kf[r][1] * kf[r][1], t[5][r][u2], t[6][r][u2]);
+                    if (!ETA_ONLY) split2(kf[r][0] * kf[r][0], kf[r][1] * kf[r][1], t[5][r][u2], t[6][r][u2]);
                 }
             }
             unsigned char* o = ops + ob * AG_OPS;
@@ -299,7 +304,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                 const int rho = 2 * pr + r;
                 const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;   // core matrix (rho/8, kg)
 #pragma unroll
-                for (int tile = 0; tile < AG_NTILE; ++tile)
+                for (int tile = ETA_ONLY ? 2 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE); ++tile)
                     *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) =
                         make_uint4(t[tile][r][0], t[tile][r][1], t[tile][r][2], t[tile][r][3]);
             }
@@ -345,7 +350,12 @@ diag_agg_tc_kernel(const AggArgs p) {
             float* dst = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S +
                          static_cast<long long>(row) * AG_D;
             float v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * AG_D + c0, v);
+            if (ETA_ONLY && half == 0) {   // J: not accumulated
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            } else {
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * AG_D + c0, v);
+            }
             if (nch == 0) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;

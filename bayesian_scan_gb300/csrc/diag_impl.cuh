@@ -723,6 +723,12 @@ cudaError_t agg_tc_prepare() {
         e = cudaFuncSetAttribute(diag_agg_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AggShape<32>::SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(diag_agg_tc_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AggShape<16>::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(diag_agg_tc_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AggShape<32>::SMEM);
+        if (e != cudaSuccess) return e;
         done[dev] = true;
     }
     return cudaSuccess;
@@ -883,10 +889,12 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                            a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, prm.d_ld, pl.part_len, wait_ns};
                 // two CTAs per SM when the grid fills them, else one wider CTA per SM
                 const dim3 grid(static_cast<unsigned>(BH), P - 1);
-                if (BH * (P - 1) >= 2LL * sm_count())
-                    diag_agg_tc_kernel<16><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
+                // (the non-metaplastic limit needs only the eta aggregates)
+                const bool two = BH * (P - 1) >= 2LL * sm_count();
+                if (two)
+                    diag_agg_tc_kernel<16, LIN><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
                 else
-                    diag_agg_tc_kernel<32><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
+                    diag_agg_tc_kernel<32, LIN><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
                 e = cudaGetLastError();
             }
         } else {
