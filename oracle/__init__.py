@@ -9,7 +9,9 @@ The arithmetic lives in ``kdn_oracle.c`` (plain token-by-token loops in fp64;
 see the header there for the equations and the page passages they follow).
 This module compiles it with gcc, loads it with ctypes and converts arrays.
 ``diag_scan_py`` / ``mobius_scan_py`` are the same definitions written as pure
-Python loops, for tiny inputs only: they cross-check the C transcription.
+Python loops, for tiny inputs only.  Both transcriptions are pinned by the same
+closed forms and invariants (``tests/oracle_pins.py``) and checked against each
+other on the smallest scan workload (``tests/test_oracle_pins.py``).
 """
 from __future__ import annotations
 

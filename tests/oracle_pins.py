@@ -50,9 +50,24 @@ def _inputs(B=1, H=2, T=24, dk=3, dv=5, A=(0.7, 1.9), I_prior=1.3, seed=RNG_SEED
     return dict(q=q, k=k, v=v, beta=beta, d=d, A=A, I_prior=I_prior, I0=I0, mu0=mu0)
 
 
+# Passing PY instead of a library handle runs a pin on the pure-Python loops
+# of the oracle (``oracle.diag_scan_py`` / ``oracle.mobius_scan_py``), so
+# those are pinned by the same facts as the C transcription.
+PY = "pure-python"
+
+
 def _run(lib, x):
+    if lib is PY:
+        return oracle.diag_scan_py(x["q"], x["k"], x["v"], x["beta"], x["d"], x["A"], x["I_prior"],
+                                   x["I0"], x["mu0"])
     return oracle.diag_scan(x["q"], x["k"], x["v"], x["beta"], x["d"], x["A"], x["I_prior"],
                             x["I0"], x["mu0"], lib=lib)
+
+
+def _mob(lib, a, b, c, d, lam0):
+    if lib is PY:
+        return oracle.mobius_scan_py(a, b, c, d, lam0)
+    return oracle.mobius_scan(a, b, c, d, lam0, lib=lib)
 
 
 def _rel(a, b):
@@ -451,7 +466,7 @@ def pin_mobius_bracketings(lib):
     """Every bracketing of the 2x2 products M_t...M_1 gives the oracle's
     lambda_t (associativity of the Moebius composition)."""
     a, b, c, d, lam0 = _mob_inputs(N=2, T=6)
-    out = oracle.mobius_scan(a, b, c, d, lam0, lib=lib)
+    out = _mob(lib, a, b, c, d, lam0)
     for n in range(a.shape[0]):
         mats = [np.array([[a[n, t], b[n, t]], [c[n, t], d[n, t]]]) for t in range(a.shape[1])]
         for t in range(1, len(mats) + 1):
@@ -467,7 +482,7 @@ def pin_mobius_matrix_power(lib):
     a0, b0, c0, d0 = 1.3, 0.4, 0.2, 0.7
     a = np.full((1, T), a0); b = np.full((1, T), b0)
     c = np.full((1, T), c0); d = np.full((1, T), d0)
-    out = oracle.mobius_scan(a, b, c, d, np.array([0.9]), lib=lib)
+    out = _mob(lib, a, b, c, d, np.array([0.9]))
     M = np.array([[a0, b0], [c0, d0]])
     for t in (1, 2, 3, 7, 50):
         assert abs(_apply(np.linalg.matrix_power(M, t), 0.9) - out[0, t - 1]) < 1e-13
@@ -480,7 +495,7 @@ def pin_mobius_affine(lib):
     lambda_t = prod_{r<=t}(a_r/d_r) lambda_0 + sum_{s<=t} (b_s/d_s) prod_{s<r<=t}(a_r/d_r)."""
     a, b, _, d, lam0 = _mob_inputs(N=3, T=9)
     c = np.zeros_like(a)
-    out = oracle.mobius_scan(a, b, c, d, lam0, lib=lib)
+    out = _mob(lib, a, b, c, d, lam0)
     for n in range(a.shape[0]):
         g = a[n] / d[n]
         for t in range(1, a.shape[1] + 1):
@@ -494,7 +509,7 @@ def pin_mobius_product(lib):
     """b = c = 0: lambda_t = lambda_0 prod_{r<=t} a_r/d_r."""
     a, _, _, d, lam0 = _mob_inputs(N=3, T=9)
     z = np.zeros_like(a)
-    out = oracle.mobius_scan(a, z, z, d, lam0, lib=lib)
+    out = _mob(lib, a, z, z, d, lam0)
     ref = lam0[:, None] * np.cumprod(a / d, axis=1)
     assert _rel(out, ref) < 1e-14
 
@@ -502,9 +517,9 @@ def pin_mobius_product(lib):
 def pin_mobius_resume(lib):
     """Carrying lambda_T of a first call into a second equals one call."""
     a, b, c, d, lam0 = _mob_inputs(N=3, T=11)
-    out = oracle.mobius_scan(a, b, c, d, lam0, lib=lib)
-    o1 = oracle.mobius_scan(a[:, :4], b[:, :4], c[:, :4], d[:, :4], lam0, lib=lib)
-    o2 = oracle.mobius_scan(a[:, 4:], b[:, 4:], c[:, 4:], d[:, 4:], o1[:, -1], lib=lib)
+    out = _mob(lib, a, b, c, d, lam0)
+    o1 = _mob(lib, a[:, :4], b[:, :4], c[:, :4], d[:, :4], lam0)
+    o2 = _mob(lib, a[:, 4:], b[:, 4:], c[:, 4:], d[:, 4:], o1[:, -1])
     assert _rel(np.concatenate([o1, o2], axis=1), out) < 1e-15
 
 

@@ -97,3 +97,46 @@ def test_mutant_is_caught(name, tmp_path):
         except (FloatingPointError, ZeroDivisionError, ValueError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught mutant {name}"
+
+
+# Mistakes planted in the pure-Python loops (``oracle.diag_scan_py`` /
+# ``oracle.mobius_scan_py``): the mutated function replaces the real one for
+# the duration of the case only, and the diagonal and Moebius pins run on it.
+PY_MUTANTS = {
+    "py_gate_sign": ("math.exp(-A[h] * d[b_][h][t])", "math.exp(A[h] * d[b_][h][t])"),
+    "py_gate_head_zero": ("math.exp(-A[h] * d[b_][h][t])", "math.exp(-A[0] * d[b_][h][t])"),
+    "py_drop_prior_leak": (" + (1 - alpha) * I_prior", ""),
+    "py_evidence_k_not_squared": ("bt[i] * kt[j] ** 2", "bt[i] * kt[j]"),
+    "py_ratio_inverted": ("alpha * I[i][j] / In * mu[i][j]", "alpha * In / I[i][j] * mu[i][j]"),
+    "py_write_uses_q": ("bt[i] * vt[i] * kt[j] / In", "bt[i] * vt[i] * qt[j] / In"),
+    "py_write_value_index": ("bt[i] * vt[i] * kt[j] / In", "bt[i] * vt[j] * kt[j] / In"),
+    "py_readout_uses_k": ("mu[i][j] * qt[j] for j", "mu[i][j] * kt[j] for j"),
+    "py_ignore_initial_importance": ("I0[b_][h][i][j] if I0 else I_prior", "I_prior"),
+    "py_ignore_initial_mean": ("mu0[b_][h][i][j] if mu0 else 0.0", "0.0"),
+    "py_mobius_swap_b_c": ("(a[n][t] * lam + b[n][t]) / (c[n][t] * lam + d[n][t])",
+                           "(a[n][t] * lam + c[n][t]) / (b[n][t] * lam + d[n][t])"),
+    "py_mobius_output_before_step": (
+        "lam = (a[n][t] * lam + b[n][t]) / (c[n][t] * lam + d[n][t])\n            row.append(lam)",
+        "row.append(lam)\n            lam = (a[n][t] * lam + b[n][t]) / (c[n][t] * lam + d[n][t])"),
+    "py_mobius_ignores_lambda0": ("lam, row = lambda0[n], []", "lam, row = 1.0, []"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pure_python_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+    old, new = PY_MUTANTS[name]
+    fn = "mobius_scan_py" if name.startswith("py_mobius") else "diag_scan_py"
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    failed = []
+    for pin in oracle_pins.DIAG_PINS + oracle_pins.MOBIUS_PINS:
+        try:
+            pin(oracle_pins.PY)
+        except (AssertionError, FloatingPointError, ZeroDivisionError, ValueError, OverflowError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
