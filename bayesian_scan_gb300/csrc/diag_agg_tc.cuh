@@ -12,13 +12,17 @@
 // run as tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor
 // memory), K = 16 or 32 tokens per chunk.
 //
-// Precision.  k is a bf16 input, so k is exact in bf16 and k^2 (at most 16
-// significant bits) is exactly hi + lo of two bf16.  The weighted row
-// factors w beta and w beta v are split the same way (hi = bf16(x), lo =
-// bf16(x - hi), relative error about 2^-16).  Delta J takes three products
-// (hi*hi2 + hi*lo2 + lo*hi2) and Delta eta two (hi*k + lo*k), all
-// accumulated in fp32.  The decay exponents are summed in fp64 (the part's
-// suffix sums) and w_t = 2^-floor(S) * exp2(-frac(S)).
+// Precision.  beta and k are bf16 inputs, so they are exact operands.  The
+// decay weight goes with k^2 for Delta J, Delta J = sum_t beta_t[i] (w_t
+// k_t[j]^2), and with beta v for Delta eta, Delta eta = sum_t (w_t beta_t[i]
+// v_t[i]) k_t[j]; the fp32 factors w k^2 and w beta v are each split into
+// three bf16 pieces (hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi -
+// mid); both differences are exact in fp32), which carry all 24 bits of the
+// fp32 value.  So each sum takes three products, accumulated in fp32, and
+// every term is as accurate as the fp32 product it stands for: the carried
+// states are fp32-accurate, not bf16-accurate.  The decay exponents are
+// summed in fp64 (the part's suffix sums) and w_t = 2^-floor(S) *
+// exp2(-frac(S)).
 //
 // Output: the same (J_w, eta_w) = W (Delta J, Delta eta) and (W, R) with
 // 2^-R / W = 2^-L, W in [1, 2), that the CUDA-core aggregate pass leaves for
@@ -32,7 +36,7 @@
 // core-matrix layout) from the raw chunk (k, beta, v, brought in by 1-D bulk
 // copies two chunks ahead) and arrive, one lane per warp, on the chunk's
 // operand barrier; the issuing warp waits there, issues the next copies into
-// the consumed raw stage and the chunk's 5 KC / 16 MMAs, and commits them to
+// the consumed raw stage and the chunk's 6 KC / 16 MMAs, and commits them to
 // an mbarrier.  Operand tiles are double-buffered on that barrier, so the
 // build threads never wait for the products to be issued (a build thread
 // that also issued held its warp, and at the chunk barrier all others, for
@@ -50,7 +54,7 @@ namespace diag {
 namespace {
 
 constexpr int AG_D = 128;                          // d_k = d_v
-constexpr int AG_NTILE = 7;                        // A_J hi/lo, A_E hi/lo, B_k, B_k2 hi/lo
+constexpr int AG_NTILE = 8;                        // A_beta, A_E hi/mid/lo, B_k, B_wk2 hi/mid/lo
 constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta in [128,256)
 constexpr uint32_t AG_LBO = 128;                   // core matrices: next 8 tokens (K)
 
@@ -82,12 +86,17 @@ __device__ __forceinline__ float exp2_neg(double S) {
     return ldexpf(exp2f(-f), -e);
 }
 
-// (x0, x1) -> bf16x2 hi = rn(x), lo = rn(x - hi), low half = x0
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+// (x0, x1) -> bf16x2 pieces hi = rn(x), mid = rn(x - hi), lo = rn(x - hi -
+// mid), low half = x0; hi + mid + lo equals x to fp32 rounding (x - hi and
+// x - hi - mid are exact in fp32)
+__device__ __forceinline__ void split3(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     hi = *reinterpret_cast<const uint32_t*>(&h);
-    const float b0 = __uint_as_float(hi << 16), b1 = __uint_as_float(hi & 0xffff0000u);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - b0, x1 - b1);
+    const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xffff0000u);
+    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
+    mid = *reinterpret_cast<const uint32_t*>(&m);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __uint_as_float(mid << 16),
+                                                   r1 - __uint_as_float(mid & 0xffff0000u));
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
@@ -113,8 +122,8 @@ struct AggArgs {
 };
 
 // ETA_ONLY: the non-metaplastic limit needs only Delta eta (its carry and
-// full pass ignore the J half): 3 operand tiles and 2 products a K step
-// instead of 7 and 5, and J written as zeros.
+// full pass ignore the J half): 4 operand tiles and 3 products a K step
+// instead of 8 and 6, and J written as zeros.
 template <int KC, bool ETA_ONLY = false>
 __global__ void __launch_bounds__(AggShape<KC>::THREADS, AggShape<KC>::CTAS_PER_SM)
 diag_agg_tc_kernel(const AggArgs p) {
@@ -203,11 +212,12 @@ diag_agg_tc_kernel(const AggArgs p) {
                     };
                     const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
                     if (!ETA_ONLY) {
-                        umma_bf16(tmem, desc(0), desc(5), IDESC, first);       // J += A_J hi  B_k2 hi
-                        umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_J hi  B_k2 lo
-                        umma_bf16(tmem, desc(1), desc(5), IDESC, 1u);          //    + A_J lo  B_k2 hi
+                        umma_bf16(tmem, desc(0), desc(5), IDESC, first);       // J += A_beta B_wk2 hi
+                        umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_beta B_wk2 mid
+                        umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);          //    + A_beta B_wk2 lo
                     }
-                    umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, first);    // eta += A_E hi B_k
+                    umma_bf16(tmem + AG_D, desc(1), desc(4), IDESC, first);    // eta += A_E hi B_k
+                    umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, 1u);       //      + A_E mid B_k
                     umma_bf16(tmem + AG_D, desc(3), desc(4), IDESC, 1u);       //      + A_E lo B_k
                 }
                 umma_commit(&mma_done[ob]);
@@ -260,17 +270,17 @@ diag_agg_tc_kernel(const AggArgs p) {
         // the operand buffer was last read by the MMAs of iteration it - 2
         if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
 
-        // ---- build the 7 operand tiles of this chunk (rows 2pr, 2pr+1; tokens 8kg..8kg+7) ----
+        // ---- build the 8 operand tiles of this chunk (rows 2pr, 2pr+1; tokens 8kg..8kg+7) ----
         {
             const unsigned char* rk = raw + st * 3 * AG_RAW;
             const unsigned char* rb = rk + AG_RAW;
             const unsigned char* rv = rb + AG_RAW;
             const float* w = wsup + (t0 - sup0);
-            uint32_t t[7][2][4];   // [tile][row of the pair][4 x bf16x2 along the tokens]
+            uint32_t t[AG_NTILE][2][4];   // [tile][row of the pair][4 x bf16x2 along the tokens]
 #pragma unroll
             for (int u2 = 0; u2 < 4; ++u2) {
-                float aj[2][2], ae[2][2], kf[2][2];
-                uint32_t kbits[2][2];
+                float ae[2][2], wk2[2][2];
+                uint32_t kbits[2][2], bbits[2][2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int tok = kg * 8 + 2 * u2 + e;
@@ -282,20 +292,23 @@ diag_agg_tc_kernel(const AggArgs p) {
                     const uint32_t kk = valid ? *reinterpret_cast<const uint32_t*>(rk + o4) : 0u;
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const float bf = __uint_as_float(r ? (bb & 0xffff0000u) : (bb << 16));
+                        bbits[r][e] = r ? (bb >> 16) : (bb & 0xffffu);
+                        const float bf = __uint_as_float(bbits[r][e] << 16);
                         const float vf = __uint_as_float(r ? (vv & 0xffff0000u) : (vv << 16));
                         kbits[r][e] = r ? (kk >> 16) : (kk & 0xffffu);
-                        kf[r][e] = __uint_as_float(kbits[r][e] << 16);
-                        aj[r][e] = wt * bf;
-                        ae[r][e] = aj[r][e] * vf;
+                        const float kf = __uint_as_float(kbits[r][e] << 16);
+                        ae[r][e] = (wt * bf) * vf;
+                        wk2[r][e] = wt * (kf * kf);   // k^2 is exact in fp32 (16 significant bits)
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    if (!ETA_ONLY) split2(aj[r][0], aj[r][1], t[0][r][u2], t[1][r][u2]);
-                    split2(ae[r][0], ae[r][1], t[2][r][u2], t[3][r][u2]);
+                    if (!ETA_ONLY) {
+                        t[0][r][u2] = bbits[r][0] | (bbits[r][1] << 16);
+                        split3(wk2[r][0], wk2[r][1], t[5][r][u2], t[6][r][u2], t[7][r][u2]);
+                    }
+                    split3(ae[r][0], ae[r][1], t[1][r][u2], t[2][r][u2], t[3][r][u2]);
                     t[4][r][u2] = kbits[r][0] | (kbits[r][1] << 16);
-                    if (!ETA_ONLY) split2(kf[r][0] * kf[r][0], kf[r][1] * kf[r][1], t[5][r][u2], t[6][r][u2]);
                 }
             }
             unsigned char* o = ops + ob * AG_OPS;
@@ -304,7 +317,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                 const int rho = 2 * pr + r;
                 const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;   // core matrix (rho/8, kg)
 #pragma unroll
-                for (int tile = ETA_ONLY ? 2 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE); ++tile)
+                for (int tile = ETA_ONLY ? 1 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE); ++tile)
                     *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) =
                         make_uint4(t[tile][r][0], t[tile][r][1], t[tile][r][2], t[tile][r][3]);
             }

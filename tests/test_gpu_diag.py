@@ -142,6 +142,6 @@ def test_output_written_only_where_expected():
                              final_state=False)
     torch.cuda.synchronize()
     ro, _, _ = parity.oracle_diag(inp)
-    assert parity.rel_err(o.cpu(), ro) < parity.TOL_DIAG
+    parity.assert_close(o.cpu(), ro, parity.TOL_DIAG)
     assert torch.all(out[:, :, 50:] == 12345.0)
     assert view.shape == (1, 2, 50, 32)

@@ -34,9 +34,9 @@ def test_host_diag_matches_oracle(T, dk, dtype):
     inp = draw(1, 2, T, dk, dk, dtype, seed=T)
     o, fs = host_diag(inp)
     ro, rmu, rI = parity.oracle_diag(inp)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
+    parity.assert_close(fs[0], rmu, parity.TOL_DIAG)
+    parity.assert_close(fs[1], rI, parity.TOL_DIAG)
 
 
 def test_host_diag_initial_state_and_pageable_buffers():
@@ -46,9 +46,9 @@ def test_host_diag_initial_state_and_pageable_buffers():
     mu0 = torch.randn(2, 1, 64, 64, generator=g)
     o, fs = host_diag(inp, I0, mu0, pin=False)
     ro, rmu, rI = parity.oracle_diag(inp, I0, mu0)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
+    parity.assert_close(fs[0], rmu, parity.TOL_DIAG)
+    parity.assert_close(fs[1], rI, parity.TOL_DIAG)
 
 
 def test_host_diag_agrees_with_device_call():
@@ -70,7 +70,7 @@ def test_host_diag_outputs_given_and_state_skipped():
                               I_prior=1.0, out=out, final_state=False)
     assert o.data_ptr() == out.data_ptr() and fs is None
     ro, _, _ = parity.oracle_diag(inp)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
 
 
 @pytest.mark.parametrize("where", ["pinned", "pinned_offset", "pageable"])
@@ -91,7 +91,7 @@ def test_host_diag_output_buffers(where):
                              I_prior=1.0, out=out, final_state=False)
     assert o.data_ptr() == out.data_ptr()
     ro, _, _ = parity.oracle_diag(inp)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
 
 
 def test_host_diag_batch_groups_match_oracle():
@@ -103,9 +103,9 @@ def test_host_diag_batch_groups_match_oracle():
     mu0 = torch.randn(5, 2, 32, 32, generator=g)
     o, fs = host_diag(inp, I0, mu0)
     ro, rmu, rI = parity.oracle_diag(inp, I0, mu0)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
+    parity.assert_close(fs[0], rmu, parity.TOL_DIAG)
+    parity.assert_close(fs[1], rI, parity.TOL_DIAG)
 
 
 def test_host_diag_batch_groups_uneven_and_pageable():
@@ -114,9 +114,9 @@ def test_host_diag_batch_groups_uneven_and_pageable():
     inp = draw(9, 2, 129, 16, 16, torch.float32, seed=23)
     o, fs = host_diag(inp, pin=False)
     ro, rmu, rI = parity.oracle_diag(inp)
-    assert parity.rel_err(o, ro) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[0], rmu) <= parity.TOL_DIAG
-    assert parity.rel_err(fs[1], rI) <= parity.TOL_DIAG
+    parity.assert_close(o, ro, parity.TOL_DIAG)
+    parity.assert_close(fs[0], rmu, parity.TOL_DIAG)
+    parity.assert_close(fs[1], rI, parity.TOL_DIAG)
 
 
 def test_host_diag_batch_groups_agree_with_device_call():
@@ -157,6 +157,6 @@ def test_host_mobius_matches_oracle_and_device(N, T):
     assert not out.is_cuda
     assert kdn.get_device_error() == 0
     ref = parity.oracle.mobius_scan(a, b, c, d, lam0)
-    assert parity.rel_err(out, ref) <= parity.TOL_MOBIUS
+    parity.assert_close(out, ref, parity.TOL_MOBIUS)
     dev = parity.gpu_mobius(a, b, c, d, lam0)
     assert parity.rel_err(out, dev) <= 1e-6

@@ -29,9 +29,9 @@ def test_step_matches_oracle(dk, dv, dtype):
                           for x in (q, k, v, beta, d)), A.cuda(), state, I_prior=1.0)
     torch.cuda.synchronize()
     ro, rmu, rI = oracle_step(q, k, v, beta, d, A, mu, I)
-    assert parity.rel_err(out.cpu(), ro[:, :, 0]) <= parity.TOL_DIAG
-    assert parity.rel_err(state[0].cpu(), rmu) <= parity.TOL_DIAG
-    assert parity.rel_err(state[1].cpu(), rI) <= parity.TOL_DIAG
+    parity.assert_close(out.cpu(), ro[:, :, 0], parity.TOL_DIAG)
+    parity.assert_close(state[0].cpu(), rmu, parity.TOL_DIAG)
+    parity.assert_close(state[1].cpu(), rI, parity.TOL_DIAG)
 
 
 def oracle_step(q, k, v, beta, d, A, mu, I):
@@ -72,6 +72,6 @@ def test_step_many_heads():
         b, h = divmod(bh, 130)
         sl = lambda x: x[b:b + 1, h:h + 1]
         ro, rmu, rI = oracle_step(sl(q), sl(k), sl(v), sl(beta), sl(d), A[h:h + 1], sl(mu), sl(I))
-        assert parity.rel_err(out[b:b + 1, h:h + 1].cpu(), ro[:, :, 0]) <= parity.TOL_DIAG
-        assert parity.rel_err(state[0, b:b + 1, h:h + 1].cpu(), rmu) <= parity.TOL_DIAG
-        assert parity.rel_err(state[1, b:b + 1, h:h + 1].cpu(), rI) <= parity.TOL_DIAG
+        parity.assert_close(out[b:b + 1, h:h + 1].cpu(), ro[:, :, 0], parity.TOL_DIAG)
+        parity.assert_close(state[0, b:b + 1, h:h + 1].cpu(), rmu, parity.TOL_DIAG)
+        parity.assert_close(state[1, b:b + 1, h:h + 1].cpu(), rI, parity.TOL_DIAG)
