@@ -59,11 +59,13 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <type_traits>
 
 #include "kdn_device.cuh"
 #include "kdn_internal.h"
+#include "mobius_device.cuh"
 
 namespace kdn {
 namespace diag {
@@ -115,11 +117,23 @@ struct Params {
     float* agg;              // [P-1][BH][2][dv][dk] part end states / carried start states
     AggScale* agg_scale;     // [P-1][BH]
     long long BH;
+    long long ctas;          // CTAs per token part (head groups)
+    int P;                   // token parts of this pass
     int H, T, dv;
     int part_len;            // tokens per part (multiple of TC)
     int TC;                  // tokens per chunk
     int d_tma;               // 1: d staged by TMA (aligned), 0: plain loads
     long long wait_ns;
+    // per-head Moebius lambda run by extra CTAs of the full pass (nlam of
+    // them, after the ctas * P scan CTAs): [BH, T] coefficients (rows 16-byte
+    // aligned, T % 4 == 0), lam0 [BH], lam_out [BH, T]; nlam = 0: none
+    const float* ma;
+    const float* mb;
+    const float* mc;
+    const float* md;
+    const float* lam0;
+    float* lam_out;
+    int nlam;
 };
 
 template <int DK>
@@ -265,9 +279,20 @@ diag_scan_kernel(const Params p) {
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long head0 = static_cast<long long>(blockIdx.x) * HPC;
+    // linear grid: part-major scan CTAs (head group fastest), then the lambda
+    // walkers of the full pass
+    const long long lin = blockIdx.x;
+    if (lin >= p.ctas * p.P) {
+        if constexpr (!AGG && !LIN) {
+            const int tps = static_cast<int>((p.T + mob::Walk<G::NTHREADS>::TILE - 1) / mob::Walk<G::NTHREADS>::TILE);
+            mob::mobius_walk<G::NTHREADS>(p.ma, p.mb, p.mc, p.md, p.lam0, p.lam_out, p.BH, p.T, tps,
+                                          lin - p.ctas * p.P, p.nlam, p.wait_ns, smem, &g_diag_error);
+        }
+        return;
+    }
+    const int part = static_cast<int>(lin / p.ctas);
+    const long long head0 = (lin - static_cast<long long>(part) * p.ctas) * HPC;
     const int nheads = static_cast<int>(min(static_cast<long long>(HPC), p.BH - head0));
-    const int part = blockIdx.y;
     const int T = p.T;
     const int tb = min(T, part * p.part_len);
     const int te = min(T, tb + p.part_len);
@@ -620,7 +645,7 @@ diag_scan_kernel(const Params p) {
             }
         // the head's scale state after the part: W of its last token, total R
         if (i0 == 0 && cg == 0) p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, r_state[hl]};
-    } else if (LIN && p.final_state && part == static_cast<int>(gridDim.y) - 1) {
+    } else if (LIN && p.final_state && part == p.P - 1) {
         // mu_T = Ew / (W I_prior)
         float* fm = p.final_state + bh * S;
         const float rw = 1.f / (W * Ip);
@@ -631,7 +656,7 @@ diag_scan_kernel(const Params p) {
                 const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
                 *reinterpret_cast<float2*>(fm + off) = __fmul2_rn(E[r][c2], f2(rw));
             }
-    } else if (p.final_state && part == static_cast<int>(gridDim.y) - 1) {
+    } else if (p.final_state && part == p.P - 1) {
         // mu_T = eta / (I_prior + J) = Ew / (Jw + W I_prior);  I_T = Jw / W + I_prior
         float* fm = p.final_state + bh * S;
         float* fi = p.final_state + (p.BH + bh) * S;
@@ -695,6 +720,8 @@ __global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* 
 #include "diag_agg_tc.cuh"
 // the non-metaplastic full pass on the tensor cores (d = 128, bf16)
 #include "lin_tc.cuh"
+// the warp-specialised full pass of the metaplastic scan (d_k = 64, 128)
+#include "diag_ws.cuh"
 
 namespace kdn {
 namespace diag {
@@ -722,9 +749,6 @@ cudaError_t agg_tc_prepare() {
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(diag_agg_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AggShape<32>::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(diag_agg_tc_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AggShape<16>::SMEM);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(diag_agg_tc_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  AggShape<32>::SMEM);
@@ -758,6 +782,9 @@ cudaError_t prepare(int dev, int smem, int* occ) {
     return e;
 }
 
+// Whether the metaplastic full pass may take the warp-specialised kernel.
+constexpr bool kWsFullPass = false;
+
 // Whether a split call's aggregate pass runs on the tensor cores.
 template <int DK, typename TIn>
 constexpr bool tc_aggregates(int dv) {
@@ -770,10 +797,41 @@ struct Plan {
     int smem = 0;
     int P = 1;
     int part_len = 1;
-    long long ctas = 0;
+    long long ctas = 0;      // CTAs per part of the CUDA-core kernel (aggregate pass)
     size_t scratch = 0;
     int kernels = 0;
+    int occ = 1;             // resident full-pass CTAs per SM
+    // full pass: the warp-specialised kernel (ws) or diag_scan_kernel
+    bool ws = false;
+    long long ctas_full = 0; // CTAs per part of the full pass
+    int TC_full = 16;
+    int smem_full = 0;
 };
+
+// Set-up of the warp-specialised full pass on the current device: opts it
+// into its shared memory and checks that it was built with the launch
+// register allocation its setmaxnreg split assumes (else the split could
+// wait forever: the caller then keeps the CUDA-core kernel).
+template <int DK, typename TIn>
+cudaError_t ws_prepare(int dev, int smem, bool* usable) {
+    static int smem_set[64] = {};
+    static int regs_ok[64] = {};   // 0 unknown, 1 yes, 2 no
+    if (dev < 0 || dev >= 64) dev = 0;
+    auto kern = diag_ws_kernel<DK, TIn>;
+    if (regs_ok[dev] == 0) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        regs_ok[dev] = fa.numRegs == WS_LAUNCH_REG ? 1 : 2;
+    }
+    *usable = regs_ok[dev] == 1;
+    if (*usable && smem > smem_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set[dev] = smem;
+    }
+    return cudaSuccess;
+}
 
 template <int DK, typename TIn, bool LIN>
 kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
@@ -797,11 +855,39 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     if (e != cudaSuccess) return from_cuda(e);
     e = prepare<DK, TIn, true, LIN>(dev, pl->smem, &occ_agg);
     if (e != cudaSuccess) return from_cuda(e);
+    pl->occ = occ;
+    pl->ctas_full = pl->ctas;
+    pl->TC_full = TC;
+    pl->smem_full = pl->smem;
+    if constexpr (kWsFullPass && !LIN && (DK == 64 || DK == 128)) {
+        // warp-specialised full pass: chunks of 16 tokens when they fit (never
+        // longer than the aggregate pass's, so parts hold whole chunks of both)
+        using WG = WsGeo<DK>;
+        if (WG::ROWS % dv == 0) {
+            int tcw = 16;
+            while (tcw > 8 && ws_smem_bytes<DK>(dv, ES, tcw) > 227 * 1024) tcw >>= 1;
+            tcw = std::min(tcw, TC);
+            const int smem_ws = std::max(ws_smem_bytes<DK>(dv, ES, tcw), mob::Walk<WS_THREADS>::SMEM);
+            bool usable = false;
+            if (tcw >= 8 && smem_ws <= 227 * 1024) {
+                e = ws_prepare<DK, TIn>(dev, smem_ws, &usable);
+                if (e != cudaSuccess) return from_cuda(e);
+            }
+            if (usable) {
+                pl->ws = true;
+                pl->TC_full = tcw;
+                pl->smem_full = smem_ws;
+                const int hpcw = WG::ROWS / dv;
+                pl->ctas_full = (BH + hpcw - 1) / hpcw;
+                pl->occ = occ = 1;
+            }
+        }
+    }
     // token split: enough parts to give every CTA slot work
     const long long slots = static_cast<long long>(sm_count()) * occ;
     int P = 1;
-    if (pl->ctas * 2 <= slots && a.T >= 8 * TC) {
-        const long long want = slots / pl->ctas;
+    if (pl->ctas_full * 2 <= slots && a.T >= 8 * TC) {
+        const long long want = slots / pl->ctas_full;
         const long long maxp = a.T / (4 * TC);
         P = static_cast<int>(want < maxp ? want : maxp);
         if (P < 1) P = 1;
@@ -813,9 +899,9 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
     // per extra (head, part) (aggregate, carry and start-state traffic) and
     // 23 for the two extra launches (fitted to GB300 timings of the 750M-shaped
     // layer); taken when it saves more than 2 %.
-    if (!LIN && P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas < slots && a.T >= 32 * TC) {
+    if (!LIN && P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas_full < slots && a.T >= 32 * TC) {
         auto est = [&](int parts, int plen) {
-            const long long waves = (pl->ctas * parts + slots - 1) / slots;
+            const long long waves = (pl->ctas_full * parts + slots - 1) / slots;
             return static_cast<double>(waves) * plen +
                    (parts > 1 ? 23.0 + 0.47 * static_cast<double>(BH) * (parts - 1) : 0.0);
         };
@@ -867,6 +953,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
     prm.out_ld = a.out_ld > 0 ? a.out_ld : a.T;
     prm.d_ld = a.d_ld > 0 ? a.d_ld : a.T;
     prm.BH = BH; prm.H = a.H; prm.T = a.T; prm.dv = dv;
+    prm.ctas = ctas; prm.P = P;
     prm.part_len = pl.part_len; prm.TC = TC; prm.wait_ns = wait_ns;
     // d chunks can be bulk-copied when every chunk starts and ends on 16 bytes
     prm.d_tma = (static_cast<long long>(a.T) * ES % 16 == 0) && (TC * ES % 16 == 0) &&
@@ -889,17 +976,25 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                            a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, prm.d_ld, pl.part_len, wait_ns};
                 // two CTAs per SM when the grid fills them, else one wider CTA per SM
                 const dim3 grid(static_cast<unsigned>(BH), P - 1);
-                // (the non-metaplastic limit needs only the eta aggregates)
-                const bool two = BH * (P - 1) >= 2LL * sm_count();
-                if (two)
-                    diag_agg_tc_kernel<16, LIN><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
-                else
-                    diag_agg_tc_kernel<32, LIN><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
+                if constexpr (LIN) {
+                    // the non-metaplastic limit needs only the eta aggregates; its
+                    // parts come from the first rule of plan_dk alone, so BH * (P - 1)
+                    // stays below one wave of full-pass CTAs: always one CTA per SM
+                    diag_agg_tc_kernel<32, true><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
+                } else {
+                    if (BH * (P - 1) >= 2LL * sm_count())
+                        diag_agg_tc_kernel<16><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
+                    else
+                        diag_agg_tc_kernel<32><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
+                }
                 e = cudaGetLastError();
             }
         } else {
+            Params pa = prm;
+            pa.P = P - 1;
+            pa.ctas = ctas;
             diag_scan_kernel<DK, TIn, true, LIN>
-                <<<dim3(static_cast<unsigned>(ctas), P - 1), Geo<DK>::NTHREADS, smem, st>>>(prm);
+                <<<static_cast<unsigned>(ctas * (P - 1)), Geo<DK>::NTHREADS, smem, st>>>(pa);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) {
@@ -934,9 +1029,49 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         }
     }
     if (e == cudaSuccess && !tc_full) {
-        diag_scan_kernel<DK, TIn, false, LIN>
-            <<<dim3(static_cast<unsigned>(ctas), P), Geo<DK>::NTHREADS, smem, st>>>(prm);
-        e = cudaGetLastError();
+        // Per-head lambda walkers: appended after the scan CTAs, so they take
+        // the CTA slots that the scan's last wave leaves free (at least one
+        // walker per 64 tiles of lambda work).
+        int launch_smem = pl.ws ? pl.smem_full : smem;
+        const long long ctas_f = pl.ws ? pl.ctas_full : ctas;
+        prm.ctas = ctas_f;
+        prm.TC = pl.TC_full;
+        if constexpr (!LIN) {
+            if (a.lam_out && a.T > 0) {
+                const int walk_tile = pl.ws ? mob::Walk<WS_THREADS>::TILE : mob::Walk<Geo<DK>::NTHREADS>::TILE;
+                const int walk_smem = pl.ws ? mob::Walk<WS_THREADS>::SMEM : mob::Walk<Geo<DK>::NTHREADS>::SMEM;
+                const long long tps = (a.T + walk_tile - 1) / walk_tile;
+                const long long slots = static_cast<long long>(sm_count()) * pl.occ;
+                const long long total = ctas_f * P;
+                const long long free_slots = (total + slots - 1) / slots * slots - total;
+                long long nl = std::max(free_slots, (BH * tps + 63) / 64);
+                nl = std::min(std::max(nl, 1LL), BH);
+                prm.nlam = static_cast<int>(nl);
+                prm.ma = a.ma; prm.mb = a.mb; prm.mc = a.mc; prm.md = a.md;
+                prm.lam0 = a.lam0; prm.lam_out = a.lam_out;
+                launch_smem = std::max(launch_smem, walk_smem);
+            }
+        }
+        const unsigned grid = static_cast<unsigned>(ctas_f * P + prm.nlam);
+        bool launched = false;
+        if constexpr (!LIN && (DK == 64 || DK == 128)) {
+            if (pl.ws) {
+                // launch_smem == pl.smem_full: the walkers' stages fit it (plan_dk)
+                diag_ws_kernel<DK, TIn><<<grid, WS_THREADS, launch_smem, st>>>(prm);
+                e = cudaGetLastError();
+                launched = true;
+            }
+        }
+        if (!launched) {
+            if (launch_smem > smem) {
+                e = cudaFuncSetAttribute(diag_scan_kernel<DK, TIn, false, LIN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, launch_smem);
+            }
+            if (e == cudaSuccess) {
+                diag_scan_kernel<DK, TIn, false, LIN><<<grid, Geo<DK>::NTHREADS, launch_smem, st>>>(prm);
+                e = cudaGetLastError();
+            }
+        }
     }
     if (scratch) {
         const cudaError_t ef = cudaFreeAsync(scratch, st);

@@ -73,6 +73,45 @@ kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v, const 
     return in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
 }
 
+kdn_status kdn_diag_mobius_scan_fwd(const void* q, const void* k, const void* v, const void* beta,
+                                    const void* d, const float* A, float I_prior, const float* I0,
+                                    const float* mu0, float* out, float* final_state, const float* ma,
+                                    const float* mb, const float* mc, const float* md,
+                                    const float* lambda0, float* lambda_out, int B, int H, int T,
+                                    int dk, int dv, kdn_dtype in_dtype, void* stream) {
+    if (B < 1 || H < 1 || T < 0) return KDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !beta || !d || !A || !out || !ma || !mb || !mc || !md ||
+                  !lambda0 || !lambda_out))
+        return KDN_ERR_INVALID_ARG;
+    if (in_dtype != KDN_F32 && in_dtype != KDN_BF16) return KDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDN_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long dmax = dk > dv ? dk : dv;
+    if (BH > (1LL << 40) || BH * (T > 0 ? T : 1) > (1LL << 62) / dmax) return KDN_ERR_INVALID_ARG;
+    const void* ptrs16[] = {q, k, v, beta, out, I0, mu0, final_state};
+    for (const void* p : ptrs16)
+        if (p && !aligned(p, 16)) return KDN_ERR_INVALID_ARG;
+    const void* ptrs4[] = {A, ma, mb, mc, md, lambda0, lambda_out};
+    for (const void* p : ptrs4)
+        if (p && !aligned(p, 4)) return KDN_ERR_INVALID_ARG;
+    if (d && !aligned(d, in_dtype == KDN_BF16 ? 2 : 4)) return KDN_ERR_INVALID_ARG;
+
+    DiagArgs a{q, k, v, beta, d, A, I_prior, I0, mu0, out, final_state, B, H, T, dk, dv, in_dtype};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long wait_ns = g_wait_ns.load();
+    // the lambda walkers stream whole 16-byte rows; other layouts take the
+    // Moebius scan as its own launch after the scan
+    const bool fused = T % 4 == 0 && aligned(ma, 16) && aligned(mb, 16) && aligned(mc, 16) &&
+                       aligned(md, 16) && aligned(lambda_out, 16);
+    if (fused) {
+        a.ma = ma; a.mb = mb; a.mc = mc; a.md = md; a.lam0 = lambda0; a.lam_out = lambda_out;
+    }
+    const kdn_status s =
+        in_dtype == KDN_BF16 ? diag_launch_bf16(a, st, wait_ns) : diag_launch_f32(a, st, wait_ns);
+    if (s != KDN_OK || fused) return s;
+    return mobius_launch(ma, mb, mc, md, lambda0, lambda_out, BH, T, st, wait_ns, -1);
+}
+
 kdn_status kdn_lin_scan_fwd(const void* q, const void* k, const void* v, const void* beta,
                             const void* d, const float* A, float I_prior, const float* mu0,
                             float* out, float* final_mu, int B, int H, int T, int dk, int dv,

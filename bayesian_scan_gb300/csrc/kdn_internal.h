@@ -29,6 +29,15 @@ struct DiagArgs {
     // the non-metaplastic limit: importance held at I_prior (I0 unused,
     // final_state is mu_T alone, [B,H,dv,dk])
     bool lin = false;
+    // per-head Moebius lambda computed in the same launch as the scan (lam_out
+    // non-null): coefficients [B*H, T] fp32 with 16-byte aligned rows (T % 4
+    // == 0), lam0 [B*H], lam_out [B*H, T]
+    const float* ma = nullptr;
+    const float* mb = nullptr;
+    const float* mc = nullptr;
+    const float* md = nullptr;
+    const float* lam0 = nullptr;
+    float* lam_out = nullptr;
 };
 
 // Per-dtype launchers (diag_bf16.cu / diag_f32.cu).

@@ -38,6 +38,7 @@
 
 #include "kdn_device.cuh"
 #include "kdn_internal.h"
+#include "mobius_device.cuh"
 
 namespace kdn {
 namespace {
@@ -52,42 +53,12 @@ constexpr unsigned int FLAG_PRE = 2u;           // inclusive lambda published
 
 __device__ int g_mobius_error = 0;
 
-struct Mat {
-    float a, b, c, d;  // [[a, b], [c, d]]
-};
-
-__device__ __forceinline__ Mat identity() { return {1.f, 0.f, 0.f, 1.f}; }
-
-// L * R (apply R first, then L)
-__device__ __forceinline__ Mat mul(const Mat& L, const Mat& R) {
-    Mat o;
-    o.a = fmaf(L.a, R.a, L.b * R.c);
-    o.b = fmaf(L.a, R.b, L.b * R.d);
-    o.c = fmaf(L.c, R.a, L.d * R.c);
-    o.d = fmaf(L.c, R.b, L.d * R.d);
-    return o;
-}
-
-// Scale by an exact power of two so that the largest |entry| lies in [1, 2):
-// the factor is built from the exponent field of the largest magnitude.  A
-// zero matrix stays zero; a largest entry at or above 2^126 is brought into
-// [1, 4) (the factor stays a normal number); infinities stay infinite and
-// NaN propagates through the products.
-__device__ __forceinline__ Mat normalize(const Mat& m) {
-    const float mx = fmaxf(fmaxf(fabsf(m.a), fabsf(m.b)), fmaxf(fabsf(m.c), fabsf(m.d)));
-    const uint32_t e = min(__float_as_uint(mx) & 0x7f800000u, 0x7e800000u);   // biased exponent E <= 253
-    const float s = __uint_as_float(0x7f000000u - e);                           // 2^(127 - E)
-    return {m.a * s, m.b * s, m.c * s, m.d * s};
-}
-
-__device__ __forceinline__ float apply(const Mat& m, float lam) {
-    return fmaf(m.a, lam, m.b) / fmaf(m.c, lam, m.d);
-}
-
-__device__ __forceinline__ Mat shfl_up(const Mat& m, int off) {
-    return {__shfl_up_sync(0xffffffffu, m.a, off), __shfl_up_sync(0xffffffffu, m.b, off),
-            __shfl_up_sync(0xffffffffu, m.c, off), __shfl_up_sync(0xffffffffu, m.d, off)};
-}
+using mob::apply;
+using mob::identity;
+using mob::Mat;
+using mob::mul;
+using mob::normalize;
+using mob::shfl_up;
 
 struct LookbackScratch {
     unsigned long long* ticket;   // tile ticket counter (zeroed per launch)
@@ -249,31 +220,13 @@ mobius_scan_kernel(const float* __restrict__ A, const float* __restrict__ B,
 // Sequence-per-CTA kernel for 16-byte aligned rows (T % 4 == 0), chosen by
 // mobius_choose_seq (many sequences, or short ones).  A persistent grid of at
 // most SQ_CTAS_PER_SM CTAs per SM gives CTA b the sequences b, b + G, b + 2G,
-// ... (G = grid size) and walks their tiles in order, so no cross-CTA
-// look-back (and no scratch) is needed:
-//   * the coefficients of the next SQ_STAGES - 1 tiles of the CTA's stream are
-//     in flight as 1-D bulk TMA copies (one per coefficient array, completing
-//     on an mbarrier) while the current tile is scanned;
-//   * each of the 256 threads owns 8 consecutive steps: it composes them as a
-//     balanced tree, a warp-shuffle scan and the 8 warp totals give its
-//     exclusive prefix, and it evaluates its 8 outputs sequentially from the
-//     lambda at its first step;
-//   * lambda at the start of the next tile is the last output of this one
-//     (the last thread's final step), so consecutive tiles continue exactly
-//     from the value that was written.
-// Two barriers per tile; the per-tile shared words (warp totals, carried
-// lambda) are double-buffered by tile parity.
+// ... (G = grid size) and walks their tiles in order (mob::mobius_walk), so no
+// cross-CTA look-back (and no scratch) is needed.
 constexpr int SQ_THREADS = 256;
-constexpr int SQ_WARPS = SQ_THREADS / 32;
-constexpr int SQ_VPT = 8;                           // steps per thread
-constexpr int SQ_TILE = SQ_THREADS * SQ_VPT;        // 2048 steps
-constexpr int SQ_STAGES = 2;
 constexpr int SQ_CTAS_PER_SM = 3;
-constexpr int SQ_STAGE_FLOATS = 4 * SQ_TILE;
-static_assert(SQ_TILE == MB_TILE, "both kernels count tiles of the same length");
-static_assert((SQ_VPT & (SQ_VPT - 1)) == 0 && SQ_VPT % 4 == 0, "tree composition of float4 groups");
+static_assert(mob::Walk<SQ_THREADS>::TILE == MB_TILE, "both kernels count tiles of the same length");
 
-__host__ __device__ constexpr int sq_smem_bytes() { return SQ_STAGES * SQ_STAGE_FLOATS * 4 + SQ_STAGES * 8; }
+__host__ __device__ constexpr int sq_smem_bytes() { return mob::Walk<SQ_THREADS>::SMEM; }
 
 __global__ void __launch_bounds__(SQ_THREADS, SQ_CTAS_PER_SM)
 mobius_seq_kernel(const float* __restrict__ A, const float* __restrict__ B,
@@ -281,138 +234,8 @@ mobius_seq_kernel(const float* __restrict__ A, const float* __restrict__ B,
                   const float* __restrict__ lambda0, float* __restrict__ out, long long N,
                   long long T, int tiles_per_seq, long long wait_ns) {
     extern __shared__ __align__(128) unsigned char smem[];
-    float* buf = reinterpret_cast<float*>(smem);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SQ_STAGES * SQ_STAGE_FLOATS * 4);
-    __shared__ Mat s_warp[2][SQ_WARPS];
-    __shared__ float s_lam[2];
-    __shared__ int s_abort;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long G = gridDim.x;
-    const long long nseq = blockIdx.x < N ? (N - 1 - blockIdx.x) / G + 1 : 0;
-    const long long ntiles = nseq * tiles_per_seq;
-
-    // producer state (thread 0): next stream tile to issue
-    long long iss_i = 0, iss_seq = blockIdx.x;
-    int iss_part = 0, iss_st = 0;
-    auto issue_next = [&]() {
-        const long long t0 = static_cast<long long>(iss_part) * SQ_TILE;
-        const long long n = min(static_cast<long long>(SQ_TILE), T - t0);
-        const uint32_t bytes = static_cast<uint32_t>(n * 4);
-        const long long off = iss_seq * T + t0;
-        float* dst = buf + iss_st * SQ_STAGE_FLOATS;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&full[iss_st], 4 * bytes);
-        bulk_g2s(dst, A + off, bytes, &full[iss_st]);
-        bulk_g2s(dst + SQ_TILE, B + off, bytes, &full[iss_st]);
-        bulk_g2s(dst + 2 * SQ_TILE, C + off, bytes, &full[iss_st]);
-        bulk_g2s(dst + 3 * SQ_TILE, D + off, bytes, &full[iss_st]);
-        ++iss_i;
-        if (++iss_part == tiles_per_seq) { iss_part = 0; iss_seq += G; }
-        if (++iss_st == SQ_STAGES) iss_st = 0;
-    };
-
-    if (tid == 0) {
-        for (int st = 0; st < SQ_STAGES; ++st) mbar_init(&full[st], 1);
-        mbar_init_fence();
-        while (iss_i < SQ_STAGES && iss_i < ntiles) issue_next();
-        s_abort = 0;
-    }
-    __syncthreads();
-
-    long long seq = blockIdx.x;
-    int part = 0, st = 0;
-    uint32_t phase = 0;
-    long long i = 0;
-    for (; i < ntiles; ++i) {
-        const int par = static_cast<int>(i & 1);
-        if (!mbar_wait(&full[st], phase, wait_ns)) {
-            record_error(&g_mobius_error, KDN_ERR_TIMEOUT);
-            s_abort = 1;
-        }
-        const long long t_first = static_cast<long long>(part) * SQ_TILE + tid * SQ_VPT;
-        const int nvalid = static_cast<int>(max(0LL, min(static_cast<long long>(SQ_VPT), T - t_first)));
-
-        // ---- 1. this thread's 16 steps from shared memory ----------------
-        Mat m[SQ_VPT];
-        {
-            const float* sb = buf + st * SQ_STAGE_FLOATS + tid * SQ_VPT;
-#pragma unroll
-            for (int h = 0; h < SQ_VPT / 4; ++h) {
-                const float4 x = *reinterpret_cast<const float4*>(sb + 4 * h);
-                const float4 y = *reinterpret_cast<const float4*>(sb + SQ_TILE + 4 * h);
-                const float4 z = *reinterpret_cast<const float4*>(sb + 2 * SQ_TILE + 4 * h);
-                const float4 w = *reinterpret_cast<const float4*>(sb + 3 * SQ_TILE + 4 * h);
-                m[4 * h + 0] = {x.x, y.x, z.x, w.x};
-                m[4 * h + 1] = {x.y, y.y, z.y, w.y};
-                m[4 * h + 2] = {x.z, y.z, z.z, w.z};
-                m[4 * h + 3] = {x.w, y.w, z.w, w.w};
-            }
-#pragma unroll
-            for (int s2 = 0; s2 < SQ_VPT; ++s2)
-                if (s2 >= nvalid) m[s2] = identity();   // past the end of the sequence
-        }
-        __syncthreads();   // stage consumed: refill it with the next stream tile
-        // s_abort is only set during the waits above (before this barrier) or
-        // in the next tile's waits (after the barrier below): all threads read
-        // the same value here
-        if (s_abort) break;
-        if (tid == 0 && iss_i < ntiles) issue_next();
-        // lambda at the start of the tile: lambda_0 for the first tile of a
-        // sequence, else the last output of the previous tile (written after
-        // the previous tile's second barrier)
-        const float lam_start = part == 0 ? __ldg(lambda0 + seq) : s_lam[par];
-
-        // ---- 2. compose (balanced tree, later steps on the left) and scan --
-        Mat tree[SQ_VPT];
-#pragma unroll
-        for (int k = 0; k < SQ_VPT; ++k) tree[k] = m[k];
-#pragma unroll
-        for (int w = SQ_VPT; w > 1; w /= 2)
-#pragma unroll
-            for (int k = 0; k < w / 2; ++k) tree[k] = normalize(mul(tree[2 * k + 1], tree[2 * k]));
-        Mat P = tree[0];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const Mat Q = shfl_up(P, off);
-            if (lane >= off) P = normalize(mul(P, Q));
-        }
-        Mat lane_excl = shfl_up(P, 1);
-        if (lane == 0) lane_excl = identity();
-        if (lane == 31) s_warp[par][warp] = P;
-        __syncthreads();
-        Mat warp_excl = identity();
-        for (int w = 0; w < warp; ++w) warp_excl = normalize(mul(s_warp[par][w], warp_excl));
-        const Mat thread_excl = normalize(mul(lane_excl, warp_excl));
-
-        // ---- 3. outputs ------------------------------------------------------
-        float lam = apply(thread_excl, lam_start);
-        float res[SQ_VPT];
-#pragma unroll
-        for (int s2 = 0; s2 < SQ_VPT; ++s2) {
-            lam = __fdividef(fmaf(m[s2].a, lam, m[s2].b), fmaf(m[s2].c, lam, m[s2].d));
-            res[s2] = lam;
-        }
-        if (tid == SQ_THREADS - 1) s_lam[par ^ 1] = lam;   // carry (unused after a sequence's last tile)
-        float* po = out + seq * T + t_first;
-        if (nvalid == SQ_VPT) {
-#pragma unroll
-            for (int h = 0; h < SQ_VPT / 4; ++h)
-                __stcs(reinterpret_cast<float4*>(po) + h,
-                       make_float4(res[4 * h], res[4 * h + 1], res[4 * h + 2], res[4 * h + 3]));
-        } else {
-#pragma unroll
-            for (int s2 = 0; s2 < SQ_VPT; ++s2)
-                if (s2 < nvalid) __stcs(po + s2, res[s2]);
-        }
-        if (++part == tiles_per_seq) { part = 0; seq += G; }
-        if (++st == SQ_STAGES) { st = 0; phase ^= 1u; }
-    }
-    // after an abort, wait (bounded) for the copies still in flight into this CTA
-    if (s_abort && tid == 0) {
-        for (long long k = i; k < iss_i; ++k)
-            mbar_wait(&full[k % SQ_STAGES], static_cast<uint32_t>((k / SQ_STAGES) & 1), wait_ns);
-    }
+    mob::mobius_walk<SQ_THREADS>(A, B, C, D, lambda0, out, N, T, tiles_per_seq, blockIdx.x, gridDim.x,
+                                 wait_ns, smem, &g_mobius_error);
 }
 
 template <bool VEC, bool LB>

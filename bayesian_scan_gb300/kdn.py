@@ -8,6 +8,7 @@ import of this module raises.
 Functions mirror the C names:
 
 * :func:`diag_scan_fwd`  -> ``kdn_diag_scan_fwd``
+* :func:`diag_mobius_scan_fwd` -> ``kdn_diag_mobius_scan_fwd`` (per-head lambda in the same launch)
 * :func:`mobius_scan`    -> ``kdn_mobius_scan``
 * :func:`mobius_scan_noalloc` -> ``kdn_mobius_scan_noalloc``
 * :func:`diag_scan_plan`, :func:`mobius_scan_plan` -> the ``*_plan`` queries
@@ -51,6 +52,9 @@ def _load():
                                       i, i, i, i, i, i, vp]
     lib.kdn_mobius_scan.restype = i
     lib.kdn_mobius_scan.argtypes = [fp, fp, fp, fp, fp, fp, ll, ll, vp]
+    lib.kdn_diag_mobius_scan_fwd.restype = i
+    lib.kdn_diag_mobius_scan_fwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp, fp,
+                                             fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
     lib.kdn_lin_scan_fwd.restype = i
     lib.kdn_lin_scan_fwd.argtypes = [vp, vp, vp, vp, vp, fp, ctypes.c_float, fp, fp, fp,
                                      i, i, i, i, i, i, vp]
@@ -115,6 +119,22 @@ def _check(t, name, dtype=None, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _on_one_device(stream, **tensors):
+    """Every given tensor must be a CUDA tensor on the current device (the
+    device whose stream the call is issued on): the C ABI receives raw
+    pointers and cannot tell host memory or another GPU's memory apart."""
+    given = [(name, t) for name, t in tensors.items() if t is not None]
+    for name, t in given:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the call takes device tensors)")
+    cur = torch.device("cuda", torch.cuda.current_device())
+    for name, t in given:
+        if t.device != cur:
+            raise ValueError(f"{name} is on {t.device} but the current device is {cur}")
+    if stream is not None and getattr(stream, "device", cur) != cur:
+        raise ValueError(f"the stream belongs to {stream.device}, not the current device {cur}")
+
+
 def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
                   final_state=True, stream=None):
     """Diagonal metaplastic scan with readout (see ``kdn_diag_scan_fwd``).
@@ -151,6 +171,8 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
         final_state = None
     if final_state is not None:
         _check(final_state, "final_state", torch.float32, (2, B, H, dv, dk))
+    _on_one_device(stream, q=q, k=k, v=v, beta=beta, d=d, A=A, I0=I0, mu0=mu0, out=out,
+                   final_state=final_state)
     st = lib.kdn_diag_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
                                float(I_prior), _ptr(I0), _ptr(mu0), _ptr(out), _ptr(final_state),
                                B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
@@ -158,6 +180,56 @@ def diag_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, I0=None, mu0=None, out=None,
     if st != KDN_OK:
         raise KdnError(st, "kdn_diag_scan_fwd")
     return out, final_state
+
+
+def diag_mobius_scan_fwd(q, k, v, beta, d, A, ma, mb, mc, md, lambda0, I_prior=1.0, I0=None,
+                         mu0=None, out=None, final_state=True, lambda_out=None, stream=None):
+    """The diagonal scan and the per-head Moebius scan in one launch (see
+    ``kdn_diag_mobius_scan_fwd``).  Diagonal-scan arguments as for
+    ``diag_scan_fwd`` (device tensors); ma, mb, mc, md [B*H,T] fp32 (row b*H +
+    h), lambda0 [B*H] fp32.  Returns (out, final_state or None, lambda
+    [B*H,T])."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("inputs must be bf16 or fp32")
+    _check(q, "q", dt)
+    _check(k, "k", dt, (B, H, T, dk))
+    _check(v, "v", dt, (B, H, T, dv))
+    _check(beta, "beta", dt, (B, H, T, dv))
+    _check(d, "d", dt, (B, H, T))
+    _check(A, "A", torch.float32, (H,))
+    for name, t in (("I0", I0), ("mu0", mu0)):
+        if t is not None:
+            _check(t, name, torch.float32, (B, H, dv, dk))
+    for name, t in (("ma", ma), ("mb", mb), ("mc", mc), ("md", md)):
+        _check(t, name, torch.float32, (B * H, T))
+    _check(lambda0, "lambda0", torch.float32, (B * H,))
+    _on_one_device(stream, q=q)
+    if out is None:
+        out = torch.empty(B, H, T, dv, device=q.device, dtype=torch.float32)
+    _check(out, "out", torch.float32, (B, H, T, dv))
+    if final_state is True:
+        final_state = torch.empty(2, B, H, dv, dk, device=q.device, dtype=torch.float32)
+    elif final_state is False:
+        final_state = None
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32, (2, B, H, dv, dk))
+    if lambda_out is None:
+        lambda_out = torch.empty(B * H, T, device=q.device, dtype=torch.float32)
+    _check(lambda_out, "lambda_out", torch.float32, (B * H, T))
+    _on_one_device(stream, q=q, k=k, v=v, beta=beta, d=d, A=A, I0=I0, mu0=mu0, out=out,
+                   final_state=final_state, ma=ma, mb=mb, mc=mc, md=md, lambda0=lambda0,
+                   lambda_out=lambda_out)
+    st = lib.kdn_diag_mobius_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
+                                      float(I_prior), _ptr(I0), _ptr(mu0), _ptr(out),
+                                      _ptr(final_state), _ptr(ma), _ptr(mb), _ptr(mc), _ptr(md),
+                                      _ptr(lambda0), _ptr(lambda_out), B, H, T, dk, dv,
+                                      KDN_BF16 if dt == torch.bfloat16 else KDN_F32, _stream(stream))
+    if st != KDN_OK:
+        raise KdnError(st, "kdn_diag_mobius_scan_fwd")
+    return out, final_state, lambda_out
 
 
 def lin_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, mu0=None, out=None, final_mu=True,
@@ -190,6 +262,7 @@ def lin_scan_fwd(q, k, v, beta, d, A, I_prior=1.0, mu0=None, out=None, final_mu=
         final_mu = None
     if final_mu is not None:
         _check(final_mu, "final_mu", torch.float32, (B, H, dv, dk))
+    _on_one_device(stream, q=q, k=k, v=v, beta=beta, d=d, A=A, mu0=mu0, out=out, final_mu=final_mu)
     st = lib.kdn_lin_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
                               float(I_prior), _ptr(mu0), _ptr(out), _ptr(final_mu),
                               B, H, T, dk, dv, KDN_BF16 if dt == torch.bfloat16 else KDN_F32,
@@ -255,6 +328,9 @@ def diag_scan_bwd(q, k, v, beta, d, A, grad_out, I_prior=1.0, I0=None, mu0=None,
         workspace = torch.empty(max(ws_bytes, 1), device=q.device, dtype=torch.uint8)
     elif workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError(f"workspace must hold {ws_bytes} bytes")
+    _on_one_device(stream, q=q, k=k, v=v, beta=beta, d=d, A=A, I0=I0, mu0=mu0, grad_out=grad_out,
+                   grad_final_state=grad_final_state, grad_init_state=grad_init_state,
+                   workspace=workspace)
     st = lib.kdn_diag_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A),
                                float(I_prior), _ptr(I0), _ptr(mu0), _ptr(grad_out),
                                _ptr(grad_final_state), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]),
@@ -286,6 +362,7 @@ def diag_step(q, k, v, beta, d, A, state, I_prior=1.0, out=None, stream=None):
     if out is None:
         out = torch.empty(B, H, dv, device=q.device, dtype=torch.float32)
     _check(out, "out", torch.float32, (B, H, dv))
+    _on_one_device(stream, q=q, k=k, v=v, beta=beta, d=d, A=A, state=state, out=out)
     st = lib.kdn_diag_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d), _ptr(A), float(I_prior),
                            _ptr(state), _ptr(out), B, H, dk, dv,
                            KDN_BF16 if dt == torch.bfloat16 else KDN_F32, _stream(stream))
@@ -307,6 +384,7 @@ def mobius_scan(a, b, c, d, lambda0, out=None, stream=None):
     if out is None:
         out = torch.empty(N, T, device=a.device, dtype=torch.float32)
     _check(out, "out", torch.float32, (N, T))
+    _on_one_device(stream, a=a, b=b, c=c, d=d, lambda0=lambda0, out=out)
     st = lib.kdn_mobius_scan(_ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(lambda0), _ptr(out),
                              N, T, _stream(stream))
     if st != KDN_OK:
@@ -346,6 +424,7 @@ def mobius_scan_noalloc(a, b, c, d, lambda0, out, stream=None):
     for name, t in (("a", a), ("b", b), ("c", c), ("d", d), ("out", out)):
         _check(t, name, torch.float32, (N, T))
     _check(lambda0, "lambda0", torch.float32, (N,))
+    _on_one_device(stream, a=a, b=b, c=c, d=d, lambda0=lambda0, out=out)
     st = lib.kdn_mobius_scan_noalloc(_ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(lambda0), _ptr(out),
                                      N, T, _stream(stream))
     if st != KDN_OK:

@@ -75,6 +75,10 @@ WORKLOADS = {
     # standalone Moebius scan over 4096 sequences of 16384 steps
     "longctx": Workload("longctx", 1, 16, 65536, 128, 128, torch.bfloat16,
                         ("uniform", 0.1, 1.0), 4096, 16384, False, 1004),
+    # the 1.3B-shaped layer's heads over 1024 tokens: one wave of the d=64
+    # kernel (inputs still larger than L2), for profiling captures
+    "layer1p3b_t1024": Workload("layer1p3b_t1024", 16, 32, 1024, 64, 64, torch.bfloat16,
+                                ("uniform", 0.5, 4.0), 512, 1024, True, 1008),
 }
 # batched decoding (one token per head per step on a device-resident state):
 # 128 x 16 heads of d=128, whose 268 MB state is twice the 129 MB L2; 32

@@ -1,12 +1,14 @@
 #!/usr/bin/env python
 """Throughput of the uncertainty-tracked linear-attention scan hot path.
 
-One step = one pass of the whole path over one batch of synthetic input: the
-diagonal metaplastic scan with readout (kdn_diag_scan_fwd) followed by the
-Moebius precision scan (kdn_mobius_scan) of the same workload, both through
-the C-ABI binding, inputs resident in HBM.  The default workload is the
-750M-shaped layer (B=8, H=16, T=4096, d_k=d_v=128, bf16 inputs, fp32 state,
-one lambda sequence per head).
+One step = one pass of the whole path over one batch of synthetic input,
+inputs resident in HBM, through the C-ABI binding.  The default workload is
+the long context (B=1, H=16, T=65536, d_k=d_v=128, bf16 inputs, fp32 state):
+one kdn_diag_scan_fwd plus the standalone Moebius scan over 4096 sequences x
+16384 steps (kdn_mobius_scan).  The same line carries, under "workloads", the
+750M-shaped layer (8x16 heads, d=128, T=4096) and the 1.3B-shaped layer
+(16x32 heads, d=64, T=4096), each timed the same way with one lambda sequence
+per head computed in the scan's own launch (kdn_diag_mobius_scan_fwd).
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch
 of the same shape on its own GPU (heads are independent: no data-path
@@ -20,7 +22,9 @@ collective; weak scaling); the timing is the max over ranks.
     python bench.py --workload decode2k        # batched one-token decoding
     python bench.py --workload layer750m_lin   # the non-metaplastic limit; also
                                                # longctx_lin, heads128_t512_lin
-    python bench.py --workload layer1p3b       # or longctx: the other scan shapes
+    python bench.py --workload layer750m       # or layer1p3b, heads32_t2048_d64:
+                                               # one scan workload (--no-extra: no
+                                               # other workloads in the line)
 
 Metric: scan tokens/s = B*H*T token-heads per second of the whole step.
 Roofline of the dominant kernel (the diagonal scan): FP32 ALU bound,
@@ -46,6 +50,8 @@ SM_MAX_MHZ_FALLBACK = 2070.0     # maximum SM clock of GB300
 HBM_GBS_FALLBACK = 6800.0
 DIAG_FLOP_PER_ELEMENT_TOKEN = 10
 MOBIUS_BYTES_PER_STEP = 20
+# scan workloads whose numbers the default line carries besides its own
+EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # dram__bytes_read.sum + dram__bytes_write.sum of one kdn_diag_scan_fwd call
 # (all its kernels: tensor-core aggregates, carry, full pass) per workload,
 # from the ncu capture of the current kernels summarised in profiles/
@@ -60,7 +66,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="layer750m")
+    ap.add_argument("--workload", default="longctx")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --workload (by default the scan workloads' line also "
+                         "carries the 750M- and 1.3B-shaped layers)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -279,13 +288,17 @@ def workload_config(w):
 # ----------------------------------------------------------------------------
 # our arm
 
-def run_ours(args, w, dist):
+def scan_numbers(args, w, dist, dev, K):
+    """Times K steps of one scan workload on this rank (inputs resident in
+    HBM, CUDA events on the launching stream, barrier + synchronize on both
+    sides) and returns its numbers.  A step is one kdn_diag_mobius_scan_fwd
+    call when the workload's lambda runs per head (the scan and lambda in one
+    launch), else one kdn_diag_scan_fwd plus one kdn_mobius_scan of the
+    standalone sequences."""
     import torch
 
     from bayesian_scan_gb300 import kdn, workloads
 
-    dev = torch.device("cuda", dist.local_rank)
-    torch.cuda.set_device(dev)
     # every rank draws its own batch of the same shape (weak scaling)
     w_rank = w if dist.rank == 0 else type(w)(**{**w.__dict__, "seed": w.seed + 7919 * dist.rank})
     host = workloads.make(w_rank)
@@ -297,13 +310,19 @@ def run_ours(args, w, dist):
     fs_buf = torch.empty(2, B, H, dv, dk, device=dev)
     lam_buf = torch.empty(w.mobius_N, w.mobius_T, device=dev)
     stream = torch.cuda.current_stream(dev)
+    fused = w.mobius_fused
 
     def diag():
-        kdn.diag_scan_fwd(*(x[n] for n in names), I_prior=w.I_prior, out=o_buf,
-                          final_state=fs_buf, stream=stream)
+        if fused:
+            kdn.diag_mobius_scan_fwd(*(x[n] for n in names + mnames), I_prior=w.I_prior, out=o_buf,
+                                     final_state=fs_buf, lambda_out=lam_buf, stream=stream)
+        else:
+            kdn.diag_scan_fwd(*(x[n] for n in names), I_prior=w.I_prior, out=o_buf,
+                              final_state=fs_buf, stream=stream)
 
     def mobius():
-        kdn.mobius_scan(*(x[n] for n in mnames), out=lam_buf, stream=stream)
+        if not fused:
+            kdn.mobius_scan(*(x[n] for n in mnames), out=lam_buf, stream=stream)
 
     plan = kdn.diag_scan_plan(B, H, T, dk, dv, w.dtype)
     mplan = kdn.mobius_scan_plan(w.mobius_N, w.mobius_T)
@@ -315,7 +334,6 @@ def run_ours(args, w, dist):
     if st != 0:
         raise RuntimeError(f"device error after warm-up: {kdn.status_string(st)}")
 
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -341,7 +359,6 @@ def run_ours(args, w, dist):
     mob_ms = sum(b.elapsed_time(c) for _, b, c in ev) / K
     max_ms = dist.max(total_ms)
     tokens = B * H * T
-    value = dist.world * tokens * K / (max_ms / 1e3)
 
     peaks = measured_peaks()
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -351,26 +368,57 @@ def run_ours(args, w, dist):
     achieved = flop / (diag_ms / 1e3) / 1e12
     hbm_peak = float(peaks.get("hbm_gbs", HBM_GBS_FALLBACK))
     mbytes = MOBIUS_BYTES_PER_STEP * w.mobius_N * w.mobius_T
-    mob_gbs = mbytes / (mob_ms / 1e3) / 1e9
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w),
-        "roofline": {"kernel": "diag_scan_kernel (whole kdn_diag_scan_fwd call)", "bound": "alu",
-                     "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak, "traffic": DIAG_TRAFFIC_BYTES.get(w.name),
-                     "peak_source": f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz"
-                                    " (recipe unit counts and max SM clock)",
+    peak_src = f"{nsm} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz (recipe unit counts and max SM clock)"
+    kernel = ("diag_scan_kernel with the per-head lambda walkers (whole kdn_diag_mobius_scan_fwd call)"
+              if fused else "diag_scan_kernel (whole kdn_diag_scan_fwd call)")
+    res = {
+        "value": dist.world * tokens * K / (max_ms / 1e3), "ms_per_step": max_ms / K,
+        "roofline": {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": alu_peak,
+                     "unit": "TFLOP/s", "frac": achieved / alu_peak,
+                     "traffic": DIAG_TRAFFIC_BYTES.get(w.name), "peak_source": peak_src,
                      "ms_per_call": diag_ms, "token_parts": plan["parts"]},
-        "mobius_roofline": {"bound": "hbm", "achieved": mob_gbs, "peak": hbm_peak, "unit": "GB/s",
-                            "frac": mob_gbs / hbm_peak, "ms_per_call": mob_ms,
-                            "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
-        "gpu_launches": K * (plan["kernels"] + mplan["kernels"]),
+        "gpu_launches": K * (plan["kernels"] + (0 if fused else mplan["kernels"])),
         "clocks": sampler.summary(),
     }
+    if fused:
+        # lambda graded inside the scan's launch: the launch's roofline time is
+        # max(FLOP / FP32 peak, all its bytes / HBM peak), its bytes the scan's
+        # plus lambda's 20 per step
+        es = 2 if w.dtype == torch.bfloat16 else 4
+        scan_bytes = tokens * ((2 * dk + 2 * dv + 1) * es + 4 * dv) + 2 * B * H * dv * dk * 4
+        t_roof = max(flop / (alu_peak * 1e12), (scan_bytes + mbytes) / (hbm_peak * 1e9))
+        res["mobius_roofline"] = {
+            "fused": True, "bound": "alu (lambda runs inside the scan launch)",
+            "lambda_bytes": mbytes, "launch_bytes": scan_bytes + mbytes,
+            "roofline_ms": t_roof * 1e3, "frac": t_roof / (diag_ms / 1e3), "ms_per_call": diag_ms,
+            "peak_source": ("measured" if "hbm_gbs" in peaks else "fallback") + " HBM; FP32 as roofline"}
+    else:
+        mob_gbs = mbytes / (mob_ms / 1e3) / 1e9
+        res["mobius_roofline"] = {"bound": "hbm", "achieved": mob_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": mob_gbs / hbm_peak, "ms_per_call": mob_ms,
+                                  "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+    del x, o_buf, fs_buf, lam_buf
+    return res, host
 
+
+def run_ours(args, w, dist):
+    import torch
+
+    from bayesian_scan_gb300 import workloads
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    K = args.steps
+    res, host = scan_numbers(args, w, dist, dev, K)
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": res["roofline"], "mobius_roofline": res["mobius_roofline"],
+        "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+    }
     if not args.no_e2e:
         line["e2e"] = measure_e2e(args, w, host, dev, dist)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -380,6 +428,18 @@ def run_ours(args, w, dist):
             "value": units / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n_heads} heads x {t_tokens} tokens of the same inputs (all "
                       f"{dv}x{dk} state rows) + their Moebius steps, fp64 oracle, {dt:.1f} s"}
+    del host
+    # the other layer configurations of the same metric, timed the same way
+    # in the same run (a step each: one fused scan + lambda launch)
+    extra = [] if args.no_extra else [n for n in EXTRA_WORKLOADS if n != w.name]
+    if extra:
+        line["workloads"] = {}
+        for name in extra:
+            we = workloads.get(name)
+            torch.cuda.empty_cache()
+            r, _ = scan_numbers(args, we, dist, dev, K)
+            r["config"] = workload_config(we)
+            line["workloads"][name] = r
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -100,6 +100,37 @@ KDN_API kdn_status kdn_diag_scan_fwd(const void* q, const void* k, const void* v
                              kdn_dtype in_dtype, void* stream);
 
 /*
+ * kdn_diag_mobius_scan_fwd -- kdn_diag_scan_fwd and, in the same launch, the
+ * per-head precision recursion of "Kalman Linear Attention (KLA)",
+ * Metodologia 2 ("Parallelizzazione tramite Trasformazioni di Moebius"):
+ * one lambda sequence per head over the same T tokens,
+ *     lambda_t = (a_t lambda_{t-1} + b_t) / (c_t lambda_{t-1} + d_t).
+ *
+ *   q ... final_state   as for kdn_diag_scan_fwd
+ *   ma, mb, mc, md  [B*H, T] fp32   the coefficients a, b, c, d of each head
+ *                   (row b*H + h)
+ *   lambda0         [B*H]    fp32   lambda_0 of each head
+ *   lambda_out      [B*H, T] fp32   lambda_1 .. lambda_T of each head
+ *   Sizes and errors as for kdn_diag_scan_fwd; the Moebius pointers must be
+ *   4-byte aligned and are required when T > 0.
+ *
+ * When T % 4 == 0 and ma, mb, mc, md, lambda_out are 16-byte aligned, the
+ * lambda sequences are walked by extra CTAs of the diagonal scan's full-pass
+ * grid, placed after the scan's CTAs so that they fill the CTA slots its last
+ * wave leaves free; otherwise the Moebius scan runs as its own launch after
+ * the scan (same results, same stream).  lambda equals kdn_mobius_scan on the
+ * same coefficients (the same tile composition and sequential evaluation).
+ */
+KDN_API kdn_status kdn_diag_mobius_scan_fwd(const void* q, const void* k, const void* v,
+                                    const void* beta, const void* d, const float* A,
+                                    float I_prior, const float* I0, const float* mu0,
+                                    float* out, float* final_state,
+                                    const float* ma, const float* mb, const float* mc,
+                                    const float* md, const float* lambda0, float* lambda_out,
+                                    int B, int H, int T, int dk, int dv,
+                                    kdn_dtype in_dtype, void* stream);
+
+/*
  * kdn_lin_scan_fwd -- the non-metaplastic limit of kdn_diag_scan_fwd: the
  * importance is held at I_prior ("Learning to Remember, Learn, and Forget in
  * Attention-Based Models", Metodologia 4, Unificazione Teorica: Mamba2 is the
@@ -302,10 +333,15 @@ KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
  * Same arguments, layouts and results as kdn_mobius_scan.  The look-back
  * scratch lives in a fixed 1 MiB array inside the library's device image,
  * which every GPU that loads the library holds until the process exits; no
- * cudaMalloc/cudaMallocAsync/cudaFree is called.  Limit: when kdn_mobius_scan
- * would take scratch (its plan reports scratch_bytes > 0), N * ceil(T / 2048)
- * may be at most 43690; larger calls return KDN_ERR_INVALID_ARG without
- * launching.  Calls that kdn_mobius_scan runs without scratch have no limit.
+ * cudaMalloc/cudaMallocAsync/cudaFree is called.  Limit: a call that needs
+ * look-back scratch may use at most 43690 tiles, N * ceil(T / 2048) <= 43690;
+ * larger calls return KDN_ERR_INVALID_ARG without launching.  A call needs
+ * look-back scratch when T > 2048 and the sequence-walk kernel does not take
+ * it: that kernel needs T % 4 == 0 and a, b, c, d, out 16-byte aligned (an
+ * offset view of a larger tensor may not be), and it is chosen when the
+ * sequences fill the GPU or a cost model prefers it.  kdn_mobius_scan_plan
+ * assumes aligned pointers: scratch_bytes > 0 there means the limit applies;
+ * scratch_bytes == 0 means it does not, provided the pointers are aligned.
  * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one array: calls whose executions overlap on the GPU

@@ -78,6 +78,31 @@ def test_diag_rejects(lib, kw, status):
     assert _diag(lib, **kw) == status
 
 
+def _fused(lib, ma=FAKE, mb=FAKE, mc=FAKE, md=FAKE, l0=FAKE, lout=FAKE, **kw):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, d=FAKE, A=FAKE, I0=None, mu0=None, out=FAKE,
+             fs=None, B=1, H=1, T=8, dk=16, dv=16, dtype=1)
+    a.update(kw)
+    return lib.kdn_diag_mobius_scan_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["beta"]), vp(a["d"]),
+                                        vp(a["A"]), 1.0, vp(a["I0"]), vp(a["mu0"]), vp(a["out"]),
+                                        vp(a["fs"]), vp(ma), vp(mb), vp(mc), vp(md), vp(l0), vp(lout),
+                                        a["B"], a["H"], a["T"], a["dk"], a["dv"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("field", ["ma", "mb", "mc", "md", "l0", "lout"])
+def test_fused_null_moebius_pointer(lib, field):
+    assert _fused(lib, **{field: None}) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(B=0), -1), (dict(dk=8), -2), (dict(dtype=3), -2),
+    (dict(ma=FAKE + 2), -1), (dict(lout=FAKE + 1), -1), (dict(l0=FAKE + 3), -1),
+    (dict(q=FAKE + 8), -1),
+])
+def test_fused_rejects(lib, kw, status):
+    assert _fused(lib, **kw) == status
+
+
 def _mob(lib, a=FAKE, b=FAKE, c=FAKE, d=FAKE, l0=FAKE, out=FAKE, N=4, T=16):
     vp = lambda x: None if x is None else ctypes.c_void_p(x)
     return lib.kdn_mobius_scan(vp(a), vp(b), vp(c), vp(d), vp(l0), vp(out), N, T, None)

@@ -80,3 +80,30 @@ def test_bwd_workspace_query(kdn):
         kdn.diag_scan_bwd_workspace(1, 1, 8, 24, 16)
     with pytest.raises(kdn.KdnError):
         kdn.diag_scan_bwd_workspace(0, 1, 8, 16, 16)
+
+
+def test_device_entry_points_reject_host_operands(kdn):
+    """Every operand of a device call is checked, not only the first: a host
+    tensor among them is refused before the C ABI sees its pointer.  (On a
+    machine without a GPU the first operand stands in for a device tensor
+    with a meta tensor, which passes the first check and fails the second.)"""
+    a = torch.ones(4, 8)
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        kdn.mobius_scan_noalloc(a, a, a, a, torch.ones(4), torch.empty(4, 8))
+    x = diag_inputs()
+    args = [x[n] for n in ("q", "k", "v", "beta", "d", "A")]
+    gout = torch.zeros(2, 3, 5, 16)
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        kdn._on_one_device(None, q=args[0], gout=gout)
+
+
+def test_mixed_host_and_device_operands_are_refused(kdn):
+    """A call whose first operand is on the device but another one is not
+    (here the device operand is a meta tensor, so no GPU is needed: it fails
+    the device check the same way a CUDA tensor on another device would)."""
+    dev_like = torch.empty(4, 8, device="meta")
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        kdn._on_one_device(None, a=torch.ones(4, 8), b=dev_like)
+    host = torch.ones(4, 8)
+    with pytest.raises(ValueError, match="lambda0 must be a CUDA tensor"):
+        kdn._on_one_device(None, lambda0=host)
