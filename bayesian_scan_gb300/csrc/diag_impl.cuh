@@ -783,7 +783,7 @@ cudaError_t prepare(int dev, int smem, int* occ) {
 }
 
 // Whether the metaplastic full pass may take the warp-specialised kernel.
-constexpr bool kWsFullPass = false;
+constexpr bool kWsFullPass = true;
 
 // Whether a split call's aggregate pass runs on the tensor cores.
 template <int DK, typename TIn>
@@ -812,12 +812,12 @@ struct Plan {
 // into its shared memory and checks that it was built with the launch
 // register allocation its setmaxnreg split assumes (else the split could
 // wait forever: the caller then keeps the CUDA-core kernel).
-template <int DK, typename TIn>
+template <int DK, typename TIn, int TC>
 cudaError_t ws_prepare(int dev, int smem, bool* usable) {
     static int smem_set[64] = {};
     static int regs_ok[64] = {};   // 0 unknown, 1 yes, 2 no
     if (dev < 0 || dev >= 64) dev = 0;
-    auto kern = diag_ws_kernel<DK, TIn>;
+    auto kern = diag_ws_kernel<DK, TIn, TC>;
     if (regs_ok[dev] == 0) {
         cudaFuncAttributes fa;
         const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -870,7 +870,8 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
             const int smem_ws = std::max(ws_smem_bytes<DK>(dv, ES, tcw), mob::Walk<WS_THREADS>::SMEM);
             bool usable = false;
             if (tcw >= 8 && smem_ws <= 227 * 1024) {
-                e = ws_prepare<DK, TIn>(dev, smem_ws, &usable);
+                e = tcw == 16 ? ws_prepare<DK, TIn, 16>(dev, smem_ws, &usable)
+                              : ws_prepare<DK, TIn, 8>(dev, smem_ws, &usable);
                 if (e != cudaSuccess) return from_cuda(e);
             }
             if (usable) {
@@ -1057,7 +1058,10 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         if constexpr (!LIN && (DK == 64 || DK == 128)) {
             if (pl.ws) {
                 // launch_smem == pl.smem_full: the walkers' stages fit it (plan_dk)
-                diag_ws_kernel<DK, TIn><<<grid, WS_THREADS, launch_smem, st>>>(prm);
+                if (pl.TC_full == 16)
+                    diag_ws_kernel<DK, TIn, 16><<<grid, WS_THREADS, launch_smem, st>>>(prm);
+                else
+                    diag_ws_kernel<DK, TIn, 8><<<grid, WS_THREADS, launch_smem, st>>>(prm);
                 e = cudaGetLastError();
                 launched = true;
             }

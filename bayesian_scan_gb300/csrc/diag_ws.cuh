@@ -23,11 +23,13 @@
 //   raw_full[3]   bulk copies of a chunk landed          (tx count)
 //   par_full[2]   a chunk's converted inputs and scalars  (128 producer threads)
 //   par_empty[2]  consumers finished a chunk              (256 consumer threads)
-//   red_full[2]   8 tokens of row partials written        (256 consumer threads)
-//   red_empty[2]  those partials summed and stored        (128 producer threads)
+//   red_full[n]   8 tokens of row partials written        (256 consumer threads)
+//   red_empty[n]  those partials summed and stored        (128 producer threads)
 // The producers prepare chunk c + 2 and issue the copies of chunk c + 3 as
 // soon as the consumers release chunk c, so the consumers never wait on them
-// in steady state; row partials are double-buffered in groups of 8 tokens.
+// in steady state.  Row partials go to n = TC / 8 + 1 buffers of 8 tokens;
+// consumers wait for a buffer at the start of a chunk, never in the token
+// loop (its registers hold the state and the token's operands only).
 //
 // A CTA owns ROWS = 8 * rows-per-warp consecutive state rows (128 for
 // d_k = 128, 256 for d_k = 64: whole heads, ROWS / d_v of them) for one
@@ -50,6 +52,11 @@ static_assert(WS_CW * 32 * WS_CREG + WS_PW * 32 * WS_PREG <= WS_THREADS * WS_LAU
 constexpr int WS_RAW = 3;                        // raw chunk stages
 constexpr int WS_PAR = 2;                        // converted chunk stages
 constexpr int WS_RB = 8;                         // tokens per reduction buffer
+// Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
+// previous flush at the start of a chunk (never inside the token loop), so
+// the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
+// previous chunk's last group to overlap the next chunk.
+__host__ __device__ constexpr int ws_nred(int TC) { return TC / WS_RB + 1; }
 
 template <int DK>
 struct WsGeo {
@@ -70,6 +77,7 @@ struct WsLayout {
     int red_buf;
     int off_par, off_red, off_bar, total;
     __host__ __device__ WsLayout(int dk, int dv, int es, int TC, int hpc, int red_floats) {
+        const int nred = ws_nred(TC);
         raw_qk = TC * dk * es;
         raw_vb = TC * dv * es;
         raw_d = (TC * es + 15) & ~15;
@@ -80,35 +88,38 @@ struct WsLayout {
         red_buf = red_floats * 4;
         off_par = WS_RAW * raw_stage;
         off_red = off_par + WS_PAR * par_stage;
-        off_bar = off_red + 2 * red_buf;
-        // barriers: raw_full[3], par_full[2], par_empty[2], red_full[2],
-        // red_empty[2]; then the scale state W[hpc], R[hpc]
-        total = off_bar + 11 * 8 + 8 * hpc;
+        off_bar = off_red + nred * red_buf;
+        // barriers: raw_full[3], par_full[2], par_empty[2], red_full[nred],
+        // red_empty[nred]; then the scale state W[hpc], R[hpc]
+        total = off_bar + (WS_RAW + 2 * WS_PAR + 2 * nred) * 8 + 8 * hpc;
     }
 };
 
 template <int DK>
 __host__ __device__ inline int ws_smem_bytes(int dv, int es, int TC) {
+    // TC: 16 or 8
     using G = WsGeo<DK>;
     return WsLayout(DK, dv, es, TC, G::ROWS / dv, G::RED_FLOATS).total;
 }
 
-template <int DK, typename TIn>
+template <int DK, typename TIn, int TC>
 __global__ void __launch_bounds__(WS_THREADS, 1)
 diag_ws_kernel(const Params p) {
     using G = WsGeo<DK>;
     constexpr int M = G::M, PF = G::PF, RSS = G::RSS, RTS = G::RTS, WR = G::WR;
     constexpr int ES = sizeof(TIn);
+    constexpr int NRED = ws_nred(TC), GPC = TC / WS_RB;   // reduction buffers, groups per chunk
+    static_assert(TC % WS_RB == 0 && TC <= 16, "whole reduction groups per chunk; rescale masks hold 16 tokens");
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int dv = p.dv, HPC = G::ROWS / dv, TC = p.TC;
+    const int dv = p.dv, HPC = G::ROWS / dv;
     const WsLayout L(DK, dv, ES, TC, HPC, G::RED_FLOATS);
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
     uint64_t* par_full = raw_full + WS_RAW;
     uint64_t* par_empty = par_full + WS_PAR;
     uint64_t* red_full = par_empty + WS_PAR;
-    uint64_t* red_empty = red_full + 2;
-    float* w_state = reinterpret_cast<float*>(red_empty + 2);   // [HPC]
+    uint64_t* red_empty = red_full + NRED;
+    float* w_state = reinterpret_cast<float*>(red_empty + NRED);   // [HPC]
     int* r_state = reinterpret_cast<int*>(w_state + HPC);       // [HPC]
     auto rawp = [&](int s, int h, int off) { return smem + s * L.raw_stage + h * L.raw_head + off; };
     auto raw_q = [&](int s, int h) { return reinterpret_cast<TIn*>(rawp(s, h, 0)); };
@@ -145,7 +156,7 @@ diag_ws_kernel(const Params p) {
             mbar_init(&par_full[s], WS_PW * 32);
             mbar_init(&par_empty[s], WS_CW * 32);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NRED; ++b) {
             mbar_init(&red_full[b], WS_CW * 32);
             mbar_init(&red_empty[b], WS_PW * 32);
         }
@@ -232,8 +243,8 @@ diag_ws_kernel(const Params p) {
         // sum the row partials of reduction group g (tokens g*8 .. of the
         // part) over the M lanes of each row and store o
         auto flush = [&](int g) {
-            const int b = g & 1;
-            if (!mbar_wait(&red_full[b], (g >> 1) & 1, p.wait_ns)) ok = false;
+            const int b = g % NRED;
+            if (!mbar_wait(&red_full[b], (g / NRED) & 1, p.wait_ns)) ok = false;
             const int t_first = tb + g * WS_RB;
             const int ntok = min(WS_RB, te - t_first);
             const float* rb = red(b);
@@ -324,6 +335,16 @@ diag_ws_kernel(const Params p) {
             const int s2 = c & 1, s3 = c % WS_RAW;
             if (!mbar_wait(&par_full[s2], (c >> 1) & 1, p.wait_ns)) ok = false;
             const int tcn = min(TC, te - (tb + c * TC));
+            // the reduction buffers of this chunk's groups: their previous
+            // groups (NRED earlier) must have been flushed
+#pragma unroll
+            for (int gg = 0; gg < GPC; ++gg) {
+                const int g = c * GPC + gg;
+                if (g >= NRED && gg * WS_RB < tcn &&
+                    !mbar_wait(&red_empty[g % NRED], (g / NRED - 1) & 1, p.wait_ns))
+                    ok = false;
+            }
+            float* redc = red(0) + warp * WS_RB * RTS + rs * RSS + 4 * cg;   // this lane's slot 0, buffer 0
             const TIn* rv = raw_v(s3, hsafe) + i0;
             const TIn* rbp = raw_b(s3, hsafe) + i0;
             const float* pbase = par(s2, hsafe);
@@ -344,12 +365,8 @@ diag_ws_kernel(const Params p) {
                 const uint32_t later = mask >> (tt + 1);   // tt + 1 <= TC <= 16
                 const int stop = later ? min(tcn, tt + __ffs(later)) : tcn;
                 for (; tt < stop; ++tt) {
-                    const int gi = c * TC + tt;             // token index within the part
-                    const int slot = gi & (WS_RB - 1);
-                    const int grp = gi / WS_RB;
-                    if (slot == 0 && grp >= 2 &&
-                        !mbar_wait(&red_empty[grp & 1], ((grp >> 1) - 1) & 1, p.wait_ns))
-                        ok = false;
+                    const int slot = tt & (WS_RB - 1);
+                    const int b = (c * GPC + tt / WS_RB) % NRED;
                     const float* ptk = pbase + tt * PF;
                     const float4 sc = *reinterpret_cast<const float4*>(ptk + 3 * DK);
                     float bet[RT], val[RT];
@@ -408,11 +425,11 @@ diag_ws_kernel(const Params p) {
                             }
                         }
                     }
-                    float* dst = red(grp & 1) + (warp * WS_RB + slot) * RTS + rs * RSS + 4 * cg;
+                    float* dst = redc + b * G::RED_FLOATS + slot * RTS;
                     *reinterpret_cast<float4*>(dst) =
                         make_float4(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y,
                                     acc[3].x + acc[3].y);
-                    if (slot == WS_RB - 1 || tb + gi == te - 1) mbar_arrive(&red_full[grp & 1]);
+                    if (slot == WS_RB - 1 || tt == tcn - 1) mbar_arrive(&red_full[b]);
                 }
             }
             mbar_arrive(&par_empty[s2]);
