@@ -894,31 +894,36 @@ kdn_status plan_dk(const DiagArgs& a, Plan* pl) {
         if (P < 1) P = 1;
     }
     // Fill split.  With d_k = d_v = 128 and bf16 inputs the aggregate pass
-    // runs on the tensor cores and costs little, so when the CTAs leave SMs
-    // idle, shorter parts in several waves can finish sooner.  Estimate in
-    // full-pass token steps of one CTA: waves x part length, plus about 0.47
-    // per extra (head, part) (aggregate, carry and start-state traffic) and
-    // 23 for the two extra launches (fitted to GB300 timings of the 750M-shaped
-    // layer); taken when it saves more than 2 %.
-    if (!LIN && P == 1 && tc_aggregates<DK, TIn>(dv) && pl->ctas_full < slots && a.T >= 32 * TC) {
+    // runs on the tensor cores and costs little, so the part count is chosen
+    // by a model in full-pass token steps of one CTA: waves x part length,
+    // plus for a split 23 (two extra launches), 0.07 per extra (head, part)
+    // (carry and start-state traffic) and 6.6e-4 per token of an extra
+    // (head, part) (the aggregate pass), fitted to GB300 timings of the
+    // 750M-shaped layer and the 65536-token context.  Every count that
+    // keeps parts at least 8 chunks long is weighed, the slot-filling one
+    // above included; a split is taken when it saves more than 2 %.
+    if (!LIN && tc_aggregates<DK, TIn>(dv) && a.T >= 32 * TC) {
         auto est = [&](int parts, int plen) {
             const long long waves = (pl->ctas_full * parts + slots - 1) / slots;
+            const double extra = static_cast<double>(BH) * (parts - 1);
             return static_cast<double>(waves) * plen +
-                   (parts > 1 ? 23.0 + 0.47 * static_cast<double>(BH) * (parts - 1) : 0.0);
+                   (parts > 1 ? 23.0 + extra * (0.07 + 6.6e-4 * plen) : 0.0);
         };
+        auto plen_of = [&](int cand) { return ((a.T + cand - 1) / cand + TC - 1) / TC * TC; };
         const double one = est(1, a.T);
         double best = one;
-        for (int cand = 2; cand <= 32; ++cand) {
-            const int plen = ((a.T + cand - 1) / cand + TC - 1) / TC * TC;
+        int bestP = 1;
+        for (int cand = 2; cand <= 64; ++cand) {
+            const int plen = plen_of(cand);
             if (plen < 8 * TC) break;
             const int pe = (a.T + plen - 1) / plen;
             const double e = est(pe, plen);
             if (e < best) {
                 best = e;
-                P = pe;
+                bestP = pe;
             }
         }
-        if (!(best < 0.98 * one)) P = 1;
+        P = best < 0.98 * one ? bestP : 1;
     }
     int part_len = a.T > 0 ? a.T : 1;
     if (P > 1) {
