@@ -52,12 +52,14 @@ DIAG_FLOP_PER_ELEMENT_TOKEN = 10
 MOBIUS_BYTES_PER_STEP = 20
 # scan workloads whose numbers the default line carries besides its own
 EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
-# dram__bytes_read.sum + dram__bytes_write.sum of one kdn_diag_scan_fwd call
-# (all its kernels: tensor-core aggregates, carry, full pass) per workload,
-# from the ncu capture of the current kernels summarised in profiles/
-# (launches_layer750m.md); workloads without such a capture report null.
-DIAG_TRAFFIC_BYTES = {"layer750m": (350_416_896 + 67_866_880) + (100_696_320 + 36_271_104)
-                      + (638_855_424 + 241_288_448)}
+# dram__bytes_read.sum + dram__bytes_write.sum of one scan call (all its
+# kernels: tensor-core aggregates, carry, full pass with the lambda walkers)
+# per workload, from the ncu captures of the current kernels summarised in
+# profiles/ (launches_*.md); workloads without such a capture report null.
+DIAG_TRAFFIC_BYTES = {
+    "layer750m": (350_300_000 + 64_600_000) + (100_700_000 + 35_800_000) + (647_300_000 + 244_700_000),
+    "layer1p3b": 1_111_900_000 + 517_500_000,
+}
 
 
 def parse_args():
