@@ -62,7 +62,7 @@ constexpr uint32_t AG_LBO = 128;                   // core matrices: next 8 toke
 // and group of 8 tokens) and one more warp that issues the products and the
 // copies.  KC = 32: 288 threads, one CTA per SM; KC = 16: 160 threads, two
 // CTAs per SM (each holding 256 of the SM's 512 TMEM columns), for grids
-// with more CTAs than SMs (half the waves of the one-CTA variant).
+// with at least two CTAs per SM.
 template <int KC>
 struct AggShape {
     static constexpr int BUILD = 8 * KC;

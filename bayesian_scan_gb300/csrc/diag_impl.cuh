@@ -980,7 +980,7 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                 AggArgs ag{static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.beta),
                            static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.d),
                            a.A, prm.agg, prm.agg_scale, BH, a.H, a.T, prm.d_ld, pl.part_len, wait_ns};
-                // two CTAs per SM when there are more CTAs than SMs, else one wider CTA per SM
+                // two CTAs per SM when the grid fills them, else one wider CTA per SM
                 const dim3 grid(static_cast<unsigned>(BH), P - 1);
                 if constexpr (LIN) {
                     // the non-metaplastic limit needs only the eta aggregates; its
@@ -988,8 +988,10 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
                     // stays below one wave of full-pass CTAs: always one CTA per SM
                     diag_agg_tc_kernel<32, true><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);
                 } else {
-                    // more CTAs than SMs: the two-CTA variant runs them in half the waves
-                    if (BH * (P - 1) > sm_count())
+                    // the two-CTA variant when it fills both slots of every SM
+                    // (288 CTAs on 152 SMs: two waves of the one-CTA variant
+                    // measured 280 us, one wave of the two-CTA variant 294 us)
+                    if (BH * (P - 1) >= 2LL * sm_count())
                         diag_agg_tc_kernel<16><<<grid, AggShape<16>::THREADS, AggShape<16>::SMEM, st>>>(ag);
                     else
                         diag_agg_tc_kernel<32><<<grid, AggShape<32>::THREADS, AggShape<32>::SMEM, st>>>(ag);

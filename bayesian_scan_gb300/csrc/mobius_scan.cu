@@ -275,15 +275,18 @@ int mobius_seq_slots() {
 // resident CTA has sequences to stream; for fewer sequences the two kernels'
 // costs are compared with a model fitted to GB300 timings (microseconds): the
 // walk costs about 3.5 + 1.6 tps; the look-back kernel about 9 + 0.0224 per
-// tile of the grid + 0.31 per look-back hop, and never less than 19 (scratch
-// allocation, flag clearing and release on the stream).  Single-tile
+// tile of the grid + 0.31 per look-back hop, and never less than 19 when it
+// allocates its scratch (allocation, flag clearing and release on the
+// stream) or 9 when the scratch is the library's fixed array (flag clearing
+// and the launch: kdn_mobius_scan_noalloc, measured 9.0 us for 1 x 4096 and
+// 11.5 us for 1 x 16384 steps against 16.7 us for the walk).  Single-tile
 // sequences need no look-back and stay on the tile kernel.
-bool mobius_choose_seq(long long N, long long tps, bool vec, int slots) {
+bool mobius_choose_seq(long long N, long long tps, bool vec, int slots, bool fixed_scratch = false) {
     if (!vec || slots <= 0 || tps < 2) return false;
     if (N >= slots) return true;
     const double n = static_cast<double>(N), t = static_cast<double>(tps);
     const double walk = 3.5 + 1.6 * t;
-    const double lookback = fmax(19.0, 9.0 + 0.0224 * n * t + 0.31 * t);
+    const double lookback = fmax(fixed_scratch ? 9.0 : 19.0, 9.0 + 0.0224 * n * t + 0.31 * t);
     return walk <= lookback;
 }
 
@@ -424,7 +427,10 @@ kdn_status mobius_launch_noalloc(const float* a, const float* b, const float* c,
     cudaError_t e;
     const int slots = vec ? mobius_seq_slots() : 0;
     if (slots < 0) return KDN_ERR_CUDA;
-    if (mobius_choose_seq(N, tps, vec, slots)) {   // no scratch at all
+    // the walk takes no scratch: it also serves aligned calls whose look-back
+    // would need more tiles than the fixed array holds
+    if (mobius_choose_seq(N, tps, vec, slots, true) ||
+        (vec && slots > 0 && tps > 1 && tiles > mobius_noalloc_max_tiles())) {   // no scratch at all
         mobius_seq_kernel<<<static_cast<unsigned>(min(static_cast<long long>(slots), N)), SQ_THREADS,
                             sq_smem_bytes(), stream>>>(a, b, c, d, lambda0, out, N, T,
                                                        static_cast<int>(tps), wait_ns);

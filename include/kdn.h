@@ -337,11 +337,14 @@ KDN_API kdn_status kdn_mobius_scan_plan(long long N, long long T, int* kernels,
  * look-back scratch may use at most 43690 tiles, N * ceil(T / 2048) <= 43690;
  * larger calls return KDN_ERR_INVALID_ARG without launching.  A call needs
  * look-back scratch when T > 2048 and the sequence-walk kernel does not take
- * it: that kernel needs T % 4 == 0 and a, b, c, d, out 16-byte aligned (an
- * offset view of a larger tensor may not be), and it is chosen when the
- * sequences fill the GPU or a cost model prefers it.  kdn_mobius_scan_plan
- * assumes aligned pointers: scratch_bytes > 0 there means the limit applies;
- * scratch_bytes == 0 means it does not, provided the pointers are aligned.
+ * it.  That kernel needs T % 4 == 0 and a, b, c, d, out 16-byte aligned (an
+ * offset view of a larger tensor may not be); on such rows it is chosen when
+ * the sequences fill the GPU, when a cost model prefers it, or when the
+ * look-back would need more tiles than the array holds.  So only calls with
+ * T % 4 != 0 or unaligned rows can meet the limit.  The cost model counts no
+ * allocation for this entry point, so it may pick the look-back where
+ * kdn_mobius_scan would walk (kdn_mobius_scan_plan reports the allocating
+ * entry point's choice).
  * The first call on a device fetches the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one array: calls whose executions overlap on the GPU
