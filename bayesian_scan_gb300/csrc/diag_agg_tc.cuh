@@ -32,15 +32,20 @@
 // Chunks of the part are visited from the last to the first (so the suffix
 // sums accumulate).  The weights w_t of a super-chunk of tokens are prepared
 // by the build threads (8 tokens each, fp64 suffix sums across them); per
-// chunk the build threads write the 7 operand tiles (128 x KC bf16 each,
-// core-matrix layout) from the raw chunk (k, beta, v, brought in by 1-D bulk
-// copies two chunks ahead) and arrive, one lane per warp, on the chunk's
-// operand barrier; the issuing warp waits there, issues the next copies into
-// the consumed raw stage and the chunk's 6 KC / 16 MMAs, and commits them to
-// an mbarrier.  Operand tiles are double-buffered on that barrier, so the
-// build threads never wait for the products to be issued (a build thread
-// that also issued held its warp, and at the chunk barrier all others, for
-// about 770 cycles a chunk).  All waits are bounded by GPU time.
+// chunk the build threads load their part of the raw chunk (k, beta, v,
+// brought in by 1-D bulk copies AG_NS chunks ahead) into registers and
+// release its stage on the stage's empty barrier, then write the 8 operand
+// tiles (128 x KC bf16 each, core-matrix layout) and arrive, one lane per
+// warp, on the chunk's operand barrier.  The issuing warp refills each
+// released stage with the copies of the chunk AG_NS later, waits for the
+// operands, issues the chunk's 6 KC / 16 MMAs and commits them to an
+// mbarrier.  Operand tiles are double-buffered on that barrier, so the build
+// threads never wait for the products to be issued (a build thread that also
+// issued held its warp, and at the chunk barrier all others, for about 770
+// cycles a chunk).  The kernel reads HBM with little arithmetic per byte, so
+// the copies in flight per SM set its speed: with two stages, each refilled
+// only after the whole build of its chunk, a chunk took about the copy
+// latency plus a build.  All waits are bounded by GPU time.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,14 +60,17 @@ namespace {
 
 constexpr int AG_D = 128;                          // d_k = d_v
 constexpr int AG_NTILE = 8;                        // A_beta, A_E hi/mid/lo, B_k, B_wk2 hi/mid/lo
-constexpr int AG_TMEM_COLS = 256;                  // J in columns [0,128), eta in [128,256)
+// tensor memory: 256 columns (J in [0,128), eta in [128,256)); the wide
+// form takes 512 (J pieces in [0,256), eta^T pieces in [256,512))
+constexpr int AG_TMEM_COLS = 256;
 constexpr uint32_t AG_LBO = 128;                   // core matrices: next 8 tokens (K)
+constexpr int AG_NS = 3;                           // raw chunk stages (copies in flight)
 
 // Chunk shapes: KC tokens per chunk, 8 KC build threads (one per row pair
 // and group of 8 tokens) and one more warp that issues the products and the
-// copies.  KC = 32: 288 threads, one CTA per SM; KC = 16: 160 threads, two
-// CTAs per SM (each holding 256 of the SM's 512 TMEM columns), for grids
-// with at least two CTAs per SM.
+// copies.  KC = 32: 288 threads, one CTA per SM (208 KB of shared memory);
+// KC = 16: 160 threads, two CTAs per SM (104 KB each; each CTA holds 256 of
+// the SM's 512 TMEM columns), for grids with at least two CTAs per SM.
 template <int KC>
 struct AggShape {
     static constexpr int BUILD = 8 * KC;
@@ -73,7 +81,15 @@ struct AggShape {
     static constexpr int RAW = KC * AG_D * 2;           // one raw array (k, beta or v) of a chunk
     static constexpr uint32_t SBO = (KC / 8) * 128;     // core matrices: next 8 rows (M or N)
     static constexpr int SUP = 8 * BUILD;               // tokens per super-chunk of decay weights
-    static constexpr int SMEM = 2 * OPS + 2 * 3 * RAW + SUP * 4 + 8 * 8 + 6 * 8 + 16;
+    // Wide products (the one-CTA shape, whose CTA may hold all 512 TMEM
+    // columns): J takes A_beta x [B_wk2 hi | B_wk2 mid] as one N = 256
+    // product (two accumulators, added in the epilogue) plus A_beta x
+    // B_wk2 lo, and eta is formed transposed, eta^T = k x [A_E hi | A_E mid]
+    // + k x A_E lo: 4 products a K step instead of 6, and a sixth less
+    // shared memory read by the tensor core (40 KB instead of 48).
+    static constexpr bool WIDE = KC == 32;
+    static constexpr int NBAR = 2 * AG_NS + 4;          // raw_full, raw_empty [AG_NS]; mma_done, ops_full [2]
+    static constexpr int SMEM = 2 * OPS + AG_NS * 3 * RAW + SUP * 4 + 8 * 8 + NBAR * 8 + 16;
 };
 
 // 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
@@ -86,19 +102,25 @@ __device__ __forceinline__ float exp2_neg(double S) {
     return ldexpf(exp2f(-f), -e);
 }
 
-// (x0, x1) -> bf16x2 pieces hi = rn(x), mid = rn(x - hi), lo = rn(x - hi -
-// mid), low half = x0; hi + mid + lo equals x to fp32 rounding (x - hi and
-// x - hi - mid are exact in fp32)
-__device__ __forceinline__ void split3(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    const float r0 = x0 - __uint_as_float(hi << 16), r1 = x1 - __uint_as_float(hi & 0xffff0000u);
-    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
-    mid = *reinterpret_cast<const uint32_t*>(&m);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __uint_as_float(mid << 16),
-                                                   r1 - __uint_as_float(mid & 0xffff0000u));
-    lo = *reinterpret_cast<const uint32_t*>(&l);
+// Three bf16 pieces of each of x.x, x.y, as fp32 bit patterns with the low
+// 16 bits zero: hi keeps the top 8 significant bits of x (truncation), mid
+// the top 8 of the remainder x - hi, and the remainder after that has at most
+// 8 significant bits, so lo holds it exactly; both differences are exact in
+// fp32, so hi + mid + lo = x exactly.  Bit operations and two packed
+// subtractions, no conversions.
+__device__ __forceinline__ void split3(float2 x, uint32_t (&h)[2], uint32_t (&m)[2], uint32_t (&l)[2]) {
+    h[0] = __float_as_uint(x.x) & 0xffff0000u;
+    h[1] = __float_as_uint(x.y) & 0xffff0000u;
+    const float2 r = __fadd2_rn(x, make_float2(-__uint_as_float(h[0]), -__uint_as_float(h[1])));
+    m[0] = __float_as_uint(r.x) & 0xffff0000u;
+    m[1] = __float_as_uint(r.y) & 0xffff0000u;
+    const float2 s = __fadd2_rn(r, make_float2(-__uint_as_float(m[0]), -__uint_as_float(m[1])));
+    l[0] = __float_as_uint(s.x);
+    l[1] = __float_as_uint(s.y);
 }
+
+// bf16x2 of the upper halves of a (low half) and b
+__device__ __forceinline__ uint32_t pack_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
 // Named CTA barrier `ID` (0 is __syncthreads) over `n` threads, whole warps.
 template <int ID>
@@ -132,12 +154,13 @@ diag_agg_tc_kernel(const AggArgs p) {
                   AG_RAW = Sh::RAW, AG_SUP = Sh::SUP;
     constexpr uint32_t AG_SBO = Sh::SBO;
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* ops = smem;                                  // [2][7 tiles]
-    unsigned char* raw = smem + 2 * AG_OPS;                     // [2 stages][k, beta, v]
-    float* wsup = reinterpret_cast<float*>(raw + 2 * 3 * AG_RAW);   // [AG_SUP] weights of a super-chunk
+    unsigned char* ops = smem;                                  // [2][8 tiles]
+    unsigned char* raw = smem + 2 * AG_OPS;                     // [AG_NS stages][k, beta, v]
+    float* wsup = reinterpret_cast<float*>(raw + AG_NS * 3 * AG_RAW);   // [AG_SUP] weights of a super-chunk
     double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [warps] warp totals
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);
-    uint64_t* mma_done = raw_full + 2;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);  // a stage's copies landed
+    uint64_t* raw_empty = raw_full + AG_NS;                     // a stage read by every build warp
+    uint64_t* mma_done = raw_empty + AG_NS;
     uint64_t* ops_full = mma_done + 2;                          // a chunk's operands built (per build warp)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ops_full + 2);
     float* s_wend = reinterpret_cast<float*>(tmem_holder + 1);
@@ -152,9 +175,9 @@ diag_agg_tc_kernel(const AggArgs p) {
     const long long S = static_cast<long long>(AG_D) * AG_D;
     bool ok = true;
 
-    // raw chunk of iteration `it` (chunk nch-1-it) into stage it & 1 (thread 0)
+    // raw chunk of iteration `it` (chunk nch-1-it) into stage it % AG_NS (one thread)
     auto issue = [&](int it) {
-        const int st = it & 1;
+        const int st = it % AG_NS;
         const int c = nch - 1 - it;
         const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
         const uint32_t bytes = static_cast<uint32_t>(n * AG_D * 2);
@@ -168,15 +191,20 @@ diag_agg_tc_kernel(const AggArgs p) {
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < AG_NS; ++i) {
             mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], AG_BUILD / 32);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&mma_done[i], 1);
             mbar_init(&ops_full[i], AG_BUILD / 32);
         }
         mbar_init_fence();
-        for (int it = 0; it < 2 && it < nch; ++it) issue(it);
+        for (int it = 0; it < AG_NS && it < nch; ++it) issue(it);
     }
-    if (warp == 0) tmem_alloc(tmem_holder, AG_TMEM_COLS);
+    constexpr bool WIDE = Sh::WIDE && !ETA_ONLY;
+    constexpr int TMEM_COLS = WIDE ? 4 * AG_D : AG_TMEM_COLS;
+    if (warp == 0) tmem_alloc(tmem_holder, TMEM_COLS);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -187,22 +215,34 @@ diag_agg_tc_kernel(const AggArgs p) {
     int sup0 = tb;           // first token of the current super-chunk
     const bool builder = tid < AG_BUILD;    // else the issuing warp
     const int pr = tid & 63;                // a builder's operand rows 2 pr, 2 pr + 1
+    // A builder keeps its two rows in the order (2 pr + flip, 2 pr + 1 -
+    // flip), flip = bit 2 of pr, so that the 8 lanes of each quarter-warp
+    // 16-byte store cover all 8 rows of a core matrix row group (8 distinct
+    // bank groups): without it a store met 2-way bank conflicts.
+    const uint32_t flip = (pr >> 2) & 1;
+    const uint32_t swap_sel = flip ? 0x1032u : 0x3210u;   // swaps the bf16 halves of a word
     const int kg = tid >> 6;                // and its group of 8 tokens of a chunk (AG_KC / 8 groups)
     static_assert(AG_BUILD == 64 * (AG_KC / 8), "one build thread per (row pair, token group)");
     static_assert(AG_SUP == 8 * AG_BUILD, "a build thread prepares 8 weights of a super-chunk");
     constexpr uint32_t IDESC = umma_idesc_bf16_f32(AG_D, AG_D);
+    constexpr uint32_t IDESC_WIDE = umma_idesc_bf16_f32(AG_D, 2 * AG_D);
 
+    int st = 0;              // raw stage of iteration it (it % AG_NS)
+    uint32_t rph = 0;        // its barriers' phase ((it / AG_NS) & 1)
     for (int it = 0; it < nch; ++it) {
-        const int st = it & 1, ob = it & 1;
+        const int ob = it & 1;
         const int c = nch - 1 - it;
         const int t0 = tb + c * AG_KC, n = min(AG_KC, te - t0);
         if (!builder) {
-            // ---- the issuing warp: once every build warp has arrived on the
-            // chunk's operand barrier, the next copies into the consumed raw
-            // stage and the chunk's products ----
+            // ---- the issuing warp: refill the stage once every build warp
+            // has read it, then the chunk's products once its operands are
+            // built ----
+            if (it + AG_NS < nch) {
+                if (!mbar_wait(&raw_empty[st], rph, p.wait_ns)) ok = false;
+                if (lane == 0) issue(it + AG_NS);
+            }
             if (!mbar_wait(&ops_full[ob], (it >> 1) & 1, p.wait_ns)) ok = false;
             if (lane == 0) {
-                if (it + 2 < nch) issue(it + 2);
                 tc_fence_after_sync();
                 const uint32_t base = smem_addr(ops + ob * AG_OPS);
 #pragma unroll
@@ -211,6 +251,14 @@ diag_agg_tc_kernel(const AggArgs p) {
                         return umma_desc_kmajor(base + tile * AG_TILE + s * 2 * 128, AG_LBO, AG_SBO);
                     };
                     const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
+                    if (WIDE) {
+                        // tiles 5, 6 (and 1, 2) are adjacent: one 256-row operand
+                        umma_bf16(tmem, desc(0), desc(5), IDESC_WIDE, first);          // J: hi | mid
+                        umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);                  //  + lo
+                        umma_bf16(tmem + 2 * AG_D, desc(4), desc(1), IDESC_WIDE, first);   // eta^T: hi | mid
+                        umma_bf16(tmem + 2 * AG_D, desc(4), desc(3), IDESC, 1u);       //  + lo
+                        continue;
+                    }
                     if (!ETA_ONLY) {
                         umma_bf16(tmem, desc(0), desc(5), IDESC, first);       // J += A_beta B_wk2 hi
                         umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_beta B_wk2 mid
@@ -223,6 +271,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                 umma_commit(&mma_done[ob]);
             }
             __syncwarp();
+            if (++st == AG_NS) { st = 0; rph ^= 1u; }
             continue;
         }
         if (it == 0 || ((c + 1) % (AG_SUP / AG_KC)) == 0) {
@@ -233,11 +282,22 @@ diag_agg_tc_kernel(const AggArgs p) {
             sup0 = tb + (c / (AG_SUP / AG_KC)) * AG_SUP;
             const int s1 = min(te, sup0 + AG_SUP);
             const int u0 = sup0 + 8 * tid;
+            const __nv_bfloat16* dp = p.d + bh * p.d_ld + u0;
+            float dv8[8];
+            if (u0 + 8 <= s1 && (reinterpret_cast<uintptr_t>(dp) & 15) == 0) {
+                const uint4 raw8 = __ldg(reinterpret_cast<const uint4*>(dp));   // 8 tokens in one load
+                const uint32_t w4[4] = {raw8.x, raw8.y, raw8.z, raw8.w};
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dv8[u] = __uint_as_float((u & 1) ? (w4[u >> 1] & 0xffff0000u) : (w4[u >> 1] << 16));
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) dv8[u] = u0 + u < s1 ? __bfloat162float(dp[u]) : 0.f;
+            }
             double x[8], loc = 0.0;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int t = u0 + u;
-                x[u] = t < s1 ? static_cast<double>(Ah * __bfloat162float(p.d[bh * p.d_ld + t]) * LOG2E) : 0.0;
+                x[u] = u0 + u < s1 ? static_cast<double>(Ah * dv8[u] * LOG2E) : 0.0;
                 loc += x[u];
             }
             // exclusive suffix sum over the threads after this one
@@ -266,55 +326,76 @@ diag_agg_tc_kernel(const AggArgs p) {
             Z += all;
             named_sync<1>(AG_BUILD);   // weights ready; wtot may be reused
         }
-        if (!mbar_wait(&raw_full[st], (it >> 1) & 1, p.wait_ns)) ok = false;
-        // the operand buffer was last read by the MMAs of iteration it - 2
-        if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
+        if (!mbar_wait(&raw_full[st], rph, p.wait_ns)) ok = false;
 
-        // ---- build the 8 operand tiles of this chunk (rows 2pr, 2pr+1; tokens 8kg..8kg+7) ----
+        // ---- this thread's part of the raw chunk (rows 2pr, 2pr+1; tokens
+        // 8kg..8kg+7) into registers, then the stage goes back to the copies ----
+        uint32_t kk[8], bb[8], vv[8];
+        float wt[8];
         {
             const unsigned char* rk = raw + st * 3 * AG_RAW;
             const unsigned char* rb = rk + AG_RAW;
             const unsigned char* rv = rb + AG_RAW;
             const float* w = wsup + (t0 - sup0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int tok = kg * 8 + u;
+                const bool valid = tok < n;
+                const int o4 = (tok * AG_D + 2 * pr) * 2;
+                wt[u] = valid ? w[tok] : 0.f;
+                bb[u] = valid ? *reinterpret_cast<const uint32_t*>(rb + o4) : 0u;
+                vv[u] = valid ? *reinterpret_cast<const uint32_t*>(rv + o4) : 0u;
+                kk[u] = valid ? *reinterpret_cast<const uint32_t*>(rk + o4) : 0u;
+                bb[u] = __byte_perm(bb[u], 0u, swap_sel);   // low half: row 2 pr + flip
+                vv[u] = __byte_perm(vv[u], 0u, swap_sel);
+                kk[u] = __byte_perm(kk[u], 0u, swap_sel);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[st]);   // this warp's reads of the stage are done
+        if (++st == AG_NS) { st = 0; rph ^= 1u; }
+        // the operand buffer was last read by the MMAs of iteration it - 2
+        if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
+
+        // ---- build the 8 operand tiles of this chunk: products packed over
+        // the row pair, pieces packed over token pairs ----
+        {
             uint32_t t[AG_NTILE][2][4];   // [tile][row of the pair][4 x bf16x2 along the tokens]
 #pragma unroll
             for (int u2 = 0; u2 < 4; ++u2) {
-                float ae[2][2], wk2[2][2];
-                uint32_t kbits[2][2], bbits[2][2];
+                uint32_t eh[2][2], em[2][2], el[2][2];   // [token of the pair][row]: pieces of w beta v
+                uint32_t jh[2][2], jm[2][2], jl[2][2];   //                                 of w k^2
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int tok = kg * 8 + 2 * u2 + e;
-                    const bool valid = tok < n;
-                    const float wt = valid ? w[tok] : 0.f;
-                    const int o4 = (tok * AG_D + 2 * pr) * 2;
-                    const uint32_t bb = valid ? *reinterpret_cast<const uint32_t*>(rb + o4) : 0u;
-                    const uint32_t vv = valid ? *reinterpret_cast<const uint32_t*>(rv + o4) : 0u;
-                    const uint32_t kk = valid ? *reinterpret_cast<const uint32_t*>(rk + o4) : 0u;
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        bbits[r][e] = r ? (bb >> 16) : (bb & 0xffffu);
-                        const float bf = __uint_as_float(bbits[r][e] << 16);
-                        const float vf = __uint_as_float(r ? (vv & 0xffff0000u) : (vv << 16));
-                        kbits[r][e] = r ? (kk >> 16) : (kk & 0xffffu);
-                        const float kf = __uint_as_float(kbits[r][e] << 16);
-                        ae[r][e] = (wt * bf) * vf;
-                        wk2[r][e] = wt * (kf * kf);   // k^2 is exact in fp32 (16 significant bits)
-                    }
+                    const int u = 2 * u2 + e;
+                    const float2 w2 = make_float2(wt[u], wt[u]);
+                    const float2 bf = make_float2(__uint_as_float(bb[u] << 16), __uint_as_float(bb[u] & 0xffff0000u));
+                    const float2 vf = make_float2(__uint_as_float(vv[u] << 16), __uint_as_float(vv[u] & 0xffff0000u));
+                    const float2 kf = make_float2(__uint_as_float(kk[u] << 16), __uint_as_float(kk[u] & 0xffff0000u));
+                    split3(__fmul2_rn(__fmul2_rn(w2, bf), vf), eh[e], em[e], el[e]);
+                    if (!ETA_ONLY)   // k^2 is exact in fp32 (16 significant bits)
+                        split3(__fmul2_rn(w2, __fmul2_rn(kf, kf)), jh[e], jm[e], jl[e]);
                 }
+                const int u = 2 * u2;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
+                    const uint32_t sel = r ? 0x7632u : 0x5410u;   // row r's halves of two tokens
                     if (!ETA_ONLY) {
-                        t[0][r][u2] = bbits[r][0] | (bbits[r][1] << 16);
-                        split3(wk2[r][0], wk2[r][1], t[5][r][u2], t[6][r][u2], t[7][r][u2]);
+                        t[0][r][u2] = __byte_perm(bb[u], bb[u + 1], sel);
+                        t[5][r][u2] = pack_hi(jh[0][r], jh[1][r]);
+                        t[6][r][u2] = pack_hi(jm[0][r], jm[1][r]);
+                        t[7][r][u2] = pack_hi(jl[0][r], jl[1][r]);
                     }
-                    split3(ae[r][0], ae[r][1], t[1][r][u2], t[2][r][u2], t[3][r][u2]);
-                    t[4][r][u2] = kbits[r][0] | (kbits[r][1] << 16);
+                    t[1][r][u2] = pack_hi(eh[0][r], eh[1][r]);
+                    t[2][r][u2] = pack_hi(em[0][r], em[1][r]);
+                    t[3][r][u2] = pack_hi(el[0][r], el[1][r]);
+                    t[4][r][u2] = __byte_perm(kk[u], kk[u + 1], sel);
                 }
             }
             unsigned char* o = ops + ob * AG_OPS;
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int rho = 2 * pr + r;
+                const int rho = 2 * pr + (r ^ static_cast<int>(flip));
                 const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;   // core matrix (rho/8, kg)
 #pragma unroll
                 for (int tile = ETA_ONLY ? 1 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE); ++tile)
@@ -324,7 +405,7 @@ diag_agg_tc_kernel(const AggArgs p) {
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ops_full[ob]);   // operands written, raw stage consumed
+        if (lane == 0) mbar_arrive(&ops_full[ob]);   // operands written
     }
 
     // ---- end state and scale of the part -------------------------------------
@@ -360,6 +441,29 @@ diag_agg_tc_kernel(const AggArgs p) {
         const int c_begin = (warp >> 2) * (2 * AG_D / QW), c_end = c_begin + 2 * AG_D / QW;
         for (int cc = c_begin; cc < c_end; cc += 32) {
             const int half = cc / AG_D, c0 = cc - half * AG_D;   // J (0) or eta (1)
+            if constexpr (WIDE) {
+                // J[row][c0 + j] = pieces' sum at columns c0 + j and 128 + c0 + j;
+                // eta^T: lane `row` is the key column, columns 256 + c0 + j
+                // (and 384 + c0 + j) the value rows c0 + j
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 2 * AG_D + c0;
+                float v[32], u[32];
+                tmem_ld32(ta, v);
+                tmem_ld32(ta + AG_D, u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = nch == 0 ? 0.f : (v[j] + u[j]) * W;
+                float* base = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S;
+                if (half == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(base + static_cast<long long>(row) * AG_D + c0 + j) =
+                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)   // a warp writes 32 consecutive key columns of a row
+                        base[static_cast<long long>(c0 + j) * AG_D + row] = v[j];
+                }
+                continue;
+            }
             float* dst = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S +
                          static_cast<long long>(row) * AG_D;
             float v[32];
@@ -381,7 +485,7 @@ diag_agg_tc_kernel(const AggArgs p) {
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, AG_TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
     if (!ok) record_error(&g_diag_error, KDN_ERR_TIMEOUT);
 }
 

@@ -229,6 +229,24 @@ def oracle_sample(w, inputs, n_heads: int, t_tokens: int):
     return dt, n_heads * t_tokens, min(oracle.max_threads(), n_heads)
 
 
+def oracle_single_core(n_heads: int = 4):
+    """The oracle on one host core: the first n_heads heads of the 32-head,
+    2048-token, d = 64 workload (all their 64x64 state rows, all tokens, their
+    Moebius steps)."""
+    import oracle
+    from bayesian_scan_gb300 import workloads
+    w1 = workloads.get("heads32_t2048_d64")
+    inputs = workloads.make(w1)
+    n = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        dt, units, _ = oracle_sample(w1, inputs, n_heads, w1.T)
+    finally:
+        oracle.set_threads(n)
+    return {"workload": w1.name, "value": units / dt, "unit": "tokens/s", "cores": 1,
+            "sample": f"{n_heads} heads x {w1.T} tokens, fp64 oracle, {dt:.2f} s"}
+
+
 def calibrate_oracle(w, inputs, budget_s: float):
     """Pick (n_heads, t_tokens) so one oracle sample takes about budget_s on
     this host: whole sequences of as many heads as fit (a multiple of the
@@ -429,7 +447,8 @@ def run_ours(args, w, dist):
         line["cpu_baseline"] = {
             "value": units / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n_heads} heads x {t_tokens} tokens of the same inputs (all "
-                      f"{dv}x{dk} state rows) + their Moebius steps, fp64 oracle, {dt:.1f} s"}
+                      f"{dv}x{dk} state rows) + their Moebius steps, fp64 oracle, {dt:.1f} s",
+            "single_core": oracle_single_core()}
     del host
     # the other layer configurations of the same metric, timed the same way
     # in the same run (a step each: one fused scan + lambda launch)
