@@ -16,12 +16,13 @@
 // decay weight goes with k^2 for Delta J, Delta J = sum_t beta_t[i] (w_t
 // k_t[j]^2), and with beta v for Delta eta, Delta eta = sum_t (w_t beta_t[i]
 // v_t[i]) k_t[j]; the fp32 factors w k^2 and w beta v are each split into
-// three bf16 pieces (hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi -
-// mid); both differences are exact in fp32), which carry all 24 bits of the
-// fp32 value.  So each sum takes three products, accumulated in fp32, and
-// every term is as accurate as the fp32 product it stands for: the carried
-// states are fp32-accurate, not bf16-accurate.  The decay exponents are
-// summed in fp64 (the part's suffix sums) and w_t = 2^-floor(S) *
+// three bf16 pieces whose sum is the fp32 value exactly (split3 below).  So
+// each sum takes three products, accumulated in fp32, and every term is as
+// accurate as the fp32 product it stands for: the carried states are
+// fp32-accurate, not bf16-accurate.  The decay exponents are summed in
+// two-float form (about 48 significant bits from error-free fp32 additions;
+// fp64 on this GPU runs at a small fraction of the fp32 rate, and fp64 sums
+// took 13-15 thousand cycles per super-chunk) and w_t = 2^-floor(S) *
 // exp2(-frac(S)).
 //
 // Output: the same (J_w, eta_w) = W (Delta J, Delta eta) and (W, R) with
@@ -31,21 +32,22 @@
 // Per CTA: one (head, part); 8 KC build threads and one issuing warp.
 // Chunks of the part are visited from the last to the first (so the suffix
 // sums accumulate).  The weights w_t of a super-chunk of tokens are prepared
-// by the build threads (8 tokens each, fp64 suffix sums across them); per
-// chunk the build threads load their part of the raw chunk (k, beta, v,
+// by the build threads (8 tokens each, two-float suffix sums across them).
+// Per chunk the build threads load their part of the raw chunk (k, beta, v,
 // brought in by 1-D bulk copies AG_NS chunks ahead) into registers and
 // release its stage on the stage's empty barrier, then write the 8 operand
 // tiles (128 x KC bf16 each, core-matrix layout) and arrive, one lane per
 // warp, on the chunk's operand barrier.  The issuing warp refills each
 // released stage with the copies of the chunk AG_NS later, waits for the
-// operands, issues the chunk's 6 KC / 16 MMAs and commits them to an
-// mbarrier.  Operand tiles are double-buffered on that barrier, so the build
-// threads never wait for the products to be issued (a build thread that also
-// issued held its warp, and at the chunk barrier all others, for about 770
-// cycles a chunk).  The kernel reads HBM with little arithmetic per byte, so
-// the copies in flight per SM set its speed: with two stages, each refilled
-// only after the whole build of its chunk, a chunk took about the copy
-// latency plus a build.  All waits are bounded by GPU time.
+// operands, issues the chunk's products and commits them to an mbarrier.
+// Operand tiles are double-buffered on that barrier, so the build threads
+// never wait for the products to be issued (a build thread that also issued
+// held its warp, and at the chunk barrier all others, for about 770 cycles a
+// chunk).  The operand build, not HBM, sets the kernel's speed: a clock64
+// timeline of a 32-token chunk showed ~1200 cycles of build arithmetic and
+// stores, ~300 of loads and ~300 waiting for the products of two chunks
+// before, against ~770 of tensor-core work.  All waits are bounded by GPU
+// time.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -92,13 +94,48 @@ struct AggShape {
     static constexpr int SMEM = 2 * OPS + AG_NS * 3 * RAW + SUP * 4 + 8 * 8 + NBAR * 8 + 16;
 };
 
-// 2^-S for S = n + f (fp64 sum of decay exponents): exact power of two times
-// exp2 of the fractional part; 0 for S beyond the float range, NaN stays NaN.
-__device__ __forceinline__ float exp2_neg(double S) {
-    if (!(S < 1.0e9)) return S != S ? __int_as_float(0x7fc00000) : 0.f;
-    const double n = floor(S);
-    const float f = static_cast<float>(S - n);                  // [0, 1)
-    const int e = static_cast<int>(fmax(fmin(n, 300.0), -300.0));
+// A sum of decay exponents in two-float form, hi + lo with |lo| at most
+// half an ulp of hi.  Addition takes the exact rounding error of hi + hi
+// (Knuth's TwoSum: six fp32 additions, no rounding-mode or FMA tricks), adds
+// the low parts to it and renormalises: about 48 significant bits.  An
+// infinite or NaN sum is kept as it is (hi), as fp64 would.
+struct Xs {
+    float hi, lo;
+};
+
+__device__ __forceinline__ Xs xs_add(Xs a, Xs b) {
+    const float s = a.hi + b.hi;
+    const float bp = s - a.hi;
+    const float e = ((a.hi - (s - bp)) + (b.hi - bp)) + (a.lo + b.lo);
+    const float h = s + e;
+    if (!(fabsf(s) <= 3.0e38f)) return {s, 0.f};
+    return {h, e - (h - s)};
+}
+
+__device__ __forceinline__ Xs xs_shfl_down(Xs a, int off) {
+    return {__shfl_down_sync(0xffffffffu, a.hi, off), __shfl_down_sync(0xffffffffu, a.lo, off)};
+}
+
+// S = n + f with n = floor(S) and f in [0, 1) (f rounded to fp32)
+__device__ __forceinline__ void xs_floor_frac(Xs S, float& n, float& f) {
+    n = floorf(S.hi);
+    f = (S.hi - n) + S.lo;        // S.hi - n is exact
+    if (f < 0.f) {
+        f += 1.f;
+        n -= 1.f;
+    } else if (f >= 1.f) {
+        f -= 1.f;
+        n += 1.f;
+    }
+}
+
+// 2^-S for a sum S of decay exponents: exact power of two times exp2 of the
+// fractional part; 0 for S beyond the float range, NaN stays NaN.
+__device__ __forceinline__ float exp2_neg(Xs S) {
+    if (!(S.hi < 1.0e9f)) return S.hi != S.hi ? __int_as_float(0x7fc00000) : 0.f;
+    float n, f;
+    xs_floor_frac(S, n, f);
+    const int e = static_cast<int>(fmaxf(fminf(n, 300.f), -300.f));
     return ldexpf(exp2f(-f), -e);
 }
 
@@ -157,7 +194,7 @@ diag_agg_tc_kernel(const AggArgs p) {
     unsigned char* ops = smem;                                  // [2][8 tiles]
     unsigned char* raw = smem + 2 * AG_OPS;                     // [AG_NS stages][k, beta, v]
     float* wsup = reinterpret_cast<float*>(raw + AG_NS * 3 * AG_RAW);   // [AG_SUP] weights of a super-chunk
-    double* wtot = reinterpret_cast<double*>(wsup + AG_SUP);        // [warps] warp totals
+    Xs* wtot = reinterpret_cast<Xs*>(wsup + AG_SUP);            // [warps] warp totals
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(wtot + 8);  // a stage's copies landed
     uint64_t* raw_empty = raw_full + AG_NS;                     // a stage read by every build warp
     uint64_t* mma_done = raw_empty + AG_NS;
@@ -211,7 +248,7 @@ diag_agg_tc_kernel(const AggArgs p) {
     const uint32_t tmem = *tmem_holder;
 
     const float Ah = p.A[bh % p.H];
-    double Z = 0.0;          // sum of the decay exponents of the tokens after the current super-chunk
+    Xs Z = {0.f, 0.f};       // sum of the decay exponents of the tokens after the current super-chunk
     int sup0 = tb;           // first token of the current super-chunk
     const bool builder = tid < AG_BUILD;    // else the issuing warp
     const int pr = tid & 63;                // a builder's operand rows 2 pr, 2 pr + 1
@@ -294,36 +331,38 @@ diag_agg_tc_kernel(const AggArgs p) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) dv8[u] = u0 + u < s1 ? __bfloat162float(dp[u]) : 0.f;
             }
-            double x[8], loc = 0.0;
+            float x[8];
+            Xs loc = {0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                x[u] = u0 + u < s1 ? static_cast<double>(Ah * dv8[u] * LOG2E) : 0.0;
-                loc += x[u];
+                x[u] = u0 + u < s1 ? Ah * dv8[u] * LOG2E : 0.f;
+                loc = xs_add(loc, {x[u], 0.f});
             }
-            // exclusive suffix sum over the threads after this one
-            double suf = loc;      // inclusive suffix within the warp
+            // inclusive suffix sum over the lanes from this one on
+            Xs suf = loc;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const double y = __shfl_down_sync(0xffffffffu, suf, off);
-                if (lane + off < 32) suf += y;
+                const Xs y = xs_shfl_down(suf, off);
+                if (lane + off < 32) suf = xs_add(suf, y);
             }
-            if (lane == 0) wtot[warp] = suf;
+            Xs later = xs_shfl_down(suf, 1);       // the lanes after this one
+            if (lane == 31) later = {0.f, 0.f};
+            if (lane == 0) wtot[warp] = suf;     // the warp's total
             named_sync<1>(AG_BUILD);
-            double later = suf - loc;
-            double all = 0.0;
+            Xs all = {0.f, 0.f};
 #pragma unroll
             for (int w = 0; w < AG_BUILD / 32; ++w) {
-                const double tw = wtot[w];
-                all += tw;
-                if (w > warp) later += tw;
+                const Xs tw = wtot[w];
+                all = xs_add(all, tw);
+                if (w > warp) later = xs_add(later, tw);
             }
-            later += Z;
+            later = xs_add(later, Z);
 #pragma unroll
             for (int u = 7; u >= 0; --u) {
                 wsup[8 * tid + u] = u0 + u < s1 ? exp2_neg(later) : 0.f;
-                later += x[u];
+                later = xs_add(later, {x[u], 0.f});
             }
-            Z += all;
+            Z = xs_add(Z, all);
             named_sync<1>(AG_BUILD);   // weights ready; wtot may be reused
         }
         if (!mbar_wait(&raw_full[st], rph, p.wait_ns)) ok = false;
@@ -414,16 +453,17 @@ diag_agg_tc_kernel(const AggArgs p) {
         // Z = L, the part's total decay exponent
         int R;
         float W;
-        if (!(Z < 1073741824.0)) {                 // decays to 0 (or NaN): 2^-R underflows
+        if (!(Z.hi < 1073741824.f)) {              // decays to 0 (or NaN): 2^-R underflows
             R = 1 << 30;
             W = 1.f;
-        } else if (!(Z > -1073741824.0)) {         // growth beyond any float
+        } else if (!(Z.hi > -1073741824.f)) {      // growth beyond any float
             R = -(1 << 30);
             W = 1.f;
         } else {
-            const double fl = floor(Z);
+            float fl, f;
+            xs_floor_frac(Z, fl, f);
             R = static_cast<int>(fl);
-            W = exp2f(static_cast<float>(Z - fl));
+            W = exp2f(f);
         }
         *s_wend = W;
         p.agg_scale[static_cast<long long>(part) * p.BH + bh] = {W, R};
