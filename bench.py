@@ -57,8 +57,10 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # per workload, from the ncu captures of the current kernels summarised in
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
-    "layer750m": (350_300_000 + 64_600_000) + (100_700_000 + 35_800_000) + (647_300_000 + 244_700_000),
-    "layer1p3b": 1_111_900_000 + 517_500_000,
+    # aggregates + carry + full pass, read + write
+    "longctx": (766_627_072 + 23_256_064) + (37_774_336 + 0) + (1_113_984_768 + 501_800_960),
+    "layer750m": (350_249_728 + 67_026_688) + (100_693_504 + 36_133_632) + (647_248_896 + 244_642_048),
+    "layer1p3b": 1_113_067_264 + 520_595_968,
 }
 
 
