@@ -78,10 +78,12 @@ struct Args {
     float* gq;
     float* gk;
     float* dinit;          // [2,BH,dv,dk] (dmu_0, dI_0) or null
-    float* ckpt;           // [BH*NCB][nC][32*NT]
-    float* prow;           // [NCB][BH*T][2*dv]
-    float* pD;             // [NCB][BH*T]  partial dL/dalpha_t
-    long long BH;
+    // per launch (heads bh0 .. bh0 + nbh - 1), indexed by the launch's own heads:
+    float* ckpt;           // [nbh*NCB][nC][32*NT]
+    float* prow;           // [NCB][nbh*T][2*dv]
+    float* pD;             // [NCB][nbh*T]  partial dL/dalpha_t
+    long long BH;          // all heads of the call
+    long long bh0, nbh;    // this launch's heads
     int H, T, dk, ncb, nC;
 };
 
@@ -200,7 +202,7 @@ __device__ __forceinline__ void issue_chunk(const Args& p, unsigned char* rb, lo
         const char* og = reinterpret_cast<const char*>(p.dout + tok0 * DV);
         for (int i = tid; i < op; i += NT) cp_async16(rb + Tl::r_do + i * 16, og + i * 16);
         const char* cg = reinterpret_cast<const char*>(
-            p.ckpt + ((bh * p.ncb + cb) * p.nC + c) * 32LL * NT);
+            p.ckpt + (((bh - p.bh0) * p.ncb + cb) * p.nC + c) * 32LL * NT);
 #pragma unroll
         for (int m = 0; m < 8; ++m) cp_async16(rb + Tl::r_ck + (m * NT + tid) * 16, cg + (m * NT + tid) * 16);
     }
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     constexpr int NR = Tl::NR, NCQ = Tl::NCQ, NT = Tl::NT, NW = Tl::NW;
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long bh = blockIdx.x / p.ncb;
+    const long long lbh = blockIdx.x / p.ncb;   // head within this launch
+    const long long bh = p.bh0 + lbh;
     const int cb = blockIdx.x % p.ncb;
     const bool valid = tid < Tl::NTA;
     const int rq = valid ? tid % NR : 0, cq = valid ? tid / NR : 0;
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     const float* sb = reinterpret_cast<const float*>(sm + Tl::s_b);
     const float* sbv = reinterpret_cast<const float*>(sm + Tl::s_bv);
     const float* sal = reinterpret_cast<const float*>(sm + Tl::s_al);
-    float* ckpt_cta = p.ckpt + (bh * p.ncb + cb) * static_cast<long long>(p.nC) * 32 * NT;
+    float* ckpt_cta = p.ckpt + (lbh * p.ncb + cb) * static_cast<long long>(p.nC) * 32 * NT;
     const int nC = p.nC;
     auto ntok = [&](int c) { return min(C, p.T - c * C); };
     // one forward step of the tile on token s of the converted chunk
@@ -643,7 +646,8 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         // ---- epilogue of the chunk: row partials, alpha sums, dq, dk -------
         {
             const long long tokbase = bh * p.T + t0;
-            float* prow = p.prow + (static_cast<long long>(cb) * p.BH * p.T + tokbase) * 2 * DV;
+            const long long ltok = lbh * p.T + t0;   // in this launch's partials
+            float* prow = p.prow + (static_cast<long long>(cb) * p.nbh * p.T + ltok) * 2 * DV;
             // 4 rows per thread and item: all NCQ partials loaded, then a tree sum
             constexpr int R4 = DV / 4;
 #pragma unroll 2
@@ -670,7 +674,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
                 float acc = 0.f;
 #pragma unroll
                 for (int w = 0; w < NW; ++w) acc += s_D[tid * NW + w];
-                p.pD[static_cast<long long>(cb) * p.BH * p.T + tokbase + tid + 1] = acc;
+                p.pD[static_cast<long long>(cb) * p.nbh * p.T + ltok + tid + 1] = acc;
             }
             for (int i = tid; i < n * CWB; i += NT) {
                 const int ss = i / CWB, j = i % CWB;
@@ -716,7 +720,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
             float acc = 0.f;
 #pragma unroll
             for (int w = 0; w < NW; ++w) acc += s_D[w];
-            p.pD[static_cast<long long>(cb) * p.BH * p.T + bh * p.T] = acc;
+            p.pD[static_cast<long long>(cb) * p.nbh * p.T + lbh * p.T] = acc;
         }
     }
     tc_fence_before_sync();
@@ -726,16 +730,18 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
 
 // Per (head, token): adds the column blocks' partials and forms dbeta, dv,
 // dd = -A alpha dL/dalpha and the token's dA term -d alpha dL/dalpha.  One
-// warp per token.
+// warp per token; the launch covers the BHT tokens from tok0 on, whose
+// partials (of one main-kernel launch) start at prow and pD.
 template <typename TIn, int NCBM>
 __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
     const TIn* __restrict__ v, const TIn* __restrict__ beta, const TIn* __restrict__ d,
     const float* __restrict__ A, const float* __restrict__ prow, const float* __restrict__ pD,
     float* __restrict__ dv_out, float* __restrict__ dbeta, float* __restrict__ dd,
-    float* __restrict__ eA, long long BHT, int T, int H, int dv, int ncb) {
-    const long long tok = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    float* __restrict__ eA, long long tok0, long long BHT, int T, int H, int dv, int ncb) {
+    const long long ltok = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (tok >= BHT) return;
+    if (ltok >= BHT) return;
+    const long long tok = tok0 + ltok;
     // 4 rows per lane: every partial is one 16-byte load, all issued before
     // the sums (at most NCBM column blocks: 4, or 8 for 16-column blocks)
     for (int i4 = lane; i4 < dv / 4; i4 += 32) {
@@ -743,7 +749,7 @@ __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
 #pragma unroll
         for (int cb = 0; cb < NCBM; ++cb) {
             if (cb < ncb) {
-                const float4* pr = reinterpret_cast<const float4*>(prow + (static_cast<long long>(cb) * BHT + tok) * 2 * dv);
+                const float4* pr = reinterpret_cast<const float4*>(prow + (static_cast<long long>(cb) * BHT + ltok) * 2 * dv);
                 pb[cb] = pr[i4];
                 pe[cb] = pr[dv / 4 + i4];
             } else {
@@ -765,7 +771,7 @@ __global__ void __launch_bounds__(256) diag_bwd_finalize_kernel(
     }
     if (lane == 0) {
         float g_alpha = 0.f;
-        for (int cb = 0; cb < ncb; ++cb) g_alpha += pD[static_cast<long long>(cb) * BHT + tok];
+        for (int cb = 0; cb < ncb; ++cb) g_alpha += pD[static_cast<long long>(cb) * BHT + ltok];
         const long long bh = tok / T;
         const float Ah = A[bh % H], dt = to_f<TIn>(d[tok]);
         const float alpha = expf(-Ah * dt);
@@ -814,19 +820,6 @@ cudaError_t launch_dv(int dv, const Args& p, long long grid, cudaStream_t st) {
     }
 }
 
-template <typename TIn>
-int threads_of(int dv, int cwb) {
-    const int nta = (dv / 4) * (cwb / 4);
-    return nta < 32 ? 32 : nta;
-}
-
-// Scratch of one call: checkpoints, row partials, alpha partials, dA terms.
-struct Scratch {
-    size_t ck, row, pd, ea, total;
-};
-
-inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 // Key columns per CTA: all of d_k below 32; else 32, or 16 when 32-column
 // blocks would leave more than half of the SMs idle (few heads: 16-column
 // blocks double the CTAs; the row partials to add up double too).
@@ -835,27 +828,93 @@ inline int bwd_cwb(long long BH, int dk) {
     return BH * (dk / 32) * 2 <= sm_count() ? 16 : 32;
 }
 
+// The main kernel's launches: heads [0, heads_a) with cwb_a-column blocks,
+// then heads [heads_a, BH) with cwb_b.  One CTA runs per SM.  When
+// 32-column blocks fill W >= 1 whole waves and leave a remainder of r CTAs
+// with 2 r <= SMs, the remainder's heads take 16-column blocks instead: one
+// partial wave of 16-column CTAs (each ~0.75 of a 32-column CTA's time)
+// instead of one of 32-column CTAs.
+struct BwdPlan {
+    int cwb_a, ncb_a, cwb_b, ncb_b;
+    long long heads_a, heads_b;
+};
+
+inline BwdPlan bwd_plan(long long BH, int dk) {
+    BwdPlan pl{};
+    pl.cwb_a = bwd_cwb(BH, dk);
+    pl.ncb_a = dk / pl.cwb_a;
+    pl.heads_a = BH;
+    pl.cwb_b = pl.cwb_a;
+    pl.ncb_b = pl.ncb_a;
+    if (pl.cwb_a == 32) {
+        const long long S = sm_count(), n = BH * pl.ncb_a;
+        const long long W = n / S, r = n % S;
+        if (W >= 1 && r > 0 && 2 * r <= S && (W * S) % pl.ncb_a == 0) {
+            pl.heads_a = W * S / pl.ncb_a;
+            pl.cwb_b = 16;
+            pl.ncb_b = dk / 16;
+        }
+    }
+    pl.heads_b = BH - pl.heads_a;
+    return pl;
+}
+
+// Scratch of one call: checkpoints, row partials, alpha partials (each per
+// launch), dA terms.
+struct Scratch {
+    size_t ck_a, row_a, pd_a, ck_b, row_b, pd_b, ea, total;
+};
+
+inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
     const long long BH = static_cast<long long>(B) * H;
-    const int cwb = bwd_cwb(BH, dk);
-    const int ncb = dk / cwb;
-    const int nta = (dv / 4) * (cwb / 4);
-    const int nt = nta < 32 ? 32 : nta;
+    const BwdPlan pl = bwd_plan(BH, dk);
     const long long nC = (static_cast<long long>(T) + C - 1) / C;
+    auto nt_of = [&](int cwb) {
+        const int nta = (dv / 4) * (cwb / 4);
+        return nta < 32 ? 32 : nta;
+    };
     Scratch s{};
-    s.ck = up256(static_cast<size_t>(BH) * ncb * nC * 32 * nt * 4);
-    s.row = up256(static_cast<size_t>(ncb) * BH * T * 2 * dv * 4);
-    s.pd = up256(static_cast<size_t>(ncb) * BH * T * 4);
+    s.ck_a = up256(static_cast<size_t>(pl.heads_a) * pl.ncb_a * nC * 32 * nt_of(pl.cwb_a) * 4);
+    s.row_a = up256(static_cast<size_t>(pl.ncb_a) * pl.heads_a * T * 2 * dv * 4);
+    s.pd_a = up256(static_cast<size_t>(pl.ncb_a) * pl.heads_a * T * 4);
+    s.ck_b = up256(static_cast<size_t>(pl.heads_b) * pl.ncb_b * nC * 32 * nt_of(pl.cwb_b) * 4);
+    s.row_b = up256(static_cast<size_t>(pl.ncb_b) * pl.heads_b * T * 2 * dv * 4);
+    s.pd_b = up256(static_cast<size_t>(pl.ncb_b) * pl.heads_b * T * 4);
     s.ea = up256(static_cast<size_t>(BH) * T * 4);
-    s.total = s.ck + s.row + s.pd + s.ea;
+    s.total = s.ck_a + s.row_a + s.pd_a + s.ck_b + s.row_b + s.pd_b + s.ea;
     return s;
+}
+
+// One main-kernel launch over heads [bh0, bh0 + nbh) and its finalize.
+template <typename TIn>
+cudaError_t launch_range(const DiagBwdArgs& a, Args p, long long bh0, long long nbh, int cwb,
+                         float* ck, float* prow, float* pD, float* eA, cudaStream_t st) {
+    if (nbh == 0) return cudaSuccess;
+    p.bh0 = bh0;
+    p.nbh = nbh;
+    p.ncb = a.dk / cwb;
+    p.ckpt = ck;
+    p.prow = prow;
+    p.pD = pD;
+    const long long grid = nbh * p.ncb;
+    cudaError_t e = cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
+    if (e == cudaSuccess && a.T > 0) {
+        const long long BHT = nbh * a.T;
+        auto fin = p.ncb <= 4 ? diag_bwd_finalize_kernel<TIn, 4> : diag_bwd_finalize_kernel<TIn, 8>;
+        fin<<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
+            static_cast<const TIn*>(a.v), static_cast<const TIn*>(a.beta), static_cast<const TIn*>(a.d),
+            a.A, prow, pD, a.grad_v, a.grad_beta, a.grad_d, eA, bh0 * a.T, BHT, a.T, a.H, a.dv, p.ncb);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 template <typename TIn>
 kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     const long long BH = static_cast<long long>(a.B) * a.H;
-    const int cwb = bwd_cwb(BH, a.dk);
-    const int ncb = a.dk / cwb;
+    const BwdPlan pl = bwd_plan(BH, a.dk);
     const int nC = (a.T + C - 1) / C;
     const Scratch sc = scratch_of(a.B, a.H, a.T, a.dk, a.dv);
     void* scratch = a.workspace;
@@ -866,25 +925,23 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return from_cuda(e);
     }
     unsigned char* base = static_cast<unsigned char*>(scratch);
+    auto at = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
     Args p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.d = a.d; p.A = a.A; p.Ip = a.I_prior;
     p.I0 = a.I0; p.mu0 = a.mu0; p.dout = a.grad_out; p.dfinal = a.grad_final_state;
     p.gq = a.grad_q; p.gk = a.grad_k; p.dinit = a.grad_init_state;
-    p.ckpt = reinterpret_cast<float*>(base);
-    p.prow = reinterpret_cast<float*>(base + sc.ck);
-    p.pD = reinterpret_cast<float*>(base + sc.ck + sc.row);
-    float* eA = reinterpret_cast<float*>(base + sc.ck + sc.row + sc.pd);
-    p.BH = BH; p.H = a.H; p.T = a.T; p.dk = a.dk; p.ncb = ncb; p.nC = nC;
-    const long long grid = BH * ncb;
-    e = cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
-    if (e == cudaSuccess && a.T > 0) {
-        const long long BHT = BH * a.T;
-        auto fin = ncb <= 4 ? diag_bwd_finalize_kernel<TIn, 4> : diag_bwd_finalize_kernel<TIn, 8>;
-        fin<<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
-            static_cast<const TIn*>(a.v), static_cast<const TIn*>(a.beta), static_cast<const TIn*>(a.d),
-            a.A, p.prow, p.pD, a.grad_v, a.grad_beta, a.grad_d, eA, BHT, a.T, a.H, a.dv, ncb);
-        e = cudaGetLastError();
-    }
+    p.BH = BH; p.H = a.H; p.T = a.T; p.dk = a.dk; p.nC = nC;
+    size_t off = 0;
+    float* ck_a = at(off);  off += sc.ck_a;
+    float* row_a = at(off); off += sc.row_a;
+    float* pd_a = at(off);  off += sc.pd_a;
+    float* ck_b = at(off);  off += sc.ck_b;
+    float* row_b = at(off); off += sc.row_b;
+    float* pd_b = at(off);  off += sc.pd_b;
+    float* eA = at(off);
+    e = launch_range<TIn>(a, p, 0, pl.heads_a, pl.cwb_a, ck_a, row_a, pd_a, eA, st);
+    if (e == cudaSuccess)
+        e = launch_range<TIn>(a, p, pl.heads_a, pl.heads_b, pl.cwb_b, ck_b, row_b, pd_b, eA, st);
     if (e == cudaSuccess && a.grad_A) {
         if (a.T > 0) {
             diag_bwd_dA_kernel<<<a.H, 256, 0, st>>>(eA, a.grad_A, a.B, a.H, a.T);
