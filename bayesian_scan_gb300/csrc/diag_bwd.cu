@@ -59,8 +59,14 @@ namespace bwd {
 namespace {
 
 constexpr int C = 8;             // tokens per chunk (TMEM history depth)
-constexpr uint32_t TMEM_COLS = 512;
-constexpr int MIN_SMEM = 120 * 1024;   // keeps one CTA per SM (the CTA owns all of TMEM)
+// Tensor memory and CTAs per SM: a thread's history takes 8 tokens x 32
+// columns of its warp's lane quarter, so CTAs of up to 4 warps need 256
+// columns and two of them share an SM; CTAs of 8 warps (two per quarter)
+// need all 512 and run alone.  The shared-memory floors keep the CTA count
+// per SM within what tensor memory holds (a third CTA would wait in
+// tcgen05.alloc holding its SM slot).
+constexpr int MIN_SMEM_ALONE = 120 * 1024;   // one CTA per SM
+constexpr int MIN_SMEM_PAIR = 80 * 1024;     // at most two CTAs per SM
 constexpr unsigned FULL = 0xffffffffu;
 
 struct Args {
@@ -119,6 +125,8 @@ struct Tile {
     static constexpr int s_D = s_dk + align16(C * CWB * 4);
     static constexpr int holder = s_D + align16(C * NW * 4);
     static constexpr int used = holder + 16;
+    static constexpr uint32_t TMEM_COLS = NT > 128 ? 512 : 256;
+    static constexpr int MIN_SMEM = TMEM_COLS == 512 ? MIN_SMEM_ALONE : MIN_SMEM_PAIR;
     static constexpr int SMEM = used < MIN_SMEM ? MIN_SMEM : used;
     static_assert(SMEM <= 227 * 1024, "shared memory");
     // The forward sweep stages F1 tokens at a time (several checkpoint
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     const float Ip = p.Ip;
     uint32_t* holder = reinterpret_cast<uint32_t*>(sm + Tl::holder);
 
-    if (warp == 0) tmem_alloc(holder, TMEM_COLS);
+    if (warp == 0) tmem_alloc(holder, Tl::TMEM_COLS);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -725,7 +733,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tbase, Tl::TMEM_COLS);
 }
 
 // Per (head, token): adds the column blocks' partials and forms dbeta, dv,
