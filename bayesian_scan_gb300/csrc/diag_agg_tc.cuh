@@ -88,7 +88,8 @@ struct AggShape {
     // product (two accumulators, added in the epilogue) plus A_beta x
     // B_wk2 lo, and eta is formed transposed, eta^T = k x [A_E hi | A_E mid]
     // + k x A_E lo: 4 products a K step instead of 6, and a sixth less
-    // shared memory read by the tensor core (40 KB instead of 48).
+    // shared memory read by the tensor core (40 KB instead of 48); the
+    // eta-only variant takes the two eta^T products instead of three.
     static constexpr bool WIDE = KC == 32;
     static constexpr int NBAR = 2 * AG_NS + 4;          // raw_full, raw_empty [AG_NS]; mma_done, ops_full [2]
     static constexpr int SMEM = 2 * OPS + AG_NS * 3 * RAW + SUP * 4 + 8 * 8 + NBAR * 8 + 16;
@@ -239,7 +240,7 @@ diag_agg_tc_kernel(const AggArgs p) {
         mbar_init_fence();
         for (int it = 0; it < AG_NS && it < nch; ++it) issue(it);
     }
-    constexpr bool WIDE = Sh::WIDE && !ETA_ONLY;
+    constexpr bool WIDE = Sh::WIDE;
     constexpr int TMEM_COLS = WIDE ? 4 * AG_D : AG_TMEM_COLS;
     if (warp == 0) tmem_alloc(tmem_holder, TMEM_COLS);
     tc_fence_before_sync();
@@ -290,8 +291,10 @@ diag_agg_tc_kernel(const AggArgs p) {
                     const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
                     if (WIDE) {
                         // tiles 5, 6 (and 1, 2) are adjacent: one 256-row operand
-                        umma_bf16(tmem, desc(0), desc(5), IDESC_WIDE, first);          // J: hi | mid
-                        umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);                  //  + lo
+                        if (!ETA_ONLY) {
+                            umma_bf16(tmem, desc(0), desc(5), IDESC_WIDE, first);      // J: hi | mid
+                            umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);              //  + lo
+                        }
                         umma_bf16(tmem + 2 * AG_D, desc(4), desc(1), IDESC_WIDE, first);   // eta^T: hi | mid
                         umma_bf16(tmem + 2 * AG_D, desc(4), desc(3), IDESC, 1u);       //  + lo
                         continue;
@@ -487,8 +490,13 @@ diag_agg_tc_kernel(const AggArgs p) {
                 // (and 384 + c0 + j) the value rows c0 + j
                 const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 2 * AG_D + c0;
                 float v[32], u[32];
-                tmem_ld32(ta, v);
-                tmem_ld32(ta + AG_D, u);
+                if (ETA_ONLY && half == 0) {   // J: not accumulated
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = u[j] = 0.f;
+                } else {
+                    tmem_ld32(ta, v);
+                    tmem_ld32(ta + AG_D, u);
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = nch == 0 ? 0.f : (v[j] + u[j]) * W;
                 float* base = p.agg + (static_cast<long long>(part) * p.BH + bh) * 2 * S + half * S;

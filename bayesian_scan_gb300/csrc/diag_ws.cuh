@@ -52,6 +52,13 @@ static_assert(WS_CW * 32 * WS_CREG + WS_PW * 32 * WS_PREG <= WS_THREADS * WS_LAU
 constexpr int WS_RAW = 3;                        // raw chunk stages
 constexpr int WS_PAR = 2;                        // converted chunk stages
 constexpr int WS_RB = 8;                         // tokens per reduction buffer
+// Column-pair groups (of 4 per lane row) whose two quotients share one
+// reciprocal: all 4 for d_k = 128, 3 for d_k = 64 (measured on GB300: with
+// all 4 paired the 65536-token call took 4.207 ms against 4.236 with 3, the
+// 1.3B layer's d_k = 64 call 2.506 against 2.498; with 2 paired both were
+// slower).
+template <int DK>
+__host__ __device__ constexpr int ws_pairs() { return DK == 128 ? 4 : 3; }
 // Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
 // previous flush at the start of a chunk (never inside the token loop), so
 // the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
@@ -107,6 +114,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
 diag_ws_kernel(const Params p) {
     using G = WsGeo<DK>;
     constexpr int M = G::M, PF = G::PF, RSS = G::RSS, RTS = G::RTS, WR = G::WR;
+    constexpr int WS_PAIRS = ws_pairs<DK>();
     constexpr int ES = sizeof(TIn);
     constexpr int NRED = ws_nred(TC), GPC = TC / WS_RB;   // reduction buffers, groups per chunk
     static_assert(TC % WS_RB == 0 && TC <= 16, "whole reduction groups per chunk; rescale masks hold 16 tokens");
@@ -414,7 +422,7 @@ diag_ws_kernel(const Params p) {
 #pragma unroll
                             for (int g = 0; g < 2; ++g) {
                                 const int x = 2 * g, y = 2 * g + 1;
-                                if (2 * g + half < PAIRS) {
+                                if (2 * g + half < WS_PAIRS) {
                                     const float2 N = __ffma2_rn(num[x], den[y], __fmul2_rn(num[y], den[x]));
                                     const float2 Dn = __fmul2_rn(den[x], den[y]);
                                     acc[r] = __ffma2_rn(N, make_float2(rcp_approx(Dn.x), rcp_approx(Dn.y)), acc[r]);
