@@ -58,9 +58,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_627_072 + 23_256_064) + (37_774_336 + 0) + (1_113_984_768 + 501_800_960),
-    "layer750m": (350_249_728 + 67_026_688) + (100_693_504 + 36_133_632) + (647_248_896 + 244_642_048),
-    "layer1p3b": 1_113_067_264 + 520_595_968,
+    "longctx": (766_602_240 + 23_228_160) + (37_774_592 + 0) + (1_115_165_696 + 502_205_952),
+    "layer750m": (350_261_760 + 67_215_872) + (100_699_648 + 36_345_600) + (647_259_904 + 244_735_488),
+    "layer1p3b": 1_111_899_392 + 520_670_720,
 }
 
 
