@@ -8,26 +8,34 @@
 //
 //  * 8 consumer warps own the state, 4 rows x 16 columns per lane, and do
 //    nothing but the element updates and the readout partials: per token they
-//    read the converted k, k^2, q and the token scalars from shared memory,
-//    beta and v of their rows from the raw chunk, update 64 elements and
-//    store 4 row partials to a reduction buffer.  After `setmaxnreg.inc` they
-//    hold 232 registers each.
+//    read the converted k, k^2, q, the token scalars and their rows' W beta,
+//    W beta v (for d_k = 64: beta and v from the raw chunk, scaled by W
+//    themselves) from shared memory, update 64 elements and store 4 row
+//    partials to a reduction buffer.  After `setmaxnreg.inc` they hold 232 registers
+//    each.
 //  * 4 producer warps (one warpgroup, 40 registers each after
 //    `setmaxnreg.dec`) keep the consumers fed: they issue the 1-D bulk copies
 //    of each chunk of q, k, v, beta, d, convert k -> (k, k^2) and q to fp32 in
-//    the consumers' interleaved layout, run the per-head scale recursion, and
-//    sum the readout partials of every 8 tokens over the lanes of a row and
-//    store o with streaming 16-byte stores.
+//    the consumers' interleaved layout, run the per-head scale recursion and
+//    (d_k = 128) scale each row's beta and beta v by the token's W, and sum
+//    the readout
+//    partials of every 8 tokens over the lanes of a row and store o with
+//    streaming 16-byte stores.  (For d_k = 128 the row scaling moved here
+//    from the consumers: it took them ~16 instructions per token, and with
+//    no consumer reading the raw chunk two raw stages are enough, which pays
+//    for the larger converted chunk.)
 //
 // Pipeline (mbarriers, every wait bounded by GPU time):
-//   raw_full[3]   bulk copies of a chunk landed          (tx count)
+//   raw_full[r]   bulk copies of a chunk landed          (tx count; r = 2 or 3)
 //   par_full[2]   a chunk's converted inputs and scalars  (128 producer threads)
 //   par_empty[2]  consumers finished a chunk              (256 consumer threads)
 //   red_full[n]   8 tokens of row partials written        (256 consumer threads)
 //   red_empty[n]  those partials summed and stored        (128 producer threads)
-// The producers prepare chunk c + 2 and issue the copies of chunk c + 3 as
-// soon as the consumers release chunk c, so the consumers never wait on them
-// in steady state.  Row partials go to n = TC / 8 + 1 buffers of 8 tokens;
+// The producers prepare chunk c + 2 as soon as the consumers release chunk
+// c; with two raw stages they then (after a producer-only named barrier)
+// refill its raw stage with the copies of chunk c + 4, with three they first
+// issue the copies of chunk c + 3 into chunk c's stage.  The consumers never
+// wait on them in steady state.  Row partials go to n = TC / 8 + 1 buffers of 8 tokens;
 // consumers wait for a buffer at the start of a chunk, never in the token
 // loop (its registers hold the state and the token's operands only).
 //
@@ -49,7 +57,15 @@ constexpr int WS_PREG = 40;                      // registers per producer threa
 constexpr int WS_LAUNCH_REG = 168;               // per thread at launch (65536 / 384, rounded down to 8)
 static_assert(WS_CW * 32 * WS_CREG + WS_PW * 32 * WS_PREG <= WS_THREADS * WS_LAUNCH_REG,
               "the register split must fit the CTA's launch allocation");
-constexpr int WS_RAW = 3;                        // raw chunk stages
+// Where each row's W beta and W beta v are formed: by the producers for
+// d_k = 128 (the consumers then read no raw input and two raw stages
+// suffice; measured 2.1 % faster on both d_k = 128 workloads), by the
+// consumers for d_k = 64, whose producers serve 4 heads per CTA and became
+// the bottleneck with the extra pass (4.8 % slower).
+__host__ __device__ constexpr bool ws_row_scale_in_producers(int dk) { return dk == 128; }
+// raw chunk stages: 2 when only the producers read them, else 3 (the
+// consumers read beta and v of a chunk while the producers prepare the next)
+__host__ __device__ constexpr int ws_raw(int dk) { return ws_row_scale_in_producers(dk) ? 2 : 3; }
 constexpr int WS_PAR = 2;                        // converted chunk stages
 constexpr int WS_RB = 8;                         // tokens per reduction buffer
 // Column-pair groups (of 4 per lane row) whose two quotients share one
@@ -64,6 +80,13 @@ __host__ __device__ constexpr int ws_pairs() { return DK == 128 ? 4 : 3; }
 // the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
 // previous chunk's last group to overlap the next chunk.
 __host__ __device__ constexpr int ws_nred(int TC) { return TC / WS_RB + 1; }
+// Floats per token and head of a converted chunk: k, k^2, q (d_k each, in
+// the consumers' interleaving), the token's scalars (rescale factor, W,
+// W I_prior sigma, rescale mask), then, when the producers scale the rows,
+// per value row W beta and W beta v (d_v each).
+__host__ __device__ constexpr int ws_par_floats(int dk, int dv) {
+    return 3 * dk + 4 + (ws_row_scale_in_producers(dk) ? 2 * dv : 0);
+}
 
 template <int DK>
 struct WsGeo {
@@ -71,7 +94,6 @@ struct WsGeo {
     static constexpr int RS = 32 / M;            // row sets per warp
     static constexpr int WR = RS * RT;           // rows per warp
     static constexpr int ROWS = WS_CW * WR;      // rows per CTA
-    static constexpr int PF = 3 * DK + 4;        // floats per token and head of a converted chunk
     static constexpr int RSS = red_rs_stride(M);
     static constexpr int RTS = red_token_stride(M);
     static constexpr int RED_FLOATS = WS_CW * WS_RB * RTS;   // one reduction buffer
@@ -90,15 +112,15 @@ struct WsLayout {
         raw_d = (TC * es + 15) & ~15;
         raw_head = 2 * raw_qk + 2 * raw_vb + raw_d;
         raw_stage = hpc * raw_head;
-        par_head = TC * (3 * dk + 4) * 4;
+        par_head = TC * ws_par_floats(dk, dv) * 4;
         par_stage = hpc * par_head;
         red_buf = red_floats * 4;
-        off_par = WS_RAW * raw_stage;
+        off_par = ws_raw(dk) * raw_stage;
         off_red = off_par + WS_PAR * par_stage;
         off_bar = off_red + nred * red_buf;
-        // barriers: raw_full[3], par_full[2], par_empty[2], red_full[nred],
+        // barriers: raw_full[2], par_full[2], par_empty[2], red_full[nred],
         // red_empty[nred]; then the scale state W[hpc], R[hpc]
-        total = off_bar + (WS_RAW + 2 * WS_PAR + 2 * nred) * 8 + 8 * hpc;
+        total = off_bar + (ws_raw(dk) + 2 * WS_PAR + 2 * nred) * 8 + 8 * hpc;
     }
 };
 
@@ -113,7 +135,7 @@ template <int DK, typename TIn, int TC>
 __global__ void __launch_bounds__(WS_THREADS, 1)
 diag_ws_kernel(const Params p) {
     using G = WsGeo<DK>;
-    constexpr int M = G::M, PF = G::PF, RSS = G::RSS, RTS = G::RTS, WR = G::WR;
+    constexpr int M = G::M, RSS = G::RSS, RTS = G::RTS, WR = G::WR;
     constexpr int WS_PAIRS = ws_pairs<DK>();
     constexpr int ES = sizeof(TIn);
     constexpr int NRED = ws_nred(TC), GPC = TC / WS_RB;   // reduction buffers, groups per chunk
@@ -121,6 +143,9 @@ diag_ws_kernel(const Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int dv = p.dv, HPC = G::ROWS / dv;
+    const int PF = ws_par_floats(DK, dv);
+    constexpr bool PSCALE = ws_row_scale_in_producers(DK);
+    constexpr int WS_RAW = ws_raw(DK);
     const WsLayout L(DK, dv, ES, TC, HPC, G::RED_FLOATS);
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
     uint64_t* par_full = raw_full + WS_RAW;
@@ -245,7 +270,35 @@ diag_ws_kernel(const Params p) {
                 w_state[h] = W;
                 r_state[h] = R;
             }
+            if constexpr (PSCALE) {
+                // the rows' scaled inputs W beta, W beta v of every token, by
+                // all producers once the tokens' W are written
+                asm volatile("bar.sync 1, %0;" ::"n"(WS_PW * 32) : "memory");
+                const int Q = dv / 4;
+                for (int x = pt; x < nheads * tcn * Q; x += WS_PW * 32) {
+                    const int i4 = x % Q, ht = x / Q;
+                    const int tt = ht % tcn, h = ht / tcn;
+                    float* ps = par(s2, h) + tt * PF + 3 * DK;
+                    const float W = ps[1];
+                    float bet[4], val[4];
+                    load4(raw_b(s3, h) + tt * dv + 4 * i4, bet);
+                    load4(raw_v(s3, h) + tt * dv + 4 * i4, val);
+                    const float4 sb = make_float4(W * bet[0], W * bet[1], W * bet[2], W * bet[3]);
+                    *reinterpret_cast<float4*>(ps + 4 + 4 * i4) = sb;
+                    *reinterpret_cast<float4*>(ps + 4 + dv + 4 * i4) =
+                        make_float4(sb.x * val[0], sb.y * val[1], sb.z * val[2], sb.w * val[3]);
+                }
+            }
             mbar_arrive(&par_full[s2]);
+        };
+        // prepare chunk c, then (once every producer has read its raw stage)
+        // refill that stage with the copies of chunk c + WS_RAW
+        auto prepare_refill = [&](int c) {
+            prepare(c);
+            if constexpr (PSCALE) {
+                asm volatile("bar.sync 1, %0;" ::"n"(WS_PW * 32) : "memory");
+                if (pt == 0 && c + WS_RAW < nch) issue(c + WS_RAW);
+            }
         };
 
         // sum the row partials of reduction group g (tokens g*8 .. of the
@@ -282,16 +335,17 @@ diag_ws_kernel(const Params p) {
 
         if (pt == 0)
             for (int c = 0; c < WS_RAW && c < nch; ++c) issue(c);
-        if (nch > 0) prepare(0);
-        if (nch > 1) prepare(1);
+        if (nch > 0) prepare_refill(0);
+        if (nch > 1) prepare_refill(1);
         int g_next = 0;   // next reduction group to flush
         for (int c = 0; c < nch; ++c) {
             const int t_end = min(te, tb + (c + 1) * TC);   // tokens before t_end belong to chunks <= c
             for (; tb + g_next * WS_RB < t_end; ++g_next) flush(g_next);
             // the consumers have released chunk c: its stages can be reused
             if (!mbar_wait(&par_empty[c & 1], (c >> 1) & 1, p.wait_ns)) ok = false;
-            if (pt == 0 && c + WS_RAW < nch) issue(c + WS_RAW);
-            if (c + 2 < nch) prepare(c + 2);
+            // (consumers reading raw beta, v: chunk c's raw stage is free now)
+            if (!PSCALE && pt == 0 && c + WS_RAW < nch) issue(c + WS_RAW);
+            if (c + 2 < nch) prepare_refill(c + 2);
         }
     } else {
         // =========================== consumers ================================
@@ -377,16 +431,24 @@ diag_ws_kernel(const Params p) {
                     const int b = (c * GPC + tt / WS_RB) % NRED;
                     const float* ptk = pbase + tt * PF;
                     const float4 sc = *reinterpret_cast<const float4*>(ptk + 3 * DK);
-                    float bet[RT], val[RT];
-                    load4(rbp + tt * dv, bet);
-                    load4(rv + tt * dv, val);
                     W = sc.y;
+                    static_assert(RT == 4, "one float4 of row scalars per lane");
                     float2 SB[RT], SBV[RT];
+                    if constexpr (PSCALE) {
+                        const float4 sb4 = *reinterpret_cast<const float4*>(ptk + 3 * DK + 4 + i0);
+                        const float4 sv4 = *reinterpret_cast<const float4*>(ptk + 3 * DK + 4 + dv + i0);
+                        SB[0] = f2(sb4.x); SB[1] = f2(sb4.y); SB[2] = f2(sb4.z); SB[3] = f2(sb4.w);
+                        SBV[0] = f2(sv4.x); SBV[1] = f2(sv4.y); SBV[2] = f2(sv4.z); SBV[3] = f2(sv4.w);
+                    } else {
+                        float bet[RT], val[RT];
+                        load4(rbp + tt * dv, bet);
+                        load4(rv + tt * dv, val);
 #pragma unroll
-                    for (int r = 0; r < RT; ++r) {
-                        const float sb = W * bet[r];
-                        SB[r] = f2(sb);
-                        SBV[r] = f2(sb * val[r]);
+                        for (int r = 0; r < RT; ++r) {
+                            const float sb = W * bet[r];
+                            SB[r] = f2(sb);
+                            SBV[r] = f2(sb * val[r]);
+                        }
                     }
                     const float2 SP = f2(sc.z), SG = f2(SIGMA);
                     float2 acc[RT];
