@@ -58,9 +58,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_602_240 + 23_228_160) + (37_774_592 + 0) + (1_115_165_696 + 502_205_952),
-    "layer750m": (350_261_760 + 67_215_872) + (100_699_648 + 36_345_600) + (647_259_904 + 244_735_488),
-    "layer1p3b": 1_111_899_392 + 520_670_720,
+    "longctx": (766_519_552 + 23_238_656) + (37_775_104 + 0) + (1_113_857_792 + 501_525_504),
+    "layer750m": (350_348_544 + 67_167_488) + (100_702_208 + 35_930_368) + (647_368_960 + 244_456_192),
+    "layer1p3b": 1_112_311_040 + 520_706_560,
 }
 
 
