@@ -113,9 +113,12 @@ def test_resume_equals_single_call():
 
 @pytest.mark.parametrize("law", [("const", 0.0), ("const", 1e-3), ("const", 30.0),
                                  ("const", 300.0), ("uniform", 0.5, 4.0)])
-def test_gate_extremes(law):
-    # A = 0 (no forgetting), tiny A, and very fast forgetting (alpha underflows)
-    parity.check_diag(draw(1, 2, 200, 64, 64, A_law=law))
+@pytest.mark.parametrize("d", [64, 128])
+def test_gate_extremes(law, d):
+    # A = 0 (no forgetting), tiny A, and very fast forgetting (alpha underflows;
+    # the working scale rescales the state on most tokens); d = 128 takes the
+    # full pass whose producers scale the rows' inputs by W
+    parity.check_diag(draw(1, 2, 203, d, d, A_law=law))
 
 
 def test_zero_gate_input():
@@ -125,8 +128,9 @@ def test_zero_gate_input():
 
 
 @pytest.mark.parametrize("I_prior", [1e-3, 1.0, 50.0, 1e4])
-def test_prior_scale(I_prior):
-    inp = draw(1, 2, 120, 64, 64)
+@pytest.mark.parametrize("d", [64, 128])
+def test_prior_scale(I_prior, d):
+    inp = draw(1, 2, 120, d, d)
     inp["I_prior"] = I_prior
     parity.check_diag(inp)
 
