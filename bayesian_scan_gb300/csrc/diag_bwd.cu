@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "kdn.h"
 #include "kdn_device.cuh"
@@ -895,10 +896,10 @@ inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
     return s;
 }
 
-// One main-kernel launch over heads [bh0, bh0 + nbh) and its finalize.
+// The main kernel over heads [bh0, bh0 + nbh).
 template <typename TIn>
-cudaError_t launch_range(const DiagBwdArgs& a, Args p, long long bh0, long long nbh, int cwb,
-                         float* ck, float* prow, float* pD, float* eA, cudaStream_t st) {
+cudaError_t launch_main_range(const DiagBwdArgs& a, Args p, long long bh0, long long nbh, int cwb,
+                              float* ck, float* prow, float* pD, cudaStream_t st) {
     if (nbh == 0) return cudaSuccess;
     p.bh0 = bh0;
     p.nbh = nbh;
@@ -907,16 +908,40 @@ cudaError_t launch_range(const DiagBwdArgs& a, Args p, long long bh0, long long 
     p.prow = prow;
     p.pD = pD;
     const long long grid = nbh * p.ncb;
-    cudaError_t e = cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
-    if (e == cudaSuccess && a.T > 0) {
-        const long long BHT = nbh * a.T;
-        auto fin = p.ncb <= 4 ? diag_bwd_finalize_kernel<TIn, 4> : diag_bwd_finalize_kernel<TIn, 8>;
-        fin<<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
-            static_cast<const TIn*>(a.v), static_cast<const TIn*>(a.beta), static_cast<const TIn*>(a.d),
-            a.A, prow, pD, a.grad_v, a.grad_beta, a.grad_d, eA, bh0 * a.T, BHT, a.T, a.H, a.dv, p.ncb);
-        e = cudaGetLastError();
+    return cwb == 16 ? launch_dv<TIn, 16>(a.dv, p, grid, st) : launch_dv<TIn, 32>(a.dv, p, grid, st);
+}
+
+// The finalize kernel over the same heads (their row and alpha partials).
+template <typename TIn>
+cudaError_t launch_finalize_range(const DiagBwdArgs& a, long long bh0, long long nbh, int cwb,
+                                  const float* prow, const float* pD, float* eA, cudaStream_t st) {
+    if (nbh == 0 || a.T <= 0) return cudaSuccess;
+    const int ncb = a.dk / cwb;
+    const long long BHT = nbh * a.T;
+    auto fin = ncb <= 4 ? diag_bwd_finalize_kernel<TIn, 4> : diag_bwd_finalize_kernel<TIn, 8>;
+    fin<<<static_cast<unsigned>((BHT + 7) / 8), 256, 0, st>>>(
+        static_cast<const TIn*>(a.v), static_cast<const TIn*>(a.beta), static_cast<const TIn*>(a.d),
+        a.A, prow, pD, a.grad_v, a.grad_beta, a.grad_d, eA, bh0 * a.T, BHT, a.T, a.H, a.dv, ncb);
+    return cudaGetLastError();
+}
+
+// A stream of the library's own per device, on which the first launch's
+// finalize (HBM-bound) runs while the second launch's main kernel (which
+// leaves SMs free) computes; joined back by events.
+cudaError_t side_stream(cudaStream_t* out) {
+    static cudaStream_t streams[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev]) {
+        e = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
     }
-    return e;
+    *out = streams[dev];
+    return cudaSuccess;
 }
 
 template <typename TIn>
@@ -947,9 +972,35 @@ kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     float* row_b = at(off); off += sc.row_b;
     float* pd_b = at(off);  off += sc.pd_b;
     float* eA = at(off);
-    e = launch_range<TIn>(a, p, 0, pl.heads_a, pl.cwb_a, ck_a, row_a, pd_a, eA, st);
-    if (e == cudaSuccess)
-        e = launch_range<TIn>(a, p, pl.heads_a, pl.heads_b, pl.cwb_b, ck_b, row_b, pd_b, eA, st);
+    e = launch_main_range<TIn>(a, p, 0, pl.heads_a, pl.cwb_a, ck_a, row_a, pd_a, st);
+    if (e == cudaSuccess && pl.heads_b == 0) {
+        e = launch_finalize_range<TIn>(a, 0, pl.heads_a, pl.cwb_a, row_a, pd_a, eA, st);
+    } else if (e == cudaSuccess) {
+        // the first launch's finalize on the side stream, concurrent with the
+        // second launch's main kernel; the caller's stream waits for it
+        cudaStream_t side = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        e = side_stream(&side);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventRecord(fork, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+        if (e == cudaSuccess) e = launch_finalize_range<TIn>(a, 0, pl.heads_a, pl.cwb_a, row_a, pd_a, eA, side);
+        const bool forked = e == cudaSuccess;   // side-stream work is enqueued from here on
+        if (forked) e = cudaEventRecord(join, side);
+        if (e == cudaSuccess)
+            e = launch_main_range<TIn>(a, p, pl.heads_a, pl.heads_b, pl.cwb_b, ck_b, row_b, pd_b, st);
+        if (e == cudaSuccess)
+            e = launch_finalize_range<TIn>(a, pl.heads_a, pl.heads_b, pl.cwb_b, row_b, pd_b, eA, st);
+        // join even after an error, so that no later work on the caller's
+        // stream (freeing the scratch) overtakes the side stream's finalize
+        if (forked) {
+            const cudaError_t ej = cudaStreamWaitEvent(st, join, 0);
+            if (e == cudaSuccess) e = ej;
+        }
+        if (fork) cudaEventDestroy(fork);
+        if (join) cudaEventDestroy(join);
+    }
     if (e == cudaSuccess && a.grad_A) {
         if (a.T > 0) {
             diag_bwd_dA_kernel<<<a.H, 256, 0, st>>>(eA, a.grad_A, a.B, a.H, a.T);
