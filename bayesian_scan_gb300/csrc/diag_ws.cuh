@@ -11,16 +11,15 @@
 //    read the converted k, k^2, q, the token scalars and their rows' W beta,
 //    W beta v (for d_k = 64: beta and v from the raw chunk, scaled by W
 //    themselves) from shared memory, update 64 elements and store 4 row
-//    partials to a reduction buffer.  After `setmaxnreg.inc` they hold 232 registers
-//    each.
+//    partials to a reduction buffer.  After `setmaxnreg.inc` they hold 232
+//    registers each.
 //  * 4 producer warps (one warpgroup, 40 registers each after
 //    `setmaxnreg.dec`) keep the consumers fed: they issue the 1-D bulk copies
 //    of each chunk of q, k, v, beta, d, convert k -> (k, k^2) and q to fp32 in
 //    the consumers' interleaved layout, run the per-head scale recursion and
 //    (d_k = 128) scale each row's beta and beta v by the token's W, and sum
-//    the readout
-//    partials of every 8 tokens over the lanes of a row and store o with
-//    streaming 16-byte stores.  (For d_k = 128 the row scaling moved here
+//    the readout partials of every 8 tokens over the lanes of a row and
+//    store o with streaming 16-byte stores.  (For d_k = 128 the row scaling moved here
 //    from the consumers: it took them ~16 instructions per token, and with
 //    no consumer reading the raw chunk two raw stages are enough, which pays
 //    for the larger converted chunk.)
@@ -35,9 +34,10 @@
 // c; with two raw stages they then (after a producer-only named barrier)
 // refill its raw stage with the copies of chunk c + 4, with three they first
 // issue the copies of chunk c + 3 into chunk c's stage.  The consumers never
-// wait on them in steady state.  Row partials go to n = TC / 8 + 1 buffers of 8 tokens;
-// consumers wait for a buffer at the start of a chunk, never in the token
-// loop (its registers hold the state and the token's operands only).
+// wait on them in steady state.  Row partials go to n = TC / 8 + 1 buffers
+// of 8 tokens; consumers wait for a buffer at the start of a chunk, never in
+// the token loop (its registers hold the state and the token's operands
+// only).
 //
 // A CTA owns ROWS = 8 * rows-per-warp consecutive state rows (128 for
 // d_k = 128, 256 for d_k = 64: whole heads, ROWS / d_v of them) for one
@@ -118,7 +118,7 @@ struct WsLayout {
         off_par = ws_raw(dk) * raw_stage;
         off_red = off_par + WS_PAR * par_stage;
         off_bar = off_red + nred * red_buf;
-        // barriers: raw_full[2], par_full[2], par_empty[2], red_full[nred],
+        // barriers: raw_full[ws_raw], par_full[2], par_empty[2], red_full[nred],
         // red_empty[nred]; then the scale state W[hpc], R[hpc]
         total = off_bar + (ws_raw(dk) + 2 * WS_PAR + 2 * nred) * 8 + 8 * hpc;
     }
