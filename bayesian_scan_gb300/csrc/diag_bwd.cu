@@ -838,17 +838,18 @@ inline int bwd_cwb(long long BH, int dk) {
 }
 
 // The main kernel's launches: heads [0, heads_a) with cwb_a-column blocks,
-// then heads [heads_a, BH) with cwb_b.  One CTA runs per SM.  When
-// 32-column blocks fill W >= 1 whole waves and leave a remainder of r CTAs
-// with 2 r <= SMs, the remainder's heads take 16-column blocks instead: one
-// partial wave of 16-column CTAs (each ~0.75 of a 32-column CTA's time)
-// instead of one of 32-column CTAs.
+// then heads [heads_a, BH) with cwb_b.  A wave is the CTA slots of the GPU
+// (one 8-warp CTA per SM, or two of up to 4 warps).  When 32-column blocks
+// fill W >= 1 whole waves and leave a remainder of r CTAs with 2 r <= one
+// wave, the remainder's heads take 16-column blocks instead: one partial
+// wave of 16-column CTAs (each ~0.75 of a 32-column CTA's time) instead of
+// one of 32-column CTAs.
 struct BwdPlan {
     int cwb_a, ncb_a, cwb_b, ncb_b;
     long long heads_a, heads_b;
 };
 
-inline BwdPlan bwd_plan(long long BH, int dk) {
+inline BwdPlan bwd_plan(long long BH, int dk, int dv) {
     BwdPlan pl{};
     pl.cwb_a = bwd_cwb(BH, dk);
     pl.ncb_a = dk / pl.cwb_a;
@@ -856,7 +857,8 @@ inline BwdPlan bwd_plan(long long BH, int dk) {
     pl.cwb_b = pl.cwb_a;
     pl.ncb_b = pl.ncb_a;
     if (pl.cwb_a == 32) {
-        const long long S = sm_count(), n = BH * pl.ncb_a;
+        const int nt = (dv / 4) * 8;   // threads of a 32-column CTA
+        const long long S = static_cast<long long>(sm_count()) * (nt > 128 ? 1 : 2), n = BH * pl.ncb_a;
         const long long W = n / S, r = n % S;
         if (W >= 1 && r > 0 && 2 * r <= S && (W * S) % pl.ncb_a == 0) {
             pl.heads_a = W * S / pl.ncb_a;
@@ -878,7 +880,7 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
     const long long BH = static_cast<long long>(B) * H;
-    const BwdPlan pl = bwd_plan(BH, dk);
+    const BwdPlan pl = bwd_plan(BH, dk, dv);
     const long long nC = (static_cast<long long>(T) + C - 1) / C;
     auto nt_of = [&](int cwb) {
         const int nta = (dv / 4) * (cwb / 4);
@@ -947,7 +949,7 @@ cudaError_t side_stream(cudaStream_t* out) {
 template <typename TIn>
 kdn_status launch(const DiagBwdArgs& a, cudaStream_t st) {
     const long long BH = static_cast<long long>(a.B) * a.H;
-    const BwdPlan pl = bwd_plan(BH, a.dk);
+    const BwdPlan pl = bwd_plan(BH, a.dk, a.dv);
     const int nC = (a.T + C - 1) / C;
     const Scratch sc = scratch_of(a.B, a.H, a.T, a.dk, a.dv);
     void* scratch = a.workspace;

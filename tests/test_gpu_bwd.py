@@ -123,17 +123,19 @@ def test_bwd_library_workspace_and_caller_workspace_agree():
         assert torch.equal(out[n].cpu(), ref[n]), n
 
 
-def _mixed_head_count(sms, dk=128):
-    """The smallest head count whose 32-column blocks fill whole waves of one
-    CTA per SM and leave a remainder of at most half a wave: the call then
-    finishes the remainder's heads with 16-column blocks (two launches of
-    the main kernel, each with its own partials and finalize)."""
+def _mixed_head_count(sms, dk=128, dv=128):
+    """The smallest head count whose 32-column blocks fill whole waves and
+    leave a remainder of at most half a wave: the call then finishes the
+    remainder's heads with 16-column blocks (two launches of the main
+    kernel, each with its own partials and finalize).  A wave is one 8-warp
+    CTA per SM (d_v = 128), or two CTAs of up to 4 warps."""
     ncb = dk // 32
-    for bh in range(1, 8 * sms):
+    slots = sms * (1 if (dv // 4) * 8 > 128 else 2)
+    for bh in range(1, 8 * slots):
         if bh * ncb * 2 <= sms:
             continue   # few heads: 16-column blocks throughout
-        waves, rem = divmod(bh * ncb, sms)
-        if waves >= 1 and rem > 0 and 2 * rem <= sms and (waves * sms) % ncb == 0:
+        waves, rem = divmod(bh * ncb, slots)
+        if waves >= 1 and rem > 0 and 2 * rem <= slots and (waves * slots) % ncb == 0:
             return bh
     raise AssertionError("no mixed plan for this SM count")
 
@@ -142,6 +144,6 @@ def _mixed_head_count(sms, dk=128):
 def test_bwd_mixed_column_blocks(dv):
     # heads split between a launch of 32-column and one of 16-column blocks
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    H = _mixed_head_count(sms)
+    H = _mixed_head_count(sms, dv=dv)
     inp, gout, gfs, I0, mu0 = make(1, H, 19, 128, dv, torch.bfloat16, seed=40 + dv, state=True)
     parity.check_bwd(inp, gout, gfs, I0, mu0)
