@@ -28,15 +28,16 @@
 //     dI_0 = GJ + GE mu_0,   dmu_0 = GE I_0.
 //
 // How.  The adjoint sweep needs every forward state in reverse order.  A CTA
-// owns all d_v rows of a head and a block of CWB (<= 32) key columns: 16
-// elements (4 rows x 4 columns) per thread, so all column sums of a token
-// (dq, dk) finish inside the CTA and the row sums leave it as CWB-column
-// partials.  The CTA first runs the forward update over the whole sequence,
+// owns all d_v rows of a head and a block of CWB (<= 32) key columns: 4
+// rows x CPT columns per thread (CPT = 4 for 32-column blocks, 2 for
+// 16-column blocks, which then have as many threads as 32-column ones), so
+// all column sums of a token (dq, dk) finish inside the CTA and the row sums
+// leave it as CWB-column partials.  The CTA first runs the forward update over the whole sequence,
 // storing its tile's state every C = 8 tokens (a checkpoint) in device
 // memory; it then walks the chunks backwards: load the chunk's checkpoint,
 // re-run the chunk's C forward steps keeping each token's state in tensor
-// memory (TMEM: 512 columns x 128 lanes = 8 tokens x 32 words per thread,
-// written with tcgen05.st, read back with tcgen05.ld), and take the C adjoint
+// memory (TMEM: 8 tokens x 8 CPT words per thread in its warp's lane
+// quarter, written with tcgen05.st, read back with tcgen05.ld), and take the C adjoint
 // steps from the last token down.  Inputs, checkpoints and dout of the next
 // chunk are brought into shared memory by cp.async while the current chunk
 // computes.  Column sums go through warp shuffles (a halving transpose-
@@ -60,14 +61,14 @@ namespace bwd {
 namespace {
 
 constexpr int C = 8;             // tokens per chunk (TMEM history depth)
-// Tensor memory and CTAs per SM: a thread's history takes 8 tokens x 32
-// columns of its warp's lane quarter, so CTAs of up to 4 warps need 256
-// columns and two of them share an SM; CTAs of 8 warps (two per quarter)
-// need all 512 and run alone.  The shared-memory floors keep the CTA count
-// per SM within what tensor memory holds (a third CTA would wait in
-// tcgen05.alloc holding its SM slot).
+// Tensor memory and CTAs per SM: a thread's history takes 8 tokens x 8 CPT
+// columns of its warp's lane quarter (256 for CPT = 4, 128 for CPT = 2),
+// doubled for CTAs of 8 warps (two per quarter).  The shared-memory floors
+// keep the CTA count per SM within what tensor memory holds (a CTA past it
+// would wait in tcgen05.alloc holding its SM slot).
 constexpr int MIN_SMEM_ALONE = 120 * 1024;   // one CTA per SM
 constexpr int MIN_SMEM_PAIR = 80 * 1024;     // at most two CTAs per SM
+constexpr int MIN_SMEM_QUAD = 48 * 1024;     // at most four CTAs per SM
 constexpr unsigned FULL = 0xffffffffu;
 
 struct Args {
@@ -86,7 +87,7 @@ struct Args {
     float* gk;
     float* dinit;          // [2,BH,dv,dk] (dmu_0, dI_0) or null
     // per launch (heads bh0 .. bh0 + nbh - 1), indexed by the launch's own heads:
-    float* ckpt;           // [nbh*NCB][nC][32*NT]
+    float* ckpt;           // [nbh*NCB][nC][SW*NT]
     float* prow;           // [NCB][nbh*T][2*dv]
     float* pD;             // [NCB][nbh*T]  partial dL/dalpha_t
     long long BH;          // all heads of the call
@@ -96,12 +97,17 @@ struct Args {
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-// Tile of one CTA: all DV rows x CWB key columns; a thread owns 4 rows x 4
-// columns (NR row quads x NCQ column quads; lanes run over the row quads).
+// Tile of one CTA: all DV rows x CWB key columns; a thread owns 4 rows x
+// CPT columns (NR row quads x NCQ column groups; lanes run over the row
+// quads): CPT = 4 for 32-column blocks, 2 for 16-column blocks, whose CTAs
+// then have as many warps as the 32-column ones (the few-head calls that
+// take 16-column blocks had one warp per scheduler with 4 columns a thread).
 template <typename TIn, int DV, int CWB>
 struct Tile {
     static constexpr int ES = sizeof(TIn);
-    static constexpr int NR = DV / 4, NCQ = CWB / 4, NTA = NR * NCQ;
+    static constexpr int CPT = CWB == 32 ? 4 : 2;
+    static constexpr int NR = DV / 4, NCQ = CWB / CPT, NTA = NR * NCQ;
+    static constexpr int SW = 8 * CPT;           // state words of a thread per token (J, eta)
     static constexpr int NT = NTA < 32 ? 32 : NTA, NW = NT / 32;
     static_assert(NT <= 256, "at most 8 warps (two per TMEM lane quarter)");
     // shared memory (byte offsets)
@@ -117,7 +123,7 @@ struct Tile {
     static constexpr int r_v = r_b + align16(C * DV * ES);
     static constexpr int r_do = r_v + align16(C * DV * ES);
     static constexpr int r_ck = r_do + align16(C * DV * 4);
-    static constexpr int RAW = r_ck + align16(32 * NT * 4);
+    static constexpr int RAW = r_ck + align16(SW * NT * 4);
     static constexpr int raw0 = s_al + align16(C * 4);
     static constexpr int raw1 = raw0 + RAW;
     static constexpr int s_row = raw1 + RAW;
@@ -126,8 +132,12 @@ struct Tile {
     static constexpr int s_D = s_dk + align16(C * CWB * 4);
     static constexpr int holder = s_D + align16(C * NW * 4);
     static constexpr int used = holder + 16;
-    static constexpr uint32_t TMEM_COLS = NT > 128 ? 512 : 256;
-    static constexpr int MIN_SMEM = TMEM_COLS == 512 ? MIN_SMEM_ALONE : MIN_SMEM_PAIR;
+    // TMEM: C tokens x SW columns of history per thread, in its warp's lane
+    // quarter; two warps share a quarter when there are more than four
+    static constexpr uint32_t HIST_COLS = C * SW;
+    static constexpr uint32_t TMEM_COLS = HIST_COLS * (NT > 128 ? 2 : 1);
+    static constexpr int MIN_SMEM = TMEM_COLS == 512 ? MIN_SMEM_ALONE
+                                    : TMEM_COLS == 256 ? MIN_SMEM_PAIR : MIN_SMEM_QUAD;
     static constexpr int SMEM = used < MIN_SMEM ? MIN_SMEM : used;
     static_assert(SMEM <= 227 * 1024, "shared memory");
     // The forward sweep stages F1 tokens at a time (several checkpoint
@@ -176,6 +186,25 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
+// CPT consecutive fp32 columns (16- or 8-byte aligned) as CPT / 2 pairs
+template <int CPT>
+__device__ __forceinline__ void ld_cols(const float* p, float2 (&o)[CPT / 2]) {
+    if constexpr (CPT == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        o[0] = make_float2(a.x, a.y);
+        o[1] = make_float2(a.z, a.w);
+    } else {
+        o[0] = *reinterpret_cast<const float2*>(p);
+    }
+}
+template <int CPT>
+__device__ __forceinline__ void st_cols(float* p, const float2 (&v)[CPT / 2]) {
+    if constexpr (CPT == 4)
+        *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    else
+        *reinterpret_cast<float2*>(p) = v[0];
+}
+
 __device__ __forceinline__ float rcp_approx(float x) {
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -211,9 +240,10 @@ __device__ __forceinline__ void issue_chunk(const Args& p, unsigned char* rb, lo
         const char* og = reinterpret_cast<const char*>(p.dout + tok0 * DV);
         for (int i = tid; i < op; i += NT) cp_async16(rb + Tl::r_do + i * 16, og + i * 16);
         const char* cg = reinterpret_cast<const char*>(
-            p.ckpt + (((bh - p.bh0) * p.ncb + cb) * p.nC + c) * 32LL * NT);
+            p.ckpt + (((bh - p.bh0) * p.ncb + cb) * p.nC + c) * static_cast<long long>(Tl::SW) * NT);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) cp_async16(rb + Tl::r_ck + (m * NT + tid) * 16, cg + (m * NT + tid) * 16);
+        for (int m = 0; m < Tl::SW / 4; ++m)
+            cp_async16(rb + Tl::r_ck + (m * NT + tid) * 16, cg + (m * NT + tid) * 16);
     }
     cp_async_commit();
 }
@@ -254,62 +284,71 @@ __device__ __forceinline__ TIn d_of(const Args& p, long long bh, long long t) {
     return static_cast<const TIn*>(p.d)[bh * p.T + t];
 }
 
-// Sum over the NR lanes sharing a column quad of 12 values (3 per column:
-// dq, dk-from-J, dk-from-eta partials).  Two halving levels leave each lane
-// 3 values that are then summed over the remaining levels; afterwards a lane
-// holds the totals of column g = 2 [rq & NR/2] + [rq & NR/4].
-template <int NR>
-__device__ __forceinline__ void column_reduce(float v[12], int rq) {
+// Sum over the NR lanes sharing a column group of 3 CPT values (3 per
+// column: dq, dk-from-J, dk-from-eta partials).  Halving levels (two for 4
+// columns, one for 2) leave each lane 3 values that are then summed over the
+// remaining levels; afterwards a lane holds the totals of column
+// g = 2 [rq & NR/2] + [rq & NR/4] (4 columns) or g = [rq & NR/2] (2).
+template <int NR, int CPT>
+__device__ __forceinline__ void column_reduce(float v[3 * CPT], int rq) {
     constexpr int o1 = NR / 2, o2 = NR / 4;
-    const bool up1 = (rq & o1) != 0, up2 = (rq & o2) != 0;
+    const bool up1 = (rq & o1) != 0;
 #pragma unroll
-    for (int m = 0; m < 6; ++m) {
-        const float send = up1 ? v[m] : v[m + 6];
-        const float keep = up1 ? v[m + 6] : v[m];
+    for (int m = 0; m < 3 * CPT / 2; ++m) {
+        const float send = up1 ? v[m] : v[m + 3 * CPT / 2];
+        const float keep = up1 ? v[m + 3 * CPT / 2] : v[m];
         v[m] = keep + __shfl_xor_sync(FULL, send, o1);
     }
+    constexpr int orest = CPT == 4 ? o2 : o1;   // the level after the halving ones
+    if constexpr (CPT == 4) {
+        const bool up2 = (rq & o2) != 0;
 #pragma unroll
-    for (int m = 0; m < 3; ++m) {
-        const float send = up2 ? v[m] : v[m + 3];
-        const float keep = up2 ? v[m + 3] : v[m];
-        v[m] = keep + __shfl_xor_sync(FULL, send, o2);
+        for (int m = 0; m < 3; ++m) {
+            const float send = up2 ? v[m] : v[m + 3];
+            const float keep = up2 ? v[m + 3] : v[m];
+            v[m] = keep + __shfl_xor_sync(FULL, send, o2);
+        }
     }
 #pragma unroll
-    for (int o = o2 / 2; o > 0; o /= 2)
+    for (int o = orest / 2; o > 0; o /= 2)
 #pragma unroll
         for (int m = 0; m < 3; ++m) v[m] += __shfl_xor_sync(FULL, v[m], o);
 }
 
-// Per-token inputs of one thread: its 4 rows and 4 columns.
+// Per-token inputs of one thread: its 4 rows and CPT columns.
+template <int CPT>
 struct TokIn {
     float bet[4], bvv[4], dov[4];
-    float2 kf[2], kq[2], qf[2];
+    float2 kf[CPT / 2], kq[CPT / 2], qf[CPT / 2];
 };
 
 // One adjoint step (token t, state st = (J_t, eta_t) as stored in TMEM): the
 // alpha sum of token t+1 with the adjoints as they come in, then the
 // adjoints of token t, then token t's partial sums.
-__device__ __forceinline__ void adjoint_step(const float st[32], const TokIn& in, float alpha_next,
-                                             float Ip, float2 (&GJ)[4][2], float2 (&GE)[4][2],
-                                             float cv[12], float rsum[8], float& dsum) {
+template <int CPT>
+__device__ __forceinline__ void adjoint_step(const float st[8 * CPT], const TokIn<CPT>& in, float alpha_next,
+                                             float Ip, float2 (&GJ)[4][CPT / 2], float2 (&GE)[4][CPT / 2],
+                                             float cv[3 * CPT], float rsum[8], float& dsum) {
+    constexpr int P = CPT / 2;
     const float2 ap = f2(alpha_next), ipp = f2(Ip);
-    float2 cdq[2], cck[2], cce[2], dacc[2];
+    float2 cdq[P], cck[P], cce[P], dacc[2];
+    dacc[0] = dacc[1] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) cdq[c2] = cck[c2] = cce[c2] = dacc[c2] = make_float2(0.f, 0.f);
+    for (int c2 = 0; c2 < P; ++c2) cdq[c2] = cck[c2] = cce[c2] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         float2 rsb = make_float2(0.f, 0.f), rse = rsb;
         const float2 dov = f2(in.dov[r]), bet = f2(in.bet[r]), bvv = f2(in.bvv[r]);
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-            const float2 Jt = make_float2(st[4 * r + 2 * c2], st[4 * r + 2 * c2 + 1]);
-            const float2 Et = make_float2(st[16 + 4 * r + 2 * c2], st[16 + 4 * r + 2 * c2 + 1]);
+        for (int c2 = 0; c2 < P; ++c2) {
+            const float2 Jt = make_float2(st[CPT * r + 2 * c2], st[CPT * r + 2 * c2 + 1]);
+            const float2 Et = make_float2(st[4 * CPT + CPT * r + 2 * c2], st[4 * CPT + CPT * r + 2 * c2 + 1]);
             const float2 den = __fadd2_rn(Jt, ipp);
             const float2 rr = make_float2(rcp_approx(den.x), rcp_approx(den.y));
             const float2 mu = __fmul2_rn(Et, rr);
             const float2 a = __fmul2_rn(__fmul2_rn(dov, in.qf[c2]), rr);
-            dacc[c2] = __ffma2_rn(GJ[r][c2], Jt, dacc[c2]);
-            dacc[c2] = __ffma2_rn(GE[r][c2], Et, dacc[c2]);
+            dacc[c2 & 1] = __ffma2_rn(GJ[r][c2], Jt, dacc[c2 & 1]);
+            dacc[c2 & 1] = __ffma2_rn(GE[r][c2], Et, dacc[c2 & 1]);
             GE[r][c2] = __ffma2_rn(ap, GE[r][c2], a);
             const float2 am = __fmul2_rn(a, mu);
             GJ[r][c2] = __ffma2_rn(ap, GJ[r][c2], make_float2(-am.x, -am.y));
@@ -323,7 +362,7 @@ __device__ __forceinline__ void adjoint_step(const float st[32], const TokIn& in
         rsum[4 + r] = rse.x + rse.y;
     }
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
+    for (int c2 = 0; c2 < P; ++c2) {
         cv[3 * (2 * c2)] = cdq[c2].x;
         cv[3 * (2 * c2) + 1] = cck[c2].x;
         cv[3 * (2 * c2) + 2] = cce[c2].x;
@@ -338,7 +377,8 @@ __device__ __forceinline__ void adjoint_step(const float st[32], const TokIn& in
 template <typename TIn, int DV, int CWB>
 __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(const Args p) {
     using Tl = Tile<TIn, DV, CWB>;
-    constexpr int NR = Tl::NR, NCQ = Tl::NCQ, NT = Tl::NT, NW = Tl::NW;
+    constexpr int NR = Tl::NR, NCQ = Tl::NCQ, NT = Tl::NT, NW = Tl::NW, CPT = Tl::CPT, P2 = CPT / 2;
+    constexpr int SW = Tl::SW;
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long lbh = blockIdx.x / p.ncb;   // head within this launch
@@ -346,7 +386,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     const int cb = blockIdx.x % p.ncb;
     const bool valid = tid < Tl::NTA;
     const int rq = valid ? tid % NR : 0, cq = valid ? tid / NR : 0;
-    const int row0 = 4 * rq, col0 = 4 * cq;                    // inside the tile
+    const int row0 = 4 * rq, col0 = CPT * cq;                  // inside the tile
     const long long S = static_cast<long long>(DV) * p.dk;
     const float Ip = p.Ip;
     uint32_t* holder = reinterpret_cast<uint32_t*>(sm + Tl::holder);
@@ -357,21 +397,48 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     tc_fence_after_sync();
     const uint32_t tbase = *holder;
     const uint32_t tlane = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
-                           static_cast<uint32_t>((warp >> 2) * 256);
+                           static_cast<uint32_t>(warp >> 2) * Tl::HIST_COLS;
 
     // ---- initial state of the tile: J = I_0 - I_prior, E = I_0 mu_0 -------
-    float2 J[4][2], E[4][2];
+    float2 J[4][P2], E[4][P2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
-        float4 i4 = make_float4(Ip, Ip, Ip, Ip), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid && p.I0) i4 = *reinterpret_cast<const float4*>(p.I0 + off);
-        if (valid && p.mu0) m4 = *reinterpret_cast<const float4*>(p.mu0 + off);
-        J[r][0] = make_float2(i4.x - Ip, i4.y - Ip);
-        J[r][1] = make_float2(i4.z - Ip, i4.w - Ip);
-        E[r][0] = make_float2(i4.x * m4.x, i4.y * m4.y);
-        E[r][1] = make_float2(i4.z * m4.z, i4.w * m4.w);
+        float2 i2[P2], m2[P2];
+#pragma unroll
+        for (int c2 = 0; c2 < P2; ++c2) {
+            i2[c2] = f2(Ip);
+            m2[c2] = f2(0.f);
+        }
+        if (valid && p.I0) ld_cols<CPT>(p.I0 + off, i2);
+        if (valid && p.mu0) ld_cols<CPT>(p.mu0 + off, m2);
+#pragma unroll
+        for (int c2 = 0; c2 < P2; ++c2) {
+            J[r][c2] = make_float2(i2[c2].x - Ip, i2[c2].y - Ip);
+            E[r][c2] = make_float2(i2[c2].x * m2[c2].x, i2[c2].y * m2[c2].y);
+        }
     }
+    // the state as SW / 4 float4 (J rows, then eta rows) and back: the
+    // layout of a checkpoint
+    auto state_f4 = [&](int m) {
+        const float2 (&X)[4][P2] = m < SW / 8 ? J : E;
+        const int r = ((m % (SW / 8)) * 4) / CPT;   // first row of the float4
+        if constexpr (CPT == 4)
+            return make_float4(X[r][0].x, X[r][0].y, X[r][1].x, X[r][1].y);
+        else
+            return make_float4(X[r][0].x, X[r][0].y, X[r + 1][0].x, X[r + 1][0].y);
+    };
+    auto set_state_f4 = [&](int m, float4 a) {
+        float2 (&X)[4][P2] = m < SW / 8 ? J : E;
+        const int r = ((m % (SW / 8)) * 4) / CPT;
+        if constexpr (CPT == 4) {
+            X[r][0] = make_float2(a.x, a.y);
+            X[r][1] = make_float2(a.z, a.w);
+        } else {
+            X[r][0] = make_float2(a.x, a.y);
+            X[r + 1][0] = make_float2(a.z, a.w);
+        }
+    };
 
     auto raw = [&](int i) { return sm + (i ? Tl::raw1 : Tl::raw0); };
     const float* sk = reinterpret_cast<const float*>(sm + Tl::s_k);
@@ -380,7 +447,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     const float* sb = reinterpret_cast<const float*>(sm + Tl::s_b);
     const float* sbv = reinterpret_cast<const float*>(sm + Tl::s_bv);
     const float* sal = reinterpret_cast<const float*>(sm + Tl::s_al);
-    float* ckpt_cta = p.ckpt + (lbh * p.ncb + cb) * static_cast<long long>(p.nC) * 32 * NT;
+    float* ckpt_cta = p.ckpt + (lbh * p.ncb + cb) * static_cast<long long>(p.nC) * SW * NT;
     const int nC = p.nC;
     auto ntok = [&](int c) { return min(C, p.T - c * C); };
     // one forward step of the tile on token s of the converted chunk
@@ -388,15 +455,14 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         const float2 al = f2(sal[s]);
         const float4 b4 = *reinterpret_cast<const float4*>(sb + s * DV + row0);
         const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * DV + row0);
-        const float4 k4 = *reinterpret_cast<const float4*>(sk + s * CWB + col0);
-        const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * CWB + col0);
         const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
-        const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
-        const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+        float2 kf[P2], kq[P2];
+        ld_cols<CPT>(sk + s * CWB + col0, kf);
+        ld_cols<CPT>(skk + s * CWB + col0, kq);
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
+            for (int c2 = 0; c2 < P2; ++c2) {
                 J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
                 E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
             }
@@ -469,25 +535,21 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         for (int s = 0; s < n; ++s) {
             if ((s & (C - 1)) == 0) {   // checkpoint: the tile's state before chunk (g F1 + s) / C
                 const int c = (g * F1 + s) / C;
-                float4* dst = reinterpret_cast<float4*>(ckpt_cta + static_cast<long long>(c) * 32 * NT);
+                float4* dst = reinterpret_cast<float4*>(ckpt_cta + static_cast<long long>(c) * SW * NT);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    dst[(2 * r) * NT + tid] = make_float4(J[r][0].x, J[r][0].y, J[r][1].x, J[r][1].y);
-                    dst[(2 * r + 1) * NT + tid] = make_float4(E[r][0].x, E[r][0].y, E[r][1].x, E[r][1].y);
-                }
+                for (int m = 0; m < SW / 4; ++m) dst[m * NT + tid] = state_f4(m);
             }
             const float2 al = f2(gal[s]);
             const float4 b4 = *reinterpret_cast<const float4*>(gb + s * DV + row0);
             const float4 v4 = *reinterpret_cast<const float4*>(gbv + s * DV + row0);
-            const float4 k4 = *reinterpret_cast<const float4*>(gk + s * CWB + col0);
-            const float4 kk4 = *reinterpret_cast<const float4*>(gkk + s * CWB + col0);
             const float bet[4] = {b4.x, b4.y, b4.z, b4.w}, bvv[4] = {v4.x, v4.y, v4.z, v4.w};
-            const float2 kf[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
-            const float2 kq[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+            float2 kf[P2], kq[P2];
+            ld_cols<CPT>(gk + s * CWB + col0, kf);
+            ld_cols<CPT>(gkk + s * CWB + col0, kq);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
+                for (int c2 = 0; c2 < P2; ++c2) {
                     J[r][c2] = __ffma2_rn(al, J[r][c2], __fmul2_rn(f2(bet[r]), kq[c2]));
                     E[r][c2] = __ffma2_rn(al, E[r][c2], __fmul2_rn(f2(bvv[r]), kf[c2]));
                 }
@@ -499,25 +561,25 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     __syncthreads();
 
     // ---- adjoints at t = T from the final-state gradients ------------------
-    float2 GJ[4][2], GE[4][2];
+    float2 GJ[4][P2], GE[4][P2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
-        float4 dm = make_float4(0.f, 0.f, 0.f, 0.f), di = dm;
-        if (valid && p.dfinal) {
-            dm = *reinterpret_cast<const float4*>(p.dfinal + off);
-            di = *reinterpret_cast<const float4*>(p.dfinal + p.BH * S + off);
-        }
-        const float dmv[4] = {dm.x, dm.y, dm.z, dm.w}, div[4] = {di.x, di.y, di.z, di.w};
+        float2 dm[P2], di[P2];
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
+        for (int c2 = 0; c2 < P2; ++c2) dm[c2] = di[c2] = f2(0.f);
+        if (valid && p.dfinal) {
+            ld_cols<CPT>(p.dfinal + off, dm);
+            ld_cols<CPT>(p.dfinal + p.BH * S + off, di);
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < P2; ++c2) {
             const float2 den = __fadd2_rn(J[r][c2], f2(Ip));
             const float2 rr = make_float2(1.f / den.x, 1.f / den.y);
             const float2 mu = __fmul2_rn(E[r][c2], rr);
-            const float2 dmu = make_float2(dmv[2 * c2], dmv[2 * c2 + 1]);
-            const float2 a = __fmul2_rn(dmu, rr);
+            const float2 a = __fmul2_rn(dm[c2], rr);
             GE[r][c2] = a;
-            GJ[r][c2] = make_float2(div[2 * c2] - a.x * mu.x, div[2 * c2 + 1] - a.y * mu.y);
+            GJ[r][c2] = make_float2(di[c2].x - a.x * mu.x, di[c2].y - a.y * mu.y);
         }
     }
 
@@ -526,9 +588,11 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
     float* s_dq = reinterpret_cast<float*>(sm + Tl::s_dq);
     float* s_dk = reinterpret_cast<float*>(sm + Tl::s_dk);
     float* s_D = reinterpret_cast<float*>(sm + Tl::s_D);
+    // after column_reduce a lane holds the totals of column g of its group;
+    // one lane per column writes them
     constexpr int o1 = NR / 2, o2 = NR / 4;
-    const int g = 2 * ((rq & o1) ? 1 : 0) + ((rq & o2) ? 1 : 0);
-    const bool col_writer = valid && (rq & (o2 - 1)) == 0;
+    const int g = CPT == 4 ? 2 * ((rq & o1) ? 1 : 0) + ((rq & o2) ? 1 : 0) : ((rq & o1) ? 1 : 0);
+    const bool col_writer = valid && (rq & ((CPT == 4 ? o2 : o1) - 1)) == 0;
     float alpha_next = 1.f;   // alpha of the token after the one being processed
     if (nC > 0) {
         const int c = nC - 1;
@@ -549,51 +613,45 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         {   // the chunk's checkpoint
             const float4* src = reinterpret_cast<const float4*>(rb + Tl::r_ck);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 a = src[(2 * r) * NT + tid], b = src[(2 * r + 1) * NT + tid];
-                J[r][0] = make_float2(a.x, a.y);
-                J[r][1] = make_float2(a.z, a.w);
-                E[r][0] = make_float2(b.x, b.y);
-                E[r][1] = make_float2(b.z, b.w);
-            }
+            for (int m = 0; m < SW / 4; ++m) set_state_f4(m, src[m * NT + tid]);
         }
         __syncthreads();   // converted inputs visible
         // forward again through the chunk; token s's state goes to TMEM slot s
         auto fwd_store = [&](int s) {
             forward_step(s);
-            float st[32];
+            float st[SW];   // J rows, then eta rows
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    st[4 * r + 2 * c2] = J[r][c2].x;
-                    st[4 * r + 2 * c2 + 1] = J[r][c2].y;
-                    st[16 + 4 * r + 2 * c2] = E[r][c2].x;
-                    st[16 + 4 * r + 2 * c2 + 1] = E[r][c2].y;
+                for (int c2 = 0; c2 < P2; ++c2) {
+                    st[CPT * r + 2 * c2] = J[r][c2].x;
+                    st[CPT * r + 2 * c2 + 1] = J[r][c2].y;
+                    st[4 * CPT + CPT * r + 2 * c2] = E[r][c2].x;
+                    st[4 * CPT + CPT * r + 2 * c2 + 1] = E[r][c2].y;
                 }
-            tmem_st32(tlane + static_cast<uint32_t>(s * 32), st);
+            if constexpr (SW == 32)
+                tmem_st32(tlane + static_cast<uint32_t>(s * SW), st);
+            else
+                tmem_st16(tlane + static_cast<uint32_t>(s * SW), st);
         };
 #pragma unroll 2
         for (int s = 0; s < n; ++s) fwd_store(s);
         tmem_wait_st();
         const float* sdo = reinterpret_cast<const float*>(rb + Tl::r_do);
-        auto load_in = [&](int s, TokIn& in) {
+        auto load_in = [&](int s, TokIn<CPT>& in) {
             const float4 b4 = *reinterpret_cast<const float4*>(sb + s * DV + row0);
             const float4 v4 = *reinterpret_cast<const float4*>(sbv + s * DV + row0);
             const float4 o4 = *reinterpret_cast<const float4*>(sdo + s * DV + row0);
-            const float4 k4 = *reinterpret_cast<const float4*>(sk + s * CWB + col0);
-            const float4 kk4 = *reinterpret_cast<const float4*>(skk + s * CWB + col0);
-            const float4 q4 = *reinterpret_cast<const float4*>(sq + s * CWB + col0);
             in.bet[0] = b4.x; in.bet[1] = b4.y; in.bet[2] = b4.z; in.bet[3] = b4.w;
             in.bvv[0] = v4.x; in.bvv[1] = v4.y; in.bvv[2] = v4.z; in.bvv[3] = v4.w;
             in.dov[0] = o4.x; in.dov[1] = o4.y; in.dov[2] = o4.z; in.dov[3] = o4.w;
-            in.kf[0] = make_float2(k4.x, k4.y); in.kf[1] = make_float2(k4.z, k4.w);
-            in.kq[0] = make_float2(kk4.x, kk4.y); in.kq[1] = make_float2(kk4.z, kk4.w);
-            in.qf[0] = make_float2(q4.x, q4.y); in.qf[1] = make_float2(q4.z, q4.w);
+            ld_cols<CPT>(sk + s * CWB + col0, in.kf);
+            ld_cols<CPT>(skk + s * CWB + col0, in.kq);
+            ld_cols<CPT>(sq + s * CWB + col0, in.qf);
         };
         // a token's partial sums into shared memory (column sums reduced here)
-        auto emit = [&](int s, float cv[12], const float rsum[8], float dsum) {
-            column_reduce<NR>(cv, rq);
+        auto emit = [&](int s, float cv[3 * CPT], const float rsum[8], float dsum) {
+            column_reduce<NR, CPT>(cv, rq);
             if (col_writer) {
                 const int j = col0 + g;
                 s_dq[s * CWB + j] = cv[0];
@@ -614,28 +672,35 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         // adjoint steps from the chunk's last token down.  Token s+1's sums are
         // reduced in the same step as token s's element arithmetic (the two are
         // independent), so the shuffle latency overlaps arithmetic.
-        float cur[32], cv[12], rsum[8], dsum;
-        tmem_ld32_async(tlane + static_cast<uint32_t>((n - 1) * 32), cur);
-        tmem_wait_ld(cur);
+        float cur[SW], cv[3 * CPT], rsum[8], dsum;
+        auto hist_load = [&](int s) {   // token s's state from TMEM into cur
+            if constexpr (SW == 32) {
+                tmem_ld32_async(tlane + static_cast<uint32_t>(s * SW), cur);
+                tmem_wait_ld(cur);
+            } else {
+                tmem_ld16_async(tlane + static_cast<uint32_t>(s * SW), cur);
+                tmem_wait_ld16(cur);
+            }
+        };
+        hist_load(n - 1);
         {
-            TokIn in;
+            TokIn<CPT> in;
             load_in(n - 1, in);
-            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cv, rsum, dsum);
+            adjoint_step<CPT>(cur, in, alpha_next, Ip, GJ, GE, cv, rsum, dsum);
             alpha_next = sal[n - 1];
         }
         // two tokens per iteration with the partial-sum buffers swapped (no
         // register copies between steps)
-        auto step_back = [&](int s, float (&cvi)[12], float (&rsi)[8], float& dsi, float (&cvo)[12],
-                             float (&rso)[8], float& dso) {
-            tmem_ld32_async(tlane + static_cast<uint32_t>(s * 32), cur);
-            tmem_wait_ld(cur);
-            TokIn in;
+        auto step_back = [&](int s, float (&cvi)[3 * CPT], float (&rsi)[8], float& dsi,
+                             float (&cvo)[3 * CPT], float (&rso)[8], float& dso) {
+            hist_load(s);
+            TokIn<CPT> in;
             load_in(s, in);
-            adjoint_step(cur, in, alpha_next, Ip, GJ, GE, cvo, rso, dso);
+            adjoint_step<CPT>(cur, in, alpha_next, Ip, GJ, GE, cvo, rso, dso);
             emit(s + 1, cvi, rsi, dsi);
             alpha_next = sal[s];
         };
-        float cvb[12], rsumb[8], dsumb;
+        float cvb[3 * CPT], rsumb[8], dsumb;
         int s = n - 2;
 #pragma unroll 1
         for (; s >= 1; s -= 2) {
@@ -645,7 +710,7 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
         if (s == 0) {
             step_back(0, cv, rsum, dsum, cvb, rsumb, dsumb);
 #pragma unroll
-            for (int m = 0; m < 12; ++m) cv[m] = cvb[m];
+            for (int m = 0; m < 3 * CPT; ++m) cv[m] = cvb[m];
 #pragma unroll
             for (int m = 0; m < 8; ++m) rsum[m] = rsumb[m];
             dsum = dsumb;
@@ -702,22 +767,30 @@ __global__ void __launch_bounds__(Tile<TIn, DV, CWB>::NT, 1) diag_bwd_kernel(con
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const long long off = bh * S + static_cast<long long>(row0 + r) * p.dk + cb * CWB + col0;
-            float4 i4 = make_float4(Ip, Ip, Ip, Ip), m4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid && p.I0) i4 = *reinterpret_cast<const float4*>(p.I0 + off);
-            if (valid && p.mu0) m4 = *reinterpret_cast<const float4*>(p.mu0 + off);
+            float2 i2[P2], m2[P2];
+#pragma unroll
+            for (int c2 = 0; c2 < P2; ++c2) {
+                i2[c2] = f2(Ip);
+                m2[c2] = f2(0.f);
+            }
+            if (valid && p.I0) ld_cols<CPT>(p.I0 + off, i2);
+            if (valid && p.mu0) ld_cols<CPT>(p.mu0 + off, m2);
             // J_0 = I_0 - I_prior, eta_0 = I_0 mu_0
-            dsum += GJ[r][0].x * (i4.x - Ip) + GJ[r][0].y * (i4.y - Ip) + GJ[r][1].x * (i4.z - Ip) +
-                    GJ[r][1].y * (i4.w - Ip);
-            dsum += GE[r][0].x * (i4.x * m4.x) + GE[r][0].y * (i4.y * m4.y) +
-                    GE[r][1].x * (i4.z * m4.z) + GE[r][1].y * (i4.w * m4.w);
+#pragma unroll
+            for (int c2 = 0; c2 < P2; ++c2) {
+                dsum += GJ[r][c2].x * (i2[c2].x - Ip) + GJ[r][c2].y * (i2[c2].y - Ip);
+                dsum += GE[r][c2].x * (i2[c2].x * m2[c2].x) + GE[r][c2].y * (i2[c2].y * m2[c2].y);
+            }
             if (p.dinit && valid) {
-                const float2 gj0 = __fmul2_rn(a0, GJ[r][0]), gj1 = __fmul2_rn(a0, GJ[r][1]);
-                const float2 ge0 = __fmul2_rn(a0, GE[r][0]), ge1 = __fmul2_rn(a0, GE[r][1]);
-                *reinterpret_cast<float4*>(p.dinit + off) =
-                    make_float4(ge0.x * i4.x, ge0.y * i4.y, ge1.x * i4.z, ge1.y * i4.w);
-                *reinterpret_cast<float4*>(p.dinit + p.BH * S + off) =
-                    make_float4(gj0.x + ge0.x * m4.x, gj0.y + ge0.y * m4.y, gj1.x + ge1.x * m4.z,
-                                gj1.y + ge1.y * m4.w);
+                float2 dmu[P2], dI[P2];
+#pragma unroll
+                for (int c2 = 0; c2 < P2; ++c2) {
+                    const float2 gj = __fmul2_rn(a0, GJ[r][c2]), ge = __fmul2_rn(a0, GE[r][c2]);
+                    dmu[c2] = make_float2(ge.x * i2[c2].x, ge.y * i2[c2].y);
+                    dI[c2] = make_float2(gj.x + ge.x * m2[c2].x, gj.y + ge.y * m2[c2].y);
+                }
+                st_cols<CPT>(p.dinit + off, dmu);
+                st_cols<CPT>(p.dinit + p.BH * S + off, dI);
             }
         }
         if (!valid) dsum = 0.f;
@@ -882,15 +955,15 @@ inline Scratch scratch_of(int B, int H, int T, int dk, int dv) {
     const long long BH = static_cast<long long>(B) * H;
     const BwdPlan pl = bwd_plan(BH, dk, dv);
     const long long nC = (static_cast<long long>(T) + C - 1) / C;
-    auto nt_of = [&](int cwb) {
-        const int nta = (dv / 4) * (cwb / 4);
-        return nta < 32 ? 32 : nta;
+    auto ck_words = [&](int cwb) {   // checkpoint words of a CTA: 8 CPT per thread
+        const int cpt = cwb == 32 ? 4 : 2, nta = (dv / 4) * (cwb / cpt);
+        return static_cast<size_t>(8 * cpt) * (nta < 32 ? 32 : nta);
     };
     Scratch s{};
-    s.ck_a = up256(static_cast<size_t>(pl.heads_a) * pl.ncb_a * nC * 32 * nt_of(pl.cwb_a) * 4);
+    s.ck_a = up256(static_cast<size_t>(pl.heads_a) * pl.ncb_a * nC * ck_words(pl.cwb_a) * 4);
     s.row_a = up256(static_cast<size_t>(pl.ncb_a) * pl.heads_a * T * 2 * dv * 4);
     s.pd_a = up256(static_cast<size_t>(pl.ncb_a) * pl.heads_a * T * 4);
-    s.ck_b = up256(static_cast<size_t>(pl.heads_b) * pl.ncb_b * nC * 32 * nt_of(pl.cwb_b) * 4);
+    s.ck_b = up256(static_cast<size_t>(pl.heads_b) * pl.ncb_b * nC * ck_words(pl.cwb_b) * 4);
     s.row_b = up256(static_cast<size_t>(pl.ncb_b) * pl.heads_b * T * 2 * dv * 4);
     s.pd_b = up256(static_cast<size_t>(pl.ncb_b) * pl.heads_b * T * 4);
     s.ea = up256(static_cast<size_t>(BH) * T * 4);
