@@ -104,6 +104,10 @@ TRAIN = {
                               ("uniform", 0.5, 4.0), 0, 0, False, 1003),
     "longctx_bwd": Workload("longctx_bwd", 1, 16, 65536, 128, 128, torch.bfloat16,
                             ("uniform", 0.1, 1.0), 0, 0, False, 1004),
+    # the long context's 16 heads over 4096 tokens (the same 16-column
+    # blocks, about 1 GB of checkpoints) for profiling captures
+    "heads16_t4096_bwd": Workload("heads16_t4096_bwd", 1, 16, 4096, 128, 128, torch.bfloat16,
+                                  ("uniform", 0.1, 1.0), 0, 0, False, 1009),
 }
 WORKLOADS.update(TRAIN)
 # the non-metaplastic limit (importance held at I_prior) on the layer shapes

@@ -18,7 +18,8 @@ collective; weak scaling); the timing is the max over ranks.
     python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
     python bench.py --workload layer750m_bwd   # the backward pass (training);
                                                # also layer1p3b_bwd, longctx_bwd,
-                                               # heads32_t1024_bwd (one wave, for ncu)
+                                               # heads32_t1024_bwd, heads16_t4096_bwd
+                                               # (one wave each, for ncu)
     python bench.py --workload decode2k        # batched one-token decoding
     python bench.py --workload layer750m_lin   # the non-metaplastic limit; also
                                                # longctx_lin, heads128_t512_lin
