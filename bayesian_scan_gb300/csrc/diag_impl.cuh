@@ -78,6 +78,7 @@ constexpr int NSTAGE = 3;        // chunks in flight
 constexpr int ROWS_PER_CTA = 128;
 constexpr int PAIRS = 3;         // of the 4 column-pair groups of a lane row, how many share reciprocals
 constexpr float SIGMA = 5.9604644775390625e-08f;   // 2^-24
+constexpr float INV_SIGMA = 16777216.f;             // 2^24
 constexpr float W_LIMIT = 281474976710656.0f;      // 2^48
 constexpr float LOG2E = 1.4426950408889634f;
 // Readout reduction through shared memory: every token each lane stores its 4

@@ -2,9 +2,11 @@
 // {64, 128}, warp-specialised ("Learning to Remember, Learn, and Forget in
 // Attention-Based Models", Metodologia 1-2; readout o_t = mu_t q_t).
 //
-// Same arithmetic as diag_scan_kernel (the scaled information form with
-// per-head power-of-two working scale, paired reciprocals, packed FP32; see
-// diag_impl.cuh), different division of labour inside the CTA:
+// Same arithmetic and results as diag_scan_kernel (the scaled information
+// form with per-head power-of-two working scale, paired reciprocals, packed
+// FP32; see diag_impl.cuh; for d_k = 64 the consumers keep J as sigma W J,
+// which moves the exact factor sigma = 2^-24 from the denominator into the
+// row factor W beta), different division of labour inside the CTA:
 //
 //  * 8 consumer warps own the state, 4 rows x 16 columns per lane, and do
 //    nothing but the element updates and the readout partials: per token they
@@ -75,6 +77,13 @@ constexpr int WS_RB = 8;                         // tokens per reduction buffer
 // slower).
 template <int DK>
 __host__ __device__ constexpr int ws_pairs() { return DK == 128 ? 4 : 3; }
+// The consumers keep J as sigma W J (sigma = 2^-24) instead of W J, so that
+// the denominator sigma W (J + I_prior) is one addition instead of a fused
+// multiply-add with sigma in a register pair (the same results: sigma is a
+// power of two).  Taken for d_k = 64 (1.3B-shaped layer 2.531 -> 2.481 ms);
+// for d_k = 128 it made the long context 0.3 % slower.
+template <int DK>
+__host__ __device__ constexpr bool ws_sigma_state() { return DK == 64; }
 // Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
 // previous flush at the start of a chunk (never inside the token loop), so
 // the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
@@ -145,6 +154,8 @@ diag_ws_kernel(const Params p) {
     const int dv = p.dv, HPC = G::ROWS / dv;
     const int PF = ws_par_floats(DK, dv);
     constexpr bool PSCALE = ws_row_scale_in_producers(DK);
+    constexpr bool SIGST = ws_sigma_state<DK>();
+    static_assert(!(PSCALE && SIGST), "the producers write W beta without sigma");
     constexpr int WS_RAW = ws_raw(DK);
     const WsLayout L(DK, dv, ES, TC, HPC, G::RED_FLOATS);
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
@@ -385,7 +396,7 @@ diag_ws_kernel(const Params p) {
                             }
                         }
                     }
-                    J[r][c2] = j2;
+                    J[r][c2] = SIGST ? __fmul2_rn(j2, f2(SIGMA)) : j2;
                     E[r][c2] = e2;
                 }
             }
@@ -446,7 +457,7 @@ diag_ws_kernel(const Params p) {
 #pragma unroll
                         for (int r = 0; r < RT; ++r) {
                             const float sb = W * bet[r];
-                            SB[r] = f2(sb);
+                            SB[r] = f2(SIGST ? sb * SIGMA : sb);
                             SBV[r] = f2(sb * val[r]);
                         }
                     }
@@ -478,7 +489,10 @@ diag_ws_kernel(const Params p) {
                                 const int c2 = half * 4 + c4;
                                 J[r][c2] = __ffma2_rn(SB[r], kk[c4], J[r][c2]);
                                 E[r][c2] = __ffma2_rn(SBV[r], kf[c4], E[r][c2]);
-                                den[c4] = __ffma2_rn(J[r][c2], SG, SP);
+                                if constexpr (SIGST)
+                                    den[c4] = __fadd2_rn(J[r][c2], SP);
+                                else
+                                    den[c4] = __ffma2_rn(J[r][c2], SG, SP);
                                 num[c4] = __fmul2_rn(qv[c4], E[r][c2]);
                             }
 #pragma unroll
@@ -515,7 +529,7 @@ diag_ws_kernel(const Params p) {
 #pragma unroll
                 for (int c2 = 0; c2 < CW / 2; ++c2) {
                     const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
-                    const float2 j2 = J[r][c2], e2 = E[r][c2];
+                    const float2 j2 = SIGST ? __fmul2_rn(J[r][c2], f2(INV_SIGMA)) : J[r][c2], e2 = E[r][c2];
                     *reinterpret_cast<float2*>(fm + off) = make_float2(e2.x / (j2.x + wI), e2.y / (j2.y + wI));
                     *reinterpret_cast<float2*>(fi + off) = make_float2(j2.x / W + Ip, j2.y / W + Ip);
                 }

@@ -61,7 +61,7 @@ DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
     "longctx": (766_519_552 + 23_238_656) + (37_775_104 + 0) + (1_113_857_792 + 501_525_504),
     "layer750m": (350_348_544 + 67_167_488) + (100_702_208 + 35_930_368) + (647_368_960 + 244_456_192),
-    "layer1p3b": 1_112_311_040 + 520_706_560,
+    "layer1p3b": 1_111_879_680 + 520_652_288,
 }
 
 
