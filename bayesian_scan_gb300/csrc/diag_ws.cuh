@@ -4,9 +4,12 @@
 //
 // Same arithmetic and results as diag_scan_kernel (the scaled information
 // form with per-head power-of-two working scale, paired reciprocals, packed
-// FP32; see diag_impl.cuh; for d_k = 64 the consumers keep J as sigma W J,
-// which moves the exact factor sigma = 2^-24 from the denominator into the
-// row factor W beta), different division of labour inside the CTA:
+// FP32; see diag_impl.cuh).  The consumers keep J as sigma W J (sigma =
+// 2^-24) rather than W J, with sigma in the row factor of the update, so
+// that the denominator sigma W (J + I_prior) is one addition (sigma is a
+// power of two: the same results).  When the producers form the row factors
+// (d_k = 128) the consumers need W only for the final state and read it
+// after the token loop.  The division of labour inside the CTA:
 //
 //  * 8 consumer warps own the state, 4 rows x 16 columns per lane, and do
 //    nothing but the element updates and the readout partials: per token they
@@ -77,13 +80,6 @@ constexpr int WS_RB = 8;                         // tokens per reduction buffer
 // slower).
 template <int DK>
 __host__ __device__ constexpr int ws_pairs() { return DK == 128 ? 4 : 3; }
-// The consumers keep J as sigma W J (sigma = 2^-24) instead of W J, so that
-// the denominator sigma W (J + I_prior) is one addition instead of a fused
-// multiply-add with sigma in a register pair (the same results: sigma is a
-// power of two).  Taken for d_k = 64 (1.3B-shaped layer 2.531 -> 2.481 ms);
-// for d_k = 128 it made the long context 0.3 % slower.
-template <int DK>
-__host__ __device__ constexpr bool ws_sigma_state() { return DK == 64; }
 // Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
 // previous flush at the start of a chunk (never inside the token loop), so
 // the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
@@ -154,8 +150,6 @@ diag_ws_kernel(const Params p) {
     const int dv = p.dv, HPC = G::ROWS / dv;
     const int PF = ws_par_floats(DK, dv);
     constexpr bool PSCALE = ws_row_scale_in_producers(DK);
-    constexpr bool SIGST = ws_sigma_state<DK>();
-    static_assert(!(PSCALE && SIGST), "the producers write W beta without sigma");
     constexpr int WS_RAW = ws_raw(DK);
     const WsLayout L(DK, dv, ES, TC, HPC, G::RED_FLOATS);
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
@@ -295,7 +289,8 @@ diag_ws_kernel(const Params p) {
                     load4(raw_b(s3, h) + tt * dv + 4 * i4, bet);
                     load4(raw_v(s3, h) + tt * dv + 4 * i4, val);
                     const float4 sb = make_float4(W * bet[0], W * bet[1], W * bet[2], W * bet[3]);
-                    *reinterpret_cast<float4*>(ps + 4 + 4 * i4) = sb;
+                    *reinterpret_cast<float4*>(ps + 4 + 4 * i4) =
+                        make_float4(sb.x * SIGMA, sb.y * SIGMA, sb.z * SIGMA, sb.w * SIGMA);
                     *reinterpret_cast<float4*>(ps + 4 + dv + 4 * i4) =
                         make_float4(sb.x * val[0], sb.y * val[1], sb.z * val[2], sb.w * val[3]);
                 }
@@ -396,7 +391,7 @@ diag_ws_kernel(const Params p) {
                             }
                         }
                     }
-                    J[r][c2] = SIGST ? __fmul2_rn(j2, f2(SIGMA)) : j2;
+                    J[r][c2] = __fmul2_rn(j2, f2(SIGMA));   // the state keeps sigma W J
                     E[r][c2] = e2;
                 }
             }
@@ -442,7 +437,7 @@ diag_ws_kernel(const Params p) {
                     const int b = (c * GPC + tt / WS_RB) % NRED;
                     const float* ptk = pbase + tt * PF;
                     const float4 sc = *reinterpret_cast<const float4*>(ptk + 3 * DK);
-                    W = sc.y;
+                    if constexpr (!PSCALE) W = sc.y;
                     static_assert(RT == 4, "one float4 of row scalars per lane");
                     float2 SB[RT], SBV[RT];
                     if constexpr (PSCALE) {
@@ -457,11 +452,11 @@ diag_ws_kernel(const Params p) {
 #pragma unroll
                         for (int r = 0; r < RT; ++r) {
                             const float sb = W * bet[r];
-                            SB[r] = f2(SIGST ? sb * SIGMA : sb);
+                            SB[r] = f2(sb * SIGMA);
                             SBV[r] = f2(sb * val[r]);
                         }
                     }
-                    const float2 SP = f2(sc.z), SG = f2(SIGMA);
+                    const float2 SP = f2(sc.z);
                     float2 acc[RT];
 #pragma unroll
                     for (int r = 0; r < RT; ++r) acc[r] = make_float2(0.f, 0.f);
@@ -489,10 +484,7 @@ diag_ws_kernel(const Params p) {
                                 const int c2 = half * 4 + c4;
                                 J[r][c2] = __ffma2_rn(SB[r], kk[c4], J[r][c2]);
                                 E[r][c2] = __ffma2_rn(SBV[r], kf[c4], E[r][c2]);
-                                if constexpr (SIGST)
-                                    den[c4] = __fadd2_rn(J[r][c2], SP);
-                                else
-                                    den[c4] = __ffma2_rn(J[r][c2], SG, SP);
+                                den[c4] = __fadd2_rn(J[r][c2], SP);
                                 num[c4] = __fmul2_rn(qv[c4], E[r][c2]);
                             }
 #pragma unroll
@@ -519,6 +511,7 @@ diag_ws_kernel(const Params p) {
             mbar_arrive(&par_empty[s2]);
         }
 
+        if constexpr (PSCALE) W = w_state[hsafe];   // the part's last W (chunks all prepared)
         if (active && p.final_state && part == p.P - 1) {
             // mu_T = eta / (I_prior + J) = Ew / (Jw + W I_prior);  I_T = Jw / W + I_prior
             float* fm = p.final_state + bh * S;
@@ -529,7 +522,7 @@ diag_ws_kernel(const Params p) {
 #pragma unroll
                 for (int c2 = 0; c2 < CW / 2; ++c2) {
                     const long long off = static_cast<long long>(i0 + r) * DK + cg * CW + 2 * c2;
-                    const float2 j2 = SIGST ? __fmul2_rn(J[r][c2], f2(INV_SIGMA)) : J[r][c2], e2 = E[r][c2];
+                    const float2 j2 = __fmul2_rn(J[r][c2], f2(INV_SIGMA)), e2 = E[r][c2];
                     *reinterpret_cast<float2*>(fm + off) = make_float2(e2.x / (j2.x + wI), e2.y / (j2.y + wI));
                     *reinterpret_cast<float2*>(fi + off) = make_float2(j2.x / W + Ip, j2.y / W + Ip);
                 }

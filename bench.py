@@ -59,9 +59,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_519_552 + 23_238_656) + (37_775_104 + 0) + (1_113_857_792 + 501_525_504),
-    "layer750m": (350_348_544 + 67_167_488) + (100_702_208 + 35_930_368) + (647_368_960 + 244_456_192),
-    "layer1p3b": 1_111_879_680 + 520_652_288,
+    "longctx": (766_467_328 + 23_127_040) + (37_774_336 + 0) + (1_113_822_208 + 501_355_008),
+    "layer750m": (350_250_240 + 67_003_136) + (100_693_760 + 36_320_000) + (647_599_872 + 244_951_552),
+    "layer1p3b": 1_111_840_256 + 520_730_112,
 }
 
 
