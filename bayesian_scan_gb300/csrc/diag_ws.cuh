@@ -436,8 +436,14 @@ diag_ws_kernel(const Params p) {
                     const int slot = tt & (WS_RB - 1);
                     const int b = (c * GPC + tt / WS_RB) % NRED;
                     const float* ptk = pbase + tt * PF;
-                    const float4 sc = *reinterpret_cast<const float4*>(ptk + 3 * DK);
-                    if constexpr (!PSCALE) W = sc.y;
+                    float SPs;   // sigma W I_prior of the token
+                    if constexpr (PSCALE) {
+                        SPs = ptk[3 * DK + 2];
+                    } else {
+                        const float4 sc = *reinterpret_cast<const float4*>(ptk + 3 * DK);
+                        W = sc.y;
+                        SPs = sc.z;
+                    }
                     static_assert(RT == 4, "one float4 of row scalars per lane");
                     float2 SB[RT], SBV[RT];
                     if constexpr (PSCALE) {
@@ -456,7 +462,7 @@ diag_ws_kernel(const Params p) {
                             SBV[r] = f2(sb * val[r]);
                         }
                     }
-                    const float2 SP = f2(sc.z);
+                    const float2 SP = f2(SPs);
                     float2 acc[RT];
 #pragma unroll
                     for (int r = 0; r < RT; ++r) acc[r] = make_float2(0.f, 0.f);
