@@ -59,9 +59,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_467_328 + 23_127_040) + (37_774_336 + 0) + (1_113_822_208 + 501_355_008),
-    "layer750m": (350_250_240 + 67_003_136) + (100_693_760 + 36_320_000) + (647_599_872 + 244_951_552),
-    "layer1p3b": 1_111_840_256 + 520_730_112,
+    "longctx": (766_470_144 + 23_221_760) + (37_780_224 + 0) + (1_114_589_952 + 501_337_600),
+    "layer750m": (350_252_288 + 66_739_968) + (100_693_248 + 36_107_776) + (647_319_552 + 244_496_128),
+    "layer1p3b": 1_111_801_856 + 520_666_112,
 }
 
 
