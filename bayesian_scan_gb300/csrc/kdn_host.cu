@@ -124,10 +124,18 @@ struct ChunkEvents {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Tokens per chunk of a host-buffer diagonal scan: about eight chunks, at
-// least 512 tokens, a multiple of 16.
+// Chunks of a host-buffer call (token ranges of a diagonal scan, groups of
+// Moebius sequences).  The first chunk's copies run before any scan and the
+// last chunk's scan after every copy, which favours more chunks, but every
+// chunk's scan has its fixed costs: on the 65536-token context with its
+// Moebius scan, 8 chunks gave 8.2e7 tokens/s end to end, 16 and 24 less
+// (6.7e7 to 8.1e7, varying from run to run).
+constexpr int kHostChunks = 8;
+
+// Tokens per chunk of a host-buffer diagonal scan: about kHostChunks chunks,
+// at least 512 tokens, a multiple of 16.
 int diag_chunk_tokens(int T) {
-    int tc = (T + 7) / 8;
+    int tc = (T + kHostChunks - 1) / kHostChunks;
     tc = (tc + 15) / 16 * 16;
     if (tc < 512) tc = 512;
     return tc < T ? tc : T;
@@ -435,9 +443,9 @@ kdn_status mobius_host(const float* ha, const float* hb, const float* hc, const 
                        const float* hl, float* hout, long long N, long long T, cudaStream_t st,
                        long long wait_ns) {
     if (N == 0 || T == 0) return KDN_OK;
-    // groups of whole sequences: about eight, each with at least 16 MB of
-    // coefficients (smaller scans run as one group)
-    long long G = (N + 7) / 8;
+    // groups of whole sequences: about kHostChunks, each with at least 16 MB
+    // of coefficients (smaller scans run as one group)
+    long long G = (N + kHostChunks - 1) / kHostChunks;
     const long long min_rows = (16LL << 20) / (16 * T) + 1;
     if (G < min_rows) G = min_rows;
     if (G > N) G = N;
