@@ -74,12 +74,11 @@ __host__ __device__ constexpr int ws_raw(int dk) { return ws_row_scale_in_produc
 constexpr int WS_PAR = 2;                        // converted chunk stages
 constexpr int WS_RB = 8;                         // tokens per reduction buffer
 // Column-pair groups (of 4 per lane row) whose two quotients share one
-// reciprocal: all 4 for d_k = 128, 3 for d_k = 64 (measured on GB300: with
-// all 4 paired the 65536-token call took 4.207 ms against 4.236 with 3, the
-// 1.3B layer's d_k = 64 call 2.506 against 2.498; with 2 paired both were
-// slower).
+// reciprocal: 3 (measured on GB300 with the denominator one addition: all 4
+// paired made the 1.3B layer's d_k = 64 call 2.477 -> 2.533 ms and the
+// 65536-token call 4.079 -> 4.087 ms; 2 paired was slower for both).
 template <int DK>
-__host__ __device__ constexpr int ws_pairs() { return DK == 128 ? 4 : 3; }
+__host__ __device__ constexpr int ws_pairs() { return 3; }
 // Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
 // previous flush at the start of a chunk (never inside the token loop), so
 // the TC / 8 groups of a chunk need TC / 8 + 1 buffers for the flush of the
