@@ -76,7 +76,8 @@ constexpr int WS_RB = 8;                         // tokens per reduction buffer
 // Column-pair groups (of 4 per lane row) whose two quotients share one
 // reciprocal: 3 (measured on GB300 with the denominator one addition: all 4
 // paired made the 1.3B layer's d_k = 64 call 2.477 -> 2.533 ms and the
-// 65536-token call 4.079 -> 4.087 ms; 2 paired was slower for both).
+// 65536-token call 4.079 -> 4.087 ms; 2 paired 2.48 -> 2.60 and 4.08 ->
+// 4.25 ms).
 template <int DK>
 __host__ __device__ constexpr int ws_pairs() { return 3; }
 // Reduction buffers for chunks of TC tokens: consumers wait for a buffer's
