@@ -59,9 +59,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_470_144 + 23_221_760) + (37_780_224 + 0) + (1_114_589_952 + 501_337_600),
-    "layer750m": (350_252_288 + 66_739_968) + (100_693_248 + 36_107_776) + (647_319_552 + 244_496_128),
-    "layer1p3b": 1_111_801_856 + 520_666_112,
+    "longctx": (766_525_440 + 23_494_144) + (37_774_848 + 0) + (1_114_360_320 + 501_451_264),
+    "layer750m": (350_250_752 + 66_865_408) + (100_698_368 + 36_356_352) + (647_612_416 + 244_458_752),
+    "layer1p3b": 1_111_859_456 + 520_771_840,
 }
 
 
