@@ -15,11 +15,14 @@
 // Precision.  beta and k are bf16 inputs, so they are exact operands.  The
 // decay weight goes with k^2 for Delta J, Delta J = sum_t beta_t[i] (w_t
 // k_t[j]^2), and with beta v for Delta eta, Delta eta = sum_t (w_t beta_t[i]
-// v_t[i]) k_t[j]; the fp32 factors w k^2 and w beta v are each split into
-// three bf16 pieces whose sum is the fp32 value exactly (split3 below).  So
-// each sum takes three products, accumulated in fp32, and every term is as
-// accurate as the fp32 product it stands for: the carried states are
-// fp32-accurate, not bf16-accurate.  The decay exponents are summed in
+// v_t[i]) k_t[j].  The fp32 factor w beta v is split into three bf16 pieces
+// whose sum is the fp32 value exactly (split3 below), so every term of
+// Delta eta, whose signed terms can cancel, is as accurate as the fp32
+// product it stands for.  The factor w k^2 is split into two (split2): a
+// term of Delta J then falls short by less than 2^-16 of itself, and with
+// beta >= 0 (a gate in (0, 1) on the pages) every term is non-negative, so
+// Delta J is within 2^-16 of its fp32 value, with no cancellation to
+// amplify it.  The carried states are fp32-accurate, not bf16-accurate.  The decay exponents are summed in
 // two-float form (about 48 significant bits from error-free fp32 additions;
 // fp64 on this GPU runs at a small fraction of the fp32 rate, and fp64 sums
 // took 13-15 thousand cycles per super-chunk) and w_t = 2^-floor(S) *
@@ -35,7 +38,7 @@
 // by the build threads (8 tokens each, two-float suffix sums across them).
 // Per chunk the build threads load their part of the raw chunk (k, beta, v,
 // brought in by 1-D bulk copies AG_NS chunks ahead) into registers and
-// release its stage on the stage's empty barrier, then write the 8 operand
+// release its stage on the stage's empty barrier, then write the 7 operand
 // tiles (128 x KC bf16 each, core-matrix layout) and arrive, one lane per
 // warp, on the chunk's operand barrier.  The issuing warp refills each
 // released stage with the copies of the chunk AG_NS later, waits for the
@@ -61,7 +64,8 @@ namespace diag {
 namespace {
 
 constexpr int AG_D = 128;                          // d_k = d_v
-constexpr int AG_NTILE = 8;                        // A_beta, A_E hi/mid/lo, B_k, B_wk2 hi/mid/lo
+constexpr int AG_NTILE = 8;                        // A_beta, A_E hi/mid/lo, B_k, B_wk2 hi/lo, (unused)
+constexpr int AG_NTILE_BUILT = 7;                  // the tiles a chunk writes
 // tensor memory: 256 columns (J in [0,128), eta in [128,256)); the wide
 // form takes 512 (J pieces in [0,256), eta^T pieces in [256,512))
 constexpr int AG_TMEM_COLS = 256;
@@ -84,12 +88,11 @@ struct AggShape {
     static constexpr uint32_t SBO = (KC / 8) * 128;     // core matrices: next 8 rows (M or N)
     static constexpr int SUP = 8 * BUILD;               // tokens per super-chunk of decay weights
     // Wide products (the one-CTA shape, whose CTA may hold all 512 TMEM
-    // columns): J takes A_beta x [B_wk2 hi | B_wk2 mid] as one N = 256
-    // product (two accumulators, added in the epilogue) plus A_beta x
-    // B_wk2 lo, and eta is formed transposed, eta^T = k x [A_E hi | A_E mid]
-    // + k x A_E lo: 4 products a K step instead of 6, and a sixth less
-    // shared memory read by the tensor core (40 KB instead of 48); the
-    // eta-only variant takes the two eta^T products instead of three.
+    // columns): J takes A_beta x [B_wk2 hi | B_wk2 lo] as one N = 256
+    // product (two accumulators, added in the epilogue), and eta is formed
+    // transposed, eta^T = k x [A_E hi | A_E mid] + k x A_E lo: 3 products a
+    // K step instead of 5, and less shared memory read by the tensor core;
+    // the eta-only variant takes the two eta^T products.
     static constexpr bool WIDE = KC == 32;
     static constexpr int NBAR = 2 * AG_NS + 4;          // raw_full, raw_empty [AG_NS]; mma_done, ops_full [2]
     static constexpr int SMEM = 2 * OPS + AG_NS * 3 * RAW + SUP * 4 + 8 * 8 + NBAR * 8 + 16;
@@ -155,6 +158,18 @@ __device__ __forceinline__ void split3(float2 x, uint32_t (&h)[2], uint32_t (&m)
     const float2 s = __fadd2_rn(r, make_float2(-__uint_as_float(m[0]), -__uint_as_float(m[1])));
     l[0] = __float_as_uint(s.x);
     l[1] = __float_as_uint(s.y);
+}
+
+// Two bf16 pieces of each of x.x, x.y (bit patterns, low 16 bits of lo not
+// cleared: packing takes the upper halves): hi keeps the top 8 significant
+// bits by truncation and lo the top 8 of the exact remainder, so hi + lo
+// falls short of x by less than 2^-16 |x|.
+__device__ __forceinline__ void split2(float2 x, uint32_t (&h)[2], uint32_t (&l)[2]) {
+    h[0] = __float_as_uint(x.x) & 0xffff0000u;
+    h[1] = __float_as_uint(x.y) & 0xffff0000u;
+    const float2 r = __fadd2_rn(x, make_float2(-__uint_as_float(h[0]), -__uint_as_float(h[1])));
+    l[0] = __float_as_uint(r.x);
+    l[1] = __float_as_uint(r.y);
 }
 
 // bf16x2 of the upper halves of a (low half) and b
@@ -291,18 +306,15 @@ diag_agg_tc_kernel(const AggArgs p) {
                     const uint32_t first = (it == 0 && s == 0) ? 0u : 1u;
                     if (WIDE) {
                         // tiles 5, 6 (and 1, 2) are adjacent: one 256-row operand
-                        if (!ETA_ONLY) {
-                            umma_bf16(tmem, desc(0), desc(5), IDESC_WIDE, first);      // J: hi | mid
-                            umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);              //  + lo
-                        }
+                        if (!ETA_ONLY)
+                            umma_bf16(tmem, desc(0), desc(5), IDESC_WIDE, first);      // J: hi | lo
                         umma_bf16(tmem + 2 * AG_D, desc(4), desc(1), IDESC_WIDE, first);   // eta^T: hi | mid
                         umma_bf16(tmem + 2 * AG_D, desc(4), desc(3), IDESC, 1u);       //  + lo
                         continue;
                     }
                     if (!ETA_ONLY) {
                         umma_bf16(tmem, desc(0), desc(5), IDESC, first);       // J += A_beta B_wk2 hi
-                        umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_beta B_wk2 mid
-                        umma_bf16(tmem, desc(0), desc(7), IDESC, 1u);          //    + A_beta B_wk2 lo
+                        umma_bf16(tmem, desc(0), desc(6), IDESC, 1u);          //    + A_beta B_wk2 lo
                     }
                     umma_bf16(tmem + AG_D, desc(1), desc(4), IDESC, first);    // eta += A_E hi B_k
                     umma_bf16(tmem + AG_D, desc(2), desc(4), IDESC, 1u);       //      + A_E mid B_k
@@ -399,14 +411,14 @@ diag_agg_tc_kernel(const AggArgs p) {
         // the operand buffer was last read by the MMAs of iteration it - 2
         if (it >= 2 && !mbar_wait(&mma_done[ob], ((it - 2) >> 1) & 1, p.wait_ns)) ok = false;
 
-        // ---- build the 8 operand tiles of this chunk: products packed over
+        // ---- build the 7 operand tiles of this chunk: products packed over
         // the row pair, pieces packed over token pairs ----
         {
             uint32_t t[AG_NTILE][2][4];   // [tile][row of the pair][4 x bf16x2 along the tokens]
 #pragma unroll
             for (int u2 = 0; u2 < 4; ++u2) {
                 uint32_t eh[2][2], em[2][2], el[2][2];   // [token of the pair][row]: pieces of w beta v
-                uint32_t jh[2][2], jm[2][2], jl[2][2];   //                                 of w k^2
+                uint32_t jh[2][2], jm[2][2];             //                                 of w k^2
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int u = 2 * u2 + e;
@@ -416,7 +428,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                     const float2 kf = make_float2(__uint_as_float(kk[u] << 16), __uint_as_float(kk[u] & 0xffff0000u));
                     split3(__fmul2_rn(__fmul2_rn(w2, bf), vf), eh[e], em[e], el[e]);
                     if (!ETA_ONLY)   // k^2 is exact in fp32 (16 significant bits)
-                        split3(__fmul2_rn(w2, __fmul2_rn(kf, kf)), jh[e], jm[e], jl[e]);
+                        split2(__fmul2_rn(w2, __fmul2_rn(kf, kf)), jh[e], jm[e]);
                 }
                 const int u = 2 * u2;
 #pragma unroll
@@ -426,7 +438,6 @@ diag_agg_tc_kernel(const AggArgs p) {
                         t[0][r][u2] = __byte_perm(bb[u], bb[u + 1], sel);
                         t[5][r][u2] = pack_hi(jh[0][r], jh[1][r]);
                         t[6][r][u2] = pack_hi(jm[0][r], jm[1][r]);
-                        t[7][r][u2] = pack_hi(jl[0][r], jl[1][r]);
                     }
                     t[1][r][u2] = pack_hi(eh[0][r], eh[1][r]);
                     t[2][r][u2] = pack_hi(em[0][r], em[1][r]);
@@ -440,7 +451,7 @@ diag_agg_tc_kernel(const AggArgs p) {
                 const int rho = 2 * pr + (r ^ static_cast<int>(flip));
                 const int off = ((rho >> 3) * (AG_KC / 8) + kg) * 128 + (rho & 7) * 16;   // core matrix (rho/8, kg)
 #pragma unroll
-                for (int tile = ETA_ONLY ? 1 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE); ++tile)
+                for (int tile = ETA_ONLY ? 1 : 0; tile < (ETA_ONLY ? 5 : AG_NTILE_BUILT); ++tile)
                     *reinterpret_cast<uint4*>(o + tile * AG_TILE + off) =
                         make_uint4(t[tile][r][0], t[tile][r][1], t[tile][r][2], t[tile][r][3]);
             }

@@ -17,9 +17,12 @@ Element-wise bars, derived from the arithmetic: an output computed in fp32
 from terms whose magnitudes sum to S carries an absolute error of a few fp32
 ulps of S; at the floor (|ref| <= 1e-3 rms) that is about 4 * 2^-24 * S /
 (1e-3 rms) ~ 2.4e-4 S/rms, with S/rms up to about sqrt(d_k) ~ 11 for the
-readout.  So every fp32 path (the scans on CUDA cores, the token split, whose
-tensor-core aggregates carry fp32-accurate terms, the decode step, the
-backward pass) takes 2e-3, and lambda 1e-5.  The non-metaplastic tensor-core
+readout.  So every fp32 path (the scans on CUDA cores, the token split, the
+decode step, the backward pass) takes 2e-3, and lambda 1e-5.  The token
+split's tensor-core aggregates carry fp32-accurate eta terms and J terms
+within 2^-16 of theirs (non-negative, so J within 2^-16); the carried start
+state's error decays within a part, and the slowest-forgetting case here
+(A = 0.02) measures 1.2e-3 element-wise.  The non-metaplastic tensor-core
 kernel keeps bf16 hi + lo pieces (2^-16 relative per term) in its products,
 256 times coarser than fp32: its element-wise bar is 1e-1 (its per-tensor bar
 stays 2e-3).
