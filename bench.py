@@ -59,9 +59,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_525_440 + 23_494_144) + (37_774_848 + 0) + (1_114_360_320 + 501_451_264),
-    "layer750m": (350_250_752 + 66_865_408) + (100_698_368 + 36_356_352) + (647_612_416 + 244_458_752),
-    "layer1p3b": 1_111_859_456 + 520_771_840,
+    "longctx": (766_463_744 + 23_119_360) + (37_774_592 + 0) + (1_113_924_608 + 501_309_440),
+    "layer750m": (350_262_272 + 68_769_280) + (100_693_248 + 36_242_688) + (647_302_656 + 244_467_456),
+    "layer1p3b": 1_113_252_864 + 520_797_952,
 }
 
 
