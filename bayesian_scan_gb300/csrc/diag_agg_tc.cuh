@@ -22,8 +22,9 @@
 // term of Delta J then falls short by less than 2^-16 of itself, and with
 // beta >= 0 (a gate in (0, 1) on the pages) every term is non-negative, so
 // Delta J is within 2^-16 of its fp32 value, with no cancellation to
-// amplify it.  The carried states are fp32-accurate, not bf16-accurate.  The decay exponents are summed in
-// two-float form (about 48 significant bits from error-free fp32 additions;
+// amplify it: the carried states are fp32-accurate (eta) or within 2^-16
+// (J), not bf16-accurate.  The decay exponents are summed in two-float form
+// (about 48 significant bits from error-free fp32 additions;
 // fp64 on this GPU runs at a small fraction of the fp32 rate, and fp64 sums
 // took 13-15 thousand cycles per super-chunk) and w_t = 2^-floor(S) *
 // exp2(-frac(S)).
