@@ -104,12 +104,12 @@ def oracle_diag(inp, I0=None, mu0=None):
                             inp["I_prior"], I0, mu0)
 
 
-def check_diag(inp, I0=None, mu0=None, tol=TOL_DIAG):
+def check_diag(inp, I0=None, mu0=None, tol=TOL_DIAG, tol_elem=TOL_ELEM):
     o, fs = gpu_diag(inp, I0, mu0)
     ro, rmu, rI = oracle_diag(inp, I0, mu0)
     errs = dict(o=both_errs(o, ro), mu=both_errs(fs[0], rmu), I=both_errs(fs[1], rI))
     for k_, (e, ee) in errs.items():
-        assert e <= tol and ee <= TOL_ELEM, (k_, errs)
+        assert e <= tol and ee <= tol_elem, (k_, errs)
     return errs
 
 

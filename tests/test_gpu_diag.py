@@ -76,6 +76,19 @@ def test_token_split_tensor_core_aggregates(law, T):
     parity.check_diag(draw(1, 2, T, 128, 128, A_law=law, seed=T))
 
 
+def test_long_memory_many_parts():
+    """8192 tokens forgetting slowly (A d ~ 0.005: a memory of about 300
+    tokens) split into 64 parts, 63 carries.  Per tensor the outputs stay
+    near 1e-6 of the oracle.  Element-wise at the 1e-3 rms floor the bar is
+    looser than 2e-3: the state is fp32 and a memory of ~300 tokens carries
+    a few tens of fp32 ulps of rounding per element, which an output that
+    cancels down to 1e-3 rms shows as ~1e-3 to 1e-2 of itself (measured
+    4e-3)."""
+    from bayesian_scan_gb300 import kdn
+    assert kdn.diag_scan_plan(1, 2, 8192, 128, 128)["parts"] >= 32
+    parity.check_diag(draw(1, 2, 8192, 128, 128, A_law=("const", 0.005), seed=12), tol_elem=1e-2)
+
+
 def test_token_split_tensor_core_aggregates_initial_state():
     inp = draw(1, 1, 2600, 128, 128, A_law=("const", 0.02))
     g = torch.Generator().manual_seed(10)
