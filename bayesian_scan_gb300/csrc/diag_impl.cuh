@@ -682,6 +682,7 @@ diag_scan_kernel(const Params p) {
 __global__ void diag_carry_kernel(float* agg, const AggScale* scl, const float* I0,
                                   const float* mu0, float I_prior, long long BH, long long S,
                                   int P) {
+    grid_dep_signal();   // the full pass may start its prologue (it waits before reading agg)
     // four consecutive elements of one head per thread (S is a multiple of 4)
     const long long idx = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
     if (idx >= BH * S) return;
@@ -1066,12 +1067,24 @@ kdn_status launch_dk(const DiagArgs& a, cudaStream_t st, long long wait_ns) {
         bool launched = false;
         if constexpr (!LIN && (DK == 64 || DK == 128)) {
             if (pl.ws) {
-                // launch_smem == pl.smem_full: the walkers' stages fit it (plan_dk)
-                if (pl.TC_full == 16)
-                    diag_ws_kernel<DK, TIn, 16><<<grid, WS_THREADS, launch_smem, st>>>(prm);
-                else
-                    diag_ws_kernel<DK, TIn, 8><<<grid, WS_THREADS, launch_smem, st>>>(prm);
-                e = cudaGetLastError();
+                // launch_smem == pl.smem_full: the walkers' stages fit it (plan_dk).
+                // After the carry kernel (P > 1) the full pass is launched as its
+                // programmatic dependent: its CTAs may start while the carry
+                // finishes (the caller's inputs were complete before the
+                // aggregate pass began) and wait for it only where they read
+                // a carried start state.
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(grid);
+                cfg.blockDim = dim3(WS_THREADS);
+                cfg.dynamicSmemBytes = static_cast<size_t>(launch_smem);
+                cfg.stream = st;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = P > 1 ? 1 : 0;
+                e = pl.TC_full == 16 ? cudaLaunchKernelEx(&cfg, diag_ws_kernel<DK, TIn, 16>, prm)
+                                     : cudaLaunchKernelEx(&cfg, diag_ws_kernel<DK, TIn, 8>, prm);
                 launched = true;
             }
         }

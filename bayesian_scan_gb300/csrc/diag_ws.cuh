@@ -368,6 +368,7 @@ diag_ws_kernel(const Params p) {
             const float* src_J = nullptr;
             const float* src_E = nullptr;
             if (part > 0) {
+                grid_dep_wait();   // the carry kernel's start states (launched ahead of it)
                 src_J = p.agg + (static_cast<long long>(part - 1) * p.BH + bh) * 2 * S;
                 src_E = src_J + S;
             }

@@ -20,6 +20,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+// A grid launched with programmatic stream serialization may start once every
+// CTA of the grid before it has signalled; its threads wait for that grid's
+// completion (and memory) only where they read its results.  In a grid
+// launched the ordinary way both are no-ops.
+__device__ __forceinline__ void grid_dep_signal() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- mbarriers (CTA scope) -------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
