@@ -59,9 +59,9 @@ EXTRA_WORKLOADS = ("layer750m", "layer1p3b")
 # profiles/ (launches_*.md); workloads without such a capture report null.
 DIAG_TRAFFIC_BYTES = {
     # aggregates + carry + full pass, read + write
-    "longctx": (766_463_744 + 23_119_360) + (37_774_592 + 0) + (1_113_924_608 + 501_309_440),
-    "layer750m": (350_262_272 + 68_769_280) + (100_693_248 + 36_242_688) + (647_302_656 + 244_467_456),
-    "layer1p3b": 1_113_252_864 + 520_797_952,
+    "longctx": (766_564_608 + 22_931_712) + (37_774_336 + 0) + (1_114_039_296 + 501_455_872),
+    "layer750m": (350_242_304 + 68_923_392) + (100_699_648 + 36_041_728) + (647_612_160 + 244_894_464),
+    "layer1p3b": 1_112_063_488 + 520_773_888,
 }
 
 
